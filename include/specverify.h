@@ -1,0 +1,230 @@
+/*
+ * specverify.h -- C ABI of the GB300 speculative-decoding verification
+ * library (libspecverify.so, sm_103a).
+ *
+ * What it computes.  Given target-model logits at every drafted position and
+ * the draft model's distributions, decide which drafted tokens a target
+ * sampler would have produced, exactly as sampling from the target would:
+ *
+ *   accept drafted x with probability min(1, p(x)/q(x)), left to right, stop
+ *   at the first rejection and draw the replacement from norm(max(0, p - q));
+ *   if every draft is accepted draw a bonus token from p at the last row.
+ *
+ * (exactness rule of "投机解码与 EAGLE"; a(x) and r(x), section 二 of
+ * "064 · 投机解码：小模型先起草，大模型怎样并行验收而不改变分布"; §2.1 of the
+ * EAGLE-2 notes.)  p and q are taken after the same temperature / top-k /
+ * top-p transform ("064 · 投机解码", section 二).  Temperature 0 selects the
+ * greedy rule (accept while the draft equals the target argmax, then emit the
+ * argmax; "贪婪情形简化" of "投机解码与 EAGLE").  Trees follow the EAGLE
+ * description (a rejected token lets the other branches be tried, EAGLE-2
+ * notes §2.2) and EAGLE-2's expand / rerank (§4.1-4.2).
+ *
+ * Conventions shared by every entry point
+ *   - All array arguments are DEVICE pointers owned by the caller, row-major
+ *     and contiguous (last dimension fastest).  The library allocates nothing
+ *     and keeps no pointer after the call.
+ *   - Work is enqueued on `stream` (a cudaStream_t passed as void*, NULL =
+ *     legacy default stream); calls return as soon as the work is enqueued.
+ *     Outputs and the workspace must not be touched by other work on other
+ *     streams until the enqueued work has finished.
+ *   - Logit dtypes: SPEC_F32 (float32) or SPEC_BF16 (bfloat16 stored as
+ *     uint16).  Token and index arrays are int32.
+ *   - Return value: SPEC_OK or a negative SPEC_ERR_* code.  Argument errors
+ *     are detected on the host before anything is enqueued.  Data-dependent
+ *     conditions found on the device (NaN logits, a drafted token with
+ *     q(x) = 0, ...) never stop a kernel: they set bits of a status word kept
+ *     in the workspace, read back with spec_get_status().
+ *   - Random numbers: one uniform per decision from Philox4x32-10 (Salmon et
+ *     al., SC'11) with key = (seed low 32 bits, seed high 32 bits) and counter
+ *     (b, i, slot, philox_offset); u = (word0 >> 8) * 2^-24.  slot 0: accept
+ *     test of drafted token i; slot 1: replacement / bonus draw at target
+ *     row i.  The draw used for a decision does not depend on other outcomes.
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- return codes ---- */
+#define SPEC_OK 0
+#define SPEC_ERR_ARG (-1)         /* NULL pointer, negative size, bad param */
+#define SPEC_ERR_DTYPE (-2)       /* unknown dtype or draft kind           */
+#define SPEC_ERR_SHAPE (-3)       /* sizes inconsistent or over the limits */
+#define SPEC_ERR_CUDA (-4)        /* a CUDA runtime call failed            */
+#define SPEC_ERR_WORKSPACE (-5)   /* workspace NULL, misaligned or small   */
+#define SPEC_ERR_UNSUPPORTED (-6) /* valid request this build cannot serve */
+
+/* ---- dtypes and draft kinds ---- */
+#define SPEC_F32 0
+#define SPEC_BF16 1
+#define SPEC_DRAFT_LOGITS 0 /* draft rows are logits: q = softmax(z / T)  */
+#define SPEC_DRAFT_PROBS 1  /* draft rows are probabilities: z = log q    */
+
+/* ---- limits ---- */
+#define SPEC_MAX_VOCAB (1 << 24)  /* V                                     */
+#define SPEC_MAX_TOP_K 1024       /* top_k when top-k / top-p is used      */
+#define SPEC_MAX_CHILDREN 64      /* children of one tree node             */
+#define SPEC_MAX_TREE_NODES 1024  /* N (tree) and K (chain)                */
+#define SPEC_EAGLE2_MAX_TOPK 32   /* children per expanded EAGLE-2 node    */
+
+/* ---- device status bits (spec_get_status) ---- */
+#define SPEC_STATUS_NAN 1u            /* a logit row had NaN / no finite value */
+#define SPEC_STATUS_QZERO_ACCEPT 2u   /* drafted token with q(x) = 0 accepted  */
+#define SPEC_STATUS_RESIDUAL_ZERO 4u  /* residual had no mass; drew from p     */
+#define SPEC_STATUS_DRAFT_EXHAUSTED 8u /* siblings' tokens held all of q       */
+#define SPEC_STATUS_CDF_FALLBACK 16u  /* rounding: inverse CDF took last token */
+#define SPEC_STATUS_BAD_TREE 32u      /* parent / q_row entry out of range     */
+#define SPEC_STATUS_TOKEN_RANGE 64u   /* drafted token outside [0, V): reject  */
+#define SPEC_STATUS_TIMEOUT 128u      /* a bounded device wait gave up         */
+
+/* ---- operations for spec_workspace_bytes ---- */
+#define SPEC_OP_CHAIN 1
+#define SPEC_OP_TREE 2
+#define SPEC_OP_EAGLE2 3
+
+/* Sampling parameters (plain data, 32 bytes). */
+typedef struct spec_params {
+  float temperature;      /* > 0: sampling rule; == 0: greedy argmax rule  */
+  int32_t top_k;          /* 0 = off; else 1 .. SPEC_MAX_TOP_K             */
+  float top_p;            /* in (0, 1]; 1 = off.  Needs 1 <= top_k         */
+  int32_t draft_kind;     /* SPEC_DRAFT_LOGITS or SPEC_DRAFT_PROBS         */
+  uint64_t seed;          /* Philox key                                    */
+  uint32_t philox_offset; /* fourth Philox counter word                    */
+  uint32_t flags;         /* reserved, must be 0                           */
+} spec_params_t;
+
+/*
+ * Workspace size in bytes for one call of `op` (SPEC_OP_CHAIN with n = K,
+ * SPEC_OP_TREE with n = N, SPEC_OP_EAGLE2 with n = number of draft rows per
+ * sequence).  The workspace must be 256-byte aligned device memory; its
+ * contents need no initialisation and are overwritten by every call.  Returns
+ * 0 for invalid sizes.
+ */
+size_t spec_workspace_bytes(int op, int B, int n, int V);
+
+/*
+ * Chain verification (the listing of "064 · 投机解码", section 三; steps 3-4 of
+ * "投机解码与 EAGLE").
+ *
+ * target_logits [B, K+1, V] dtype_target: target logits at the K drafted
+ *     positions and the bonus position.
+ * draft [B, K, V] dtype_draft: draft logits or probabilities
+ *     (prm->draft_kind).  Not read, and may be NULL, when temperature == 0.
+ * draft_tokens [B, K] int32: the drafted tokens x_0 .. x_{K-1}.
+ * accepted [B] int32 (out): number n of accepted drafts, 0 .. K.
+ * out_tokens [B, K+1] int32 (out): x_0 .. x_{n-1}, then the replacement
+ *     (n < K) or bonus (n == K) token, then -1 padding.
+ * accept_mass [B, K] float32 (out): alpha_k = sum_x min(p_k(x), q_k(x)) for
+ *     every k (also after the first rejection); at temperature 0 the
+ *     indicator 1[x_k == argmax_k].
+ * B >= 0 (0 = nothing to do), 0 <= K <= SPEC_MAX_TREE_NODES,
+ * 1 <= V <= SPEC_MAX_VOCAB.
+ */
+int spec_verify_chain(const void* target_logits, const void* draft,
+                      const int32_t* draft_tokens, int B, int K, int V,
+                      int dtype_target, int dtype_draft,
+                      const spec_params_t* prm, int32_t* accepted,
+                      int32_t* out_tokens, float* accept_mass,
+                      void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Tree verification (EAGLE static or dynamic trees; EAGLE-2 notes §2.2 and
+ * §4.2; "EAGLE:树形草稿" of "投机解码与 EAGLE").
+ *
+ * Drafted nodes j = 0 .. N-1; parent[b, j] = -1 for a child of the root, else
+ * an index in [0, j) (parents precede children).  Tree row r = 0 is the root
+ * position, row r = j + 1 the position after node j.
+ *
+ * target_logits [B, N+1, V]: target logits per tree row.
+ * draft [B, R, V]: draft rows; q_row [B, N+1] int32 names the draft row of
+ *     each tree row (-1 = none; required for rows that have children).  Not
+ *     read when temperature == 0 (draft and q_row may then be NULL).
+ * node_tokens [B, N], parent [B, N] int32.
+ * At each row the children are tried in index order: accept child c with
+ * token x iff u(b, c, 0) < p'(x)/q'(x); on rejection p' <- norm(max(0,
+ * p' - q')) and x leaves q' (siblings are drafted without replacement); if
+ * no child is accepted the emitted token is drawn from p' with u(b, r, 1)
+ * (a leaf: bonus from p).  The walk follows accepted children from the root.
+ * path_len [B] (out): accepted drafted nodes on the path.
+ * path_nodes [B, N] (out): their node indices, -1 padded.
+ * out_tokens [B, N+1] (out): their tokens, then the sampled token, -1 padded.
+ * accept_mass [B, N+1] float32 (out): alpha per tree row (NaN where the row
+ *     has no draft row; at temperature 0: 1 if a child matches the argmax,
+ *     0 if none does, NaN for a row without children).
+ */
+int spec_verify_tree(const void* target_logits, const void* draft,
+                     const int32_t* q_row, const int32_t* node_tokens,
+                     const int32_t* parent, int B, int N, int R, int V,
+                     int dtype_target, int dtype_draft,
+                     const spec_params_t* prm, int32_t* path_len,
+                     int32_t* path_nodes, int32_t* out_tokens,
+                     float* accept_mass, void* workspace, size_t ws_bytes,
+                     void* stream);
+
+/*
+ * Tree attention mask (EAGLE-2 notes §4.2: each token sees only its
+ * ancestors; the chain case is the lower-triangular causal mask).
+ * mask [B, N, N] uint8 (out): mask[b, i, j] = 1 iff j is i or an ancestor of
+ *     i; the committed prefix is visible to every node and is not included.
+ * mask_bits [B, N] uint64 (out, may be NULL; requires N <= 64): bit j of
+ *     mask_bits[b, i] = mask[b, i, j].  Either output may be NULL, not both.
+ * An out-of-range parent ends that node's ancestor walk.
+ */
+int spec_tree_mask(const int32_t* parent, int B, int N, uint8_t* mask,
+                   uint64_t* mask_bits, void* stream);
+
+/*
+ * EAGLE-2 dynamic tree: expand and rerank (EAGLE-2 notes §4.1-4.2).
+ *
+ * draft_logits [B, 1 + (depth-1)*width, V]: row 0 is the draft distribution
+ *     at the root; row 1 + (d-1)*width + r is the one after the r-th kept node
+ *     of layer d (the draft forward between layers is the caller's).
+ * q = softmax(z / prm->temperature) (temperature > 0; top_k / top_p unused).
+ * Layer 1 = the `topk` most probable tokens of row 0 (ties: lower index),
+ * value = log q.  Layer d+1 = the `topk` best tokens of each kept node's row,
+ * value = parent value + log q.  Each layer keeps its `width` best nodes by
+ * (value desc, candidate id asc), id = (layer, parent rank, child rank).
+ * All candidates of all layers are reranked by (value desc, depth asc, id
+ * asc) and the best `total` kept, in that order (parents before children).
+ * node_tokens [B, total], parent [B, total] (-1 = root child),
+ * q_row [B, total+1] (draft row of each tree row or -1; row 0 -> 0),
+ * value [B, total] float32 (sum of log q along the path),
+ * mask [B, total, total] uint8 (may be NULL) as spec_tree_mask.
+ * Limits: 1 <= topk <= SPEC_EAGLE2_MAX_TOPK, width <= topk * width of the
+ * layer above, total <= number of candidates, total <= SPEC_MAX_TREE_NODES.
+ */
+int spec_eagle2_expand_rerank(const void* draft_logits, int B, int V,
+                              int dtype, int depth, int topk, int width,
+                              int total, const spec_params_t* prm,
+                              int32_t* node_tokens, int32_t* parent,
+                              int32_t* q_row, float* value, uint8_t* mask,
+                              void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Synchronously read the status word of the last call that used `workspace`
+ * (waits for `stream`).  SPEC_STATUS_* bits; 0 = nothing to report.
+ */
+int spec_get_status(const void* workspace, uint32_t* status, void* stream);
+
+/*
+ * The uniforms the kernels draw: out[i] = u(b[i], idx[i], slot[i]) for the
+ * given seed and offset (all arrays device, length n).  Lets callers and
+ * tests check the device generator bit for bit.
+ */
+int spec_philox_uniforms(uint64_t seed, uint32_t offset, const int32_t* b,
+                         const int32_t* idx, const int32_t* slot, int n,
+                         float* out, void* stream);
+
+/* Human-readable name of a return code. */
+const char* spec_error_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECVERIFY_H */

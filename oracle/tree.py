@@ -56,11 +56,15 @@ from .sampling import (accept, acceptance_mass, argmax_first, inverse_cdf,
 
 
 def ancestors(parent, j):
-    """Set of drafted-node ancestors of node j (excluding j)."""
+    """Set of drafted-node ancestors of node j (excluding j).  The walk ends
+    at the root (-1) or at the first link that does not point to an earlier
+    node (an invalid parent array)."""
     out = set()
+    cur = j
     a = int(parent[j])
-    while a >= 0:
+    while 0 <= a < cur:
         out.add(a)
+        cur = a
         a = int(parent[a])
     return out
 

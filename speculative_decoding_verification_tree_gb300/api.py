@@ -1,0 +1,161 @@
+"""Torch-facing wrappers with the C ABI's names.
+
+Argument marshalling only: shapes and dtypes are read off the tensors, outputs
+and the workspace are allocated with torch when the caller passes none, and the
+call is enqueued on torch's current CUDA stream.  All computation happens in
+libspecverify.so.
+"""
+
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import SpecParams
+
+_DT = {torch.float32: _lib.SPEC_F32, torch.bfloat16: _lib.SPEC_BF16}
+_KIND = {"logits": _lib.SPEC_DRAFT_LOGITS, "probs": _lib.SPEC_DRAFT_PROBS}
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("device tensors are required")
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _dt(t):
+    if t is None:
+        return _lib.SPEC_F32
+    if t.dtype not in _DT:
+        raise ValueError(f"unsupported dtype {t.dtype}")
+    return _DT[t.dtype]
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def params(temperature=1.0, top_k=0, top_p=1.0, draft_kind="logits", seed=0,
+           offset=0) -> SpecParams:
+    return SpecParams(float(temperature), int(top_k), float(top_p),
+                      _KIND[draft_kind], int(seed) & (2**64 - 1),
+                      int(offset) & 0xFFFFFFFF, 0)
+
+
+def spec_workspace_bytes(op: int, B: int, n: int, V: int) -> int:
+    return int(_lib.call("spec_workspace_bytes", op, B, n, V))
+
+
+def workspace(op, B, n, V, device=None):
+    nbytes = spec_workspace_bytes(op, B, n, V)
+    if nbytes == 0:
+        raise ValueError("invalid sizes for the workspace")
+    return torch.empty(nbytes, dtype=torch.uint8,
+                       device=device or torch.cuda.current_device())
+
+
+def spec_verify_chain(target, draft, draft_tokens, *, temperature=1.0,
+                      top_k=0, top_p=1.0, draft_kind="logits", seed=0,
+                      offset=0, out=None, ws=None, stream=None):
+    """target [B, K+1, V]; draft [B, K, V] (None at temperature 0);
+    draft_tokens [B, K] int32.  Returns (accepted [B], tokens [B, K+1],
+    accept_mass [B, K])."""
+    B, K1, V = target.shape
+    K = K1 - 1
+    dev = target.device
+    if out is None:
+        out = (torch.empty(B, dtype=torch.int32, device=dev),
+               torch.empty(B, K + 1, dtype=torch.int32, device=dev),
+               torch.empty(B, K, dtype=torch.float32, device=dev))
+    if ws is None:
+        ws = workspace(_lib.SPEC_OP_CHAIN, B, K, V, dev)
+    prm = params(temperature, top_k, top_p, draft_kind, seed, offset)
+    _lib.call("spec_verify_chain", _ptr(target), _ptr(draft),
+              _ptr(draft_tokens), B, K, V, _dt(target), _dt(draft),
+              ctypes.byref(prm), _ptr(out[0]), _ptr(out[1]), _ptr(out[2]),
+              _ptr(ws), ws.numel(), _stream(stream))
+    return out
+
+
+def spec_verify_tree(target, draft, q_row, node_tokens, parent, *,
+                     temperature=1.0, top_k=0, top_p=1.0, draft_kind="logits",
+                     seed=0, offset=0, out=None, ws=None, stream=None):
+    """target [B, N+1, V]; draft [B, R, V]; q_row [B, N+1]; node_tokens and
+    parent [B, N].  Returns (path_len [B], path_nodes [B, N],
+    tokens [B, N+1], accept_mass [B, N+1])."""
+    B, N1, V = target.shape
+    N = N1 - 1
+    R = 0 if draft is None else draft.shape[1]
+    dev = target.device
+    if out is None:
+        out = (torch.empty(B, dtype=torch.int32, device=dev),
+               torch.empty(B, N, dtype=torch.int32, device=dev),
+               torch.empty(B, N + 1, dtype=torch.int32, device=dev),
+               torch.empty(B, N + 1, dtype=torch.float32, device=dev))
+    if ws is None:
+        ws = workspace(_lib.SPEC_OP_TREE, B, N, V, dev)
+    prm = params(temperature, top_k, top_p, draft_kind, seed, offset)
+    _lib.call("spec_verify_tree", _ptr(target), _ptr(draft), _ptr(q_row),
+              _ptr(node_tokens), _ptr(parent), B, N, R, V, _dt(target),
+              _dt(draft), ctypes.byref(prm), _ptr(out[0]), _ptr(out[1]),
+              _ptr(out[2]), _ptr(out[3]), _ptr(ws), ws.numel(),
+              _stream(stream))
+    return out
+
+
+def spec_tree_mask(parent, *, bits=False, mask=True, stream=None):
+    """parent [B, N] int32 -> (mask [B, N, N] uint8 or None,
+    bits [B, N] int64 (uint64 bit patterns) or None)."""
+    B, N = parent.shape
+    dev = parent.device
+    m = torch.empty(B, N, N, dtype=torch.uint8, device=dev) if mask else None
+    bt = torch.empty(B, N, dtype=torch.int64, device=dev) if bits else None
+    _lib.call("spec_tree_mask", _ptr(parent), B, N, _ptr(m), _ptr(bt),
+              _stream(stream))
+    return m, bt
+
+
+def spec_eagle2_expand_rerank(draft_logits, *, temperature, depth=6, topk=10,
+                              width=10, total=60, mask=True, out=None,
+                              ws=None, stream=None):
+    """draft_logits [B, 1 + (depth-1)*width, V].  Returns (node_tokens,
+    parent, q_row, value, mask)."""
+    B, R, V = draft_logits.shape
+    dev = draft_logits.device
+    if out is None:
+        out = (torch.empty(B, total, dtype=torch.int32, device=dev),
+               torch.empty(B, total, dtype=torch.int32, device=dev),
+               torch.empty(B, total + 1, dtype=torch.int32, device=dev),
+               torch.empty(B, total, dtype=torch.float32, device=dev),
+               torch.empty(B, total, total, dtype=torch.uint8, device=dev)
+               if mask else None)
+    if ws is None:
+        ws = workspace(_lib.SPEC_OP_EAGLE2, B, R, V, dev)
+    prm = params(temperature)
+    _lib.call("spec_eagle2_expand_rerank", _ptr(draft_logits), B, V,
+              _dt(draft_logits), depth, topk, width, total, ctypes.byref(prm),
+              _ptr(out[0]), _ptr(out[1]), _ptr(out[2]), _ptr(out[3]),
+              _ptr(out[4]), _ptr(ws), ws.numel(), _stream(stream))
+    return out
+
+
+def spec_get_status(ws, stream=None) -> int:
+    v = ctypes.c_uint32(0)
+    _lib.call("spec_get_status", _ptr(ws), ctypes.byref(v), _stream(stream))
+    return int(v.value)
+
+
+def spec_philox_uniforms(seed, offset, b, idx, slot, stream=None):
+    n = b.numel()
+    out = torch.empty(n, dtype=torch.float32, device=b.device)
+    _lib.call("spec_philox_uniforms", int(seed) & (2**64 - 1),
+              int(offset) & 0xFFFFFFFF, _ptr(b), _ptr(idx), _ptr(slot), n,
+              _ptr(out), _stream(stream))
+    return out

@@ -1,0 +1,137 @@
+"""Host-only checks of the C ABI: the library builds, loads and exports every
+symbol include/specverify.h declares, and rejects bad arguments before any
+device work (these calls never reach the GPU)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__ as g
+    g.build()
+    from speculative_decoding_verification_tree_gb300 import _lib
+    return _lib
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "specverify.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(spec_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert len(names) >= 8
+    handle = lib.load()
+    for n in names:
+        assert hasattr(handle, n), n
+    assert set(names) == set(lib.EXPORTED)
+
+
+def test_params_struct_layout(lib):
+    P = lib.SpecParams
+    assert ctypes.sizeof(P) == 32
+    assert P.seed.offset == 16 and P.philox_offset.offset == 24
+
+
+def test_workspace_sizes(lib):
+    f = lib.load().spec_workspace_bytes
+    assert f(lib.SPEC_OP_CHAIN, 4, 5, 1000) % 256 == 0
+    assert f(lib.SPEC_OP_CHAIN, 4, 5, 1000) > 0
+    assert f(lib.SPEC_OP_TREE, 0, 0, 1) > 0
+    assert f(lib.SPEC_OP_CHAIN, -1, 5, 1000) == 0
+    assert f(lib.SPEC_OP_TREE, 1, 5000, 1000) == 0
+    assert f(lib.SPEC_OP_CHAIN, 1, 5, 0) == 0
+    assert f(99, 1, 5, 10) == 0
+    assert f(lib.SPEC_OP_EAGLE2, 128, 51, 128256) > 128 * 51 * 8
+
+
+def _prm(lib, **kw):
+    d = dict(temperature=1.0, top_k=0, top_p=1.0, draft_kind=0, seed=0,
+             philox_offset=0, flags=0)
+    d.update(kw)
+    return lib.SpecParams(**d)
+
+
+FAKE = ctypes.c_void_p(0x7f0000000000)  # never dereferenced: calls fail early
+
+
+def _chain(lib, B=2, K=3, V=100, prm=None, ws=FAKE, ws_bytes=1 << 20,
+           target=FAKE, draft=FAKE, dt=0):
+    prm = prm or _prm(lib)
+    return lib.raw("spec_verify_chain", target, draft, FAKE, B, K, V, dt, dt,
+                   ctypes.byref(prm), FAKE, FAKE, FAKE, ws, ws_bytes, None)
+
+
+def test_chain_argument_errors(lib):
+    assert _chain(lib, B=-1) == lib.SPEC_ERR_SHAPE
+    assert _chain(lib, V=0) == lib.SPEC_ERR_SHAPE
+    assert _chain(lib, K=5000) == lib.SPEC_ERR_SHAPE
+    assert _chain(lib, dt=7) == lib.SPEC_ERR_DTYPE
+    assert _chain(lib, target=None) == lib.SPEC_ERR_ARG
+    assert _chain(lib, draft=None) == lib.SPEC_ERR_ARG
+    assert _chain(lib, prm=_prm(lib, temperature=-1.0)) == lib.SPEC_ERR_ARG
+    assert _chain(lib, prm=_prm(lib, temperature=float("nan"))) == lib.SPEC_ERR_ARG
+    assert _chain(lib, prm=_prm(lib, top_p=0.0)) == lib.SPEC_ERR_ARG
+    assert _chain(lib, prm=_prm(lib, top_p=1.5)) == lib.SPEC_ERR_ARG
+    assert _chain(lib, prm=_prm(lib, top_k=-2)) == lib.SPEC_ERR_ARG
+    assert _chain(lib, prm=_prm(lib, draft_kind=3)) == lib.SPEC_ERR_DTYPE
+    assert _chain(lib, prm=_prm(lib, flags=1)) == lib.SPEC_ERR_ARG
+    assert _chain(lib, prm=_prm(lib, top_p=0.9)) == lib.SPEC_ERR_UNSUPPORTED
+    assert _chain(lib, V=5000, prm=_prm(lib, top_k=2000)) == \
+        lib.SPEC_ERR_UNSUPPORTED
+    assert _chain(lib, ws=None) == lib.SPEC_ERR_WORKSPACE
+    assert _chain(lib, ws=ctypes.c_void_p(0x7f0000000010)) == \
+        lib.SPEC_ERR_WORKSPACE
+    assert _chain(lib, ws_bytes=16) == lib.SPEC_ERR_WORKSPACE
+    # greedy needs no draft
+    assert _chain(lib, draft=None, ws=None,
+                  prm=_prm(lib, temperature=0.0)) == lib.SPEC_ERR_WORKSPACE
+
+
+def test_tree_and_mask_argument_errors(lib):
+    prm = _prm(lib)
+    f = lib.raw
+    assert f("spec_verify_tree", FAKE, FAKE, FAKE, FAKE, FAKE, 1, -1, 1, 10,
+             0, 0, ctypes.byref(prm), FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 20,
+             None) == lib.SPEC_ERR_SHAPE
+    assert f("spec_verify_tree", FAKE, FAKE, None, FAKE, FAKE, 1, 3, 4, 10,
+             0, 0, ctypes.byref(prm), FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 20,
+             None) == lib.SPEC_ERR_ARG
+    assert f("spec_tree_mask", FAKE, 1, 65, None, FAKE, None) == \
+        lib.SPEC_ERR_SHAPE
+    assert f("spec_tree_mask", FAKE, 1, 5, None, None, None) == \
+        lib.SPEC_ERR_ARG
+    assert f("spec_tree_mask", FAKE, -1, 5, FAKE, None, None) == \
+        lib.SPEC_ERR_SHAPE
+
+
+def test_eagle2_argument_errors(lib):
+    prm = _prm(lib, temperature=0.8)
+    f = lib.raw
+
+    def call(B=2, V=1000, dt=1, depth=6, topk=10, width=10, total=60,
+             p=prm, ws_bytes=1 << 24):
+        return f("spec_eagle2_expand_rerank", FAKE, B, V, dt, depth, topk,
+                 width, total, ctypes.byref(p), FAKE, FAKE, FAKE, FAKE, FAKE,
+                 FAKE, ws_bytes, None)
+    assert call(topk=40) == lib.SPEC_ERR_SHAPE
+    assert call(topk=11, V=10) == lib.SPEC_ERR_SHAPE
+    assert call(total=511) == lib.SPEC_ERR_SHAPE
+    assert call(depth=0) == lib.SPEC_ERR_SHAPE
+    assert call(dt=4) == lib.SPEC_ERR_DTYPE
+    assert call(p=_prm(lib, temperature=0.0)) == lib.SPEC_ERR_ARG
+    assert call(ws_bytes=8) == lib.SPEC_ERR_WORKSPACE
+
+
+def test_error_strings(lib):
+    h = lib.load()
+    for code in range(-6, 1):
+        assert h.spec_error_string(code)
+    assert h.spec_error_string(-99) == b"unknown error"

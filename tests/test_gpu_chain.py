@@ -1,0 +1,121 @@
+"""Sampled chain verification (full vocabulary) vs the oracle.
+
+Accept / reject decisions, replacement and bonus tokens must be bit-exact
+except on sequences where a uniform lies within 1e-5 of its threshold or CDF
+boundary (the oracle flags those); the acceptance mass agrees to rel 1e-4."""
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle.chain import verify_chain
+from tests._parity import compare_chain, lib_ready, np64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    lib_ready()
+
+
+def api():
+    from speculative_decoding_verification_tree_gb300 import api as a
+    return a
+
+
+def run(w, seqs=None, target=None, draft=None, toks=None, seed=None):
+    if target is None:
+        target, draft, toks = synth.chain_inputs(w, "cuda")
+    seed = w.decision_seed if seed is None else seed
+    gpu = api().spec_verify_chain(target, draft, toks,
+                                  temperature=w.temperature, top_k=w.top_k,
+                                  top_p=w.top_p, draft_kind=w.draft_kind,
+                                  seed=seed)
+    torch.cuda.synchronize()
+    sel = slice(None) if seqs is None else seqs
+    ref = verify_chain(np64(target[sel]), np64(draft[sel]),
+                       toks[sel].cpu().numpy(), temperature=w.temperature,
+                       top_k=w.top_k, top_p=w.top_p,
+                       draft_kind=w.draft_kind, seed=seed)
+    return gpu, ref
+
+
+def test_chain_sample_workload_exact():
+    # B=1, K=4, V=32000 float32, the pages' alpha ~ 0.8 chain
+    w = synth.workload("chain_sample")
+    for seed in range(1, 41):
+        gpu, ref = run(w, seed=seed)
+        compare_chain(gpu, ref)
+
+
+@pytest.mark.parametrize("V", [1, 2, 37, 1000, 4099, 32000, 70001])
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_chain_vocab_sizes(V, dt):
+    tdt = torch.float32 if dt == "f32" else torch.bfloat16
+    w = synth.workload("chain_sample", B=6, K=3, V=V, target_dtype=tdt,
+                       draft_dtype=tdt, seed=77 + V)
+    gpu, ref = run(w)
+    ex = compare_chain(gpu, ref)
+    assert ex <= 1
+
+
+@pytest.mark.parametrize("T", [1.0, 0.6])
+def test_chain_probs_draft(T):
+    w = synth.workload("chain_sample", B=8, K=4, V=5000, draft_kind="probs",
+                       temperature=T, seed=5)
+    gpu, ref = run(w)
+    compare_chain(gpu, ref)
+
+
+def test_chain_mixed_dtypes_and_low_alpha():
+    w = synth.workload("chain_sample", B=16, K=6, V=20000,
+                       target_dtype=torch.bfloat16, draft_dtype=torch.float32,
+                       draft_noise=3.0, seed=9)
+    gpu, ref = run(w)
+    compare_chain(gpu, ref)
+    assert (ref.accepted < 6).any()
+
+
+def test_chain_identical_rows_accept_all_and_bonus():
+    w = synth.workload("chain_sample", B=4, K=3, V=3000, seed=2)
+    target, draft, toks = synth.chain_inputs(w, "cuda")
+    draft = target[:, :3].contiguous()
+    gpu, ref = run(w, target=target, draft=draft, toks=toks)
+    compare_chain(gpu, ref)
+    assert (gpu[0].cpu() == 3).all()
+    np.testing.assert_allclose(gpu[2].cpu().numpy(), 1.0, rtol=1e-5)
+
+
+def test_chain_zero_q_and_out_of_range_tokens():
+    from speculative_decoding_verification_tree_gb300 import _lib
+    V = 700
+    w = synth.workload("chain_sample", B=3, K=2, V=V, seed=3)
+    target, draft, toks = synth.chain_inputs(w, "cuda")
+    draft[0, 0, 11] = float("-inf")
+    toks[0, 0] = 11             # q(x) = 0: accepted
+    toks[1, 1] = V + 5          # out of range: rejected
+    toks[2, 0] = -1
+    a = api()
+    ws = a.workspace(_lib.SPEC_OP_CHAIN, 3, 2, V)
+    gpu = a.spec_verify_chain(target, draft, toks, temperature=1.0,
+                              seed=w.decision_seed, ws=ws)
+    st = a.spec_get_status(ws)
+    ref = verify_chain(np64(target), np64(draft), toks.cpu().numpy(),
+                       temperature=1.0, seed=w.decision_seed)
+    compare_chain(gpu, ref)
+    assert st & _lib.SPEC_STATUS_QZERO_ACCEPT
+    assert st & _lib.SPEC_STATUS_TOKEN_RANGE
+    assert st == ref.status
+
+
+def test_chain_batched_full_vocab_llama_size():
+    # many sequences at V = 128256, compared on a sample of sequences
+    w = synth.workload("chain_sample", B=48, K=5, V=128256,
+                       target_dtype=torch.bfloat16,
+                       draft_dtype=torch.bfloat16, seed=11)
+    target, draft, toks = synth.chain_inputs(w, "cuda")
+    seqs = [0, 7, 23, 47]
+    gpu, ref = run(w, seqs=seqs, target=target, draft=draft, toks=toks)
+    compare_chain(gpu, ref, seqs=seqs)
