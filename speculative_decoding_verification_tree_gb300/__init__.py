@@ -14,6 +14,6 @@ __all__ = ["api", "_lib", "SpecError", "SpecParams"]
 
 def __getattr__(name):
     if name == "api":
-        from . import api
-        return api
+        import importlib
+        return importlib.import_module(__name__ + ".api")
     raise AttributeError(name)

@@ -95,8 +95,23 @@ def _normal(shape, std, g, device):
 
 
 # ----------------------------------------------------------------- drafter
+def _sample(q, m, g, replacement):
+    """Draw m tokens per row from q.  The probabilities are checked on the
+    host first, so a bad distribution raises here instead of tripping a
+    device-side assert inside torch's sampler."""
+    ok = torch.isfinite(q).all() & (q >= 0).all() & (q.sum(-1) > 0).all()
+    if not bool(ok):
+        raise ValueError("draft distribution is not a valid probability row")
+    if not replacement and int((q > 0).sum(-1).min()) < m:
+        replacement = True  # too few tokens for distinct siblings
+    return torch.multinomial(q, m, replacement=replacement, generator=g)
+
+
 def _draft_dist(logits, w: Workload):
-    """Draft model's sampling distribution (stand-in drafter; torch ops)."""
+    """Draft model's sampling distribution (stand-in drafter; torch ops).
+    Temperature must be positive (greedy drafting uses top-m instead)."""
+    if not w.temperature > 0:
+        raise ValueError("sampling drafter needs temperature > 0")
     z = logits.float()
     if w.draft_kind == "probs":
         z = torch.log(z)
@@ -132,7 +147,7 @@ def chain_inputs(w: Workload, device="cpu"):
     else:
         draft = noisy.to(w.draft_dtype)
     q = _draft_dist(draft, w).reshape(B * K, V)
-    tokens = torch.multinomial(q, 1, generator=gd).reshape(B, K)
+    tokens = _sample(q, 1, gd, False).reshape(B, K)
     return target, draft, tokens.to(torch.int32).contiguous()
 
 
@@ -186,8 +201,11 @@ def tree_inputs(w: Workload, device="cpu", parent=None):
     for j, p in enumerate(pl):
         kids.setdefault(p + 1, []).append(j)
     for r, ks in kids.items():
-        q = _draft_dist(draft[:, r], w)
-        draws = torch.multinomial(q, len(ks), replacement=False, generator=gd)
+        if w.temperature > 0:
+            q = _draft_dist(draft[:, r], w)
+            draws = _sample(q, len(ks), gd, False)
+        else:  # greedy drafter: the len(ks) most likely tokens
+            draws = torch.topk(draft[:, r].float(), len(ks), dim=-1).indices
         tokens[:, ks] = draws.to(torch.int32)
     par = parent.unsqueeze(0).expand(B, N).contiguous()
     return target, draft, q_row, tokens, par
@@ -204,6 +222,8 @@ def eagle2_target(w: Workload, draft, q_row, device="cpu"):
     """Target rows for the reranked tree: draft row + N(0, 1) where the tree
     row has a draft row, fresh N(0, std^2) + N(0, 1) elsewhere."""
     B, M1 = q_row.shape
+    if int(q_row.max()) >= draft.shape[1] or int(q_row.min()) < -1:
+        raise ValueError("q_row names a draft row that does not exist")
     g = _gen(device, w.seed + 1)
     fresh = _normal((B, M1, w.V), w.target_std, g, device)
     noise = _normal((B, M1, w.V), w.draft_noise, g, device)
