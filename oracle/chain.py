@@ -42,9 +42,12 @@ class ChainResult:
     accepted: np.ndarray      # [B] int32
     tokens: np.ndarray        # [B, K+1] int32, -1 padded
     mass: np.ndarray          # [B, K] float64
-    near_tie: np.ndarray      # [B] bool: a decision on the path was a near tie
+    near_tie: np.ndarray      # [B] bool: an accept test or a top-p cut on
+                              # the path was within NEAR_TIE of its threshold
     status: int = 0
     near_rows: list = field(default_factory=list)  # (b, k) of near-tie rows
+    sample_near: np.ndarray = None  # [B] bool: final draw near a CDF boundary
+    final: list = field(default_factory=list)      # per b: (weights, u)
 
 
 def verify_chain(target, draft, draft_tokens, *, temperature: float,
@@ -67,6 +70,8 @@ def verify_chain(target, draft, draft_tokens, *, temperature: float,
     status = 0
     near_rows = []
 
+    snear = np.zeros(B, dtype=bool)
+    final = []
     if temperature == 0:
         for b in range(B):
             g = [argmax_first(target[b, k]) for k in range(K + 1)]
@@ -80,7 +85,8 @@ def verify_chain(target, draft, draft_tokens, *, temperature: float,
             accepted[b] = n
             out[b, :n] = toks[b, :n]
             out[b, n] = g[n]
-        return ChainResult(accepted, out, mass, near, status, near_rows)
+        return ChainResult(accepted, out, mass, near, status, near_rows,
+                           snear, final)
 
     draft = np.asarray(draft)
     for b in range(B):
@@ -118,10 +124,13 @@ def verify_chain(target, draft, draft_tokens, *, temperature: float,
                 status |= ST_RESIDUAL_ZERO
         else:
             w = ps[K]
-        y, nt = inverse_cdf(w, uniform(b, n, 1))
-        path_near |= nt
+        u1 = uniform(b, n, 1)
+        y, nt = inverse_cdf(w, u1)
+        snear[b] = nt
+        final.append((w, u1))
         accepted[b] = n
         out[b, :n] = toks[b, :n]
         out[b, n] = y
         near[b] = path_near
-    return ChainResult(accepted, out, mass, near, status, near_rows)
+    return ChainResult(accepted, out, mass, near, status, near_rows, snear,
+                       final)

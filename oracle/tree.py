@@ -101,9 +101,11 @@ class TreeResult:
     path_nodes: np.ndarray    # [B, N] int32, -1 padded
     tokens: np.ndarray        # [B, N+1] int32, -1 padded
     mass: np.ndarray          # [B, N+1] float64 (NaN where no draft row)
-    near_tie: np.ndarray      # [B] bool
+    near_tie: np.ndarray      # [B] bool: accept test / top-p cut near tie
     status: int = 0
     outcome: list = field(default_factory=list)  # per b: {row: child or None}
+    sample_near: np.ndarray = None  # [B] bool: final draw near a CDF boundary
+    final: list = field(default_factory=list)      # per b: (weights, u)
 
 
 def verify_tree(target, draft, q_row, node_tokens, parent, *,
@@ -127,6 +129,8 @@ def verify_tree(target, draft, q_row, node_tokens, parent, *,
     out = np.full((B, N + 1), -1, dtype=np.int32)
     mass = np.full((B, N + 1), np.nan, dtype=np.float64)
     near = np.zeros(B, dtype=bool)
+    snear = np.zeros(B, dtype=bool)
+    final = []
     status = 0
     outcomes = []
 
@@ -142,6 +146,7 @@ def verify_tree(target, draft, q_row, node_tokens, parent, *,
         acc = {}
         tok = {}
         nrow = {}
+        draw = {}   # row -> (weights, u, near) of its sampled token
         for r in range(N + 1):
             kids = children[r]
             if temperature == 0:
@@ -149,6 +154,7 @@ def verify_tree(target, draft, q_row, node_tokens, parent, *,
                 acc[r] = next((j for j in kids if toks[b, j] == g), None)
                 tok[r] = g
                 nrow[r] = False
+                draw[r] = (None, None, False)
                 if kids:  # greedy point masses: overlap is 1 iff a child hits
                     mass[b, r] = 1.0 if acc[r] is not None else 0.0
                 continue
@@ -188,9 +194,10 @@ def verify_tree(target, draft, q_row, node_tokens, parent, *,
                     status |= ST_DRAFT_EXHAUSTED
                     break
             if acc[r] is None:
-                y, nt = inverse_cdf(pc, uniform(b, r, 1))
-                row_near |= nt
+                u1 = uniform(b, r, 1)
+                y, nt = inverse_cdf(pc, u1)
                 tok[r] = y
+                draw[r] = (pc, u1, nt)
             nrow[r] = row_near
         # walk from the root
         r = 0
@@ -201,10 +208,13 @@ def verify_tree(target, draft, q_row, node_tokens, parent, *,
             path.append(j)
             r = j + 1
             path_near |= nrow[r]
+        snear[b] = draw[r][2]
+        final.append(draw[r][:2])
         path_len[b] = len(path)
         path_nodes[b, :len(path)] = path
         out[b, :len(path)] = [toks[b, j] for j in path]
         out[b, len(path)] = tok[r]
         near[b] = path_near
         outcomes.append({"acc": acc, "tok": tok, "near": nrow})
-    return TreeResult(path_len, path_nodes, out, mass, near, status, outcomes)
+    return TreeResult(path_len, path_nodes, out, mass, near, status, outcomes,
+                      snear, final)

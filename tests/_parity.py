@@ -26,9 +26,39 @@ def np64(t):
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
+# band (in u units) around a CDF boundary inside which a float32 draw may land
+# on the neighbouring token
+CDF_BAND = 1e-5
+
+
+def draw_in_band(weights, u, y):
+    """True iff token y is the inverse-CDF draw of `weights` for some uniform
+    within CDF_BAND of u (the oracle's exact draw is the case u itself)."""
+    w = np.asarray(weights, dtype=np.float64)
+    if y < 0 or y >= w.size or w[y] <= 0:
+        return False
+    c = np.cumsum(w)
+    z = c[-1]
+    lo = c[y - 1] / z if y > 0 else 0.0
+    hi = c[y] / z
+    return lo - CDF_BAND <= u <= hi + CDF_BAND
+
+
+def _check_final(ref, i, got, want):
+    """Final (replacement / bonus) token: equal, or a float32 neighbour of a
+    boundary draw.  Returns 1 if the band was needed."""
+    if got == want:
+        return 0
+    w, u = ref.final[i]
+    assert ref.sample_near is not None and ref.sample_near[i], (i, got, want)
+    assert draw_in_band(w, u, got), (i, got, want, u)
+    return 1
+
+
 def compare_chain(gpu, ref, *, greedy=False, check_mass=True, seqs=None):
     """gpu = (accepted, tokens, mass) tensors; ref = oracle ChainResult.
-    Returns the number of sequences excluded as near ties."""
+    Returns the number of sequences excluded as near ties (an accept test on
+    the path within 1e-5 of its threshold, or a top-p cut)."""
     acc, tok, mass = (x.cpu().numpy() for x in gpu)
     B = ref.accepted.shape[0]
     seqs = range(B) if seqs is None else seqs
@@ -37,8 +67,14 @@ def compare_chain(gpu, ref, *, greedy=False, check_mass=True, seqs=None):
         if ref.near_tie[i]:
             excluded += 1
             continue
-        assert acc[b] == ref.accepted[i], (b, acc[b], ref.accepted[i])
-        assert np.array_equal(tok[b], ref.tokens[i]), (b, tok[b], ref.tokens[i])
+        n = ref.accepted[i]
+        assert acc[b] == n, (b, acc[b], n)
+        assert np.array_equal(tok[b, :n], ref.tokens[i, :n]), b
+        assert np.array_equal(tok[b, n + 1:], ref.tokens[i, n + 1:]), b
+        if greedy:
+            assert tok[b, n] == ref.tokens[i, n], b
+        else:
+            _check_final(ref, i, int(tok[b, n]), int(ref.tokens[i, n]))
     if check_mass:
         m = mass[list(seqs)]
         if greedy:
@@ -58,9 +94,15 @@ def compare_tree(gpu, ref, *, greedy=False, seqs=None):
         if ref.near_tie[i]:
             excluded += 1
             continue
-        assert plen[b] == ref.path_len[i], (b, plen[b], ref.path_len[i])
+        n = ref.path_len[i]
+        assert plen[b] == n, (b, plen[b], n)
         assert np.array_equal(pnodes[b], ref.path_nodes[i]), b
-        assert np.array_equal(tok[b], ref.tokens[i]), (b, tok[b], ref.tokens[i])
+        assert np.array_equal(tok[b, :n], ref.tokens[i, :n]), b
+        assert np.array_equal(tok[b, n + 1:], ref.tokens[i, n + 1:]), b
+        if greedy:
+            assert tok[b, n] == ref.tokens[i, n], b
+        else:
+            _check_final(ref, i, int(tok[b, n]), int(ref.tokens[i, n]))
     m = mass[list(seqs)]
     nan_g, nan_r = np.isnan(m), np.isnan(ref.mass)
     assert np.array_equal(nan_g, nan_r)
