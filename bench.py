@@ -1,0 +1,467 @@
+#!/usr/bin/env python
+"""Throughput of speculative-decoding verification on GB300.
+
+One step = one call of the verification path over one batch of synthetic
+logits already resident in HBM (the workload's whole hot path: for the EAGLE
+tree workloads that is the tree mask plus tree verification, for eagle2 also
+expand + rerank).  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--impl ours|reference]
+
+Multi-GPU (torchrun, one rank per GPU): every rank verifies its own batch
+(sequences are independent, no collective on the data path); the time is the
+max over ranks and the value counts the rows of all ranks (weak scaling).
+
+--impl reference times the float64 CPU oracle (tests' ground truth) on a
+bounded sample of the same workload on the host cores.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verified draft rows/s at V=128256"
+UNIT = "rows/s"
+DEFAULT_WORKLOAD = "tree_static"
+
+
+def _args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=None)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                   choices=["tree_static", "greedy", "eagle2", "chain_topk",
+                            "chain_sample"])
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--no-extend", action="store_true",
+                   help="do not keep the load running for the clock sampler "
+                        "after a short timed region (profiler runs)")
+    return p.parse_args()
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------- workloads
+class Work:
+    """Device inputs, outputs and one step of a workload (GPU arm)."""
+
+    def __init__(self, name, device):
+        import torch
+
+        import synth
+        from speculative_decoding_verification_tree_gb300 import _lib, api
+        self.torch, self.api, self.lib = torch, api, _lib
+        self.name = name
+        self.w = w = synth.workload(name)
+        self.device = device
+        if name in ("greedy", "chain_topk", "chain_sample"):
+            self.kind = "chain"
+            self.target, self.draft, self.toks = synth.chain_inputs(w, device)
+            B, K, V = w.B, w.K, w.V
+            self.rows = B * K
+            self.ws = api.workspace(_lib.SPEC_OP_CHAIN, B, K, V, device)
+            self.out = (torch.empty(B, dtype=torch.int32, device=device),
+                        torch.empty(B, K + 1, dtype=torch.int32, device=device),
+                        torch.empty(B, K, dtype=torch.float32, device=device))
+            self.inputs = [self.target, self.draft, self.toks]
+            self.prof_kind = (_lib.SPEC_PROF_ARGMAX if w.temperature == 0
+                              else _lib.SPEC_PROF_VERIFY)
+            tb = self.target.element_size()
+            self.kernel_bytes = B * (K + 1) * V * tb
+            if w.temperature > 0:
+                self.kernel_bytes += B * K * V * self.draft.element_size()
+            self.launches_per_step = 2
+        elif name == "tree_static":
+            self.kind = "tree"
+            (self.target, self.draft, self.q_row, self.toks,
+             self.parent) = synth.tree_inputs(w, device)
+            B, N, V = w.B, self.toks.shape[1], w.V
+            self.N = N
+            self.rows = B * (N + 1)
+            self.ws = api.workspace(_lib.SPEC_OP_TREE, B, N, V, device)
+            self.out = (torch.empty(B, dtype=torch.int32, device=device),
+                        torch.empty(B, N, dtype=torch.int32, device=device),
+                        torch.empty(B, N + 1, dtype=torch.int32, device=device),
+                        torch.empty(B, N + 1, dtype=torch.float32,
+                                    device=device))
+            self.mask = torch.empty(B, N, N, dtype=torch.uint8, device=device)
+            self.inputs = [self.target, self.draft, self.q_row, self.toks,
+                           self.parent]
+            self.prof_kind = _lib.SPEC_PROF_VERIFY
+            self.kernel_bytes = B * (N + 1) * V * (
+                self.target.element_size() + self.draft.element_size())
+            self.launches_per_step = 3  # mask, row verification, walk
+        else:
+            raise SystemExit(f"workload {name} is not wired into the bench")
+
+    def step(self, inputs=None):
+        """Enqueue one step on the current stream."""
+        api, w = self.api, self.w
+        x = self.inputs if inputs is None else inputs
+        if self.kind == "chain":
+            api.spec_verify_chain(x[0], x[1], x[2], temperature=w.temperature,
+                                  top_k=w.top_k, top_p=w.top_p,
+                                  draft_kind=w.draft_kind,
+                                  seed=w.decision_seed, out=self.out,
+                                  ws=self.ws)
+        else:
+            from speculative_decoding_verification_tree_gb300.api import (
+                _ptr, _stream)
+            B, N = self.w.B, self.N
+            self.lib.call("spec_tree_mask", _ptr(x[4]), B, N, _ptr(self.mask),
+                          None, _stream(None))
+            api.spec_verify_tree(x[0], x[1], x[2], x[3], x[4],
+                                 temperature=w.temperature, top_k=w.top_k,
+                                 top_p=w.top_p, draft_kind=w.draft_kind,
+                                 seed=w.decision_seed, out=self.out,
+                                 ws=self.ws)
+
+    def host_copy(self):
+        """The step's inputs on the host, for the CPU oracle."""
+        keys = (["target", "draft", "toks"] if self.kind == "chain" else
+                ["target", "draft", "q_row", "toks", "parent"])
+        return self.w, {k: (None if x is None else x.cpu())
+                        for k, x in zip(keys, self.inputs)}
+
+    def emitted_tokens(self):
+        return int(self.out[0].sum().item()) + self.w.B
+
+    def outputs(self):
+        return [o for o in self.out if o is not None]
+
+
+# ------------------------------------------------------------------ clocks
+class Clocks:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100", "-i",
+                 str(self.index)], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+            self.t0 = time.time()
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "samples": 0}
+        # under load: drop idle samples at the edges of the window
+        top = max(sm)
+        load = [x for x in sm if x >= 0.5 * top] or sm
+        return {"sm_mhz": statistics.median(load), "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# -------------------------------------------------------------- CPU oracle
+def oracle_step(w, host, seqs):
+    """Run the oracle on sequences `seqs` of the host copy of the inputs."""
+    import numpy as np
+    from oracle.chain import verify_chain
+    from oracle.tree import tree_mask, verify_tree
+    t = host["target"][seqs].float().numpy().astype(np.float64)
+    if w.name in ("greedy", "chain_topk", "chain_sample"):
+        d = None if host["draft"] is None else \
+            host["draft"][seqs].float().numpy().astype(np.float64)
+        verify_chain(t, d, host["toks"][seqs].numpy(),
+                     temperature=w.temperature, top_k=w.top_k, top_p=w.top_p,
+                     draft_kind=w.draft_kind, seed=w.decision_seed,
+                     batch_ids=seqs)
+        return len(seqs) * w.K
+    d = host["draft"][seqs].float().numpy().astype(np.float64)
+    par = host["parent"][seqs].numpy()
+    tree_mask(par)
+    verify_tree(t, d, host["q_row"][seqs].numpy(), host["toks"][seqs].numpy(),
+                par, temperature=w.temperature, top_k=w.top_k, top_p=w.top_p,
+                draft_kind=w.draft_kind, seed=w.decision_seed,
+                batch_ids=seqs)
+    return len(seqs) * (par.shape[1] + 1)
+
+
+def host_inputs(name):
+    """The workload's inputs generated on the host (CPU generator)."""
+    import synth
+    w = synth.workload(name)
+    if name in ("greedy", "chain_topk", "chain_sample"):
+        t, d, k = synth.chain_inputs(w, "cpu")
+        return w, {"target": t, "draft": d, "toks": k}
+    t, d, q, k, p = synth.tree_inputs(w, "cpu")
+    return w, {"target": t, "draft": d, "q_row": q, "toks": k, "parent": p}
+
+
+def time_oracle(name, seconds, host=None):
+    """Oracle rows/s on a bounded sample: sequences one by one until
+    `seconds` of CPU work."""
+    w, host = host_inputs(name) if host is None else host
+    rows, t0, b = 0, time.perf_counter(), 0
+    while True:
+        rows += oracle_step(w, host, [b % w.B])
+        b += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or b >= w.B:
+            break
+    return rows / el, b, el
+
+
+def cpu_sample_text(name, nseq, el):
+    return (f"{nseq} of the workload's sequences, one by one, "
+            f"{el:.1f} s of single-thread numpy float64")
+
+
+# ------------------------------------------------------------------- main
+def main():
+    args = _args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        return reference_arm(args, world, rank)
+
+    import torch
+    import __graft_entry__ as g
+    g.build()
+    from speculative_decoding_verification_tree_gb300 import _lib
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    work = Work(args.workload, dev)
+    steps = args.steps or (3000 if args.workload != "eagle2" else 800)
+    warm = max(3, args.warmup)
+    for _ in range(warm):
+        work.step()
+    torch.cuda.synchronize()
+
+    clocks = Clocks(local)
+    clocks.start()
+    time.sleep(0.3)
+    h = _lib.load()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    h.spec_profile_enable(1)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    for _ in range(steps):
+        work.step()
+    ev1.record()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    ms = ev0.elapsed_time(ev1)
+    import ctypes
+    tot = ctypes.c_double(0)
+    nl = ctypes.c_int(0)
+    rc = h.spec_profile_read(work.prof_kind, ctypes.byref(tot),
+                             ctypes.byref(nl))
+    h.spec_profile_enable(0)
+    t_region = ms / 1e3
+    if t_region < 1.0 and not args.no_extend:
+        # keep the clock sampler running on the same load
+        t_end = time.time() + 1.0
+        while time.time() < t_end:
+            for _ in range(50):
+                work.step()
+            torch.cuda.synchronize()
+    clocks.stop()
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_step = ms / steps
+    rows_total = work.rows * steps * world
+    value = rows_total / (ms / 1e3)
+    tokens_per_step = work.emitted_tokens()
+
+    peak, peak_kind = _peaks()
+    kern_ms = (tot.value / nl.value) if nl.value else None
+    roof = None
+    if kern_ms:
+        achieved = work.kernel_bytes / (kern_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1),
+                "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": None,
+                "kernel": {0: "argmax_partial", 1: "unit_full",
+                           2: "eagle2_rows"}[work.prof_kind],
+                "bytes_per_launch": work.kernel_bytes,
+                "avg_launch_ms": round(kern_ms, 5),
+                "peak_source": peak_kind, "profile_rc": rc}
+
+    # end to end through the public API from pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        host_in = [None if x is None else x.cpu().pin_memory()
+                   for x in work.inputs]
+        dev_in = [None if x is None else torch.empty_like(x)
+                  for x in work.inputs]
+        host_out = [o.cpu().pin_memory() for o in work.outputs()]
+        h2d = sum(x.numel() * x.element_size() for x in host_in
+                  if x is not None)
+        d2h = sum(x.numel() * x.element_size() for x in host_out)
+        n_e2e = max(3, min(steps, 20))
+
+        def e2e_step():
+            for d, s in zip(dev_in, host_in):
+                if d is not None:
+                    d.copy_(s, non_blocking=True)
+            work.step(dev_in)
+            for d, s in zip(host_out, work.outputs()):
+                d.copy_(s, non_blocking=True)
+        e2e_step()
+        torch.cuda.synchronize()
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record()
+        for _ in range(n_e2e):
+            e2e_step()
+        a1.record()
+        torch.cuda.synchronize()
+        ems = a0.elapsed_time(a1)
+        if dist:
+            t = torch.tensor([ems], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": round(work.rows * n_e2e * world / (ems / 1e3), 1),
+               "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": n_e2e,
+               "ms_per_step": round(ems / n_e2e, 4)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        rps, nseq, el = time_oracle(args.workload, args.cpu_seconds,
+                                    work.host_copy())
+        cpu = {"value": round(rps, 2), "unit": UNIT, "cores": 1,
+               "kind": "oracle",
+               "sample": cpu_sample_text(args.workload, nseq, el)}
+
+    w = work.w
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": UNIT,
+            "n_gpus": world, "steps": steps, "warmup": warm,
+            "ms_per_step": round(ms_step, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": dtype_name(w),
+            "data": "synthetic (seeded; shapes and distributions of the "
+                    "pages' workloads)",
+            "config": {"workload": args.workload, "B": w.B,
+                       "drafts_per_seq": w.K, "V": w.V,
+                       "temperature": w.temperature,
+                       "rows_per_step": work.rows,
+                       "parallelism": f"replicas x{world} (sequences split)",
+                       "l2": "inputs exceed L2 (no flush)"},
+            "tokens_per_s": round(tokens_per_step * steps * world
+                                  / (ms / 1e3), 1),
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "clocks": clocks.summary(),
+            "gpu_launches": work.launches_per_step * steps,
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def dtype_name(w):
+    import torch
+    n = {torch.bfloat16: "bf16", torch.float32: "f32"}
+    if w.temperature == 0:
+        return n[w.target_dtype]
+    return f"{n[w.target_dtype]}+{n[w.draft_dtype]} (f32 accumulate)"
+
+
+def reference_arm(args, world, rank):
+    if rank != 0:
+        return
+    steps = args.steps or 3
+    w, host = host_inputs(args.workload)
+    per_step = max(1.0, min(20.0, 150.0 / (steps + args.warmup)))
+    for _ in range(args.warmup):
+        time_oracle(args.workload, per_step, (w, host))
+    rows, el = 0, 0.0
+    nseq = 0
+    for _ in range(steps):
+        r, n, e = time_oracle(args.workload, per_step, (w, host))
+        rows += r * e
+        el += e
+        nseq += n
+    value = rows / el
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 2),
+            "unit": UNIT, "n_gpus": world, "steps": steps,
+            "warmup": args.warmup, "ms_per_step": round(el / steps * 1e3, 2),
+            "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "B": w.B, "V": w.V},
+            "cpu_baseline": {"kind": "oracle", "cores": 1,
+                             "sample": cpu_sample_text(args.workload, nseq,
+                                                       el),
+                             "value": round(value, 2), "unit": UNIT},
+            "e2e": {"value": round(value, 2), "unit": UNIT,
+                    "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -223,6 +223,23 @@ int spec_philox_uniforms(uint64_t seed, uint32_t offset, const int32_t* b,
 /* Human-readable name of a return code. */
 const char* spec_error_string(int code);
 
+/*
+ * Kernel timing for benchmarks.  spec_profile_enable(1) clears the record and
+ * makes every later call bracket its dominant kernel with a pair of CUDA
+ * events recorded on the caller's stream (at most 16384 pairs); 0 turns it
+ * off.  spec_profile_read waits for the recorded events and returns the total
+ * milliseconds and number of launches of one kernel kind:
+ *   SPEC_PROF_ARGMAX    greedy argmax streaming kernel,
+ *   SPEC_PROF_VERIFY    sampled row-verification kernel,
+ *   SPEC_PROF_EXPAND    EAGLE-2 draft-row top-k kernel.
+ * Returns SPEC_ERR_SHAPE if pairs were dropped.  Not thread-safe.
+ */
+#define SPEC_PROF_ARGMAX 0
+#define SPEC_PROF_VERIFY 1
+#define SPEC_PROF_EXPAND 2
+int spec_profile_enable(int on);
+int spec_profile_read(int kind, double* total_ms, int* launches);
+
 #ifdef __cplusplus
 }
 #endif

@@ -52,7 +52,8 @@ class ChainResult:
 
 def verify_chain(target, draft, draft_tokens, *, temperature: float,
                  top_k: int = 0, top_p: float = 1.0, draft_kind="logits",
-                 seed: int = 0, offset: int = 0, uniform=None) -> ChainResult:
+                 seed: int = 0, offset: int = 0, uniform=None,
+                 batch_ids=None) -> ChainResult:
     """target [B, K+1, V], draft [B, K, V] (or None when temperature == 0),
     draft_tokens [B, K].  ``uniform(b, i, slot)`` overrides Philox."""
     target = np.asarray(target)
@@ -60,8 +61,13 @@ def verify_chain(target, draft, draft_tokens, *, temperature: float,
     K = K1 - 1
     toks = np.asarray(draft_tokens).reshape(B, K)
     if uniform is None:
+        # batch_ids: the sequence index each row had in the full batch (the
+        # Philox counter uses it), when the oracle checks a subset
+        ids = list(range(B)) if batch_ids is None else [int(x) for x in
+                                                         batch_ids]
+
         def uniform(b, i, slot):
-            return philox.uniform(seed, b, i, slot, offset)
+            return philox.uniform(seed, ids[b], i, slot, offset)
 
     accepted = np.zeros(B, dtype=np.int32)
     out = np.full((B, K + 1), -1, dtype=np.int32)

@@ -111,7 +111,7 @@ class TreeResult:
 def verify_tree(target, draft, q_row, node_tokens, parent, *,
                 temperature: float, top_k: int = 0, top_p: float = 1.0,
                 draft_kind="logits", seed: int = 0, offset: int = 0,
-                uniform=None) -> TreeResult:
+                uniform=None, batch_ids=None) -> TreeResult:
     """target [B, N+1, V], draft [B, R, V] (None at temperature 0),
     q_row [B, N+1], node_tokens [B, N], parent [B, N]."""
     target = np.asarray(target)
@@ -121,8 +121,13 @@ def verify_tree(target, draft, q_row, node_tokens, parent, *,
     toks = np.asarray(node_tokens).reshape(B, N)
     parent = np.asarray(parent).reshape(B, N)
     if uniform is None:
+        # batch_ids: the sequence index each row had in the full batch (the
+        # Philox counter uses it), when the oracle checks a subset
+        ids = list(range(B)) if batch_ids is None else [int(x) for x in
+                                                         batch_ids]
+
         def uniform(b, i, slot):
-            return philox.uniform(seed, b, i, slot, offset)
+            return philox.uniform(seed, ids[b], i, slot, offset)
 
     path_len = np.zeros(B, dtype=np.int32)
     path_nodes = np.full((B, N), -1, dtype=np.int32)

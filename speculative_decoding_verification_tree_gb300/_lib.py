@@ -81,7 +81,14 @@ _SIGNATURES = {
     "spec_philox_uniforms": (_I, [ctypes.c_uint64, ctypes.c_uint32, _P, _P,
                                   _P, _I, _P, _P]),
     "spec_error_string": (ctypes.c_char_p, [_I]),
+    "spec_profile_enable": (_I, [_I]),
+    "spec_profile_read": (_I, [_I, ctypes.POINTER(ctypes.c_double),
+                               ctypes.POINTER(ctypes.c_int)]),
 }
+
+SPEC_PROF_ARGMAX = 0
+SPEC_PROF_VERIFY = 1
+SPEC_PROF_EXPAND = 2
 
 EXPORTED = tuple(_SIGNATURES)
 

@@ -188,6 +188,7 @@ cudaError_t launch_greedy(const VerifyShape& s, const VerifyArgs& a, cudaStream_
   const size_t esz = a.dt_target == SPEC_BF16 ? 2 : 4;
   const bool vec = ((uintptr_t)a.target % 16 == 0) && ((s.V * esz) % 16 == 0);
   if (items > 0) {
+    prof_begin(SPEC_PROF_ARGMAX, st);
     if (a.dt_target == SPEC_BF16) {
       const uint16_t* t = (const uint16_t*)a.target;
       if (vec)
@@ -202,6 +203,7 @@ cudaError_t launch_greedy(const VerifyShape& s, const VerifyArgs& a, cudaStream_
         argmax_partial<float, false><<<(unsigned)items, kThreads, 0, st>>>(t, s.V, S, a.arg_part);
     }
     cudaError_t e = cudaGetLastError();
+    prof_end(SPEC_PROF_ARGMAX, st);
     if (e != cudaSuccess) return e;
   }
   const size_t smem = (size_t)3 * (s.n + 1) * sizeof(int32_t);

@@ -50,6 +50,10 @@ struct VerifyArgs {
   ArgPart* arg_part;    // [rows * arg_splits(V)] (greedy)
 };
 
+// Event pair around a dominant kernel launch (no-op unless profiling is on).
+void prof_begin(int kind, cudaStream_t st);
+void prof_end(int kind, cudaStream_t st);
+
 cudaError_t launch_greedy(const VerifyShape& s, const VerifyArgs& a, cudaStream_t st);
 cudaError_t launch_sampled(const VerifyShape& s, const VerifyArgs& a, cudaStream_t st);
 cudaError_t launch_tree_mask(const int32_t* parent, int B, int N, uint8_t* mask,

@@ -699,7 +699,8 @@ cudaError_t launch_sampled(const VerifyShape& s, const VerifyArgs& a, cudaStream
   P.invT = 1.f / T;
   const int qk = a.prm.draft_kind == SPEC_DRAFT_LOGITS ? Q_LOGITS : (T == 1.f ? Q_PROBS_T1 : Q_PROBS_T);
   cudaError_t e = cudaSuccess;
-#define SV_DISPATCH(TT, TD)                                       \
+  prof_begin(SPEC_PROF_VERIFY, st);
+#define SV_DISPATCH(TT, TD)                                     \
   if (qk == Q_LOGITS) e = launch_units<TT, TD, Q_LOGITS>(P, C, st); \
   else if (qk == Q_PROBS_T1) e = launch_units<TT, TD, Q_PROBS_T1>(P, C, st); \
   else e = launch_units<TT, TD, Q_PROBS_T>(P, C, st);
@@ -711,6 +712,7 @@ cudaError_t launch_sampled(const VerifyShape& s, const VerifyArgs& a, cudaStream
     else { SV_DISPATCH(float, float) }
   }
 #undef SV_DISPATCH
+  prof_end(SPEC_PROF_VERIFY, st);
   if (e != cudaSuccess) return e;
   sampled_walk<<<(s.B + 127) / 128, 128, 0, st>>>(s, a);
   return cudaGetLastError();

@@ -38,7 +38,8 @@ def run(w, seqs=None, target=None, draft=None, toks=None, seed=None):
     ref = verify_chain(np64(target[sel]), np64(draft[sel]),
                        toks[sel].cpu().numpy(), temperature=w.temperature,
                        top_k=w.top_k, top_p=w.top_p,
-                       draft_kind=w.draft_kind, seed=seed)
+                       draft_kind=w.draft_kind, seed=seed,
+                       batch_ids=None if seqs is None else seqs)
     return gpu, ref
 
 

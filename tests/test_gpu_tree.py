@@ -96,7 +96,7 @@ def run_tree(w, target, draft, q_row, toks, par, seqs=None, seed=None):
                       q_row[sel].cpu().numpy(), toks[sel].cpu().numpy(),
                       par[sel].cpu().numpy(), temperature=w.temperature,
                       top_k=w.top_k, top_p=w.top_p, draft_kind=w.draft_kind,
-                      seed=seed)
+                      seed=seed, batch_ids=None if seqs is None else seqs)
     return gpu, ref
 
 
