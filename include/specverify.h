@@ -234,6 +234,32 @@ const char* spec_error_string(int code);
  *   SPEC_PROF_EXPAND    EAGLE-2 draft-row top-k kernel.
  * Returns SPEC_ERR_SHAPE if pairs were dropped.  Not thread-safe.
  */
+/*
+ * Chain verification without a workspace, for callers that cannot allocate
+ * device memory (an engine plugin handed only its input and output buffers,
+ * or a decode loop where cudaMalloc is not allowed).  No counterpart on the
+ * pages: it computes exactly what spec_verify_chain computes (same arguments
+ * minus the workspace) and differs only in where its scratch lives.
+ *
+ * The scratch is one fixed array inside the library (about 576 KiB) that
+ * every GPU which loads the library holds until the process exits.  The first
+ * call on a device looks up that array's device address with the device
+ * current, so make the first call before any stream capture.  All calls on a
+ * device share the array and leave their contents in it: calls whose GPU work
+ * overlaps (several streams or host threads on one device) race and must be
+ * serialised by the caller.  Limits: B*(K+1) <= SPEC_NOALLOC_MAX_ROWS and
+ * B*(K+1)*ceil(V/16384) <= SPEC_NOALLOC_MAX_PARTS; larger requests return
+ * SPEC_ERR_SHAPE before any GPU work.  Allocates nothing.
+ */
+#define SPEC_NOALLOC_MAX_ROWS 8192
+#define SPEC_NOALLOC_MAX_PARTS 65536
+int spec_verify_chain_noalloc(const void* target_logits, const void* draft,
+                              const int32_t* draft_tokens, int B, int K, int V,
+                              int dtype_target, int dtype_draft,
+                              const spec_params_t* prm, int32_t* accepted,
+                              int32_t* out_tokens, float* accept_mass,
+                              void* stream);
+
 #define SPEC_PROF_ARGMAX 0
 #define SPEC_PROF_VERIFY 1
 #define SPEC_PROF_EXPAND 2

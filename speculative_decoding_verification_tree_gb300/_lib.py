@@ -31,6 +31,8 @@ SPEC_MAX_TOP_K = 1024
 SPEC_MAX_CHILDREN = 64
 SPEC_MAX_TREE_NODES = 1024
 SPEC_EAGLE2_MAX_TOPK = 32
+SPEC_NOALLOC_MAX_ROWS = 8192
+SPEC_NOALLOC_MAX_PARTS = 65536
 
 SPEC_STATUS_NAN = 1
 SPEC_STATUS_QZERO_ACCEPT = 2
@@ -81,6 +83,9 @@ _SIGNATURES = {
     "spec_philox_uniforms": (_I, [ctypes.c_uint64, ctypes.c_uint32, _P, _P,
                                   _P, _I, _P, _P]),
     "spec_error_string": (ctypes.c_char_p, [_I]),
+    "spec_verify_chain_noalloc": (_I, [_P, _P, _P, _I, _I, _I, _I, _I,
+                                       ctypes.POINTER(SpecParams), _P, _P, _P,
+                                       _P]),
     "spec_profile_enable": (_I, [_I]),
     "spec_profile_read": (_I, [_I, ctypes.POINTER(ctypes.c_double),
                                ctypes.POINTER(ctypes.c_int)]),

@@ -1,0 +1,123 @@
+// spec_verify_chain_noalloc: chain verification for callers that cannot
+// allocate device memory.
+//
+// Who needs it: code that is handed only its input and output buffers and no
+// way to get more device memory -- for example an operator plugin inside an
+// inference engine that has already carved up all of the GPU's memory, or a
+// latency-critical decode loop whose owner forbids cudaMalloc there (it may
+// synchronise the device and it can fail at run time).  Such a caller cannot
+// provide the workspace spec_verify_chain asks for.
+//
+// What it does instead: the scratch the verification kernels need (status
+// word, per-row outcomes, argmax partials) lives in one file-scope __device__
+// array of fixed size, which every GPU that loads this library holds until
+// the process exits.  Nothing is allocated per call.
+//
+// Rules for callers:
+//  * The first call on each device looks up the array's device address
+//    (cudaGetSymbolAddress) with that device current; make that first call
+//    before any stream capture.
+//  * Every call on a device shares the one array and leaves the last call's
+//    contents in it; the status word is cleared at the start of each call.
+//    Calls whose work overlaps on the GPU (other streams, other host threads
+//    on the same device) race on the array and must be serialised by the
+//    caller.
+//  * Sizes: B * (K + 1) <= SPEC_NOALLOC_MAX_ROWS rows and
+//    B * (K + 1) * ceil(V / 16384) <= SPEC_NOALLOC_MAX_PARTS argmax partials;
+//    larger requests are rejected with SPEC_ERR_SHAPE before any GPU work.
+#include <cmath>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace sv {
+namespace {
+
+constexpr size_t kStatusBytes = 256;
+constexpr size_t kRowBytes = (size_t)SPEC_NOALLOC_MAX_ROWS * sizeof(int32_t);
+constexpr size_t kPartBytes = (size_t)SPEC_NOALLOC_MAX_PARTS * sizeof(ArgPart);
+constexpr size_t kScratchBytes = kStatusBytes + 2 * kRowBytes + kPartBytes;
+
+// The scratch itself (~576 KiB per device).  In host code this name is only
+// a stand-in; its device address comes from cudaGetSymbolAddress below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+void* g_addr[kMaxDevices] = {};
+
+// Device address of the scratch for the current device (looked up once).
+int scratch_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return SPEC_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return SPEC_ERR_CUDA;
+    g_addr[dev] = p;
+  }
+  *out = g_addr[dev];
+  return SPEC_OK;
+}
+
+}  // namespace
+}  // namespace sv
+
+using namespace sv;
+
+extern "C" int spec_verify_chain_noalloc(const void* target_logits, const void* draft,
+                                         const int32_t* draft_tokens, int B, int K, int V,
+                                         int dtype_target, int dtype_draft,
+                                         const spec_params_t* prm, int32_t* accepted,
+                                         int32_t* out_tokens, float* accept_mass,
+                                         void* stream) {
+  if (B < 0 || K < 0 || V < 1) return SPEC_ERR_SHAPE;
+  if (V > SPEC_MAX_VOCAB || K > SPEC_MAX_TREE_NODES) return SPEC_ERR_SHAPE;
+  const int64_t rows = (int64_t)B * (K + 1);
+  if (rows > SPEC_NOALLOC_MAX_ROWS) return SPEC_ERR_SHAPE;
+  if (rows * arg_splits(V) > SPEC_NOALLOC_MAX_PARTS) return SPEC_ERR_SHAPE;
+  if (!prm) return SPEC_ERR_ARG;
+  if (!(prm->temperature >= 0.f) || !std::isfinite(prm->temperature)) return SPEC_ERR_ARG;
+  if (prm->flags != 0 || prm->top_k < 0) return SPEC_ERR_ARG;
+  if (prm->draft_kind != SPEC_DRAFT_LOGITS && prm->draft_kind != SPEC_DRAFT_PROBS)
+    return SPEC_ERR_DTYPE;
+  if (!(prm->top_p > 0.f && prm->top_p <= 1.f)) return SPEC_ERR_ARG;
+  if (prm->temperature > 0.f && (prm->top_k != 0 || prm->top_p < 1.f)) return SPEC_ERR_UNSUPPORTED;
+  if (dtype_target != SPEC_F32 && dtype_target != SPEC_BF16) return SPEC_ERR_DTYPE;
+  const bool greedy = prm->temperature == 0.f;
+  const bool dt_ok = dtype_draft == SPEC_F32 || dtype_draft == SPEC_BF16;
+  if (!greedy && K > 0 && !dt_ok) return SPEC_ERR_DTYPE;
+  if (B > 0) {
+    if (!target_logits || !accepted || !out_tokens) return SPEC_ERR_ARG;
+    if (K > 0 && (!draft_tokens || !accept_mass)) return SPEC_ERR_ARG;
+    if (!greedy && K > 0 && !draft) return SPEC_ERR_ARG;
+  }
+  void* base = nullptr;
+  int rc = scratch_address(&base);
+  if (rc != SPEC_OK) return rc;
+  cudaStream_t st = (cudaStream_t)stream;
+  char* p = (char*)base;
+  VerifyShape s{B, K, K, V, true};
+  VerifyArgs a{};
+  a.target = target_logits;
+  a.draft = greedy ? nullptr : draft;
+  a.node_tokens = draft_tokens;
+  a.dt_target = dtype_target;
+  a.dt_draft = dt_ok ? dtype_draft : SPEC_F32;
+  a.prm = *prm;
+  a.count = accepted;
+  a.out_tokens = out_tokens;
+  a.mass = accept_mass;
+  a.status = (uint32_t*)p;
+  a.row_child = (int32_t*)(p + kStatusBytes);
+  a.row_token = (int32_t*)(p + kStatusBytes + kRowBytes);
+  a.arg_part = (ArgPart*)(p + kStatusBytes + 2 * kRowBytes);
+  // the status word must start at zero; everything else is written before it
+  // is read within the call
+  if (cudaMemsetAsync(a.status, 0, sizeof(uint32_t), st) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (B == 0) return SPEC_OK;
+  const cudaError_t e = greedy ? launch_greedy(s, a, st) : launch_sampled(s, a, st);
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
