@@ -112,8 +112,46 @@ class Work:
             self.kernel_bytes = B * (N + 1) * V * (
                 self.target.element_size() + self.draft.element_size())
             self.launches_per_step = 3  # mask, row verification, walk
+        elif name == "eagle2":
+            self.kind = "eagle2"
+            self.draft = synth.eagle2_draft(w, device)
+            B, V, M = w.B, w.V, w.total
+            self.N = M
+            self.R = self.draft.shape[1]
+            self.ews = api.workspace(_lib.SPEC_OP_EAGLE2, B, self.R, V, device)
+            self.tree = (torch.empty(B, M, dtype=torch.int32, device=device),
+                         torch.empty(B, M, dtype=torch.int32, device=device),
+                         torch.empty(B, M + 1, dtype=torch.int32,
+                                     device=device),
+                         torch.empty(B, M, dtype=torch.float32, device=device),
+                         torch.empty(B, M, M, dtype=torch.uint8,
+                                     device=device))
+            self._expand(self.draft)
+            torch.cuda.synchronize()
+            # target rows for the reranked tree (synthetic target forward)
+            self.target = synth.eagle2_target(w, self.draft, self.tree[2],
+                                              device)
+            self.rows = B * (M + 1)
+            self.ws = api.workspace(_lib.SPEC_OP_TREE, B, M, V, device)
+            self.out = (torch.empty(B, dtype=torch.int32, device=device),
+                        torch.empty(B, M, dtype=torch.int32, device=device),
+                        torch.empty(B, M + 1, dtype=torch.int32, device=device),
+                        torch.empty(B, M + 1, dtype=torch.float32,
+                                    device=device))
+            self.inputs = [self.draft, self.target]
+            self.prof_kind = _lib.SPEC_PROF_VERIFY
+            qrows = int((self.tree[2] >= 0).sum().item())
+            self.kernel_bytes = (B * (M + 1) + qrows) * V * 2
+            self.expand_bytes = B * self.R * V * 2
+            self.launches_per_step = 5  # rows, select, mask, verify, walk
         else:
             raise SystemExit(f"workload {name} is not wired into the bench")
+
+    def _expand(self, draft):
+        w = self.w
+        self.api.spec_eagle2_expand_rerank(
+            draft, temperature=w.temperature, depth=w.depth, topk=w.topk,
+            width=w.width, total=w.total, out=self.tree, ws=self.ews)
 
     def step(self, inputs=None):
         """Enqueue one step on the current stream."""
@@ -125,6 +163,13 @@ class Work:
                                   draft_kind=w.draft_kind,
                                   seed=w.decision_seed, out=self.out,
                                   ws=self.ws)
+        elif self.kind == "eagle2":
+            self._expand(x[0])
+            tok, par, qrow = self.tree[0], self.tree[1], self.tree[2]
+            api.spec_verify_tree(x[1], x[0], qrow, tok, par,
+                                 temperature=w.temperature,
+                                 seed=w.decision_seed, out=self.out,
+                                 ws=self.ws)
         else:
             from speculative_decoding_verification_tree_gb300.api import (
                 _ptr, _stream)
@@ -139,16 +184,21 @@ class Work:
 
     def host_copy(self):
         """The step's inputs on the host, for the CPU oracle."""
+        if self.kind == "eagle2":
+            return self.w, {"draft": self.draft.cpu(),
+                            "target": self.target.cpu()}
         keys = (["target", "draft", "toks"] if self.kind == "chain" else
                 ["target", "draft", "q_row", "toks", "parent"])
         return self.w, {k: (None if x is None else x.cpu())
                         for k, x in zip(keys, self.inputs)}
 
+    def outputs(self):
+        if self.kind == "eagle2":
+            return list(self.out) + list(self.tree)
+        return [o for o in self.out if o is not None]
+
     def emitted_tokens(self):
         return int(self.out[0].sum().item()) + self.w.B
-
-    def outputs(self):
-        return [o for o in self.out if o is not None]
 
 
 # ------------------------------------------------------------------ clocks
@@ -217,8 +267,17 @@ def oracle_step(w, host, seqs):
     """Run the oracle on sequences `seqs` of the host copy of the inputs."""
     import numpy as np
     from oracle.chain import verify_chain
+    from oracle.eagle2 import expand_rerank
     from oracle.tree import tree_mask, verify_tree
     t = host["target"][seqs].float().numpy().astype(np.float64)
+    if w.name == "eagle2":
+        d = host["draft"][seqs].float().numpy().astype(np.float64)
+        tr = expand_rerank(d, temperature=w.temperature, depth=w.depth,
+                           topk=w.topk, width=w.width, total=w.total)
+        verify_tree(t, d, tr.q_row, tr.node_tokens, tr.parent,
+                    temperature=w.temperature, seed=w.decision_seed,
+                    batch_ids=seqs)
+        return len(seqs) * (w.total + 1)
     if w.name in ("greedy", "chain_topk", "chain_sample"):
         d = None if host["draft"] is None else \
             host["draft"][seqs].float().numpy().astype(np.float64)
@@ -237,13 +296,27 @@ def oracle_step(w, host, seqs):
     return len(seqs) * (par.shape[1] + 1)
 
 
-def host_inputs(name):
-    """The workload's inputs generated on the host (CPU generator)."""
+def host_inputs(name, nseq=8):
+    """The first `nseq` sequences of the workload's shape, generated on the
+    host (CPU generator); the oracle is timed per sequence."""
     import synth
     w = synth.workload(name)
+    w = synth.workload(name, B=min(w.B, nseq))
     if name in ("greedy", "chain_topk", "chain_sample"):
         t, d, k = synth.chain_inputs(w, "cpu")
         return w, {"target": t, "draft": d, "toks": k}
+    if name == "eagle2":
+        import torch
+        d = synth.eagle2_draft(w, "cpu")
+        # host-side stand-in for the target forward of the reranked tree:
+        # tree row r reuses draft row r where it exists (the oracle's cost
+        # does not depend on which rows these are)
+        R = d.shape[1]
+        r = torch.arange(w.total + 1, dtype=torch.int32)
+        q_row = torch.where(r < R, r, torch.full_like(r, -1))
+        q_row = q_row.unsqueeze(0).expand(w.B, -1).contiguous()
+        return w, {"draft": d, "target": synth.eagle2_target(w, d, q_row,
+                                                              "cpu")}
     t, d, q, k, p = synth.tree_inputs(w, "cpu")
     return w, {"target": t, "draft": d, "q_row": q, "toks": k, "parent": p}
 
@@ -318,6 +391,18 @@ def main():
     nl = ctypes.c_int(0)
     rc = h.spec_profile_read(work.prof_kind, ctypes.byref(tot),
                              ctypes.byref(nl))
+    other = {}
+    if work.kind == "eagle2":
+        t2, n2 = ctypes.c_double(0), ctypes.c_int(0)
+        h.spec_profile_read(_lib.SPEC_PROF_EXPAND, ctypes.byref(t2),
+                            ctypes.byref(n2))
+        if n2.value:
+            ems_k = t2.value / n2.value
+            other["eagle2_rows"] = {
+                "avg_launch_ms": round(ems_k, 5),
+                "bytes_per_launch": work.expand_bytes,
+                "achieved_gbs": round(work.expand_bytes / (ems_k / 1e3) / 1e9,
+                                      1)}
     h.spec_profile_enable(0)
     t_region = ms / 1e3
     if t_region < 1.0 and not args.no_extend:
@@ -349,7 +434,8 @@ def main():
                            2: "eagle2_rows"}[work.prof_kind],
                 "bytes_per_launch": work.kernel_bytes,
                 "avg_launch_ms": round(kern_ms, 5),
-                "peak_source": peak_kind, "profile_rc": rc}
+                "peak_source": peak_kind, "profile_rc": rc,
+                "other_kernels": other}
 
     # end to end through the public API from pinned host buffers
     e2e = None

@@ -71,6 +71,8 @@ extern "C" {
 #define SPEC_MAX_CHILDREN 64      /* children of one tree node             */
 #define SPEC_MAX_TREE_NODES 1024  /* N (tree) and K (chain)                */
 #define SPEC_EAGLE2_MAX_TOPK 32   /* children per expanded EAGLE-2 node    */
+#define SPEC_EAGLE2_MAX_WIDTH 2048 /* nodes kept per EAGLE-2 layer          */
+#define SPEC_EAGLE2_MAX_CANDIDATES 4096 /* EAGLE-2 candidates per sequence */
 
 /* ---- device status bits (spec_get_status) ---- */
 #define SPEC_STATUS_NAN 1u            /* a logit row had NaN / no finite value */

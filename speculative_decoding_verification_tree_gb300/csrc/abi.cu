@@ -175,7 +175,8 @@ int spec_eagle2_expand_rerank(const void* draft_logits, int B, int V, int dtype,
     ncand += layer;
     layer = (int64_t)(layer < width ? layer : width) * topk;
   }
-  if (total > ncand) return SPEC_ERR_SHAPE;
+  if (total > ncand || ncand > SPEC_EAGLE2_MAX_CANDIDATES) return SPEC_ERR_SHAPE;
+  if (width > SPEC_EAGLE2_MAX_WIDTH) return SPEC_ERR_SHAPE;
   if (!prm || !(prm->temperature > 0.f) || !std::isfinite(prm->temperature)) return SPEC_ERR_ARG;
   if (!dtype_ok(dtype)) return SPEC_ERR_DTYPE;
   const int R = 1 + (depth - 1) * width;
