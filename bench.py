@@ -47,6 +47,9 @@ def _args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--B", type=int, default=None,
+                   help="override the workload's batch (small profiling "
+                        "cases); the default is the workload's own batch")
     p.add_argument("--no-extend", action="store_true",
                    help="do not keep the load running for the clock sampler "
                         "after a short timed region (profiler runs)")
@@ -66,14 +69,15 @@ def _peaks():
 class Work:
     """Device inputs, outputs and one step of a workload (GPU arm)."""
 
-    def __init__(self, name, device):
+    def __init__(self, name, device, B=None):
         import torch
 
         import synth
         from speculative_decoding_verification_tree_gb300 import _lib, api
         self.torch, self.api, self.lib = torch, api, _lib
         self.name = name
-        self.w = w = synth.workload(name)
+        self.w = w = (synth.workload(name) if B is None else
+                      synth.workload(name, B=B))
         self.device = device
         if name in ("greedy", "chain_topk", "chain_sample"):
             self.kind = "chain"
@@ -361,7 +365,7 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
-    work = Work(args.workload, dev)
+    work = Work(args.workload, dev, args.B)
     steps = args.steps or (3000 if args.workload != "eagle2" else 800)
     warm = max(3, args.warmup)
     for _ in range(warm):

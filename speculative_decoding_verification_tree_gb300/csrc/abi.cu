@@ -15,15 +15,18 @@ inline size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 // Workspace of a verification call: [status | row_child | row_token | argmax parts]
 struct VerifyWs {
-  size_t off_child, off_token, off_parts, total;
+  size_t off_child, off_token, off_parts, off_alpha, off_meta, off_qres, total;
 };
-VerifyWs verify_ws(int B, int n, int V) {
+VerifyWs verify_ws(int B, int n, int V, bool chain) {
   const size_t rows = (size_t)B * (n + 1);
   VerifyWs w;
   w.off_child = kAlign;
   w.off_token = w.off_child + up(rows * sizeof(int32_t));
   w.off_parts = w.off_token + up(rows * sizeof(int32_t));
-  w.total = w.off_parts + up(rows * (size_t)arg_splits(V) * sizeof(ArgPart));
+  w.off_alpha = w.off_parts + up(rows * (size_t)arg_splits(V) * sizeof(ArgPart));
+  w.off_meta = w.off_alpha + up(rows * kAlphaSlots * sizeof(float));
+  w.off_qres = w.off_meta + up(rows * (size_t)meta_rec_bytes(chain));
+  w.total = w.off_qres + up(rows * sizeof(int32_t));
   return w;
 }
 struct Eagle2Ws {
@@ -56,7 +59,7 @@ int check_params(const spec_params_t* prm, int V) {
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA; }
 
 int run_verify(const VerifyShape& s, VerifyArgs& a, void* ws, size_t ws_bytes, cudaStream_t st) {
-  const VerifyWs w = verify_ws(s.B, s.n, s.V);
+  const VerifyWs w = verify_ws(s.B, s.n, s.V, s.chain);
   if (!ws || ((uintptr_t)ws % kAlign) != 0) return SPEC_ERR_WORKSPACE;
   if (ws_bytes < w.total) return SPEC_ERR_WORKSPACE;
   char* base = (char*)ws;
@@ -64,6 +67,9 @@ int run_verify(const VerifyShape& s, VerifyArgs& a, void* ws, size_t ws_bytes, c
   a.row_child = (int32_t*)(base + w.off_child);
   a.row_token = (int32_t*)(base + w.off_token);
   a.arg_part = (ArgPart*)(base + w.off_parts);
+  a.alpha_part = (float*)(base + w.off_alpha);
+  a.meta = (unsigned char*)(base + w.off_meta);
+  a.qres = (int32_t*)(base + w.off_qres);
   cudaError_t e = cudaMemsetAsync(a.status, 0, sizeof(uint32_t), st);
   if (e != cudaSuccess) return SPEC_ERR_CUDA;
   if (s.B == 0) return SPEC_OK;
@@ -82,7 +88,7 @@ size_t spec_workspace_bytes(int op, int B, int n, int V) {
   if (B < 0 || n < 0 || V < 1 || V > SPEC_MAX_VOCAB) return 0;
   if (op == SPEC_OP_CHAIN || op == SPEC_OP_TREE) {
     if (n > SPEC_MAX_TREE_NODES) return 0;
-    return verify_ws(B, n, V).total;
+    return verify_ws(B, n, V, op == SPEC_OP_CHAIN).total;
   }
   if (op == SPEC_OP_EAGLE2) return eagle2_ws(B, n).total;
   return 0;

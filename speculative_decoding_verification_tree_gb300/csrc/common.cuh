@@ -191,6 +191,45 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t phase)
   return true;
 }
 
+// Plain arrive (count 1) on a barrier of this CTA.
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+// 16-byte store into another CTA's shared memory (cluster address) that
+// completes 16 transaction bytes on that CTA's barrier (cluster address).
+__device__ __forceinline__ void st_async_v4(uint32_t remote_addr, float4 v, uint32_t remote_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::
+          "r"(remote_addr),
+      "r"(__float_as_uint(v.x)), "r"(__float_as_uint(v.y)), "r"(__float_as_uint(v.z)),
+      "r"(__float_as_uint(v.w)), "r"(remote_bar)
+      : "memory");
+}
+// Barrier wait with acquire at cluster scope (data written by peers through
+// st.async becomes visible).  Bounded like mbar_wait_bounded.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t phase) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(phase)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_t phase) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait_cluster(bar, phase)) {
+    if (clock64() - t0 > (1LL << 31)) return false;
+  }
+  return true;
+}
+// Named barrier over `n` threads (id 1..15; id 0 is __syncthreads).
+__device__ __forceinline__ void named_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
 __device__ __forceinline__ void flag_status(uint32_t* status, uint32_t bits) {
   if (bits) atomicOr(status, bits);
 }

@@ -26,7 +26,7 @@ struct VerifyShape {
   int R;         // draft rows per sequence
   int V;
   bool chain;
-  int64_t rows() const { return (int64_t)B * (n + 1); }
+  __host__ __device__ int64_t rows() const { return (int64_t)B * (n + 1); }
 };
 
 // Device pointers of one verification call.
@@ -48,7 +48,37 @@ struct VerifyArgs {
   int32_t* row_child;   // [rows] accepted child per row (-1 none)
   int32_t* row_token;   // [rows] sampled / argmax token per row
   ArgPart* arg_part;    // [rows * arg_splits(V)] (greedy)
+  float* alpha_part;    // [rows * 8] per-CTA acceptance-mass partials
+  unsigned char* meta;  // [rows * meta_rec_bytes(chain)] per-row records
+  int32_t* qres;        // [rows] resolved draft row per tree row (-1 none)
 };
+
+// Per-row record of the pipelined kernel: a 16-byte header and 16 bytes per
+// child slot (one slot for a chain, SPEC_MAX_CHILDREN for a tree).
+inline int meta_kidcap(bool chain) { return chain ? 1 : SPEC_MAX_CHILDREN; }
+inline int meta_rec_bytes(bool chain) { return 16 * (1 + meta_kidcap(chain)); }
+
+// Per-row slots of alpha partials (one per CTA of a cluster of up to 8).
+constexpr int kAlphaSlots = 8;
+
+// Launch parameters of the pipelined sampled-verification kernel.
+struct PipeParams {
+  VerifyShape s;
+  VerifyArgs a;
+  int slice;      // vocabulary elements per CTA
+  int stages;     // shared-memory stages per CTA
+  int nclusters;  // persistent clusters (set by the launcher)
+  float kt;       // log2(e) / T
+  float invT;     // 1 / T
+  int kidcap;     // child slots per row record
+  int rec_bytes;  // row record stride
+};
+bool pipe_geometry(int V, int tsz, int dsz, int* C, int* ept, int* stages, int* slice);
+cudaError_t launch_pipe_bf16(const PipeParams& P, int C, int ept, int qk, int dt_draft,
+                             cudaStream_t st);
+cudaError_t launch_pipe_f32(const PipeParams& P, int C, int ept, int qk, int dt_draft,
+                            cudaStream_t st);
+cudaError_t launch_pipe_walk(const VerifyShape& s, const VerifyArgs& a, int C, cudaStream_t st);
 
 // Event pair around a dominant kernel launch (no-op unless profiling is on).
 void prof_begin(int kind, cudaStream_t st);

@@ -9,7 +9,9 @@
 // provide the workspace spec_verify_chain asks for.
 //
 // What it does instead: the scratch the verification kernels need (status
-// word, per-row outcomes, argmax partials) lives in one file-scope __device__
+// word, per-row outcomes and records, argmax and acceptance-mass partials)
+// lives in one
+// file-scope __device__
 // array of fixed size, which every GPU that loads this library holds until
 // the process exits.  Nothing is allocated per call.
 //
@@ -37,9 +39,12 @@ namespace {
 constexpr size_t kStatusBytes = 256;
 constexpr size_t kRowBytes = (size_t)SPEC_NOALLOC_MAX_ROWS * sizeof(int32_t);
 constexpr size_t kPartBytes = (size_t)SPEC_NOALLOC_MAX_PARTS * sizeof(ArgPart);
-constexpr size_t kScratchBytes = kStatusBytes + 2 * kRowBytes + kPartBytes;
+constexpr size_t kAlphaBytes = (size_t)SPEC_NOALLOC_MAX_ROWS * kAlphaSlots * sizeof(float);
+constexpr size_t kMetaBytes = (size_t)SPEC_NOALLOC_MAX_ROWS * 32;  // chain row records
+constexpr size_t kScratchBytes =
+    kStatusBytes + 3 * kRowBytes + kPartBytes + kAlphaBytes + kMetaBytes;
 
-// The scratch itself (~576 KiB per device).  In host code this name is only
+// The scratch itself (~1.1 MiB per device).  In host code this name is only
 // a stand-in; its device address comes from cudaGetSymbolAddress below.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
@@ -114,6 +119,10 @@ extern "C" int spec_verify_chain_noalloc(const void* target_logits, const void* 
   a.row_child = (int32_t*)(p + kStatusBytes);
   a.row_token = (int32_t*)(p + kStatusBytes + kRowBytes);
   a.arg_part = (ArgPart*)(p + kStatusBytes + 2 * kRowBytes);
+  a.alpha_part = (float*)(p + kStatusBytes + 2 * kRowBytes + kPartBytes);
+  a.meta = (unsigned char*)(p + kStatusBytes + 2 * kRowBytes + kPartBytes + kAlphaBytes);
+  a.qres = (int32_t*)(p + kStatusBytes + 2 * kRowBytes + kPartBytes + kAlphaBytes + kMetaBytes);
+  static_assert(32 == 16 * (1 + 1), "chain row record size");
   // the status word must start at zero; everything else is written before it
   // is read within the call
   if (cudaMemsetAsync(a.status, 0, sizeof(uint32_t), st) != cudaSuccess) return SPEC_ERR_CUDA;

@@ -699,6 +699,17 @@ cudaError_t launch_sampled(const VerifyShape& s, const VerifyArgs& a, cudaStream
   P.invT = 1.f / T;
   const int qk = a.prm.draft_kind == SPEC_DRAFT_LOGITS ? Q_LOGITS : (T == 1.f ? Q_PROBS_T1 : Q_PROBS_T);
   cudaError_t e = cudaSuccess;
+  // bandwidth path: persistent pipelined clusters (aligned rows that fit)
+  int pc, pept, pst, psl;
+  if (P.bulk && a.meta && a.qres && pipe_geometry(s.V, tsz, dsz, &pc, &pept, &pst, &psl)) {
+    PipeParams Q{s, a, psl, pst, 0, P.kt, P.invT, meta_kidcap(s.chain), meta_rec_bytes(s.chain)};
+    prof_begin(SPEC_PROF_VERIFY, st);
+    e = (a.dt_target == SPEC_BF16) ? launch_pipe_bf16(Q, pc, pept, qk, a.dt_draft, st)
+                                   : launch_pipe_f32(Q, pc, pept, qk, a.dt_draft, st);
+    prof_end(SPEC_PROF_VERIFY, st);
+    if (e != cudaSuccess) return e;
+    return launch_pipe_walk(s, a, pc, st);
+  }
   prof_begin(SPEC_PROF_VERIFY, st);
 #define SV_DISPATCH(TT, TD)                                     \
   if (qk == Q_LOGITS) e = launch_units<TT, TD, Q_LOGITS>(P, C, st); \

@@ -1,0 +1,782 @@
+// Pipelined sampled verification (temperature > 0, full vocabulary), the
+// bandwidth path for rows up to 131072 logits.
+//
+// Same method as unit_full in sample_full.cu (accept test u < p'(x)/q'(x),
+// residual max(0, p - C q), inverse-CDF draw in vocabulary order), organised
+// for HBM streaming on GB300:
+//  * persistent thread-block clusters, one 512-thread CTA per SM; each CTA of
+//    a cluster owns one contiguous vocabulary slice of every row the cluster
+//    verifies;
+//  * row_meta (a small kernel ahead of it) writes one record per row: draft
+//    row, children in index order, their tokens and the target / draft logits
+//    at those tokens, so the streaming kernel does no dependent global loads;
+//  * thread 0 keeps S shared-memory stages in flight with TMA bulk copies of
+//    the next rows' target / draft slices, and the next rows' records;
+//  * all 16 warps copy a landed slice into registers (up to 32 logits of each
+//    row per thread), the stage is refilled at once, and every pass runs out
+//    of registers: base-2 exps relative to the thread max (kept, so pass B
+//    rescales instead of recomputing them), then alpha, max(0, p - q) and p;
+//  * the cluster exchanges per-CTA statistics by pushing 16-byte st.async
+//    stores into every peer's shared memory, each completing transaction bytes
+//    on the peer's mbarrier -- no cluster-wide barrier per row.  A second
+//    exchange happens only when a child is rejected; a leaf's bonus draw needs
+//    nothing beyond the first (the per-rank mass of p follows from the
+//    statistics);
+//  * alpha leaves as per-CTA partials, summed in rank order by the walk.
+#pragma once
+
+#include <climits>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace sv {
+namespace pipe {
+namespace {  // internal to each translation unit that instantiates it
+
+constexpr int kCW = 16;                 // consumer warps
+constexpr int kCT = kCW * 32;           // consumer threads
+constexpr int kThreads = kCT;           // thread 0 also issues the bulk copies
+constexpr int kTile = 128;              // elements per warp per tile
+constexpr int kMaxC = 8;
+constexpr int kMaxStages = 4;
+constexpr int kMaxKids = SPEC_MAX_CHILDREN;
+constexpr int kBarCons = 1;             // named barrier id of the consumers
+
+enum QKind { Q_LOGITS = 0, Q_PROBS_T1 = 1, Q_PROBS_T = 2 };
+
+using Params = ::sv::PipeParams;  // slice = kCW * (EPT / 4) * kTile elements
+
+// Per-row record built by row_meta (global memory, stride 16 * (1 + kidcap)
+// bytes) and copied by the producer into shared memory with one bulk copy.
+struct Kid {
+  int node;     // drafted node index (its accept uniform is u(b, node, 0))
+  int tok;      // its token
+  float raw_t;  // target logit at the token
+  float raw_q;  // draft logit / probability at the token
+};
+struct __align__(16) Meta {
+  int qr;   // draft row index within the sequence, or -1
+  int nk;
+  uint32_t bad;
+  int pad;
+  Kid kid[kMaxKids];
+};
+
+// One warp per tree row: draft row, children in index order (parent scan),
+// their tokens and the target / draft logits at those tokens.  Rows are
+// independent, so this runs fully parallel ahead of the streaming kernel.
+template <typename TT, typename TD>
+__global__ void __launch_bounds__(256) row_meta(VerifyShape s, VerifyArgs a, int kidcap,
+                                                int rec_bytes) {
+  const int lane = threadIdx.x & 31;
+  const int64_t unit = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (unit >= s.rows()) return;
+  const int n = s.n, V = s.V;
+  const int b = (int)(unit / (n + 1));
+  const int r = (int)(unit - (int64_t)b * (n + 1));
+  uint32_t bad = 0;
+  int qr = -1;
+  if (s.chain) {
+    qr = (r < n) ? r : -1;
+  } else if (a.q_row) {
+    qr = a.q_row[unit];
+    if (qr < -1 || qr >= s.R) {
+      bad |= SPEC_STATUS_BAD_TREE;
+      qr = -1;
+    }
+  }
+  const TT* trow = reinterpret_cast<const TT*>(a.target) + unit * (int64_t)V;
+  const TD* drow =
+      qr >= 0 ? reinterpret_cast<const TD*>(a.draft) + ((int64_t)b * s.R + qr) * V : nullptr;
+  Meta* rec = reinterpret_cast<Meta*>(a.meta + unit * (int64_t)rec_bytes);
+  auto put = [&](int pos, int node, int tok) {
+    float rt = 0.f, rq = 0.f;
+    if (tok >= 0 && tok < V) {
+      rt = ElemIO<TT>::get(trow, tok);
+      rq = drow ? ElemIO<TD>::get(drow, tok) : 0.f;
+    }
+    rec->kid[pos] = Kid{node, tok, rt, rq};
+  };
+  int cnt = 0;
+  if (s.chain) {
+    if (r < n) {
+      cnt = 1;
+      if (lane == 0) put(0, r, a.node_tokens[(int64_t)b * n + r]);
+    }
+  } else {
+    const int32_t* par = a.parent + (int64_t)b * n;
+    for (int j0 = 0; j0 < n; j0 += 32) {
+      const int j = j0 + lane;
+      const int p = (j < n) ? par[j] : -2;
+      const bool valid = (p >= -1 && p < j);
+      if (j < n && !valid) bad |= SPEC_STATUS_BAD_TREE;
+      const uint32_t m = __ballot_sync(0xffffffffu, j < n && valid && p == r - 1);
+      if (m & (1u << lane)) {
+        const int pos = cnt + __popc(m & ((1u << lane) - 1));
+        if (pos < kidcap) put(pos, j, a.node_tokens[(int64_t)b * n + j]);
+        else bad |= SPEC_STATUS_BAD_TREE;
+      }
+      cnt += __popc(m);
+    }
+    cnt = min(cnt, kidcap);
+  }
+  if (cnt > 0 && qr < 0) {
+    bad |= SPEC_STATUS_BAD_TREE;
+    cnt = 0;
+  }
+  bad = __reduce_or_sync(0xffffffffu, bad);
+  if (lane == 0) {
+    rec->qr = qr;
+    rec->nk = cnt;
+    rec->bad = bad;
+    rec->pad = 0;
+    a.qres[unit] = qr;
+  }
+}
+
+struct Smem {
+  uint64_t full[kMaxStages];
+  uint64_t mfull[2];
+  uint64_t xbar[2];
+  float4 xslot[2][kMaxC];   // incoming per-rank payloads (two in flight)
+  float4 stats[kMaxC];      // per-rank softmax statistics of the current row
+  Meta meta[2];
+  float wred[kCW][4];
+  float wr[kCW], wp[kCW], wx[2][kCW];
+  float rk_r[kMaxC], rkx[2][kMaxC];
+  float4 bc;                // thread 0 -> consumers
+  int ibc[4];
+};
+
+__device__ __forceinline__ float resid_w(float p, float q, float C) {
+  return C == 0.f ? p : fmaxf(0.f, fmaf(-C, q, p));
+}
+
+template <typename T>
+__device__ __forceinline__ T pad_logit();
+template <>
+__device__ __forceinline__ float pad_logit<float>() { return neg_inf(); }
+template <>
+__device__ __forceinline__ uint16_t pad_logit<uint16_t>() { return (uint16_t)0xff80u; }
+
+// Consumer-side exchange: every consumer thread returns with the C payloads
+// of exchange number xq in sm.xslot[xq & 1].  `mine` must already be in
+// sm.bc (written by thread 0 before the call).
+__device__ __forceinline__ void exchange(Smem& sm, int xq, int C, uint32_t rank, int tid,
+                                         uint32_t* status) {
+  const int sl = xq & 1;
+  if (tid == 0) mbar_expect_tx(&sm.xbar[sl], (uint32_t)C * 16u);
+  named_sync(kBarCons, kCT);
+  if (tid < C) {
+    const uint32_t slot = mapa(smem_u32(&sm.xslot[sl][rank]), (uint32_t)tid);
+    const uint32_t bar = mapa(smem_u32(&sm.xbar[sl]), (uint32_t)tid);
+    st_async_v4(slot, sm.bc, bar);
+  }
+  if (!mbar_wait_cluster_bounded(&sm.xbar[sl], (uint32_t)((xq >> 1) & 1)))
+    flag_status(status, SPEC_STATUS_TIMEOUT);
+  // a sender may still be reading sm.bc; nobody rewrites it before this
+  named_sync(kBarCons, kCT);
+}
+
+template <typename TT, typename TD, int QK, int EPT>
+__global__ void __launch_bounds__(kThreads, 1) unit_pipe(Params P) {
+  constexpr int kTPW = EPT / 4;  // tiles per consumer warp
+  extern __shared__ __align__(128) unsigned char dyn[];
+  __shared__ Smem sm;
+  const VerifyShape& s = P.s;
+  const VerifyArgs& a = P.a;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t rank = cluster_ctarank();
+  const int C = (int)cluster_nctarank();
+  const int cid = blockIdx.x / C;
+  const int ncl = P.nclusters;
+  const int n = s.n;
+  const int64_t nunits = s.rows();
+  const int V = s.V;
+  const int slice = P.slice;
+  const int S = P.stages;
+  const int s0 = (int)rank * slice;
+  const int len = max(0, min(slice, V - s0));
+  const size_t tbytes = (size_t)slice * sizeof(TT);
+  const size_t stage_bytes = tbytes + (size_t)slice * sizeof(TD);
+  auto stage_t = [&](int st) { return reinterpret_cast<TT*>(dyn + st * stage_bytes); };
+  auto stage_d = [&](int st) { return reinterpret_cast<TD*>(dyn + st * stage_bytes + tbytes); };
+
+  if (tid == 0) {
+    for (int i = 0; i < S; ++i) mbar_init(&sm.full[i], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sm.mfull[i], 1);
+      mbar_init(&sm.xbar[i], 1);
+    }
+    fence_mbar_init();
+  }
+  // the part of each stage past the row end never changes: pad it once
+  for (int st = 0; st < S; ++st) {
+    TT* tb = stage_t(st);
+    TD* db = stage_d(st);
+    for (int i = len + tid; i < slice; i += kThreads) {
+      tb[i] = pad_logit<TT>();
+      db[i] = (QK == Q_LOGITS) ? pad_logit<TD>() : (TD)0;
+    }
+  }
+  cluster_sync();  // every CTA's barriers exist before the first st.async
+
+  // Thread 0 issues every bulk copy: the slices of a row into a stage (once
+  // all threads have copied the previous row of that stage into registers)
+  // and the row's record into one of two record buffers (once the row two
+  // before it is finished).
+  auto issue_slices = [&](int64_t u, int q, int stg) {
+    const int bb = (int)(u / (n + 1));
+    const TT* trow = reinterpret_cast<const TT*>(a.target) + u * (int64_t)V;
+    const uint32_t tb = (uint32_t)len * sizeof(TT);
+    const uint32_t db = q >= 0 ? (uint32_t)len * sizeof(TD) : 0u;
+    mbar_expect_tx(&sm.full[stg], tb + db);
+    if (tb) bulk_g2s(stage_t(stg), trow + s0, tb, &sm.full[stg]);
+    if (db) {
+      const TD* drow = reinterpret_cast<const TD*>(a.draft) + ((int64_t)bb * s.R + q) * V;
+      bulk_g2s(stage_d(stg), drow + s0, db, &sm.full[stg]);
+    }
+  };
+  auto issue_meta = [&](int64_t u, int buf) {
+    mbar_expect_tx(&sm.mfull[buf], (uint32_t)P.rec_bytes);
+    bulk_g2s(&sm.meta[buf], a.meta + u * (int64_t)P.rec_bytes, (uint32_t)P.rec_bytes,
+             &sm.mfull[buf]);
+  };
+  if (tid == 0) {
+    for (int i = 0; i < S; ++i) {
+      const int64_t u = cid + (int64_t)i * ncl;
+      if (u < nunits) issue_slices(u, a.qres[u], i);
+    }
+    for (int i = 0; i < 2; ++i) {
+      const int64_t u = cid + (int64_t)i * ncl;
+      if (u < nunits) issue_meta(u, i);
+    }
+  }
+  {
+    int xq = 0;
+    for (int it = 0;; ++it) {
+      const int64_t unit = cid + (int64_t)it * ncl;
+      if (unit >= nunits) break;
+      const int st = it % S, mb = it & 1;
+      const int b = (int)(unit / (n + 1));
+      const int r = (int)(unit - (int64_t)b * (n + 1));
+      // the row whose slices refill this stage; its draft row is loaded now
+      const int64_t u_pre = unit + (int64_t)S * ncl;
+      const int q_pre = (tid == 0 && u_pre < nunits) ? a.qres[u_pre] : -1;
+      bool ok = mbar_wait_bounded(&sm.full[st], (uint32_t)((it / S) & 1));
+      ok &= mbar_wait_bounded(&sm.mfull[mb], (uint32_t)((it >> 1) & 1));
+      if (!ok) flag_status(a.status, SPEC_STATUS_TIMEOUT);
+      const Meta& M = sm.meta[mb];
+      const bool has_q = M.qr >= 0;
+      const int nk = M.nk;
+
+      // slice -> registers; release the stage
+      float ep[EPT], eq[EPT];
+      {
+        const TT* tb = stage_t(st);
+        const TD* db = stage_d(st);
+#pragma unroll
+        for (int t = 0; t < kTPW; ++t) {
+          const int e = (warp * kTPW + t) * kTile + lane * 4;
+          ElemIO<TT>::get4(tb + e, &ep[4 * t]);
+          if (has_q) {
+            ElemIO<TD>::get4(db + e, &eq[4 * t]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) eq[4 * t + j] = 0.f;
+          }
+        }
+      }
+      named_sync(kBarCons, kCT);  // every thread has its part of stage st
+      if (tid == 0 && u_pre < nunits) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        issue_slices(u_pre, q_pre, st);
+      }
+
+      // pass A: thread max, then base-2 exps relative to it (kept)
+      float mt = neg_inf();
+#pragma unroll
+      for (int j = 0; j < EPT; ++j) mt = fmaxf(mt, __fmul_rn(ep[j], P.kt));
+      float zt = 0.f;
+#pragma unroll
+      for (int j = 0; j < EPT; ++j) {
+        ep[j] = (mt == neg_inf()) ? 0.f : ex2(fmaf(ep[j], P.kt, -mt));
+        zt += ep[j];
+      }
+      float mq = neg_inf(), zq = 0.f;
+      if (has_q) {
+        if constexpr (QK == Q_PROBS_T1) {
+#pragma unroll
+          for (int j = 0; j < EPT; ++j) zq += eq[j];
+        } else {
+#pragma unroll
+          for (int j = 0; j < EPT; ++j) {
+            const float sq = (QK == Q_LOGITS) ? __fmul_rn(eq[j], P.kt) : __fmul_rn(lg2(eq[j]), P.invT);
+            eq[j] = sq;
+            mq = fmaxf(mq, sq);
+          }
+#pragma unroll
+          for (int j = 0; j < EPT; ++j) {
+            eq[j] = (mq == neg_inf()) ? 0.f : ex2(eq[j] - mq);
+            zq += eq[j];
+          }
+        }
+      }
+      {
+        MaxSum A = warp_ms(MaxSum{mt, zt});
+        MaxSum Bq{mq, zq};
+        float zsum = zq;
+        if (QK == Q_PROBS_T1) zsum = warp_sum(zq);
+        else Bq = warp_ms(Bq);
+        if (lane == 0) {
+          sm.wred[warp][0] = A.m;
+          sm.wred[warp][1] = A.z;
+          sm.wred[warp][2] = (QK == Q_PROBS_T1) ? 0.f : Bq.m;
+          sm.wred[warp][3] = (QK == Q_PROBS_T1) ? zsum : Bq.z;
+        }
+      }
+      named_sync(kBarCons, kCT);
+      if (tid == 0) {
+        MaxSum A{sm.wred[0][0], sm.wred[0][1]}, Bq{sm.wred[0][2], sm.wred[0][3]};
+        float z1 = sm.wred[0][3];
+        for (int w = 1; w < kCW; ++w) {
+          A = ms_combine(A, MaxSum{sm.wred[w][0], sm.wred[w][1]});
+          if (QK == Q_PROBS_T1) z1 += sm.wred[w][3];
+          else Bq = ms_combine(Bq, MaxSum{sm.wred[w][2], sm.wred[w][3]});
+        }
+        sm.bc = make_float4(A.m, A.z, QK == Q_PROBS_T1 ? 0.f : Bq.m, QK == Q_PROBS_T1 ? z1 : Bq.z);
+      }
+      exchange(sm, xq, C, rank, tid, a.status);
+      // global statistics (every consumer thread, same order)
+      float Lp, Lq = 0.f, invZq = 0.f;
+      {
+        const float4* xs = sm.xslot[xq & 1];
+        MaxSum A{neg_inf(), 0.f}, Bq{neg_inf(), 0.f};
+        float z1 = 0.f;
+        for (int k = 0; k < C; ++k) {
+          const float4 v = xs[k];
+          A = ms_combine(A, MaxSum{v.x, v.y});
+          if (QK == Q_PROBS_T1) z1 += v.w;
+          else Bq = ms_combine(Bq, MaxSum{v.z, v.w});
+        }
+        Lp = A.m + log2f(A.z);
+        if (has_q) {
+          if (QK == Q_PROBS_T1) invZq = 1.f / z1;
+          else Lq = Bq.m + log2f(Bq.z);
+        }
+        if (tid < C) sm.stats[tid] = xs[tid];
+        if (tid == 0 && rank == 0) {
+          uint32_t bad = M.bad;
+          if (!(A.z > 0.f) || isnan(A.z)) bad |= SPEC_STATUS_NAN;
+          if (has_q && ((QK == Q_PROBS_T1) ? !(z1 > 0.f) : !(Bq.z > 0.f))) bad |= SPEC_STATUS_NAN;
+          flag_status(a.status, bad);
+        }
+      }
+      ++xq;
+      // pass B: p, q in place; alpha, max(0, p - q) and p per warp
+      {
+        const float sp = (mt == neg_inf()) ? 0.f : ex2(mt - Lp);
+        const float sq = (QK == Q_PROBS_T1) ? invZq : ((mq == neg_inf()) ? 0.f : ex2(mq - Lq));
+        float acc_a = 0.f, acc_r = 0.f, acc_p = 0.f;
+#pragma unroll
+        for (int j = 0; j < EPT; ++j) {
+          const float p = ep[j] * sp;
+          ep[j] = p;
+          acc_p += p;
+          if (has_q) {
+            const float q = eq[j] * sq;
+            eq[j] = q;
+            const float mn = fminf(p, q);
+            acc_a += mn;
+            acc_r += p - mn;
+          }
+        }
+        acc_a = warp_sum(acc_a);
+        acc_r = warp_sum(acc_r);
+        acc_p = warp_sum(acc_p);
+        if (lane == 0) {
+          sm.wred[warp][0] = acc_a;
+          sm.wr[warp] = acc_r;
+          sm.wp[warp] = acc_p;
+        }
+      }
+      named_sync(kBarCons, kCT);
+      float Rcta = 0.f;
+      if (tid == 0) {
+        float A = 0.f;
+        for (int w = 0; w < kCW; ++w) {
+          A += sm.wred[w][0];
+          Rcta += sm.wr[w];
+        }
+        if (has_q) a.alpha_part[unit * kMaxC + rank] = A;
+      }
+
+      // sibling recursion (cluster-uniform control flow)
+      const float negLp = -Lp, negLq = -Lq;
+      float Cc = 0.f, W = 1.f, D = 1.f;
+      int accepted = -1;
+      int src = 0, xb = 0;
+      uint32_t st_bits = 0;
+      for (int k = 0; k < nk; ++k) {
+        if (tid == 0) {
+          const int x = M.kid[k].tok;
+          int dec = 0;
+          if (x < 0 || x >= V) {
+            st_bits |= SPEC_STATUS_TOKEN_RANGE;
+          } else {
+            bool removed = false;
+            for (int i = 0; i < k; ++i) removed |= (M.kid[i].tok == x);
+            const float pv = ex2(fmaf(M.kid[k].raw_t, P.kt, negLp));
+            float qv;
+            if constexpr (QK == Q_LOGITS) qv = ex2(fmaf(M.kid[k].raw_q, P.kt, negLq));
+            else if constexpr (QK == Q_PROBS_T1) qv = __fmul_rn(M.kid[k].raw_q, invZq);
+            else qv = ex2(fmaf(lg2(M.kid[k].raw_q), P.invT, negLq));
+            const float ax = resid_w(pv, qv, Cc);
+            const float qj = removed ? 0.f : qv / D;
+            if (qj == 0.f) {
+              dec = 1;
+              st_bits |= SPEC_STATUS_QZERO_ACCEPT;
+            } else {
+              const float u = philox_uniform(a.prm.seed, a.prm.philox_offset, (uint32_t)b,
+                                             (uint32_t)M.kid[k].node, 0u);
+              dec = (u < (ax / W) / qj) ? 1 : 0;
+            }
+          }
+          sm.ibc[0] = dec;
+          sm.bc.x = Cc + W / D;
+        }
+        named_sync(kBarCons, kCT);
+        const int dec = sm.ibc[0];
+        const float Cn = sm.bc.x;
+        if (dec) {
+          accepted = M.kid[k].node;
+          break;
+        }
+        float Wn = 0.f;
+        int nsrc;
+        named_sync(kBarCons, kCT);  // bc is rewritten below
+        if (Cc == 0.f && Cn == 1.f) {
+          // residual max(0, p - q): per-rank totals by one exchange
+          if (tid == 0) sm.bc = make_float4(Rcta, 0.f, 0.f, 0.f);
+          exchange(sm, xq, C, rank, tid, a.status);
+          if (tid == 0) {
+            for (int i = 0; i < C; ++i) {
+              sm.rk_r[i] = sm.xslot[xq & 1][i].x;
+              Wn += sm.rk_r[i];
+            }
+          }
+          ++xq;
+          nsrc = 1;
+        } else {
+          float acc = 0.f;
+#pragma unroll
+          for (int j = 0; j < EPT; ++j) acc += resid_w(ep[j], eq[j], Cn);
+          acc = warp_sum(acc);
+          if (lane == 0) sm.wx[xb][warp] = acc;
+          named_sync(kBarCons, kCT);
+          if (tid == 0) {
+            float tot = 0.f;
+            for (int i = 0; i < kCW; ++i) tot += sm.wx[xb][i];
+            sm.bc = make_float4(tot, 0.f, 0.f, 0.f);
+          }
+          exchange(sm, xq, C, rank, tid, a.status);
+          if (tid == 0) {
+            for (int i = 0; i < C; ++i) {
+              sm.rkx[xb][i] = sm.xslot[xq & 1][i].x;
+              Wn += sm.rkx[xb][i];
+            }
+          }
+          ++xq;
+          nsrc = 2 + xb;
+        }
+        if (tid == 0) {
+          int upd = 0;
+          if (Wn > 0.f) {
+            Cc = Cn;
+            W = Wn;
+            upd = 1;
+          } else {
+            st_bits |= SPEC_STATUS_RESIDUAL_ZERO;
+          }
+          const int x = M.kid[k].tok;
+          bool removed = false;
+          for (int i = 0; i < k; ++i) removed |= (M.kid[i].tok == x);
+          if (x >= 0 && x < V && !removed) {
+            // q(x) at the point, as in the decision
+            float qv;
+            if constexpr (QK == Q_LOGITS) qv = ex2(fmaf(M.kid[k].raw_q, P.kt, negLq));
+            else if constexpr (QK == Q_PROBS_T1) qv = __fmul_rn(M.kid[k].raw_q, invZq);
+            else qv = ex2(fmaf(lg2(M.kid[k].raw_q), P.invT, negLq));
+            D -= qv;
+          }
+          if (D <= 0.f) st_bits |= SPEC_STATUS_DRAFT_EXHAUSTED;
+          sm.bc = make_float4(Cc, (D <= 0.f) ? 1.f : 0.f, (float)upd, 0.f);
+        }
+        named_sync(kBarCons, kCT);
+        Cc = sm.bc.x;
+        const bool exhausted = sm.bc.y != 0.f;
+        if (sm.bc.z != 0.f) {
+          src = nsrc;
+          if (nsrc >= 2) xb ^= 1;
+        }
+        named_sync(kBarCons, kCT);
+        if (exhausted) break;
+      }
+
+      // draw from p' (leaf: bonus from p) when no child was accepted
+      if (accepted < 0) {
+        if (tid == 0) {
+          float rk[kMaxC];
+          float tot = 0.f;
+          for (int i = 0; i < C; ++i) {
+            if (src == 0) {
+              const float4 v = sm.stats[i];
+              rk[i] = (v.y > 0.f) ? v.y * ex2(v.x - Lp) : 0.f;
+            } else {
+              rk[i] = (src == 1) ? sm.rk_r[i] : sm.rkx[src - 2][i];
+            }
+            tot += rk[i];
+          }
+          const float u =
+              philox_uniform(a.prm.seed, a.prm.philox_offset, (uint32_t)b, (uint32_t)r, 1u);
+          float t = u * tot;
+          int sel = -1;
+          float pre = 0.f;
+          for (int i = 0; i < C; ++i) {
+            if (rk[i] > 0.f && pre + rk[i] > t) {
+              sel = i;
+              break;
+            }
+            pre += rk[i];
+          }
+          if (sel < 0) {
+            for (int i = C - 1; i >= 0; --i)
+              if (rk[i] > 0.f) {
+                sel = i;
+                break;
+              }
+            pre = 0.f;
+            for (int i = 0; i < sel; ++i) pre += rk[i];
+            t = 3.0e38f;
+          }
+          const float* wt = src == 0 ? sm.wp : (src == 1 ? sm.wr : sm.wx[src - 2]);
+          int wsel = -1;
+          float wpre = 0.f;
+          const float tt = t - pre;
+          if (sel == (int)rank) {
+            for (int i = 0; i < kCW; ++i) {
+              if (wt[i] > 0.f && wpre + wt[i] > tt) {
+                wsel = i;
+                break;
+              }
+              wpre += wt[i];
+            }
+            if (wsel < 0) {
+              for (int i = kCW - 1; i >= 0; --i)
+                if (wt[i] > 0.f) {
+                  wsel = i;
+                  break;
+                }
+              wpre = 0.f;
+              for (int i = 0; i < wsel; ++i) wpre += wt[i];
+            }
+          }
+          sm.ibc[1] = sel;
+          sm.ibc[2] = wsel;
+          sm.bc.w = tt - wpre;
+          if (sel < 0) {
+            st_bits |= SPEC_STATUS_CDF_FALLBACK;
+            if (rank == 0) a.row_token[unit] = 0;
+          }
+        }
+        named_sync(kBarCons, kCT);
+        const int sel = sm.ibc[1], wsel = sm.ibc[2];
+        if (sel == (int)rank && warp == wsel && wsel >= 0) {
+          const float thr = sm.bc.w;
+          float run = 0.f;
+          int found = -1, lastpos = -1;
+#pragma unroll
+          for (int t = 0; t < kTPW; ++t) {
+            if (found < 0) {
+              const int e = (warp * kTPW + t) * kTile + lane * 4;
+              float wv[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) wv[j] = resid_w(ep[4 * t + j], eq[4 * t + j], Cc);
+              const float ls = (wv[0] + wv[1]) + (wv[2] + wv[3]);
+              float inc = ls;
+#pragma unroll
+              for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, inc, o);
+                if (lane >= o) inc += y;
+              }
+              const uint32_t cross = __ballot_sync(0xffffffffu, ls > 0.f && run + inc > thr);
+              const uint32_t pos = __ballot_sync(0xffffffffu, ls > 0.f);
+              if (pos) {
+                const int hl = 31 - __clz(pos);
+                int lp = -1;
+                if (lane == hl) {
+#pragma unroll
+                  for (int j = 3; j >= 0; --j)
+                    if (lp < 0 && wv[j] > 0.f) lp = e + j;
+                }
+                lastpos = __shfl_sync(0xffffffffu, lp, hl);
+              }
+              if (cross) {
+                const int fl = __ffs(cross) - 1;
+                int tok = -1;
+                if (lane == fl) {
+                  float c = run + inc - ls;
+                  int last = -1;
+#pragma unroll
+                  for (int j = 0; j < 4; ++j) {
+                    if (tok < 0) {
+                      if (wv[j] > 0.f) last = e + j;
+                      c += wv[j];
+                      if (wv[j] > 0.f && c > thr) tok = e + j;
+                    }
+                  }
+                  if (tok < 0) tok = last;
+                }
+                found = __shfl_sync(0xffffffffu, tok, fl);
+              }
+              run += __shfl_sync(0xffffffffu, inc, 31);
+            }
+          }
+          if (lane == 0) {
+            int tok = found;
+            if (tok < 0) {
+              tok = lastpos;
+              flag_status(a.status, SPEC_STATUS_CDF_FALLBACK);
+            }
+            a.row_token[unit] = (tok < 0) ? 0 : s0 + tok;
+          }
+        }
+      }
+      if (tid == 0) {
+        if (rank == 0) a.row_child[unit] = accepted;
+        if (st_bits && rank == 0) flag_status(a.status, st_bits);
+      }
+      named_sync(kBarCons, kCT);  // meta[mb] and the broadcasts are free again
+      if (tid == 0) {
+        const int64_t u_meta = unit + 2 * (int64_t)ncl;
+        if (u_meta < nunits) {
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          issue_meta(u_meta, mb);
+        }
+      }
+    }
+  }
+  cluster_sync();  // no CTA leaves while a peer may still push to it
+}
+
+// Walk every sequence along accepted children; reduce alpha partials.
+__global__ void pipe_walk(VerifyShape s, VerifyArgs a, int C) {
+  const int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (row >= s.rows()) return;
+  const int n = s.n;
+  const int b = (int)(row / (n + 1));
+  const int r = (int)(row - (int64_t)b * (n + 1));
+  bool has_q;
+  if (s.chain) {
+    has_q = r < n;
+  } else {
+    const int q = a.q_row ? a.q_row[row] : -1;
+    has_q = q >= 0 && q < s.R;
+  }
+  float m = __int_as_float(0x7fc00000);
+  if (has_q) {
+    m = 0.f;
+    for (int k = 0; k < C; ++k) m += a.alpha_part[row * kMaxC + k];
+  }
+  if (s.chain) {
+    if (r < n) a.mass[(int64_t)b * n + r] = m;
+  } else {
+    a.mass[row] = m;
+  }
+  if (r != 0) return;
+  const int64_t row0 = row;
+  int32_t* out = a.out_tokens + row0;
+  int rr = 0, len = 0;
+  while (true) {
+    const int j = a.row_child[row0 + rr];
+    if (j < 0 || j >= n || len >= n) break;
+    if (!s.chain) a.path_nodes[(int64_t)b * n + len] = j;
+    out[len] = a.node_tokens[(int64_t)b * n + j];
+    ++len;
+    rr = j + 1;
+  }
+  out[len] = a.row_token[row0 + rr];
+  for (int k = len + 1; k <= n; ++k) out[k] = -1;
+  if (!s.chain)
+    for (int k = len; k < n; ++k) a.path_nodes[(int64_t)b * n + k] = -1;
+  a.count[b] = len;
+}
+
+// Geometry: cluster size C, elements per consumer thread EPT and stages for
+// a row of V logits; false when the pipelined kernel does not apply.
+inline bool geometry(int V, int tsz, int dsz, int* C, int* ept, int* stages, int* slice) {
+  const int eptc[3] = {8, 16, 32};
+  for (int c = 1; c <= kMaxC; c *= 2) {
+    for (int e : eptc) {
+      const int sl = kCT * e;  // kCW warps * (e / 4) tiles * 128 elements
+      if ((int64_t)c * sl < V) continue;
+      const int64_t stage = (int64_t)sl * (tsz + dsz);
+      const int ns = (int)((200 * 1024) / stage);
+      if (ns < 2) break;
+      *C = c;
+      *ept = e;
+      *stages = ns < kMaxStages ? ns : kMaxStages;
+      *slice = sl;
+      return true;
+    }
+  }
+  return false;
+}
+
+template <typename TT, typename TD, int QK, int EPT>
+cudaError_t launch_pipe_t(Params P, int C, cudaStream_t st) {
+  auto kern = unit_pipe<TT, TD, QK, EPT>;
+  const size_t dyn = (size_t)P.stages * P.slice * (sizeof(TT) + sizeof(TD));
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = dyn;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int maxc = 0;
+  cfg.gridDim = dim3(C);
+  e = cudaOccupancyMaxActiveClusters(&maxc, kern, &cfg);
+  if (e != cudaSuccess) return e;
+  if (maxc < 1) return cudaErrorInvalidConfiguration;
+  const int64_t units = P.s.rows();
+  P.nclusters = (int)(units < maxc ? units : maxc);
+  row_meta<TT, TD><<<(unsigned)((units + 7) / 8), 256, 0, st>>>(P.s, P.a, P.kidcap, P.rec_bytes);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  cfg.gridDim = dim3((unsigned)(P.nclusters * C));
+  return cudaLaunchKernelEx(&cfg, kern, P);
+}
+
+template <typename TT, typename TD>
+cudaError_t launch_pipe_dt(const Params& P, int C, int ept, int qk, cudaStream_t st) {
+#define SV_PIPE_EPT(QK)                                                   \
+  if (ept == 8) return launch_pipe_t<TT, TD, QK, 8>(P, C, st);            \
+  if (ept == 16) return launch_pipe_t<TT, TD, QK, 16>(P, C, st);          \
+  return launch_pipe_t<TT, TD, QK, 32>(P, C, st);
+  if (qk == Q_LOGITS) { SV_PIPE_EPT(Q_LOGITS) }
+  if (qk == Q_PROBS_T1) { SV_PIPE_EPT(Q_PROBS_T1) }
+  SV_PIPE_EPT(Q_PROBS_T)
+#undef SV_PIPE_EPT
+}
+
+}  // namespace
+}  // namespace pipe
+}  // namespace sv
