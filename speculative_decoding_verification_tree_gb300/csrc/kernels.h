@@ -53,10 +53,13 @@ struct VerifyArgs {
   int32_t* qres;        // [rows] resolved draft row per tree row (-1 none)
 };
 
-// Per-row record of the pipelined kernel: a 16-byte header and 16 bytes per
-// child slot (one slot for a chain, SPEC_MAX_CHILDREN for a tree).
+// Per-row record of the pipelined kernel: a 16-byte header, 16 bytes per
+// child slot and 4 bytes of accept uniform per slot, padded to 16 bytes (one
+// slot for a chain, SPEC_MAX_CHILDREN for a tree).
 inline int meta_kidcap(bool chain) { return chain ? 1 : SPEC_MAX_CHILDREN; }
-inline int meta_rec_bytes(bool chain) { return 16 * (1 + meta_kidcap(chain)); }
+inline int meta_rec_bytes(bool chain) {
+  return (16 + 20 * meta_kidcap(chain) + 15) / 16 * 16;
+}
 
 // Per-row slots of alpha partials (one per CTA of a cluster of up to 8).
 constexpr int kAlphaSlots = 8;

@@ -40,7 +40,7 @@ constexpr size_t kStatusBytes = 256;
 constexpr size_t kRowBytes = (size_t)SPEC_NOALLOC_MAX_ROWS * sizeof(int32_t);
 constexpr size_t kPartBytes = (size_t)SPEC_NOALLOC_MAX_PARTS * sizeof(ArgPart);
 constexpr size_t kAlphaBytes = (size_t)SPEC_NOALLOC_MAX_ROWS * kAlphaSlots * sizeof(float);
-constexpr size_t kMetaBytes = (size_t)SPEC_NOALLOC_MAX_ROWS * 32;  // chain row records
+constexpr size_t kMetaBytes = (size_t)SPEC_NOALLOC_MAX_ROWS * 48;  // chain row records
 constexpr size_t kScratchBytes =
     kStatusBytes + 3 * kRowBytes + kPartBytes + kAlphaBytes + kMetaBytes;
 
@@ -122,7 +122,7 @@ extern "C" int spec_verify_chain_noalloc(const void* target_logits, const void* 
   a.alpha_part = (float*)(p + kStatusBytes + 2 * kRowBytes + kPartBytes);
   a.meta = (unsigned char*)(p + kStatusBytes + 2 * kRowBytes + kPartBytes + kAlphaBytes);
   a.qres = (int32_t*)(p + kStatusBytes + 2 * kRowBytes + kPartBytes + kAlphaBytes + kMetaBytes);
-  static_assert(32 == 16 * (1 + 1), "chain row record size");
+  if (meta_rec_bytes(true) != 48) return SPEC_ERR_CUDA;  // chain row record size
   // the status word must start at zero; everything else is written before it
   // is read within the call
   if (cudaMemsetAsync(a.status, 0, sizeof(uint32_t), st) != cudaSuccess) return SPEC_ERR_CUDA;

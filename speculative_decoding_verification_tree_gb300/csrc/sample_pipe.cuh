@@ -4,24 +4,26 @@
 // Same method as unit_full in sample_full.cu (accept test u < p'(x)/q'(x),
 // residual max(0, p - C q), inverse-CDF draw in vocabulary order), organised
 // for HBM streaming on GB300:
+//  * row_meta (a small kernel ahead of it) writes one record per row: draft
+//    row, children in index order with their tokens, the target / draft
+//    logits at those tokens, and the row's Philox uniforms -- so the
+//    streaming kernel issues no dependent global loads and no Philox rounds;
 //  * persistent thread-block clusters, one 512-thread CTA per SM; each CTA of
 //    a cluster owns one contiguous vocabulary slice of every row the cluster
-//    verifies;
-//  * row_meta (a small kernel ahead of it) writes one record per row: draft
-//    row, children in index order, their tokens and the target / draft logits
-//    at those tokens, so the streaming kernel does no dependent global loads;
-//  * thread 0 keeps S shared-memory stages in flight with TMA bulk copies of
-//    the next rows' target / draft slices, and the next rows' records;
+//    verifies; thread 0 keeps S shared-memory stages in flight with TMA bulk
+//    copies of the next rows' slices and records;
 //  * all 16 warps copy a landed slice into registers (up to 32 logits of each
 //    row per thread), the stage is refilled at once, and every pass runs out
 //    of registers: base-2 exps relative to the thread max (kept, so pass B
 //    rescales instead of recomputing them), then alpha, max(0, p - q) and p;
-//  * the cluster exchanges per-CTA statistics by pushing 16-byte st.async
-//    stores into every peer's shared memory, each completing transaction bytes
-//    on the peer's mbarrier -- no cluster-wide barrier per row.  A second
-//    exchange happens only when a child is rejected; a leaf's bonus draw needs
-//    nothing beyond the first (the per-rank mass of p follows from the
-//    statistics);
+//  * CTA reductions are warp-0 shuffle trees; cluster statistics travel as
+//    16-byte st.async stores from warp 0's registers into every peer's shared
+//    memory, completing transaction bytes on the peer's mbarrier, and every
+//    warp combines the received statistics itself (same shuffle order in all
+//    CTAs) -- no cluster barrier and no extra CTA barrier per exchange;
+//  * a second exchange happens only after a rejected child; a leaf's bonus
+//    draw needs nothing beyond the first (the per-rank mass of p follows from
+//    the statistics);
 //  * alpha leaves as per-CTA partials, summed in rank order by the walk.
 #pragma once
 
@@ -34,38 +36,40 @@ namespace sv {
 namespace pipe {
 namespace {  // internal to each translation unit that instantiates it
 
-constexpr int kCW = 16;                 // consumer warps
-constexpr int kCT = kCW * 32;           // consumer threads
-constexpr int kThreads = kCT;           // thread 0 also issues the bulk copies
+constexpr int kCW = 16;                 // warps
+constexpr int kCT = kCW * 32;           // threads
+constexpr int kThreads = kCT;
 constexpr int kTile = 128;              // elements per warp per tile
 constexpr int kMaxC = 8;
 constexpr int kMaxStages = 4;
 constexpr int kMaxKids = SPEC_MAX_CHILDREN;
-constexpr int kBarCons = 1;             // named barrier id of the consumers
+constexpr int kBar = 1;                 // named barrier id
 
 enum QKind { Q_LOGITS = 0, Q_PROBS_T1 = 1, Q_PROBS_T = 2 };
 
 using Params = ::sv::PipeParams;  // slice = kCW * (EPT / 4) * kTile elements
 
-// Per-row record built by row_meta (global memory, stride 16 * (1 + kidcap)
-// bytes) and copied by the producer into shared memory with one bulk copy.
+// Per-row record built by row_meta.  Global layout (stride rec_bytes):
+// header, kid[kidcap], then kidcap floats of accept uniforms.  It is copied
+// byte for byte to the start of a shared-memory Meta, so the uniforms of a
+// record with kidcap slots start at &kid[kidcap].
 struct Kid {
-  int node;     // drafted node index (its accept uniform is u(b, node, 0))
+  int node;     // drafted node index
   int tok;      // its token
   float raw_t;  // target logit at the token
   float raw_q;  // draft logit / probability at the token
 };
 struct __align__(16) Meta {
-  int qr;   // draft row index within the sequence, or -1
-  int nk;
-  uint32_t bad;
-  int pad;
+  int qr;          // draft row index within the sequence, or -1
+  int nk;          // children (capped at kidcap)
+  uint32_t bad;    // status bits found while building the record
+  float u_draw;    // u(b, r, 1): the row's replacement / bonus draw
   Kid kid[kMaxKids];
+  float uspace[kMaxKids];
 };
 
-// One warp per tree row: draft row, children in index order (parent scan),
-// their tokens and the target / draft logits at those tokens.  Rows are
-// independent, so this runs fully parallel ahead of the streaming kernel.
+static_assert(sizeof(Meta) == 16 + 20 * kMaxKids, "record layout");
+
 template <typename TT, typename TD>
 __global__ void __launch_bounds__(256) row_meta(VerifyShape s, VerifyArgs a, int kidcap,
                                                 int rec_bytes) {
@@ -89,14 +93,17 @@ __global__ void __launch_bounds__(256) row_meta(VerifyShape s, VerifyArgs a, int
   const TT* trow = reinterpret_cast<const TT*>(a.target) + unit * (int64_t)V;
   const TD* drow =
       qr >= 0 ? reinterpret_cast<const TD*>(a.draft) + ((int64_t)b * s.R + qr) * V : nullptr;
-  Meta* rec = reinterpret_cast<Meta*>(a.meta + unit * (int64_t)rec_bytes);
+  unsigned char* recb = a.meta + unit * (int64_t)rec_bytes;
+  Kid* kids = reinterpret_cast<Kid*>(recb + 16);
+  float* ukid = reinterpret_cast<float*>(recb + 16 + 16 * kidcap);
   auto put = [&](int pos, int node, int tok) {
     float rt = 0.f, rq = 0.f;
     if (tok >= 0 && tok < V) {
       rt = ElemIO<TT>::get(trow, tok);
       rq = drow ? ElemIO<TD>::get(drow, tok) : 0.f;
     }
-    rec->kid[pos] = Kid{node, tok, rt, rq};
+    kids[pos] = Kid{node, tok, rt, rq};
+    ukid[pos] = philox_uniform(a.prm.seed, a.prm.philox_offset, (uint32_t)b, (uint32_t)node, 0u);
   };
   int cnt = 0;
   if (s.chain) {
@@ -127,10 +134,11 @@ __global__ void __launch_bounds__(256) row_meta(VerifyShape s, VerifyArgs a, int
   }
   bad = __reduce_or_sync(0xffffffffu, bad);
   if (lane == 0) {
-    rec->qr = qr;
-    rec->nk = cnt;
-    rec->bad = bad;
-    rec->pad = 0;
+    Meta* h = reinterpret_cast<Meta*>(recb);
+    h->qr = qr;
+    h->nk = cnt;
+    h->bad = bad;
+    h->u_draw = philox_uniform(a.prm.seed, a.prm.philox_offset, (uint32_t)b, (uint32_t)r, 1u);
     a.qres[unit] = qr;
   }
 }
@@ -140,13 +148,13 @@ struct Smem {
   uint64_t mfull[2];
   uint64_t xbar[2];
   float4 xslot[2][kMaxC];   // incoming per-rank payloads (two in flight)
-  float4 stats[kMaxC];      // per-rank softmax statistics of the current row
   Meta meta[2];
-  float wred[kCW][4];
+  float4 wred[kCW];         // per-warp partials
   float wr[kCW], wp[kCW], wx[2][kCW];
-  float rk_r[kMaxC], rkx[2][kMaxC];
-  float4 bc;                // thread 0 -> consumers
+  float rk_p[kMaxC], rk_r[kMaxC], rkx[2][kMaxC];
+  float4 bc;                // warp 0 -> all
   int ibc[4];
+  int qring[4];             // draft rows of upcoming refills (index & 3)
 };
 
 __device__ __forceinline__ float resid_w(float p, float q, float C) {
@@ -160,28 +168,31 @@ __device__ __forceinline__ float pad_logit<float>() { return neg_inf(); }
 template <>
 __device__ __forceinline__ uint16_t pad_logit<uint16_t>() { return (uint16_t)0xff80u; }
 
-// Consumer-side exchange: every consumer thread returns with the C payloads
-// of exchange number xq in sm.xslot[xq & 1].  `mine` must already be in
-// sm.bc (written by thread 0 before the call).
-__device__ __forceinline__ void exchange(Smem& sm, int xq, int C, uint32_t rank, int tid,
-                                         uint32_t* status) {
+// Warp-wide sum with a fixed tree (identical in every warp and CTA).
+__device__ __forceinline__ float tree_sum(float v) { return warp_sum(v); }
+
+// Exchange number xq: lanes 0..C-1 of warp 0 push `mine` to every CTA of the
+// cluster (lane k -> CTA k); every thread then waits for the C payloads of
+// this exchange in sm.xslot[xq & 1].  Only warp 0 may call with real data;
+// the other warps only wait.
+__device__ __forceinline__ void exchange(Smem& sm, int xq, int C, uint32_t rank, int warp,
+                                         int lane, float4 mine, uint32_t* status) {
   const int sl = xq & 1;
-  if (tid == 0) mbar_expect_tx(&sm.xbar[sl], (uint32_t)C * 16u);
-  named_sync(kBarCons, kCT);
-  if (tid < C) {
-    const uint32_t slot = mapa(smem_u32(&sm.xslot[sl][rank]), (uint32_t)tid);
-    const uint32_t bar = mapa(smem_u32(&sm.xbar[sl]), (uint32_t)tid);
-    st_async_v4(slot, sm.bc, bar);
+  if (warp == 0) {
+    if (lane == 0) mbar_expect_tx(&sm.xbar[sl], (uint32_t)C * 16u);
+    if (lane < C) {
+      const uint32_t slot = mapa(smem_u32(&sm.xslot[sl][rank]), (uint32_t)lane);
+      const uint32_t bar = mapa(smem_u32(&sm.xbar[sl]), (uint32_t)lane);
+      st_async_v4(slot, mine, bar);
+    }
   }
   if (!mbar_wait_cluster_bounded(&sm.xbar[sl], (uint32_t)((xq >> 1) & 1)))
     flag_status(status, SPEC_STATUS_TIMEOUT);
-  // a sender may still be reading sm.bc; nobody rewrites it before this
-  named_sync(kBarCons, kCT);
 }
 
 template <typename TT, typename TD, int QK, int EPT>
 __global__ void __launch_bounds__(kThreads, 1) unit_pipe(Params P) {
-  constexpr int kTPW = EPT / 4;  // tiles per consumer warp
+  constexpr int kTPW = EPT / 4;  // tiles per warp
   extern __shared__ __align__(128) unsigned char dyn[];
   __shared__ Smem sm;
   const VerifyShape& s = P.s;
@@ -222,10 +233,6 @@ __global__ void __launch_bounds__(kThreads, 1) unit_pipe(Params P) {
   }
   cluster_sync();  // every CTA's barriers exist before the first st.async
 
-  // Thread 0 issues every bulk copy: the slices of a row into a stage (once
-  // all threads have copied the previous row of that stage into registers)
-  // and the row's record into one of two record buffers (once the row two
-  // before it is finished).
   auto issue_slices = [&](int64_t u, int q, int stg) {
     const int bb = (int)(u / (n + 1));
     const TT* trow = reinterpret_cast<const TT*>(a.target) + u * (int64_t)V;
@@ -243,6 +250,13 @@ __global__ void __launch_bounds__(kThreads, 1) unit_pipe(Params P) {
     bulk_g2s(&sm.meta[buf], a.meta + u * (int64_t)P.rec_bytes, (uint32_t)P.rec_bytes,
              &sm.mfull[buf]);
   };
+  // draft row of loop index j (-1 past the end); loop index j refills its
+  // stage at iteration j - S, reading qring[j & 3], which iteration j - S - 2
+  // loaded (two rows of latency hidden)
+  auto q_of_index = [&](int j) -> int {
+    const int64_t u = cid + (int64_t)j * ncl;
+    return (u < nunits) ? a.qres[u] : -1;
+  };
   if (tid == 0) {
     for (int i = 0; i < S; ++i) {
       const int64_t u = cid + (int64_t)i * ncl;
@@ -251,337 +265,372 @@ __global__ void __launch_bounds__(kThreads, 1) unit_pipe(Params P) {
     for (int i = 0; i < 2; ++i) {
       const int64_t u = cid + (int64_t)i * ncl;
       if (u < nunits) issue_meta(u, i);
+      sm.qring[(S + i) & 3] = q_of_index(S + i);
     }
   }
-  {
-    int xq = 0;
-    for (int it = 0;; ++it) {
-      const int64_t unit = cid + (int64_t)it * ncl;
-      if (unit >= nunits) break;
-      const int st = it % S, mb = it & 1;
-      const int b = (int)(unit / (n + 1));
-      const int r = (int)(unit - (int64_t)b * (n + 1));
-      // the row whose slices refill this stage; its draft row is loaded now
-      const int64_t u_pre = unit + (int64_t)S * ncl;
-      const int q_pre = (tid == 0 && u_pre < nunits) ? a.qres[u_pre] : -1;
-      bool ok = mbar_wait_bounded(&sm.full[st], (uint32_t)((it / S) & 1));
-      ok &= mbar_wait_bounded(&sm.mfull[mb], (uint32_t)((it >> 1) & 1));
-      if (!ok) flag_status(a.status, SPEC_STATUS_TIMEOUT);
-      const Meta& M = sm.meta[mb];
-      const bool has_q = M.qr >= 0;
-      const int nk = M.nk;
 
-      // slice -> registers; release the stage
-      float ep[EPT], eq[EPT];
-      {
-        const TT* tb = stage_t(st);
-        const TD* db = stage_d(st);
-#pragma unroll
-        for (int t = 0; t < kTPW; ++t) {
-          const int e = (warp * kTPW + t) * kTile + lane * 4;
-          ElemIO<TT>::get4(tb + e, &ep[4 * t]);
-          if (has_q) {
-            ElemIO<TD>::get4(db + e, &eq[4 * t]);
-          } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) eq[4 * t + j] = 0.f;
-          }
-        }
-      }
-      named_sync(kBarCons, kCT);  // every thread has its part of stage st
-      if (tid == 0 && u_pre < nunits) {
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        issue_slices(u_pre, q_pre, st);
-      }
+  int xq = 0;
+  for (int it = 0;; ++it) {
+    const int64_t unit = cid + (int64_t)it * ncl;
+    if (unit >= nunits) break;
+    const int st = it % S, mb = it & 1;
+    // the row whose slices refill this stage (its draft row was loaded two
+    // iterations ago); start loading the draft row needed two iterations on
+    const int64_t u_pre = unit + (int64_t)S * ncl;
+    const int q_later = (tid == 0) ? q_of_index(it + S + 2) : -1;
+    bool ok = mbar_wait_bounded(&sm.full[st], (uint32_t)((it / S) & 1));
+    ok &= mbar_wait_bounded(&sm.mfull[mb], (uint32_t)((it >> 1) & 1));
+    if (!ok) flag_status(a.status, SPEC_STATUS_TIMEOUT);
+    const Meta& M = sm.meta[mb];
+    const bool has_q = M.qr >= 0;
+    const int nk = M.nk;
 
-      // pass A: thread max, then base-2 exps relative to it (kept)
-      float mt = neg_inf();
+    // slice -> registers
+    float ep[EPT], eq[EPT];
+    {
+      const TT* tb = stage_t(st);
+      const TD* db = stage_d(st);
 #pragma unroll
-      for (int j = 0; j < EPT; ++j) mt = fmaxf(mt, __fmul_rn(ep[j], P.kt));
-      float zt = 0.f;
-#pragma unroll
-      for (int j = 0; j < EPT; ++j) {
-        ep[j] = (mt == neg_inf()) ? 0.f : ex2(fmaf(ep[j], P.kt, -mt));
-        zt += ep[j];
-      }
-      float mq = neg_inf(), zq = 0.f;
-      if (has_q) {
-        if constexpr (QK == Q_PROBS_T1) {
-#pragma unroll
-          for (int j = 0; j < EPT; ++j) zq += eq[j];
+      for (int t = 0; t < kTPW; ++t) {
+        const int e = (warp * kTPW + t) * kTile + lane * 4;
+        ElemIO<TT>::get4(tb + e, &ep[4 * t]);
+        if (has_q) {
+          ElemIO<TD>::get4(db + e, &eq[4 * t]);
         } else {
 #pragma unroll
-          for (int j = 0; j < EPT; ++j) {
-            const float sq = (QK == Q_LOGITS) ? __fmul_rn(eq[j], P.kt) : __fmul_rn(lg2(eq[j]), P.invT);
-            eq[j] = sq;
-            mq = fmaxf(mq, sq);
-          }
+          for (int j = 0; j < 4; ++j) eq[4 * t + j] = 0.f;
+        }
+      }
+    }
+
+    // pass A: thread max, then base-2 exps relative to it (kept)
+    float mt = neg_inf();
 #pragma unroll
-          for (int j = 0; j < EPT; ++j) {
-            eq[j] = (mq == neg_inf()) ? 0.f : ex2(eq[j] - mq);
-            zq += eq[j];
+    for (int j = 0; j < EPT; ++j) mt = fmaxf(mt, __fmul_rn(ep[j], P.kt));
+    float zt = 0.f;
+#pragma unroll
+    for (int j = 0; j < EPT; ++j) {
+      ep[j] = (mt == neg_inf()) ? 0.f : ex2(fmaf(ep[j], P.kt, -mt));
+      zt += ep[j];
+    }
+    float mq = neg_inf(), zq = 0.f;
+    if (has_q) {
+      if constexpr (QK == Q_PROBS_T1) {
+#pragma unroll
+        for (int j = 0; j < EPT; ++j) zq += eq[j];
+      } else {
+#pragma unroll
+        for (int j = 0; j < EPT; ++j) {
+          const float sq = (QK == Q_LOGITS) ? __fmul_rn(eq[j], P.kt) : __fmul_rn(lg2(eq[j]), P.invT);
+          eq[j] = sq;
+          mq = fmaxf(mq, sq);
+        }
+#pragma unroll
+        for (int j = 0; j < EPT; ++j) {
+          eq[j] = (mq == neg_inf()) ? 0.f : ex2(eq[j] - mq);
+          zq += eq[j];
+        }
+      }
+    }
+    {
+      const MaxSum A = warp_ms(MaxSum{mt, zt});
+      float m2 = 0.f, z2;
+      if (QK == Q_PROBS_T1) {
+        z2 = warp_sum(zq);
+      } else {
+        const MaxSum Bq = warp_ms(MaxSum{mq, zq});
+        m2 = Bq.m;
+        z2 = Bq.z;
+      }
+      if (lane == 0) sm.wred[warp] = make_float4(A.m, A.z, m2, z2);
+    }
+    named_sync(kBar, kCT);  // partials ready; every thread is done with stage st
+    if (tid == 0 && u_pre < nunits) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      issue_slices(u_pre, sm.qring[(it + S) & 3], st);
+    }
+    // CTA statistics (warp 0, 16-lane tree) -> exchange 1
+    {
+      float4 mine = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (warp == 0) {
+        const float4 v = (lane < kCW) ? sm.wred[lane] : make_float4(neg_inf(), 0.f, neg_inf(), 0.f);
+        MaxSum A{v.x, v.y}, Bq{v.z, v.w};
+        float z1 = (lane < kCW) ? v.w : 0.f;
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) {
+          A = ms_combine(A, MaxSum{__shfl_xor_sync(0xffffffffu, A.m, o),
+                                   __shfl_xor_sync(0xffffffffu, A.z, o)});
+          if (QK == Q_PROBS_T1) {
+            z1 += __shfl_xor_sync(0xffffffffu, z1, o);
+          } else {
+            Bq = ms_combine(Bq, MaxSum{__shfl_xor_sync(0xffffffffu, Bq.m, o),
+                                       __shfl_xor_sync(0xffffffffu, Bq.z, o)});
           }
         }
+        A.m = __shfl_sync(0xffffffffu, A.m, 0);
+        A.z = __shfl_sync(0xffffffffu, A.z, 0);
+        z1 = __shfl_sync(0xffffffffu, z1, 0);
+        Bq.m = __shfl_sync(0xffffffffu, Bq.m, 0);
+        Bq.z = __shfl_sync(0xffffffffu, Bq.z, 0);
+        mine = make_float4(A.m, A.z, QK == Q_PROBS_T1 ? 0.f : Bq.m, QK == Q_PROBS_T1 ? z1 : Bq.z);
       }
-      {
-        MaxSum A = warp_ms(MaxSum{mt, zt});
-        MaxSum Bq{mq, zq};
-        float zsum = zq;
-        if (QK == Q_PROBS_T1) zsum = warp_sum(zq);
-        else Bq = warp_ms(Bq);
-        if (lane == 0) {
-          sm.wred[warp][0] = A.m;
-          sm.wred[warp][1] = A.z;
-          sm.wred[warp][2] = (QK == Q_PROBS_T1) ? 0.f : Bq.m;
-          sm.wred[warp][3] = (QK == Q_PROBS_T1) ? zsum : Bq.z;
-        }
-      }
-      named_sync(kBarCons, kCT);
-      if (tid == 0) {
-        MaxSum A{sm.wred[0][0], sm.wred[0][1]}, Bq{sm.wred[0][2], sm.wred[0][3]};
-        float z1 = sm.wred[0][3];
-        for (int w = 1; w < kCW; ++w) {
-          A = ms_combine(A, MaxSum{sm.wred[w][0], sm.wred[w][1]});
-          if (QK == Q_PROBS_T1) z1 += sm.wred[w][3];
-          else Bq = ms_combine(Bq, MaxSum{sm.wred[w][2], sm.wred[w][3]});
-        }
-        sm.bc = make_float4(A.m, A.z, QK == Q_PROBS_T1 ? 0.f : Bq.m, QK == Q_PROBS_T1 ? z1 : Bq.z);
-      }
-      exchange(sm, xq, C, rank, tid, a.status);
-      // global statistics (every consumer thread, same order)
-      float Lp, Lq = 0.f, invZq = 0.f;
-      {
-        const float4* xs = sm.xslot[xq & 1];
-        MaxSum A{neg_inf(), 0.f}, Bq{neg_inf(), 0.f};
-        float z1 = 0.f;
-        for (int k = 0; k < C; ++k) {
-          const float4 v = xs[k];
-          A = ms_combine(A, MaxSum{v.x, v.y});
-          if (QK == Q_PROBS_T1) z1 += v.w;
-          else Bq = ms_combine(Bq, MaxSum{v.z, v.w});
-        }
-        Lp = A.m + log2f(A.z);
-        if (has_q) {
-          if (QK == Q_PROBS_T1) invZq = 1.f / z1;
-          else Lq = Bq.m + log2f(Bq.z);
-        }
-        if (tid < C) sm.stats[tid] = xs[tid];
-        if (tid == 0 && rank == 0) {
-          uint32_t bad = M.bad;
-          if (!(A.z > 0.f) || isnan(A.z)) bad |= SPEC_STATUS_NAN;
-          if (has_q && ((QK == Q_PROBS_T1) ? !(z1 > 0.f) : !(Bq.z > 0.f))) bad |= SPEC_STATUS_NAN;
-          flag_status(a.status, bad);
+      exchange(sm, xq, C, rank, warp, lane, mine, a.status);
+    }
+    // cluster statistics: every warp combines the C payloads (8-lane tree)
+    float Lp, Lq = 0.f, invZq = 0.f, zq_tot = 0.f, zp_tot;
+    {
+      const float4* xs = sm.xslot[xq & 1];
+      const float4 v = (lane < C) ? xs[lane] : make_float4(neg_inf(), 0.f, neg_inf(), 0.f);
+      MaxSum A{v.x, v.y}, Bq{v.z, v.w};
+      float z1 = (lane < C) ? v.w : 0.f;
+#pragma unroll
+      for (int o = 4; o > 0; o >>= 1) {
+        A = ms_combine(A, MaxSum{__shfl_xor_sync(0xffffffffu, A.m, o),
+                                 __shfl_xor_sync(0xffffffffu, A.z, o)});
+        if (QK == Q_PROBS_T1) {
+          z1 += __shfl_xor_sync(0xffffffffu, z1, o);
+        } else {
+          Bq = ms_combine(Bq, MaxSum{__shfl_xor_sync(0xffffffffu, Bq.m, o),
+                                     __shfl_xor_sync(0xffffffffu, Bq.z, o)});
         }
       }
-      ++xq;
-      // pass B: p, q in place; alpha, max(0, p - q) and p per warp
-      {
-        const float sp = (mt == neg_inf()) ? 0.f : ex2(mt - Lp);
-        const float sq = (QK == Q_PROBS_T1) ? invZq : ((mq == neg_inf()) ? 0.f : ex2(mq - Lq));
-        float acc_a = 0.f, acc_r = 0.f, acc_p = 0.f;
+      A.m = __shfl_sync(0xffffffffu, A.m, 0);
+      A.z = __shfl_sync(0xffffffffu, A.z, 0);
+      z1 = __shfl_sync(0xffffffffu, z1, 0);
+      Bq.m = __shfl_sync(0xffffffffu, Bq.m, 0);
+      Bq.z = __shfl_sync(0xffffffffu, Bq.z, 0);
+      Lp = A.m + log2f(A.z);
+      zp_tot = A.z;
+      if (has_q) {
+        if (QK == Q_PROBS_T1) {
+          invZq = 1.f / z1;
+          zq_tot = z1;
+        } else {
+          Lq = Bq.m + log2f(Bq.z);
+          zq_tot = Bq.z;
+        }
+      }
+      // per-rank mass of p (bonus draw) from the statistics
+      if (warp == 0 && lane < C) sm.rk_p[lane] = (v.y > 0.f) ? v.y * ex2(v.x - Lp) : 0.f;
+    }
+    ++xq;
+
+    // pass B: p, q in place; alpha, max(0, p - q) and p per warp
+    {
+      const float sp = (mt == neg_inf()) ? 0.f : ex2(mt - Lp);
+      const float sq = (QK == Q_PROBS_T1) ? invZq : ((mq == neg_inf()) ? 0.f : ex2(mq - Lq));
+      // sum of p: only a row without children draws from p (bonus); the
+      // rare zero-residual fallback of a row with children recomputes it
+      float acc_a = 0.f, acc_r = 0.f, acc_p = 0.f;
+      if (has_q) {
 #pragma unroll
         for (int j = 0; j < EPT; ++j) {
           const float p = ep[j] * sp;
+          const float q = eq[j] * sq;
           ep[j] = p;
-          acc_p += p;
-          if (has_q) {
-            const float q = eq[j] * sq;
-            eq[j] = q;
-            const float mn = fminf(p, q);
-            acc_a += mn;
-            acc_r += p - mn;
-          }
+          eq[j] = q;
+          const float mn = fminf(p, q);
+          acc_a += mn;
+          acc_r += p - mn;
         }
-        acc_a = warp_sum(acc_a);
-        acc_r = warp_sum(acc_r);
-        acc_p = warp_sum(acc_p);
-        if (lane == 0) {
-          sm.wred[warp][0] = acc_a;
-          sm.wr[warp] = acc_r;
-          sm.wp[warp] = acc_p;
-        }
-      }
-      named_sync(kBarCons, kCT);
-      float Rcta = 0.f;
-      if (tid == 0) {
-        float A = 0.f;
-        for (int w = 0; w < kCW; ++w) {
-          A += sm.wred[w][0];
-          Rcta += sm.wr[w];
-        }
-        if (has_q) a.alpha_part[unit * kMaxC + rank] = A;
-      }
-
-      // sibling recursion (cluster-uniform control flow)
-      const float negLp = -Lp, negLq = -Lq;
-      float Cc = 0.f, W = 1.f, D = 1.f;
-      int accepted = -1;
-      int src = 0, xb = 0;
-      uint32_t st_bits = 0;
-      for (int k = 0; k < nk; ++k) {
-        if (tid == 0) {
-          const int x = M.kid[k].tok;
-          int dec = 0;
-          if (x < 0 || x >= V) {
-            st_bits |= SPEC_STATUS_TOKEN_RANGE;
-          } else {
-            bool removed = false;
-            for (int i = 0; i < k; ++i) removed |= (M.kid[i].tok == x);
-            const float pv = ex2(fmaf(M.kid[k].raw_t, P.kt, negLp));
-            float qv;
-            if constexpr (QK == Q_LOGITS) qv = ex2(fmaf(M.kid[k].raw_q, P.kt, negLq));
-            else if constexpr (QK == Q_PROBS_T1) qv = __fmul_rn(M.kid[k].raw_q, invZq);
-            else qv = ex2(fmaf(lg2(M.kid[k].raw_q), P.invT, negLq));
-            const float ax = resid_w(pv, qv, Cc);
-            const float qj = removed ? 0.f : qv / D;
-            if (qj == 0.f) {
-              dec = 1;
-              st_bits |= SPEC_STATUS_QZERO_ACCEPT;
-            } else {
-              const float u = philox_uniform(a.prm.seed, a.prm.philox_offset, (uint32_t)b,
-                                             (uint32_t)M.kid[k].node, 0u);
-              dec = (u < (ax / W) / qj) ? 1 : 0;
-            }
-          }
-          sm.ibc[0] = dec;
-          sm.bc.x = Cc + W / D;
-        }
-        named_sync(kBarCons, kCT);
-        const int dec = sm.ibc[0];
-        const float Cn = sm.bc.x;
-        if (dec) {
-          accepted = M.kid[k].node;
-          break;
-        }
-        float Wn = 0.f;
-        int nsrc;
-        named_sync(kBarCons, kCT);  // bc is rewritten below
-        if (Cc == 0.f && Cn == 1.f) {
-          // residual max(0, p - q): per-rank totals by one exchange
-          if (tid == 0) sm.bc = make_float4(Rcta, 0.f, 0.f, 0.f);
-          exchange(sm, xq, C, rank, tid, a.status);
-          if (tid == 0) {
-            for (int i = 0; i < C; ++i) {
-              sm.rk_r[i] = sm.xslot[xq & 1][i].x;
-              Wn += sm.rk_r[i];
-            }
-          }
-          ++xq;
-          nsrc = 1;
-        } else {
-          float acc = 0.f;
+        if (nk == 0) {
 #pragma unroll
-          for (int j = 0; j < EPT; ++j) acc += resid_w(ep[j], eq[j], Cn);
-          acc = warp_sum(acc);
-          if (lane == 0) sm.wx[xb][warp] = acc;
-          named_sync(kBarCons, kCT);
-          if (tid == 0) {
-            float tot = 0.f;
-            for (int i = 0; i < kCW; ++i) tot += sm.wx[xb][i];
-            sm.bc = make_float4(tot, 0.f, 0.f, 0.f);
-          }
-          exchange(sm, xq, C, rank, tid, a.status);
-          if (tid == 0) {
-            for (int i = 0; i < C; ++i) {
-              sm.rkx[xb][i] = sm.xslot[xq & 1][i].x;
-              Wn += sm.rkx[xb][i];
-            }
-          }
-          ++xq;
-          nsrc = 2 + xb;
+          for (int j = 0; j < EPT; ++j) acc_p += ep[j];
         }
-        if (tid == 0) {
-          int upd = 0;
-          if (Wn > 0.f) {
-            Cc = Cn;
-            W = Wn;
-            upd = 1;
-          } else {
-            st_bits |= SPEC_STATUS_RESIDUAL_ZERO;
-          }
-          const int x = M.kid[k].tok;
+      } else {
+#pragma unroll
+        for (int j = 0; j < EPT; ++j) {
+          ep[j] *= sp;
+          acc_p += ep[j];
+        }
+      }
+      acc_a = warp_sum(acc_a);
+      acc_r = warp_sum(acc_r);
+      acc_p = warp_sum(acc_p);
+      if (lane == 0) {
+        sm.wred[warp].x = acc_a;
+        sm.wr[warp] = acc_r;
+        sm.wp[warp] = acc_p;
+      }
+    }
+    named_sync(kBar, kCT);
+    const float negLp = -Lp, negLq = -Lq;
+    auto q_point = [&](float raw) -> float {
+      if constexpr (QK == Q_LOGITS) return ex2(fmaf(raw, P.kt, negLq));
+      else if constexpr (QK == Q_PROBS_T1) return __fmul_rn(raw, invZq);
+      else return ex2(fmaf(lg2(raw), P.invT, negLq));
+    };
+    // warp 0: alpha partial, CTA residual mass, first child's decision
+    float Rcta = 0.f;
+    if (warp == 0) {
+      float va = (lane < kCW) ? sm.wred[lane].x : 0.f;
+      float vr = (lane < kCW) ? sm.wr[lane] : 0.f;
+      va = warp_sum(va);
+      vr = warp_sum(vr);
+      Rcta = vr;
+      if (lane == 0) {
+        if (has_q) a.alpha_part[unit * kMaxC + rank] = va;
+        if (rank == 0) {
+          uint32_t bad = M.bad;
+          if (!(zp_tot > 0.f) || isnan(zp_tot)) bad |= SPEC_STATUS_NAN;
+          if (has_q && !(zq_tot > 0.f)) bad |= SPEC_STATUS_NAN;
+          flag_status(a.status, bad);
+        }
+      }
+    }
+
+    // sibling recursion (cluster-uniform control flow); decisions by lane 0
+    // of warp 0 from the record's point logits and uniforms
+    const float* ukid = reinterpret_cast<const float*>(&M.kid[P.kidcap]);
+    float Cc = 0.f, W = 1.f, D = 1.f;
+    int accepted = -1;
+    int src = 0, xb = 0;
+    uint32_t st_bits = 0;
+    for (int k = 0; k < nk; ++k) {
+      if (tid == 0) {
+        const int x = M.kid[k].tok;
+        int dec = 0;
+        if (x < 0 || x >= V) {
+          st_bits |= SPEC_STATUS_TOKEN_RANGE;
+        } else {
           bool removed = false;
           for (int i = 0; i < k; ++i) removed |= (M.kid[i].tok == x);
-          if (x >= 0 && x < V && !removed) {
-            // q(x) at the point, as in the decision
-            float qv;
-            if constexpr (QK == Q_LOGITS) qv = ex2(fmaf(M.kid[k].raw_q, P.kt, negLq));
-            else if constexpr (QK == Q_PROBS_T1) qv = __fmul_rn(M.kid[k].raw_q, invZq);
-            else qv = ex2(fmaf(lg2(M.kid[k].raw_q), P.invT, negLq));
-            D -= qv;
+          const float pv = ex2(fmaf(M.kid[k].raw_t, P.kt, negLp));
+          const float qv = q_point(M.kid[k].raw_q);
+          const float ax = resid_w(pv, qv, Cc);
+          const float qj = removed ? 0.f : qv / D;
+          if (qj == 0.f) {
+            dec = 1;
+            st_bits |= SPEC_STATUS_QZERO_ACCEPT;
+          } else {
+            dec = (ukid[k] < (ax / W) / qj) ? 1 : 0;
           }
-          if (D <= 0.f) st_bits |= SPEC_STATUS_DRAFT_EXHAUSTED;
-          sm.bc = make_float4(Cc, (D <= 0.f) ? 1.f : 0.f, (float)upd, 0.f);
         }
-        named_sync(kBarCons, kCT);
-        Cc = sm.bc.x;
-        const bool exhausted = sm.bc.y != 0.f;
-        if (sm.bc.z != 0.f) {
-          src = nsrc;
-          if (nsrc >= 2) xb ^= 1;
-        }
-        named_sync(kBarCons, kCT);
-        if (exhausted) break;
+        sm.ibc[0] = dec;
+        sm.bc.x = Cc + W / D;
       }
-
-      // draw from p' (leaf: bonus from p) when no child was accepted
-      if (accepted < 0) {
+      named_sync(kBar, kCT);
+      const int dec = sm.ibc[0];
+      const float Cn = sm.bc.x;
+      if (dec) {
+        accepted = M.kid[k].node;
+        break;
+      }
+      float Wn = 0.f;
+      int nsrc;
+      if (Cc == 0.f && Cn == 1.f) {
+        // residual max(0, p - q): per-rank totals by one exchange
+        exchange(sm, xq, C, rank, warp, lane, make_float4(Rcta, 0.f, 0.f, 0.f), a.status);
         if (tid == 0) {
-          float rk[kMaxC];
-          float tot = 0.f;
           for (int i = 0; i < C; ++i) {
-            if (src == 0) {
-              const float4 v = sm.stats[i];
-              rk[i] = (v.y > 0.f) ? v.y * ex2(v.x - Lp) : 0.f;
-            } else {
-              rk[i] = (src == 1) ? sm.rk_r[i] : sm.rkx[src - 2][i];
-            }
-            tot += rk[i];
+            sm.rk_r[i] = sm.xslot[xq & 1][i].x;
+            Wn += sm.rk_r[i];
           }
-          const float u =
-              philox_uniform(a.prm.seed, a.prm.philox_offset, (uint32_t)b, (uint32_t)r, 1u);
-          float t = u * tot;
-          int sel = -1;
-          float pre = 0.f;
+        }
+        ++xq;
+        nsrc = 1;
+      } else {
+        float acc = 0.f;
+#pragma unroll
+        for (int j = 0; j < EPT; ++j) acc += resid_w(ep[j], eq[j], Cn);
+        acc = warp_sum(acc);
+        if (lane == 0) sm.wx[xb][warp] = acc;
+        named_sync(kBar, kCT);
+        float tot = 0.f;
+        if (warp == 0) tot = warp_sum((lane < kCW) ? sm.wx[xb][lane] : 0.f);
+        exchange(sm, xq, C, rank, warp, lane, make_float4(tot, 0.f, 0.f, 0.f), a.status);
+        if (tid == 0) {
           for (int i = 0; i < C; ++i) {
-            if (rk[i] > 0.f && pre + rk[i] > t) {
-              sel = i;
-              break;
-            }
-            pre += rk[i];
+            sm.rkx[xb][i] = sm.xslot[xq & 1][i].x;
+            Wn += sm.rkx[xb][i];
           }
-          if (sel < 0) {
-            for (int i = C - 1; i >= 0; --i)
-              if (rk[i] > 0.f) {
-                sel = i;
-                break;
-              }
-            pre = 0.f;
-            for (int i = 0; i < sel; ++i) pre += rk[i];
-            t = 3.0e38f;
-          }
+        }
+        ++xq;
+        nsrc = 2 + xb;
+      }
+      if (tid == 0) {
+        int upd = 0;
+        if (Wn > 0.f) {
+          Cc = Cn;
+          W = Wn;
+          upd = 1;
+        } else {
+          st_bits |= SPEC_STATUS_RESIDUAL_ZERO;
+        }
+        const int x = M.kid[k].tok;
+        bool removed = false;
+        for (int i = 0; i < k; ++i) removed |= (M.kid[i].tok == x);
+        if (x >= 0 && x < V && !removed) D -= q_point(M.kid[k].raw_q);
+        if (D <= 0.f) st_bits |= SPEC_STATUS_DRAFT_EXHAUSTED;
+        sm.bc = make_float4(Cc, (D <= 0.f) ? 1.f : 0.f, (float)upd, 0.f);
+      }
+      named_sync(kBar, kCT);
+      Cc = sm.bc.x;
+      const bool exhausted = sm.bc.y != 0.f;
+      if (sm.bc.z != 0.f) {
+        src = nsrc;
+        if (nsrc >= 2) xb ^= 1;
+      }
+      named_sync(kBar, kCT);
+      if (exhausted) break;
+    }
+
+    // draw from p' (leaf: bonus from p) when no child was accepted
+    if (accepted < 0) {
+      if (src == 0 && nk > 0) {  // fallback to p in a row with children
+        float acc = 0.f;
+#pragma unroll
+        for (int j = 0; j < EPT; ++j) acc += ep[j];
+        acc = warp_sum(acc);
+        if (lane == 0) sm.wp[warp] = acc;
+        named_sync(kBar, kCT);
+      }
+      if (warp == 0) {
+        // rank: first with running total above t (8-lane inclusive scan)
+        const float rkv = (lane < C) ? (src == 0 ? sm.rk_p[lane]
+                                                 : (src == 1 ? sm.rk_r[lane] : sm.rkx[src - 2][lane]))
+                                     : 0.f;
+        float inc = rkv;
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+          const float y = __shfl_up_sync(0xffffffffu, inc, o);
+          if (lane >= o) inc += y;
+        }
+        const float tot = __shfl_sync(0xffffffffu, inc, 7);
+        float t = M.u_draw * tot;
+        uint32_t cr = __ballot_sync(0xffffffffu, lane < C && rkv > 0.f && inc > t);
+        int sel;
+        if (cr) {
+          sel = __ffs(cr) - 1;
+        } else {  // rounding: last rank with mass, no crossing inside it
+          const uint32_t pos = __ballot_sync(0xffffffffu, lane < C && rkv > 0.f);
+          sel = pos ? 31 - __clz(pos) : -1;
+          t = 3.0e38f;
+        }
+        const float pre = (sel >= 0) ? __shfl_sync(0xffffffffu, inc - rkv, sel & 31) : 0.f;
+        const float tt = t - pre;
+        // warp inside the selected CTA (16-lane scan over the per-warp sums)
+        int wsel = -1;
+        float wpre = 0.f;
+        if (sel == (int)rank) {
           const float* wt = src == 0 ? sm.wp : (src == 1 ? sm.wr : sm.wx[src - 2]);
-          int wsel = -1;
-          float wpre = 0.f;
-          const float tt = t - pre;
-          if (sel == (int)rank) {
-            for (int i = 0; i < kCW; ++i) {
-              if (wt[i] > 0.f && wpre + wt[i] > tt) {
-                wsel = i;
-                break;
-              }
-              wpre += wt[i];
-            }
-            if (wsel < 0) {
-              for (int i = kCW - 1; i >= 0; --i)
-                if (wt[i] > 0.f) {
-                  wsel = i;
-                  break;
-                }
-              wpre = 0.f;
-              for (int i = 0; i < wsel; ++i) wpre += wt[i];
-            }
+          const float wv = (lane < kCW) ? wt[lane] : 0.f;
+          float winc = wv;
+#pragma unroll
+          for (int o = 1; o < 16; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, winc, o);
+            if (lane >= o) winc += y;
           }
+          uint32_t wc = __ballot_sync(0xffffffffu, lane < kCW && wv > 0.f && winc > tt);
+          if (wc) {
+            wsel = __ffs(wc) - 1;
+          } else {
+            const uint32_t wp2 = __ballot_sync(0xffffffffu, lane < kCW && wv > 0.f);
+            wsel = wp2 ? 31 - __clz(wp2) : -1;
+          }
+          wpre = (wsel >= 0) ? __shfl_sync(0xffffffffu, winc - wv, wsel & 31) : 0.f;
+        }
+        if (lane == 0) {
           sm.ibc[1] = sel;
           sm.ibc[2] = wsel;
           sm.bc.w = tt - wpre;
@@ -590,80 +639,83 @@ __global__ void __launch_bounds__(kThreads, 1) unit_pipe(Params P) {
             if (rank == 0) a.row_token[unit] = 0;
           }
         }
-        named_sync(kBarCons, kCT);
-        const int sel = sm.ibc[1], wsel = sm.ibc[2];
-        if (sel == (int)rank && warp == wsel && wsel >= 0) {
-          const float thr = sm.bc.w;
-          float run = 0.f;
-          int found = -1, lastpos = -1;
+      }
+      named_sync(kBar, kCT);
+      const int sel = sm.ibc[1], wsel = sm.ibc[2];
+      if (sel == (int)rank && warp == wsel && wsel >= 0) {
+        const float thr = sm.bc.w;
+        float run = 0.f;
+        int found = -1, lastpos = -1;
 #pragma unroll
-          for (int t = 0; t < kTPW; ++t) {
-            if (found < 0) {
-              const int e = (warp * kTPW + t) * kTile + lane * 4;
-              float wv[4];
+        for (int t = 0; t < kTPW; ++t) {
+          if (found < 0) {
+            const int e = (warp * kTPW + t) * kTile + lane * 4;
+            float wv[4];
 #pragma unroll
-              for (int j = 0; j < 4; ++j) wv[j] = resid_w(ep[4 * t + j], eq[4 * t + j], Cc);
-              const float ls = (wv[0] + wv[1]) + (wv[2] + wv[3]);
-              float inc = ls;
+            for (int j = 0; j < 4; ++j) wv[j] = resid_w(ep[4 * t + j], eq[4 * t + j], Cc);
+            const float ls = (wv[0] + wv[1]) + (wv[2] + wv[3]);
+            float inc = ls;
 #pragma unroll
-              for (int o = 1; o < 32; o <<= 1) {
-                const float y = __shfl_up_sync(0xffffffffu, inc, o);
-                if (lane >= o) inc += y;
+            for (int o = 1; o < 32; o <<= 1) {
+              const float y = __shfl_up_sync(0xffffffffu, inc, o);
+              if (lane >= o) inc += y;
+            }
+            const uint32_t cross = __ballot_sync(0xffffffffu, ls > 0.f && run + inc > thr);
+            const uint32_t pos = __ballot_sync(0xffffffffu, ls > 0.f);
+            if (pos) {
+              const int hl = 31 - __clz(pos);
+              int lp = -1;
+              if (lane == hl) {
+#pragma unroll
+                for (int j = 3; j >= 0; --j)
+                  if (lp < 0 && wv[j] > 0.f) lp = e + j;
               }
-              const uint32_t cross = __ballot_sync(0xffffffffu, ls > 0.f && run + inc > thr);
-              const uint32_t pos = __ballot_sync(0xffffffffu, ls > 0.f);
-              if (pos) {
-                const int hl = 31 - __clz(pos);
-                int lp = -1;
-                if (lane == hl) {
+              lastpos = __shfl_sync(0xffffffffu, lp, hl);
+            }
+            if (cross) {
+              const int fl = __ffs(cross) - 1;
+              int tok = -1;
+              if (lane == fl) {
+                float c = run + inc - ls;
+                int last = -1;
 #pragma unroll
-                  for (int j = 3; j >= 0; --j)
-                    if (lp < 0 && wv[j] > 0.f) lp = e + j;
-                }
-                lastpos = __shfl_sync(0xffffffffu, lp, hl);
-              }
-              if (cross) {
-                const int fl = __ffs(cross) - 1;
-                int tok = -1;
-                if (lane == fl) {
-                  float c = run + inc - ls;
-                  int last = -1;
-#pragma unroll
-                  for (int j = 0; j < 4; ++j) {
-                    if (tok < 0) {
-                      if (wv[j] > 0.f) last = e + j;
-                      c += wv[j];
-                      if (wv[j] > 0.f && c > thr) tok = e + j;
-                    }
+                for (int j = 0; j < 4; ++j) {
+                  if (tok < 0) {
+                    if (wv[j] > 0.f) last = e + j;
+                    c += wv[j];
+                    if (wv[j] > 0.f && c > thr) tok = e + j;
                   }
-                  if (tok < 0) tok = last;
                 }
-                found = __shfl_sync(0xffffffffu, tok, fl);
+                if (tok < 0) tok = last;
               }
-              run += __shfl_sync(0xffffffffu, inc, 31);
+              found = __shfl_sync(0xffffffffu, tok, fl);
             }
-          }
-          if (lane == 0) {
-            int tok = found;
-            if (tok < 0) {
-              tok = lastpos;
-              flag_status(a.status, SPEC_STATUS_CDF_FALLBACK);
-            }
-            a.row_token[unit] = (tok < 0) ? 0 : s0 + tok;
+            run += __shfl_sync(0xffffffffu, inc, 31);
           }
         }
-      }
-      if (tid == 0) {
-        if (rank == 0) a.row_child[unit] = accepted;
-        if (st_bits && rank == 0) flag_status(a.status, st_bits);
-      }
-      named_sync(kBarCons, kCT);  // meta[mb] and the broadcasts are free again
-      if (tid == 0) {
-        const int64_t u_meta = unit + 2 * (int64_t)ncl;
-        if (u_meta < nunits) {
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          issue_meta(u_meta, mb);
+        if (lane == 0) {
+          int tok = found;
+          if (tok < 0) {
+            tok = lastpos;
+            flag_status(a.status, SPEC_STATUS_CDF_FALLBACK);
+          }
+          a.row_token[unit] = (tok < 0) ? 0 : s0 + tok;
         }
+      }
+    }
+    if (tid == 0) {
+      if (rank == 0) {
+        a.row_child[unit] = accepted;
+        if (st_bits) flag_status(a.status, st_bits);
+      }
+    }
+    named_sync(kBar, kCT);  // meta[mb] and the broadcasts are free again
+    if (tid == 0) {
+      sm.qring[(it + S + 2) & 3] = q_later;
+      const int64_t u_meta = unit + 2 * (int64_t)ncl;
+      if (u_meta < nunits) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        issue_meta(u_meta, mb);
       }
     }
   }
@@ -713,8 +765,8 @@ __global__ void pipe_walk(VerifyShape s, VerifyArgs a, int C) {
   a.count[b] = len;
 }
 
-// Geometry: cluster size C, elements per consumer thread EPT and stages for
-// a row of V logits; false when the pipelined kernel does not apply.
+// Geometry: cluster size C, elements per thread EPT and stages for a row of
+// V logits; false when the pipelined kernel does not apply.
 inline bool geometry(int V, int tsz, int dsz, int* C, int* ept, int* stages, int* slice) {
   const int eptc[3] = {8, 16, 32};
   for (int c = 1; c <= kMaxC; c *= 2) {
