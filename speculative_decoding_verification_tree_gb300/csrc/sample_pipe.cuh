@@ -10,8 +10,9 @@
 //    streaming kernel issues no dependent global loads and no Philox rounds;
 //  * persistent thread-block clusters, one 512-thread CTA per SM; each CTA of
 //    a cluster owns one contiguous vocabulary slice of every row the cluster
-//    verifies; thread 0 keeps S shared-memory stages in flight with TMA bulk
-//    copies of the next rows' slices and records;
+//    verifies; one loader thread keeps S shared-memory stages in flight with
+//    TMA bulk copies of the next rows' slices and records, issued while its
+//    warp waits for a cluster exchange anyway;
 //  * all 16 warps copy a landed slice into registers (up to 32 logits of each
 //    row per thread), the stage is refilled at once, and every pass runs out
 //    of registers: base-2 exps relative to the thread max (kept, so pass B
@@ -145,16 +146,16 @@ __global__ void __launch_bounds__(256) row_meta(VerifyShape s, VerifyArgs a, int
 
 struct Smem {
   uint64_t full[kMaxStages];
-  uint64_t mfull[2];
+  uint64_t mfull[3];
   uint64_t xbar[2];
   float4 xslot[2][kMaxC];   // incoming per-rank payloads (two in flight)
-  Meta meta[2];
+  Meta meta[3];
   float4 wred[kCW];         // per-warp partials
   float wr[kCW], wp[kCW], wx[2][kCW];
   float rk_p[kMaxC], rk_r[kMaxC], rkx[2][kMaxC];
   float4 bc;                // warp 0 -> all
   int ibc[4];
-  int qring[4];             // draft rows of upcoming refills (index & 3)
+  int qring[4];             // draft rows of upcoming refills (loop index & 3)
 };
 
 __device__ __forceinline__ float resid_w(float p, float q, float C) {
@@ -216,8 +217,8 @@ __global__ void __launch_bounds__(kThreads, 1) unit_pipe(Params P) {
 
   if (tid == 0) {
     for (int i = 0; i < S; ++i) mbar_init(&sm.full[i], 1);
+    for (int i = 0; i < 3; ++i) mbar_init(&sm.mfull[i], 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&sm.mfull[i], 1);
       mbar_init(&sm.xbar[i], 1);
     }
     fence_mbar_init();
@@ -250,14 +251,18 @@ __global__ void __launch_bounds__(kThreads, 1) unit_pipe(Params P) {
     bulk_g2s(&sm.meta[buf], a.meta + u * (int64_t)P.rec_bytes, (uint32_t)P.rec_bytes,
              &sm.mfull[buf]);
   };
-  // draft row of loop index j (-1 past the end); loop index j refills its
-  // stage at iteration j - S, reading qring[j & 3], which iteration j - S - 2
-  // loaded (two rows of latency hidden)
+  // The loader thread (lane 0 of the last warp) issues every bulk copy, and
+  // does so while its warp waits for the first cluster exchange of a row, so
+  // no warp ever waits behind a copy being issued.  Row j's slices refill
+  // stage j % S (freed when row j - S was copied into registers); its record
+  // goes to buffer j % 3 (freed when row j - 3 finished).  The draft row of
+  // row j is loaded two rows before it is needed (qring).
   auto q_of_index = [&](int j) -> int {
     const int64_t u = cid + (int64_t)j * ncl;
     return (u < nunits) ? a.qres[u] : -1;
   };
-  if (tid == 0) {
+  const bool ldr = (tid == kCT - 32);
+  if (ldr) {
     for (int i = 0; i < S; ++i) {
       const int64_t u = cid + (int64_t)i * ncl;
       if (u < nunits) issue_slices(u, a.qres[u], i);
@@ -273,13 +278,12 @@ __global__ void __launch_bounds__(kThreads, 1) unit_pipe(Params P) {
   for (int it = 0;; ++it) {
     const int64_t unit = cid + (int64_t)it * ncl;
     if (unit >= nunits) break;
-    const int st = it % S, mb = it & 1;
-    // the row whose slices refill this stage (its draft row was loaded two
-    // iterations ago); start loading the draft row needed two iterations on
-    const int64_t u_pre = unit + (int64_t)S * ncl;
-    const int q_later = (tid == 0) ? q_of_index(it + S + 2) : -1;
+    const int st = it % S, mb = it % 3;
+    const int64_t u_pre = unit + (int64_t)S * ncl;  // refills stage st
+    const int64_t u_meta = unit + 2 * (int64_t)ncl;  // record into (it + 2) % 3
+    const int q_later = ldr ? q_of_index(it + S + 2) : -1;
     bool ok = mbar_wait_bounded(&sm.full[st], (uint32_t)((it / S) & 1));
-    ok &= mbar_wait_bounded(&sm.mfull[mb], (uint32_t)((it >> 1) & 1));
+    ok &= mbar_wait_bounded(&sm.mfull[mb], (uint32_t)((it / 3) & 1));
     if (!ok) flag_status(a.status, SPEC_STATUS_TIMEOUT);
     const Meta& M = sm.meta[mb];
     const bool has_q = M.qr >= 0;
@@ -345,9 +349,11 @@ __global__ void __launch_bounds__(kThreads, 1) unit_pipe(Params P) {
       if (lane == 0) sm.wred[warp] = make_float4(A.m, A.z, m2, z2);
     }
     named_sync(kBar, kCT);  // partials ready; every thread is done with stage st
-    if (tid == 0 && u_pre < nunits) {
+    if (ldr) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      issue_slices(u_pre, sm.qring[(it + S) & 3], st);
+      if (u_pre < nunits) issue_slices(u_pre, sm.qring[(it + S) & 3], st);
+      if (u_meta < nunits) issue_meta(u_meta, (it + 2) % 3);
+      sm.qring[(it + S + 2) & 3] = q_later;
     }
     // CTA statistics (warp 0, 16-lane tree) -> exchange 1
     {
@@ -709,15 +715,7 @@ __global__ void __launch_bounds__(kThreads, 1) unit_pipe(Params P) {
         if (st_bits) flag_status(a.status, st_bits);
       }
     }
-    named_sync(kBar, kCT);  // meta[mb] and the broadcasts are free again
-    if (tid == 0) {
-      sm.qring[(it + S + 2) & 3] = q_later;
-      const int64_t u_meta = unit + 2 * (int64_t)ncl;
-      if (u_meta < nunits) {
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        issue_meta(u_meta, mb);
-      }
-    }
+    named_sync(kBar, kCT);  // the broadcasts are free again
   }
   cluster_sync();  // no CTA leaves while a peer may still push to it
 }
