@@ -67,7 +67,7 @@ extern "C" {
 
 /* ---- limits ---- */
 #define SPEC_MAX_VOCAB (1 << 24)  /* V                                     */
-#define SPEC_MAX_TOP_K 1024       /* top_k when top-k / top-p is used      */
+#define SPEC_MAX_TOP_K 128        /* tokens a truncating transform keeps   */
 #define SPEC_MAX_CHILDREN 64      /* children of one tree node             */
 #define SPEC_MAX_TREE_NODES 1024  /* N (tree) and K (chain)                */
 #define SPEC_EAGLE2_MAX_TOPK 32   /* children per expanded EAGLE-2 node    */
@@ -92,8 +92,10 @@ extern "C" {
 /* Sampling parameters (plain data, 32 bytes). */
 typedef struct spec_params {
   float temperature;      /* > 0: sampling rule; == 0: greedy argmax rule  */
-  int32_t top_k;          /* 0 = off; else 1 .. SPEC_MAX_TOP_K             */
-  float top_p;            /* in (0, 1]; 1 = off.  Needs 1 <= top_k         */
+  int32_t top_k;          /* 0 = off; keeps min(top_k, V) tokens           */
+  float top_p;            /* in (0, 1]; 1 = off                            */
+  /* With top-k or top-p the kept set min(top_k, V) (V when top_k = 0) must
+     hold at most SPEC_MAX_TOP_K tokens, else SPEC_ERR_UNSUPPORTED. */
   int32_t draft_kind;     /* SPEC_DRAFT_LOGITS or SPEC_DRAFT_PROBS         */
   uint64_t seed;          /* Philox key                                    */
   uint32_t philox_offset; /* fourth Philox counter word                    */

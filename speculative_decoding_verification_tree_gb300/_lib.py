@@ -27,7 +27,7 @@ SPEC_DRAFT_LOGITS = 0
 SPEC_DRAFT_PROBS = 1
 
 SPEC_MAX_VOCAB = 1 << 24
-SPEC_MAX_TOP_K = 1024
+SPEC_MAX_TOP_K = 128
 SPEC_MAX_CHILDREN = 64
 SPEC_MAX_TREE_NODES = 1024
 SPEC_EAGLE2_MAX_TOPK = 32

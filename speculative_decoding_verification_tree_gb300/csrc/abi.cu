@@ -15,7 +15,8 @@ inline size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 // Workspace of a verification call: [status | row_child | row_token | argmax parts]
 struct VerifyWs {
-  size_t off_child, off_token, off_parts, off_alpha, off_meta, off_qres, total;
+  size_t off_child, off_token, off_parts, off_alpha, off_meta, off_qres;
+  size_t off_tidx, off_tval, off_tcnt, total;
 };
 VerifyWs verify_ws(int B, int n, int V, bool chain) {
   const size_t rows = (size_t)B * (n + 1);
@@ -26,7 +27,10 @@ VerifyWs verify_ws(int B, int n, int V, bool chain) {
   w.off_alpha = w.off_parts + up(rows * (size_t)arg_splits(V) * sizeof(ArgPart));
   w.off_meta = w.off_alpha + up(rows * kAlphaSlots * sizeof(float));
   w.off_qres = w.off_meta + up(rows * (size_t)meta_rec_bytes(chain));
-  w.total = w.off_qres + up(rows * sizeof(int32_t));
+  w.off_tidx = w.off_qres + up(rows * sizeof(int32_t));
+  w.off_tval = w.off_tidx + up(2 * rows * SPEC_MAX_TOP_K * sizeof(int32_t));
+  w.off_tcnt = w.off_tval + up(2 * rows * SPEC_MAX_TOP_K * sizeof(float));
+  w.total = w.off_tcnt + up(2 * rows * sizeof(int32_t));
   return w;
 }
 struct Eagle2Ws {
@@ -49,9 +53,9 @@ int check_params(const spec_params_t* prm, int V) {
   if (prm->top_k < 0) return SPEC_ERR_ARG;
   if (!(prm->top_p > 0.f && prm->top_p <= 1.f)) return SPEC_ERR_ARG;
   if (prm->temperature > 0.f) {
-    if (prm->top_k > SPEC_MAX_TOP_K && prm->top_k < V) return SPEC_ERR_UNSUPPORTED;
-    if (prm->top_p < 1.f && prm->top_k == 0) return SPEC_ERR_UNSUPPORTED;
-    if (prm->top_k != 0 || prm->top_p < 1.f) return SPEC_ERR_UNSUPPORTED;  // top-k path not built yet
+    // a truncating transform runs on candidate lists of k_eff tokens
+    const int keff = truncation_k(prm, V);
+    if (keff > SPEC_MAX_TOP_K) return SPEC_ERR_UNSUPPORTED;
   }
   return SPEC_OK;
 }
@@ -70,6 +74,9 @@ int run_verify(const VerifyShape& s, VerifyArgs& a, void* ws, size_t ws_bytes, c
   a.alpha_part = (float*)(base + w.off_alpha);
   a.meta = (unsigned char*)(base + w.off_meta);
   a.qres = (int32_t*)(base + w.off_qres);
+  a.topk_idx = (int32_t*)(base + w.off_tidx);
+  a.topk_val = (float*)(base + w.off_tval);
+  a.topk_cnt = (int32_t*)(base + w.off_tcnt);
   cudaError_t e = cudaMemsetAsync(a.status, 0, sizeof(uint32_t), st);
   if (e != cudaSuccess) return SPEC_ERR_CUDA;
   if (s.B == 0) return SPEC_OK;

@@ -51,7 +51,21 @@ struct VerifyArgs {
   float* alpha_part;    // [rows * 8] per-CTA acceptance-mass partials
   unsigned char* meta;  // [rows * meta_rec_bytes(chain)] per-row records
   int32_t* qres;        // [rows] resolved draft row per tree row (-1 none)
+  int32_t* topk_idx;    // [2 * rows * SPEC_MAX_TOP_K] top-k candidates
+  float* topk_val;      //   (target rows, then draft rows)
+  int32_t* topk_cnt;    // [2 * rows]
 };
+
+// Tokens a truncating sampling transform keeps per row: min(top_k, V), with
+// top_k = 0 meaning V; 0 when neither top-k nor top-p truncates anything.
+inline int truncation_k(const spec_params_t* p, int V) {
+  const int k = (p->top_k <= 0 || p->top_k >= V) ? V : p->top_k;
+  if (p->top_p >= 1.f && k == V) return 0;
+  return k;
+}
+
+// Sampled verification with top-k / top-p truncation (k <= SPEC_MAX_TOP_K).
+cudaError_t launch_sparse(const VerifyShape& s, const VerifyArgs& a, int k, cudaStream_t st);
 
 // Per-row record of the pipelined kernel: a 16-byte header, 16 bytes per
 // child slot and 4 bytes of accept uniform per slot, padded to 16 bytes (one

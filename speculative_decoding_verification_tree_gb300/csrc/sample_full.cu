@@ -683,6 +683,11 @@ void full_geometry(int V, int bytes_per_elem, int* C, int* slice) {
 
 cudaError_t launch_sampled(const VerifyShape& s, const VerifyArgs& a, cudaStream_t st) {
   if (s.B == 0) return cudaSuccess;
+  const int tk = truncation_k(&a.prm, s.V);
+  if (tk > 0) {
+    if (!a.topk_idx || !a.topk_val || !a.topk_cnt || !a.meta) return cudaErrorInvalidValue;
+    return launch_sparse(s, a, tk, st);
+  }
   UnitParams P{};
   P.s = s;
   P.a = a;

@@ -83,7 +83,9 @@ def test_chain_argument_errors(lib):
     assert _chain(lib, prm=_prm(lib, top_k=-2)) == lib.SPEC_ERR_ARG
     assert _chain(lib, prm=_prm(lib, draft_kind=3)) == lib.SPEC_ERR_DTYPE
     assert _chain(lib, prm=_prm(lib, flags=1)) == lib.SPEC_ERR_ARG
-    assert _chain(lib, prm=_prm(lib, top_p=0.9)) == lib.SPEC_ERR_UNSUPPORTED
+    # top-p alone keeps up to V tokens: fine for V <= 128, not beyond
+    assert _chain(lib, V=1000, prm=_prm(lib, top_p=0.9)) == \
+        lib.SPEC_ERR_UNSUPPORTED
     assert _chain(lib, V=5000, prm=_prm(lib, top_k=2000)) == \
         lib.SPEC_ERR_UNSUPPORTED
     assert _chain(lib, ws=None) == lib.SPEC_ERR_WORKSPACE
