@@ -45,45 +45,83 @@ __device__ __forceinline__ bool before(uint32_t ka, int ia, uint32_t kb, int ib)
   return ka > kb || (ka == kb && ia < ib);
 }
 
-// Warp: keep the k best entries of buf[0, n) in buf[0, min(n, k)), sorted.
-__device__ int warp_compact(Cand* buf, int n, int k, int lane) {
-  const int m = min(n, k);
-  Cand keep[kMaxK / 32];
-#pragma unroll
-  for (int i = 0; i < kMaxK / 32; ++i) keep[i] = Cand{0u, INT_MAX};
-  for (int r = 0; r < m; ++r) {
-    uint32_t bk = 0u;
-    int bi = INT_MAX, bp = -1;
+// Warp: keep the k best entries of buf[0, n) -- larger key first, equal keys
+// by position -- in place and in their original order (buf is in increasing
+// index order, so position order is index order).  The k-th best key is found
+// by a 4-round radix select (8 bits per round, per-warp histogram `hist` of
+// 256 counters), then one stable compaction pass keeps every key above it and
+// the first `need` keys equal to it.  Returns min(n, k); *kth is the k-th best
+// key (0 when n < k).
+__device__ int warp_select(Cand* buf, int n, int k, int lane, uint32_t* hist, uint32_t* kth) {
+  if (n < k) {
+    *kth = 0u;
+    return n;
+  }
+  const uint32_t lt = (1u << lane) - 1u;
+  uint32_t prefix = 0u;
+  int need = k;
+#pragma unroll 1
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = lane; i < 256; i += 32) hist[i] = 0u;
+    __syncwarp();
+    const uint32_t hmask = (shift == 24) ? 0u : (0xFFFFFFFFu << (shift + 8));
     for (int p = lane; p < n; p += 32) {
-      const Cand c = buf[p];
-      if (c.idx >= 0 && (bp < 0 || before(c.key, c.idx, bk, bi))) {
-        bk = c.key;
-        bi = c.idx;
-        bp = p;
+      const uint32_t key = buf[p].key;
+      if ((key & hmask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+    }
+    __syncwarp();
+    // lane l holds digits 255 - 8l down to 248 - 8l
+    uint32_t c[8], lsum = 0u;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      c[j] = hist[255 - 8 * lane - j];
+      lsum += c[j];
+    }
+    uint32_t incl = lsum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const uint32_t excl = incl - lsum;
+    const bool mine = excl < (uint32_t)need && (uint32_t)need <= incl;
+    uint32_t digit = 0u, above = 0u;
+    if (mine) {
+      uint32_t run = excl;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (run + c[j] >= (uint32_t)need) {
+          digit = 255u - 8u * lane - j;
+          above = run;
+          break;
+        }
+        run += c[j];
       }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const uint32_t ok = __shfl_xor_sync(0xffffffffu, bk, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      const int op = __shfl_xor_sync(0xffffffffu, bp, o);
-      if (op >= 0 && (bp < 0 || before(ok, oi, bk, bi))) {
-        bk = ok;
-        bi = oi;
-        bp = op;
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < kMaxK / 32; ++i)
-      if (r == i * 32 + lane) keep[i] = Cand{bk, bi};
-    if (lane == 0 && bp >= 0) buf[bp].idx = -1;
+    const int src = __ffs(__ballot_sync(0xffffffffu, mine)) - 1;
+    digit = __shfl_sync(0xffffffffu, digit, src & 31);
+    above = __shfl_sync(0xffffffffu, above, src & 31);
+    prefix |= digit << shift;
+    need -= (int)above;
     __syncwarp();
   }
-#pragma unroll
-  for (int i = 0; i < kMaxK / 32; ++i)
-    if (i * 32 + lane < m) buf[i * 32 + lane] = keep[i];
-  __syncwarp();
-  return m;
+  int out = 0, ties = 0;
+  for (int base = 0; base < n; base += 32) {
+    const int p = base + lane;
+    const Cand c = (p < n) ? buf[p] : Cand{0u, -1};
+    const bool gt = p < n && c.key > prefix;
+    const bool eq = p < n && c.key == prefix;
+    const uint32_t eqm = __ballot_sync(0xffffffffu, eq);
+    const bool keep = gt || (eq && ties + __popc(eqm & lt) < need);
+    const uint32_t km = __ballot_sync(0xffffffffu, keep);
+    __syncwarp();  // every lane has read its entry; writes go to lower slots
+    if (keep) buf[out + __popc(km & lt)] = c;
+    out += __popc(km);
+    ties += __popc(eqm);
+    __syncwarp();
+  }
+  *kth = prefix;
+  return out;
 }
 
 // Top-k of the row at `rp` (V logits); smem holds kWarps * kBufCap Cands.
@@ -95,6 +133,7 @@ template <typename T, bool kVec>
 __device__ void row_topk(const T* __restrict__ rp, int V, int k, float kt, Cand* smem,
                          int32_t* out_idx, float* out_val, int* out_n, float* lse) {
   __shared__ int cnt[kWarps];
+  __shared__ uint32_t hist[kWarps][256];
   __shared__ float red_m[kWarps], red_z[kWarps];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   Cand* buf = smem + warp * kBufCap;
@@ -160,12 +199,14 @@ __device__ void row_topk(const T* __restrict__ rp, int V, int k, float kt, Cand*
       n += tot;
       __syncwarp();
       if (n > kBufCap - 256) {
-        n = warp_compact(buf, n, k, lane);
-        th = (n >= k) ? buf[k - 1].key : 0u;
+        n = warp_select(buf, n, k, lane, hist[warp], &th);
       }
     }
   }
-  n = warp_compact(buf, n, k, lane);
+  {
+    uint32_t unused;
+    n = warp_select(buf, n, k, lane, hist[warp], &unused);
+  }
   if (lse) ms = warp_ms(ms);
   if (lane == 0) {
     cnt[warp] = n;
@@ -180,10 +221,19 @@ __device__ void row_topk(const T* __restrict__ rp, int V, int k, float kt, Cand*
       m += cnt[w];
     }
     __syncwarp();
-    m = warp_compact(buf, m, k, lane);
+    // the warps' lists concatenate in index order; select, then order the
+    // kept entries best first (equal keys: lower index first)
+    uint32_t unused;
+    m = warp_select(buf, m, k, lane, hist[0], &unused);
     for (int i = lane; i < m; i += 32) {
-      out_idx[i] = buf[i].idx;
-      out_val[i] = funkey(buf[i].key);
+      const Cand c = buf[i];
+      int rk = 0;
+      for (int j = 0; j < m; ++j) {
+        const uint32_t kj = buf[j].key;
+        rk += (kj > c.key || (kj == c.key && j < i)) ? 1 : 0;
+      }
+      out_idx[rk] = c.idx;
+      out_val[rk] = funkey(c.key);
     }
     if (lane == 0) {
       *out_n = m;

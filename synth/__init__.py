@@ -117,8 +117,11 @@ def _draft_dist(logits, w: Workload):
         z = torch.log(z)
     z = z / w.temperature
     if w.top_k > 0 and w.top_k < z.shape[-1]:
-        kth = torch.topk(z, w.top_k, dim=-1).values[..., -1:]
-        z = torch.where(z >= kth, z, torch.full_like(z, float("-inf")))
+        # exactly k tokens; ties at the k-th value go to the lower index
+        order = torch.sort(z, dim=-1, descending=True, stable=True).indices
+        keep = torch.zeros_like(z, dtype=torch.bool).scatter_(
+            -1, order[..., :w.top_k], True)
+        z = torch.where(keep, z, torch.full_like(z, float("-inf")))
     probs = torch.softmax(z, dim=-1)
     if w.top_p < 1.0:
         sp, idx = torch.sort(probs, dim=-1, descending=True, stable=True)
