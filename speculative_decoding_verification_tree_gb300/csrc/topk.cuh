@@ -25,7 +25,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxK = 128;
-constexpr int kBufCap = 1024;  // per-warp candidate buffer (entries)
+constexpr int kBufCap = 512;   // per-warp candidate buffer (entries)
 
 // Order-preserving 32-bit key of a float (NaN -> 0, below every number).
 __device__ __forceinline__ uint32_t fkey(float v) {
@@ -35,6 +35,14 @@ __device__ __forceinline__ uint32_t fkey(float v) {
 }
 __device__ __forceinline__ float funkey(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+__device__ __forceinline__ uint4 ldg_stream16(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
 }
 
 struct Cand {
@@ -143,30 +151,8 @@ __device__ void row_topk(const T* __restrict__ rp, int V, int k, float kt, Cand*
   uint32_t th = 0u;  // key of the warp's current k-th best (0: none yet)
   int n = 0;
   MaxSum ms{neg_inf(), 0.f};
-  for (int gb = g0; gb < g1; gb += 32) {
-    const int g = gb + lane;
-    float v[8];
-    if (g < g1) {
-      const int e = g * 8;
-      if constexpr (kVec) {
-        if constexpr (sizeof(T) == 2) {
-          const uint4 w = *reinterpret_cast<const uint4*>(rp + e);
-          v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x); v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
-          v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z); v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
-        } else {
-          const float4 a = *reinterpret_cast<const float4*>(rp + e);
-          const float4 b = *reinterpret_cast<const float4*>(rp + e + 4);
-          v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-          v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = (e + j < V) ? ElemIO<T>::get(rp, e + j) : neg_inf();
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = neg_inf();
-    }
+  // one group = 8 consecutive logits of one lane (elements past V read -inf)
+  auto consume = [&](int g, const float* v) {
     if (lse) {
       float mt = neg_inf();
 #pragma unroll
@@ -198,9 +184,60 @@ __device__ void row_topk(const T* __restrict__ rp, int V, int k, float kt, Cand*
       }
       n += tot;
       __syncwarp();
-      if (n > kBufCap - 256) {
-        n = warp_select(buf, n, k, lane, hist[warp], &th);
+      if (n > kBufCap - 256) n = warp_select(buf, n, k, lane, hist[warp], &th);
+    }
+  };
+  if constexpr (kVec) {
+    // aligned rows: 16-byte loads kept three groups ahead in registers
+    constexpr int kU = sizeof(T) == 2 ? 1 : 2;  // uint4 per group
+    uint4 ring[3][kU];
+    auto issue = [&](uint4* dst, int g) {
+      if (g < g1) {
+        const uint4* src = reinterpret_cast<const uint4*>(rp + (int64_t)g * 8);
+#pragma unroll
+        for (int u = 0; u < kU; ++u) dst[u] = ldg_stream16(src + u);
       }
+    };
+    auto decode = [&](const uint4* w, int g, float* v) {
+      if (g < g1) {
+        if constexpr (sizeof(T) == 2) {
+          v[0] = bf16_lo(w[0].x); v[1] = bf16_hi(w[0].x); v[2] = bf16_lo(w[0].y);
+          v[3] = bf16_hi(w[0].y); v[4] = bf16_lo(w[0].z); v[5] = bf16_hi(w[0].z);
+          v[6] = bf16_lo(w[0].w); v[7] = bf16_hi(w[0].w);
+        } else {
+          v[0] = __uint_as_float(w[0].x); v[1] = __uint_as_float(w[0].y);
+          v[2] = __uint_as_float(w[0].z); v[3] = __uint_as_float(w[0].w);
+          v[4] = __uint_as_float(w[kU - 1].x); v[5] = __uint_as_float(w[kU - 1].y);
+          v[6] = __uint_as_float(w[kU - 1].z); v[7] = __uint_as_float(w[kU - 1].w);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = neg_inf();
+      }
+    };
+    issue(ring[0], g0 + lane);
+    issue(ring[1], g0 + 32 + lane);
+    issue(ring[2], g0 + 64 + lane);
+    for (int gb = g0; gb < g1; gb += 96) {
+#pragma unroll
+      for (int s = 0; s < 3; ++s) {
+        const int g = gb + 32 * s + lane;
+        if (gb + 32 * s < g1) {  // warp-uniform
+          float v[8];
+          decode(ring[s], g, v);
+          issue(ring[s], g + 96);
+          consume(g, v);
+        }
+      }
+    }
+  } else {
+    for (int gb = g0; gb < g1; gb += 32) {
+      const int g = gb + lane;
+      float v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        v[j] = (g < g1 && g * 8 + j < V) ? ElemIO<T>::get(rp, g * 8 + j) : neg_inf();
+      consume(g, v);
     }
   }
   {
@@ -215,12 +252,21 @@ __device__ void row_topk(const T* __restrict__ rp, int V, int k, float kt, Cand*
   }
   __syncthreads();
   if (warp == 0) {
+    // pack the lists to the front of the whole buffer area (moves are to
+    // lower addresses; each 32-entry chunk is read before it is written)
     int m = cnt[0];
     for (int w = 1; w < kWarps; ++w) {
-      for (int i = lane; i < cnt[w]; i += 32) buf[m + i] = smem[w * kBufCap + i];
+      const Cand* src = smem + w * kBufCap;
+      for (int i0 = 0; i0 < cnt[w]; i0 += 32) {
+        const int i = i0 + lane;
+        Cand c{0u, -1};
+        if (i < cnt[w]) c = src[i];
+        __syncwarp();
+        if (i < cnt[w]) smem[m + i] = c;
+        __syncwarp();
+      }
       m += cnt[w];
     }
-    __syncwarp();
     // the warps' lists concatenate in index order; select, then order the
     // kept entries best first (equal keys: lower index first)
     uint32_t unused;
