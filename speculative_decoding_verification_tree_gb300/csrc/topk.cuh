@@ -148,88 +148,97 @@ __device__ void row_topk(const T* __restrict__ rp, int V, int k, float kt, Cand*
   const int groups = (V + 7) / 8;
   const int gpw = (groups + kWarps - 1) / kWarps;
   const int g0 = warp * gpw, g1 = min(groups, g0 + gpw);
-  uint32_t th = 0u;  // key of the warp's current k-th best (0: none yet)
+  float thf = neg_inf();  // value of the warp's current k-th best
   int n = 0;
   MaxSum ms{neg_inf(), 0.f};
-  // one group = 8 consecutive logits of one lane (elements past V read -inf)
-  auto consume = [&](int g, const float* v) {
-    if (lse) {
-      float mt = neg_inf();
+  // Rare path of a group: append its elements above the threshold (in index
+  // order) and compact when the buffer is full.
+  auto append = [&](int g, const float (&v)[8]) {
+    int mine = 0;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) mt = fmaxf(mt, __fmul_rn(v[j], kt));
+    for (int j = 0; j < 8; ++j) mine += (g < g1 && g * 8 + j < V && v[j] > thf) ? 1 : 0;
+    int pre = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, pre, o);
+      if (lane >= o) pre += y;
+    }
+    const int tot = __shfl_sync(0xffffffffu, pre, 31);
+    int pos = n + pre - mine;  // n <= kBufCap - 256 and tot <= 256: fits
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (g < g1 && g * 8 + j < V && v[j] > thf) buf[pos++] = Cand{fkey(v[j]), g * 8 + j};
+    n += tot;
+    __syncwarp();
+    if (n > kBufCap - 256) {
+      uint32_t kth;
+      n = warp_select(buf, n, k, lane, hist[warp], &kth);
+      if (n >= k) thf = funkey(kth);
+    }
+  };
+  // Common path: log-sum-exp update and one ballot for the whole group.
+  auto consume = [&](int g, const float (&v)[8]) {
+    if (lse) {
+      float mx = fmaxf(fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3])),
+                       fmaxf(fmaxf(v[4], v[5]), fmaxf(v[6], v[7])));
+      const float mt = __fmul_rn(mx, kt);
       if (mt > ms.m) {
         ms.z *= ex2(ms.m - mt);
         ms.m = mt;
       }
       if (ms.m != neg_inf()) {
+        float z = 0.f;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) ms.z += ex2(fmaf(v[j], kt, -ms.m));
+        for (int j = 0; j < 8; ++j) z += ex2(fmaf(v[j], kt, -ms.m));
+        ms.z += z;
       }
     }
-    int mine = 0;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) mine += (g < g1 && g * 8 + j < V && fkey(v[j]) > th) ? 1 : 0;
-    if (__ballot_sync(0xffffffffu, mine)) {
-      int pre = mine;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, pre, o);
-        if (lane >= o) pre += y;
-      }
-      const int tot = __shfl_sync(0xffffffffu, pre, 31);
-      int pos = n + pre - mine;  // n <= kBufCap - 256 and tot <= 256: fits
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (g < g1 && g * 8 + j < V && fkey(v[j]) > th) buf[pos++] = Cand{fkey(v[j]), g * 8 + j};
-      }
-      n += tot;
-      __syncwarp();
-      if (n > kBufCap - 256) n = warp_select(buf, n, k, lane, hist[warp], &th);
-    }
+    const bool c = (v[0] > thf) | (v[1] > thf) | (v[2] > thf) | (v[3] > thf) | (v[4] > thf) |
+                   (v[5] > thf) | (v[6] > thf) | (v[7] > thf);
+    if (__ballot_sync(0xffffffffu, c)) append(g, v);
   };
   if constexpr (kVec) {
-    // aligned rows: 16-byte loads kept three groups ahead in registers
+    // aligned rows (V % 8 == 0): 16-byte loads three groups ahead
     constexpr int kU = sizeof(T) == 2 ? 1 : 2;  // uint4 per group
-    uint4 ring[3][kU];
-    auto issue = [&](uint4* dst, int g) {
-      if (g < g1) {
-        const uint4* src = reinterpret_cast<const uint4*>(rp + (int64_t)g * 8);
-#pragma unroll
-        for (int u = 0; u < kU; ++u) dst[u] = ldg_stream16(src + u);
-      }
-    };
-    auto decode = [&](const uint4* w, int g, float* v) {
-      if (g < g1) {
-        if constexpr (sizeof(T) == 2) {
-          v[0] = bf16_lo(w[0].x); v[1] = bf16_hi(w[0].x); v[2] = bf16_lo(w[0].y);
-          v[3] = bf16_hi(w[0].y); v[4] = bf16_lo(w[0].z); v[5] = bf16_hi(w[0].z);
-          v[6] = bf16_lo(w[0].w); v[7] = bf16_hi(w[0].w);
-        } else {
-          v[0] = __uint_as_float(w[0].x); v[1] = __uint_as_float(w[0].y);
-          v[2] = __uint_as_float(w[0].z); v[3] = __uint_as_float(w[0].w);
-          v[4] = __uint_as_float(w[kU - 1].x); v[5] = __uint_as_float(w[kU - 1].y);
-          v[6] = __uint_as_float(w[kU - 1].z); v[7] = __uint_as_float(w[kU - 1].w);
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = neg_inf();
-      }
-    };
-    issue(ring[0], g0 + lane);
-    issue(ring[1], g0 + 32 + lane);
-    issue(ring[2], g0 + 64 + lane);
-    for (int gb = g0; gb < g1; gb += 96) {
-#pragma unroll
-      for (int s = 0; s < 3; ++s) {
-        const int g = gb + 32 * s + lane;
-        if (gb + 32 * s < g1) {  // warp-uniform
-          float v[8];
-          decode(ring[s], g, v);
-          issue(ring[s], g + 96);
-          consume(g, v);
-        }
-      }
+    const uint4* base = reinterpret_cast<const uint4*>(rp);
+    uint4 r0[kU], r1[kU], r2[kU];
+#define SV_TOPK_ISSUE(R, G)                                              \
+    if ((G) < g1) {                                                      \
+      _Pragma("unroll") for (int u = 0; u < kU; ++u)                      \
+        R[u] = ldg_stream16(base + (int64_t)(G) * kU + u);               \
     }
+#define SV_TOPK_STEP(R, S)                                               \
+    if (gb + 32 * (S) < g1) {                                            \
+      const int g = gb + 32 * (S) + lane;                                \
+      float v[8];                                                        \
+      if (g < g1) {                                                      \
+        if constexpr (sizeof(T) == 2) {                                  \
+          v[0] = bf16_lo(R[0].x); v[1] = bf16_hi(R[0].x);                \
+          v[2] = bf16_lo(R[0].y); v[3] = bf16_hi(R[0].y);                \
+          v[4] = bf16_lo(R[0].z); v[5] = bf16_hi(R[0].z);                \
+          v[6] = bf16_lo(R[0].w); v[7] = bf16_hi(R[0].w);                \
+        } else {                                                         \
+          v[0] = __uint_as_float(R[0].x); v[1] = __uint_as_float(R[0].y);  \
+          v[2] = __uint_as_float(R[0].z); v[3] = __uint_as_float(R[0].w);  \
+          v[4] = __uint_as_float(R[kU - 1].x); v[5] = __uint_as_float(R[kU - 1].y); \
+          v[6] = __uint_as_float(R[kU - 1].z); v[7] = __uint_as_float(R[kU - 1].w); \
+        }                                                                \
+      } else {                                                           \
+        _Pragma("unroll") for (int j = 0; j < 8; ++j) v[j] = neg_inf();   \
+      }                                                                  \
+      SV_TOPK_ISSUE(R, g + 96)                                           \
+      consume(g, v);                                                     \
+    }
+    SV_TOPK_ISSUE(r0, g0 + lane)
+    SV_TOPK_ISSUE(r1, g0 + 32 + lane)
+    SV_TOPK_ISSUE(r2, g0 + 64 + lane)
+    for (int gb = g0; gb < g1; gb += 96) {
+      SV_TOPK_STEP(r0, 0)
+      SV_TOPK_STEP(r1, 1)
+      SV_TOPK_STEP(r2, 2)
+    }
+#undef SV_TOPK_STEP
+#undef SV_TOPK_ISSUE
   } else {
     for (int gb = g0; gb < g1; gb += 32) {
       const int g = gb + lane;
@@ -238,6 +247,36 @@ __device__ void row_topk(const T* __restrict__ rp, int V, int k, float kt, Cand*
       for (int j = 0; j < 8; ++j)
         v[j] = (g < g1 && g * 8 + j < V) ? ElemIO<T>::get(rp, g * 8 + j) : neg_inf();
       consume(g, v);
+    }
+  }
+  // Fewer than k elements above -inf in this warp's part (the threshold never
+  // rose): the k best are completed by its -inf entries, lowest index first.
+  if (n < k) {
+    for (int gb = g0; gb < g1 && n < k; gb += 32) {
+      const int g = gb + lane;
+      int mine = 0;
+      float v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        v[j] = (g < g1 && g * 8 + j < V) ? ElemIO<T>::get(rp, g * 8 + j) : 0.f;
+        mine += (g < g1 && g * 8 + j < V && v[j] == neg_inf()) ? 1 : 0;
+      }
+      int pre = mine;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, pre, o);
+        if (lane >= o) pre += y;
+      }
+      const int tot = __shfl_sync(0xffffffffu, pre, 31);
+      int pos = n + pre - mine;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (g < g1 && g * 8 + j < V && v[j] == neg_inf()) {
+          if (pos < kBufCap) buf[pos] = Cand{fkey(v[j]), g * 8 + j};
+          ++pos;
+        }
+      n = min(n + tot, kBufCap);
+      __syncwarp();
     }
   }
   {
