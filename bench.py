@@ -56,6 +56,39 @@ def _args():
     return p.parse_args()
 
 
+# DRAM traffic per launch of the profiled kernel, from one ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum of a smaller batch, scaled
+# to the workload's rows), keyed by workload, with a hash of the sources the
+# kernel is built from at capture time.  Reported as null once they changed.
+_PIPE_SRC = ("sample_pipe.cuh", "sample_pipe_bf16.cu", "sample_pipe_f32.cu",
+             "common.cuh", "kernels.h")
+TRAFFIC = {
+    # unit_pipe, tree_static at B=4: 188.17 MB read + 3.32 MB written, 244 rows
+    "tree_static": {"bytes_per_row": 191.489e6 / 244, "src": _PIPE_SRC,
+                    "hash": "3a5579863f442555"},
+}
+
+
+def _src_hash(files):
+    import hashlib
+    d = os.path.join(ROOT, "speculative_decoding_verification_tree_gb300",
+                     "csrc")
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
+    with open(os.path.join(ROOT, "include", "specverify.h"), "rb") as fh:
+        h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(name, rows):
+    t = TRAFFIC.get(name)
+    if not t or t["hash"] != _src_hash(t["src"]):
+        return None
+    return int(t["bytes_per_row"] * rows)
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -91,6 +124,11 @@ class Work:
             self.inputs = [self.target, self.draft, self.toks]
             self.prof_kind = (_lib.SPEC_PROF_ARGMAX if w.temperature == 0
                               else _lib.SPEC_PROF_VERIFY)
+            # the profiled launch: the argmax pass (greedy), the candidate
+            # top-k pass (top-k / top-p sampling) or the full-row pipeline
+            self.kernel_name = ("argmax_partial" if w.temperature == 0 else
+                                "topk_rows" if (w.top_k > 0 or w.top_p < 1)
+                                else "unit_pipe")
             tb = self.target.element_size()
             self.kernel_bytes = B * (K + 1) * V * tb
             if w.temperature > 0:
@@ -113,6 +151,8 @@ class Work:
             self.inputs = [self.target, self.draft, self.q_row, self.toks,
                            self.parent]
             self.prof_kind = _lib.SPEC_PROF_VERIFY
+            self.kernel_name = ("topk_rows" if (w.top_k > 0 or w.top_p < 1)
+                                else "unit_pipe")
             self.kernel_bytes = B * (N + 1) * V * (
                 self.target.element_size() + self.draft.element_size())
             self.launches_per_step = 3  # mask, row verification, walk
@@ -144,6 +184,7 @@ class Work:
                                     device=device))
             self.inputs = [self.draft, self.target]
             self.prof_kind = _lib.SPEC_PROF_VERIFY
+            self.kernel_name = "unit_pipe"
             qrows = int((self.tree[2] >= 0).sum().item())
             self.kernel_bytes = (B * (M + 1) + qrows) * V * 2
             self.expand_bytes = B * self.R * V * 2
@@ -433,9 +474,9 @@ def main():
         achieved = work.kernel_bytes / (kern_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1),
                 "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": None,
-                "kernel": {0: "argmax_partial", 1: "unit_full",
-                           2: "eagle2_rows"}[work.prof_kind],
+                "frac": round(achieved / peak, 4),
+                "traffic": _traffic(args.workload, work.rows),
+                "kernel": work.kernel_name,
                 "bytes_per_launch": work.kernel_bytes,
                 "avg_launch_ms": round(kern_ms, 5),
                 "peak_source": peak_kind, "profile_rc": rc,

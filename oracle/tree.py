@@ -9,13 +9,14 @@ flattened order of the EAGLE-2 notes §4.2 gives).  Target row r = 0 is the
 root; row r = j + 1 is the position after drafted node j.  ``q_row[r]`` names
 the draft row holding q at tree row r, or -1.
 
-Mask ("构造验证阶段的输入与注意力掩码", EAGLE-2 notes §4.2): drafted token i
+Mask (EAGLE-2 notes §4.2, the paragraph on the verification input and
+its attention mask): drafted token i
 sees drafted token j iff j is an ancestor of i or i itself (the chain case is
 the lower-triangular causal mask); the committed prefix is visible to all and
 is not part of the N x N mask.
 
 Verification.  A tree lets a rejected branch give way to its siblings
-("如果一个草稿令牌被拒绝，可以尝试其他分支", EAGLE-2 notes §2.2).  The pages do not
+(EAGLE-2 notes §2.2, the verification stage of tree drafts).  The pages do not
 spell the multi-sibling rule out; we take the lossless reading that the
 exactness requirement of every page forces: recursive rejection sampling over
 the children of a node, tried in node-index order, with siblings drawn

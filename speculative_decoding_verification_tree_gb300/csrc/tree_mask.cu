@@ -1,4 +1,4 @@
-// Tree attention mask (EAGLE-2 notes §4.2, "构造验证阶段的输入与注意力掩码"):
+// Tree attention mask (EAGLE-2 notes §4.2, verification input and its mask):
 // a drafted token sees only itself and its ancestors; for a chain this is the
 // lower-triangular causal mask.  Parents precede children, so row i of the
 // mask is row parent(i) plus the diagonal bit, and the rows can be built in
