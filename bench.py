@@ -386,6 +386,21 @@ def cpu_sample_text(name, nseq, el):
 
 
 # ------------------------------------------------------------------- main
+def max_over_ranks(dist, ms, dev):
+    """The slowest rank's time (every rank gets it); `dist` None = 1 rank."""
+    if not dist:
+        return ms
+    import torch
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank, steps, world, ms):
+    """Whole-job throughput: the units all ranks processed / the time."""
+    return units_per_rank * steps * world / (ms / 1e3)
+
+
 def main():
     args = _args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -458,13 +473,9 @@ def main():
                 work.step()
             torch.cuda.synchronize()
     clocks.stop()
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(dist, ms, dev)
     ms_step = ms / steps
-    rows_total = work.rows * steps * world
-    value = rows_total / (ms / 1e3)
+    value = job_rate(work.rows, steps, world, ms)
     tokens_per_step = work.emitted_tokens()
 
     peak, peak_kind = _peaks()
@@ -512,11 +523,8 @@ def main():
         a1.record()
         torch.cuda.synchronize()
         ems = a0.elapsed_time(a1)
-        if dist:
-            t = torch.tensor([ems], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
-        e2e = {"value": round(work.rows * n_e2e * world / (ems / 1e3), 1),
+        ems = max_over_ranks(dist, ems, dev)
+        e2e = {"value": round(job_rate(work.rows, n_e2e, world, ems), 1),
                "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": n_e2e,
                "ms_per_step": round(ems / n_e2e, 4)}

@@ -1,0 +1,70 @@
+"""Host side of the multi-process bench path, on CPU with gloo ranks.
+
+Sequences are independent, so N GPUs run N replicas with no collective on
+the data path; the only cross-rank steps are the barrier around the timed
+region and the max-over-ranks of the elapsed time.  These run here as
+world-size-2 gloo process groups on 127.0.0.1."""
+
+import json
+import os
+import socket
+import sys
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out_dir):
+    sys.path.insert(0, ROOT)
+    import bench
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        dist.barrier()
+        # rank r measured (r + 1) * 10 ms over 5 steps of 100 rows each
+        ms = bench.max_over_ranks(dist, 10.0 * (rank + 1), torch.device("cpu"))
+        rate = bench.job_rate(100, 5, world, ms)
+        with open(os.path.join(out_dir, f"r{rank}.json"), "w") as f:
+            json.dump({"ms": ms, "rate": rate}, f)
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_and_job_rate_gloo(tmp_path):
+    world = 2
+    mp.spawn(_worker, args=(world, _free_port(), str(tmp_path)), nprocs=world,
+             join=True)
+    got = [json.load(open(tmp_path / f"r{r}.json")) for r in range(world)]
+    for g in got:
+        assert g["ms"] == 20.0           # the slowest rank's time, on all ranks
+        # 100 rows x 5 steps on each of 2 ranks in 20 ms
+        assert g["rate"] == pytest.approx(100 * 5 * 2 / 0.020)
+
+
+def test_single_rank_needs_no_process_group():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks(None, 3.5, None) == 3.5
+    assert bench.job_rate(10, 4, 1, 2.0) == pytest.approx(20000.0)
+
+
+def test_reference_arm_only_rank0_reports(capsys):
+    sys.path.insert(0, ROOT)
+    import bench
+
+    class A:
+        steps, warmup, workload = 1, 0, "chain_sample"
+    assert bench.reference_arm(A(), 2, 1) is None
+    assert capsys.readouterr().out == ""
