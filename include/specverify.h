@@ -245,7 +245,7 @@ const char* spec_error_string(int code);
  * pages: it computes exactly what spec_verify_chain computes (same arguments
  * minus the workspace) and differs only in where its scratch lives.
  *
- * The scratch is one fixed array inside the library (about 1.1 MiB) that
+ * The scratch is one fixed array inside the library (about 1.7 MiB) that
  * every GPU which loads the library holds until the process exits.  The first
  * call on a device looks up that array's device address with the device
  * current, so make the first call before any stream capture.  All calls on a

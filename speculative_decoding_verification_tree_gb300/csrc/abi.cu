@@ -16,7 +16,7 @@ inline size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 // Workspace of a verification call: [status | row_child | row_token | argmax parts]
 struct VerifyWs {
   size_t off_child, off_token, off_parts, off_alpha, off_meta, off_qres;
-  size_t off_tidx, off_tval, off_tcnt, total;
+  size_t off_tidx, off_tval, off_tcnt, off_out, total;
 };
 VerifyWs verify_ws(int B, int n, int V, bool chain) {
   const size_t rows = (size_t)B * (n + 1);
@@ -30,7 +30,8 @@ VerifyWs verify_ws(int B, int n, int V, bool chain) {
   w.off_tidx = w.off_qres + up(rows * sizeof(int32_t));
   w.off_tval = w.off_tidx + up(2 * rows * SPEC_MAX_TOP_K * sizeof(int32_t));
   w.off_tcnt = w.off_tval + up(2 * rows * SPEC_MAX_TOP_K * sizeof(float));
-  w.total = w.off_tcnt + up(2 * rows * sizeof(int32_t));
+  w.off_out = w.off_tcnt + up(2 * rows * sizeof(int32_t));
+  w.total = w.off_out + up(rows * sizeof(RowOut));
   return w;
 }
 struct Eagle2Ws {
@@ -77,6 +78,7 @@ int run_verify(const VerifyShape& s, VerifyArgs& a, void* ws, size_t ws_bytes, c
   a.topk_idx = (int32_t*)(base + w.off_tidx);
   a.topk_val = (float*)(base + w.off_tval);
   a.topk_cnt = (int32_t*)(base + w.off_tcnt);
+  a.rowout = (RowOut*)(base + w.off_out);
   cudaError_t e = cudaMemsetAsync(a.status, 0, sizeof(uint32_t), st);
   if (e != cudaSuccess) return SPEC_ERR_CUDA;
   if (s.B == 0) return SPEC_OK;

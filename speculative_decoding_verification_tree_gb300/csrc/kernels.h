@@ -29,6 +29,27 @@ struct VerifyShape {
   __host__ __device__ int64_t rows() const { return (int64_t)B * (n + 1); }
 };
 
+// Outcome of a row's sibling recursion as far as the streaming verifier
+// takes it (the walk finishes it for the rows on the accepted path).
+//   child >= 0: that drafted child was accepted;
+//   child == -1: every child was rejected (or a leaf): the row's token is
+//     drawn from max(0, p - Cn q) (p when Cn = 0), or from max(0, p - Cc q)
+//     (p when Cc = 0) if the former has no mass;
+//   child == -2: child k was rejected and a later child needs the mass of
+//     max(0, p - Cn q), which takes another pass over the row.
+// Cc, W, D are the recursion state: current residual coefficient, its mass
+// and the draft mass left.  Lp / Lq are the row's base-2 log normalisers
+// (invZq = 1 / sum q for probability rows at T = 1).
+struct RowOut {
+  int child;
+  int k;
+  float Cc, W, D, Cn;
+  float Lp, Lq, invZq;
+  uint32_t bits;
+  int pad[6];
+};
+static_assert(sizeof(RowOut) == 64, "row outcome layout");
+
 // Device pointers of one verification call.
 struct VerifyArgs {
   const void* target;
@@ -54,6 +75,7 @@ struct VerifyArgs {
   int32_t* topk_idx;    // [2 * rows * SPEC_MAX_TOP_K] top-k candidates
   float* topk_val;      //   (target rows, then draft rows)
   int32_t* topk_cnt;    // [2 * rows]
+  RowOut* rowout;       // [rows] row outcomes of the streaming verifier
 };
 
 // Tokens a truncating sampling transform keeps per row: min(top_k, V), with
@@ -78,24 +100,24 @@ inline int meta_rec_bytes(bool chain) {
 // Per-row slots of alpha partials (one per CTA of a cluster of up to 8).
 constexpr int kAlphaSlots = 8;
 
-// Launch parameters of the pipelined sampled-verification kernel.
-struct PipeParams {
+// Launch parameters of the streaming sampled-verification kernel.
+struct StreamParams {
   VerifyShape s;
   VerifyArgs a;
-  int slice;      // vocabulary elements per CTA
-  int stages;     // shared-memory stages per CTA
+  int C;          // CTAs per cluster (vocabulary slices per row)
+  int slice;      // vocabulary elements per CTA (multiple of 8)
+  int nch;        // 4096-element chunks per slice
+  int stages;     // shared-memory ring stages
   int nclusters;  // persistent clusters (set by the launcher)
+  int qk;         // draft kind: 0 logits, 1 probabilities at T = 1, 2 probabilities
   float kt;       // log2(e) / T
   float invT;     // 1 / T
   int kidcap;     // child slots per row record
   int rec_bytes;  // row record stride
 };
-bool pipe_geometry(int V, int tsz, int dsz, int* C, int* ept, int* stages, int* slice);
-cudaError_t launch_pipe_bf16(const PipeParams& P, int C, int ept, int qk, int dt_draft,
-                             cudaStream_t st);
-cudaError_t launch_pipe_f32(const PipeParams& P, int C, int ept, int qk, int dt_draft,
-                            cudaStream_t st);
-cudaError_t launch_pipe_walk(const VerifyShape& s, const VerifyArgs& a, int C, cudaStream_t st);
+bool stream_geometry(int V, int tsz, int dsz, int* C, int* slice, int* nch, int* stages);
+cudaError_t launch_stream_bf16(StreamParams P, cudaStream_t st);
+cudaError_t launch_stream_f32(StreamParams P, cudaStream_t st);
 
 // Event pair around a dominant kernel launch (no-op unless profiling is on).
 void prof_begin(int kind, cudaStream_t st);

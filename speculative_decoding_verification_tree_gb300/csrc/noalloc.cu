@@ -41,10 +41,11 @@ constexpr size_t kRowBytes = (size_t)SPEC_NOALLOC_MAX_ROWS * sizeof(int32_t);
 constexpr size_t kPartBytes = (size_t)SPEC_NOALLOC_MAX_PARTS * sizeof(ArgPart);
 constexpr size_t kAlphaBytes = (size_t)SPEC_NOALLOC_MAX_ROWS * kAlphaSlots * sizeof(float);
 constexpr size_t kMetaBytes = (size_t)SPEC_NOALLOC_MAX_ROWS * 48;  // chain row records
+constexpr size_t kOutBytes = (size_t)SPEC_NOALLOC_MAX_ROWS * sizeof(RowOut);
 constexpr size_t kScratchBytes =
-    kStatusBytes + 3 * kRowBytes + kPartBytes + kAlphaBytes + kMetaBytes;
+    kStatusBytes + 3 * kRowBytes + kPartBytes + kAlphaBytes + kMetaBytes + kOutBytes;
 
-// The scratch itself (~1.1 MiB per device).  In host code this name is only
+// The scratch itself (~1.7 MiB per device).  In host code this name is only
 // a stand-in; its device address comes from cudaGetSymbolAddress below.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
@@ -122,6 +123,7 @@ extern "C" int spec_verify_chain_noalloc(const void* target_logits, const void* 
   a.alpha_part = (float*)(p + kStatusBytes + 2 * kRowBytes + kPartBytes);
   a.meta = (unsigned char*)(p + kStatusBytes + 2 * kRowBytes + kPartBytes + kAlphaBytes);
   a.qres = (int32_t*)(p + kStatusBytes + 2 * kRowBytes + kPartBytes + kAlphaBytes + kMetaBytes);
+  a.rowout = (RowOut*)(p + kStatusBytes + 3 * kRowBytes + kPartBytes + kAlphaBytes + kMetaBytes);
   if (meta_rec_bytes(true) != 48) return SPEC_ERR_CUDA;  // chain row record size
   // the status word must start at zero; everything else is written before it
   // is read within the call

@@ -704,16 +704,18 @@ cudaError_t launch_sampled(const VerifyShape& s, const VerifyArgs& a, cudaStream
   P.invT = 1.f / T;
   const int qk = a.prm.draft_kind == SPEC_DRAFT_LOGITS ? Q_LOGITS : (T == 1.f ? Q_PROBS_T1 : Q_PROBS_T);
   cudaError_t e = cudaSuccess;
-  // bandwidth path: persistent pipelined clusters (aligned rows that fit)
-  int pc, pept, pst, psl;
-  if (P.bulk && a.meta && a.qres && pipe_geometry(s.V, tsz, dsz, &pc, &pept, &pst, &psl)) {
-    PipeParams Q{s, a, psl, pst, 0, P.kt, P.invT, meta_kidcap(s.chain), meta_rec_bytes(s.chain)};
-    prof_begin(SPEC_PROF_VERIFY, st);
-    e = (a.dt_target == SPEC_BF16) ? launch_pipe_bf16(Q, pc, pept, qk, a.dt_draft, st)
-                                   : launch_pipe_f32(Q, pc, pept, qk, a.dt_draft, st);
-    prof_end(SPEC_PROF_VERIFY, st);
-    if (e != cudaSuccess) return e;
-    return launch_pipe_walk(s, a, pc, st);
+  // bandwidth path: persistent streaming clusters (16-byte aligned rows)
+  StreamParams Q{};
+  if (P.bulk && a.meta && a.qres && a.rowout &&
+      stream_geometry(s.V, tsz, dsz, &Q.C, &Q.slice, &Q.nch, &Q.stages)) {
+    Q.s = s;
+    Q.a = a;
+    Q.qk = qk;
+    Q.kt = P.kt;
+    Q.invT = P.invT;
+    Q.kidcap = meta_kidcap(s.chain);
+    Q.rec_bytes = meta_rec_bytes(s.chain);
+    return (a.dt_target == SPEC_BF16) ? launch_stream_bf16(Q, st) : launch_stream_f32(Q, st);
   }
   prof_begin(SPEC_PROF_VERIFY, st);
 #define SV_DISPATCH(TT, TD)                                     \

@@ -15,9 +15,10 @@
 //   * no child accepted: inverse-CDF draw from the final weights in
 //     vocabulary order (a leaf: the bonus token from p).
 // Kernels: topk_rows (one CTA per target row and per draft row, one HBM
-// pass), row_meta (children and uniforms, shared with the pipelined path),
-// sparse_units (one CTA per row, all math on the candidate lists), pipe_walk.
-#include "sample_pipe.cuh"
+// pass), row_meta (children and uniforms, shared with the streaming path),
+// sparse_units (one CTA per row, all math on the candidate lists),
+// sparse_walk.
+#include "sample_stream.cuh"
 #include "topk.cuh"
 
 namespace sv {
@@ -111,7 +112,7 @@ __global__ void __launch_bounds__(kK) sparse_units(VerifyShape s, VerifyArgs a, 
   const int64_t rows = s.rows();
   const int tid = threadIdx.x;
   const int V = s.V;
-  const pipe::Meta* M = reinterpret_cast<const pipe::Meta*>(a.meta + u * (int64_t)rec_bytes);
+  const stream::Meta* M = reinterpret_cast<const stream::Meta*>(a.meta + u * (int64_t)rec_bytes);
   const float* ukid = reinterpret_cast<const float*>(a.meta + u * (int64_t)rec_bytes + 16 +
                                                      16 * kidcap);
   const bool probs = a.prm.draft_kind == SPEC_DRAFT_PROBS;
@@ -231,6 +232,45 @@ __global__ void __launch_bounds__(kK) sparse_units(VerifyShape s, VerifyArgs a, 
   if (st_bits) flag_status(a.status, st_bits);
 }
 
+// Per row: acceptance mass; per sequence (row 0's thread): the walk along
+// accepted children and the token drawn at the row where it stops.
+__global__ void sparse_walk(VerifyShape s, VerifyArgs a) {
+  const int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (row >= s.rows()) return;
+  const int n = s.n;
+  const int b = (int)(row / (n + 1));
+  const int r = (int)(row - (int64_t)b * (n + 1));
+  bool has_q;
+  if (s.chain) {
+    has_q = r < n;
+  } else {
+    const int q = a.q_row ? a.q_row[row] : -1;
+    has_q = q >= 0 && q < s.R;
+  }
+  const float m = has_q ? a.alpha_part[row * kAlphaSlots] : __int_as_float(0x7fc00000);
+  if (s.chain) {
+    if (r < n) a.mass[(int64_t)b * n + r] = m;
+  } else {
+    a.mass[row] = m;
+  }
+  if (r != 0) return;
+  int32_t* out = a.out_tokens + row;
+  int rr = 0, len = 0;
+  while (true) {
+    const int j = a.row_child[row + rr];
+    if (j < 0 || j >= n || len >= n) break;
+    if (!s.chain) a.path_nodes[(int64_t)b * n + len] = j;
+    out[len] = a.node_tokens[(int64_t)b * n + j];
+    ++len;
+    rr = j + 1;
+  }
+  out[len] = a.row_token[row + rr];
+  for (int k = len + 1; k <= n; ++k) out[k] = -1;
+  if (!s.chain)
+    for (int k = len; k < n; ++k) a.path_nodes[(int64_t)b * n + k] = -1;
+  a.count[b] = len;
+}
+
 template <typename TT, typename TD>
 cudaError_t launch_sparse_t(const VerifyShape& s, const VerifyArgs& a, int k, cudaStream_t st) {
   const int64_t rows = s.rows();
@@ -255,14 +295,14 @@ cudaError_t launch_sparse_t(const VerifyShape& s, const VerifyArgs& a, int k, cu
   prof_end(SPEC_PROF_VERIFY, st);
   if (e != cudaSuccess) return e;
   const int kidcap = meta_kidcap(s.chain), rec = meta_rec_bytes(s.chain);
-  pipe::row_meta<TT, TD><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(s, a, kidcap, rec);
+  stream::row_meta<TT, TD><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(s, a, kidcap, rec);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const float T = a.prm.temperature;
   sparse_units<TT, TD><<<(unsigned)rows, kK, 0, st>>>(s, a, o, kLog2e / T, 1.f / T, rec, kidcap);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  pipe::pipe_walk<<<(unsigned)((rows + 127) / 128), 128, 0, st>>>(s, a, 1);
+  sparse_walk<<<(unsigned)((rows + 127) / 128), 128, 0, st>>>(s, a);
   return cudaGetLastError();
 }
 
