@@ -114,6 +114,8 @@ struct StreamParams {
   float invT;     // 1 / T
   int kidcap;     // child slots per row record
   int rec_bytes;  // row record stride
+  int wC;         // CTAs per sequence in the walk (its own vocabulary split)
+  int wslice;     // vocabulary elements per walk CTA
 };
 bool stream_geometry(int V, int tsz, int dsz, int* C, int* slice, int* nch, int* stages);
 cudaError_t launch_stream_bf16(StreamParams P, cudaStream_t st);

@@ -552,29 +552,30 @@ __global__ void __launch_bounds__(kThreads, 1) unit_stream(StreamParams P) {
         mbar_arrive(&sm.recfree[rr % 3]);
       }
 
-      // 3. first decision of row j - 1 (needs only its normalisers)
-      if (hB && tid == 0) {
+      // 3. first decision of row j - 1 (needs only its normalisers); every
+      // thread takes it (no broadcast needed), thread 0 records it
+      if (hB) {
         const int rb = (j - 1) % 3;
         wait_cta(sm, &sm.mrec[rb], (uint32_t)(((j - 1) / 3) & 1), a.status);
         const Meta& M = sm.rec[rb];
-        RowState& S = sm.rs[(j - 1) & 1];
-        S.Lp = Lp;
-        S.Lq = Lq;
-        S.invZq = invZq;
+        const RowState S0{Lp, Lq, invZq, -1, 0, 0u};
         uint32_t bits = 0;
-        if (rank == 0) {
-          if (!(zp_tot > 0.f) || isnan(zp_tot)) bits |= SPEC_STATUS_NAN;
-          if (qb >= 0 && (!(zq_tot > 0.f) || isnan(zq_tot))) bits |= SPEC_STATUS_NAN;
+        int acc0 = -1;
+        if (M.nk > 0 && child_test<QK>(M, P.kidcap, 0, 0.f, 1.f, 1.f, S0, kt, invT, V, &bits))
+          acc0 = M.kid[0].node;
+        if (tid == 0) {
+          if (rank == 0) {
+            if (!(zp_tot > 0.f) || isnan(zp_tot)) bits |= SPEC_STATUS_NAN;
+            if (qb >= 0 && (!(zq_tot > 0.f) || isnan(zq_tot))) bits |= SPEC_STATUS_NAN;
+          }
+          RowState& S = sm.rs[(j - 1) & 1];
+          S.Lp = Lp;
+          S.Lq = Lq;
+          S.invZq = invZq;
+          S.accepted = acc0;
+          S.pending = (M.nk > 0 && acc0 < 0) ? 1 : 0;
+          S.bits = bits;
         }
-        S.accepted = -1;
-        S.pending = 0;
-        if (M.nk > 0) {
-          if (child_test<QK>(M, P.kidcap, 0, 0.f, 1.f, 1.f, S, kt, invT, V, &bits))
-            S.accepted = M.kid[0].node;
-          else
-            S.pending = 1;
-        }
-        S.bits = bits;
       }
 
       // 4. one row-time of chunks: pass A of row j, pass B of row j - 1
@@ -627,14 +628,15 @@ __global__ void __launch_bounds__(kThreads, 1) unit_stream(StreamParams P) {
             float x[8], y[8];
             load8<TT>(reinterpret_cast<const TT*>(sb) + tid * kEPT, x);
             load8<TD>(reinterpret_cast<const TD*>(sb + kTB) + tid * kEPT, y);
+            float lr = 0.f;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               const float p = ex2(fmaf(x[i], kt, negLp));
-              const float q = q_of<QK>(y[i], kt, invT, negLq, invZq);
-              const float mn = fminf(p, q);
+              const float mn = fminf(p, q_of<QK>(y[i], kt, invT, negLq, invZq));
               acc_a += mn;
-              acc_r += p - mn;
+              lr += p - mn;
             }
+            acc_r += lr;
           }
         }
         __syncwarp();
@@ -715,10 +717,12 @@ __global__ void __launch_bounds__(kThreads, 1) unit_stream(StreamParams P) {
 constexpr int kWalkThreads = 512;
 constexpr int kWalkWarps = kWalkThreads / 32;
 
+constexpr int kMaxW = 8;  // CTAs per sequence in the walk
+
 struct WalkSmem {
   float wsum[kMaxTiles][kWalkWarps];  // per (chunk, warp) masses of the draw
   float red[kWalkWarps];
-  float xs[2][kMaxC];                 // cluster exchange slots (by parity)
+  float xs[2][kMaxW];                 // cluster exchange slots (by parity)
   RowOut st;                          // walk state (thread 0 writes)
   int act;                            // 0 done, 1 pass, 2 draw
   int rr, len, rsel, tile, wsel;
@@ -730,15 +734,15 @@ __global__ void __launch_bounds__(kWalkThreads) stream_walk(StreamParams P) {
   __shared__ WalkSmem ws;
   const VerifyShape& s = P.s;
   const VerifyArgs& a = P.a;
-  const int C = P.C;
+  const int C = P.wC;  // the walk's own split of the vocabulary
   const uint32_t rank = cluster_ctarank();
   const int b = blockIdx.x / C;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int n = s.n, V = s.V;
   const int64_t u0 = (int64_t)b * (n + 1);
   const float kt = P.kt, invT = P.invT;
-  const int r0 = (int)rank * P.slice;
-  const int len = max(0, min(P.slice, V - r0));
+  const int r0 = (int)rank * P.wslice;
+  const int len = max(0, min(P.wslice, V - r0));
   const int nch = (len + kCH - 1) / kCH;
   if (rank == 0) {
     for (int r = tid; r <= n; r += kWalkThreads) {
@@ -753,7 +757,7 @@ __global__ void __launch_bounds__(kWalkThreads) stream_walk(StreamParams P) {
       float m = __int_as_float(0x7fc00000);
       if (has_q) {
         m = 0.f;
-        for (int k = 0; k < C; ++k) m += a.alpha_part[row * kAlphaSlots + k];
+        for (int k = 0; k < P.C; ++k) m += a.alpha_part[row * kAlphaSlots + k];
       }
       if (s.chain) {
         if (r < n) a.mass[(int64_t)b * n + r] = m;
@@ -762,10 +766,31 @@ __global__ void __launch_bounds__(kWalkThreads) stream_walk(StreamParams P) {
       }
     }
   }
+  int xe = 0;  // cluster exchanges so far
+  // CTA sum of every thread's `v`, exchanged: the cluster total (the same
+  // in every CTA; per-rank totals stay in ws.xs).
+  auto reduce_exchange = [&](float v) -> float {
+    v = warp_sum(v);
+    if (lane == 0) ws.red[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+      float t = (lane < kWalkWarps) ? ws.red[lane] : 0.f;
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+      if (lane < C) {  // this CTA's total into every CTA's slot `rank`
+        const uint32_t dst = mapa(smem_u32(&ws.xs[xe & 1][rank]), (uint32_t)lane);
+        asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dst), "f"(t) : "memory");
+      }
+    }
+    cluster_sync();
+    float tot = 0.f;
+    for (int i = 0; i < C; ++i) tot += ws.xs[xe & 1][i];
+    ++xe;
+    return tot;
+  };
   // Sum over this CTA's slice of row u of max(0, p - Cx q) (p when Cx = 0),
   // optionally keeping the per (chunk, warp) masses; the cluster total
   // comes back from exchange number `xe`.
-  int xe = 0;
   auto pass = [&](int64_t u, int qr, float Cx, const RowOut& st, bool keep) -> float {
     const TT* tr = reinterpret_cast<const TT*>(a.target) + u * (int64_t)V + r0;
     const TD* dr = (Cx != 0.f && qr >= 0)
@@ -773,7 +798,7 @@ __global__ void __launch_bounds__(kWalkThreads) stream_walk(StreamParams P) {
                        : nullptr;
     const float nLp = -st.Lp, nLq = -st.Lq, iZ = st.invZq;
     float acc = 0.f;
-    constexpr int kIn = inflight<TT, TD>();
+    constexpr int kIn = 2 * inflight<TT, TD>();
     for (int c0 = 0; c0 < nch; c0 += kIn) {
       Raw8<TT> xt[kIn];
       Raw8<TD> xd[kIn];
@@ -806,23 +831,7 @@ __global__ void __launch_bounds__(kWalkThreads) stream_walk(StreamParams P) {
         }
       }
     }
-    acc = warp_sum(acc);
-    if (lane == 0) ws.red[warp] = acc;
-    __syncthreads();
-    if (warp == 0) {
-      float t = (lane < kWalkWarps) ? ws.red[lane] : 0.f;
-#pragma unroll
-      for (int o = 8; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-      if (lane < C) {  // this CTA's total into every CTA's slot `rank`
-        const uint32_t dst = mapa(smem_u32(&ws.xs[xe & 1][rank]), (uint32_t)lane);
-        asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dst), "f"(t) : "memory");
-      }
-    }
-    cluster_sync();
-    float tot = 0.f;
-    for (int i = 0; i < C; ++i) tot += ws.xs[xe & 1][i];
-    ++xe;
-    return tot;
+    return reduce_exchange(acc);
   };
 
   // walk (thread 0 of every CTA, identical decisions)
@@ -1080,11 +1089,33 @@ cudaError_t launch_t(StreamParams P, cudaStream_t st) {
   e = cudaLaunchKernelEx(&cfg, kern, P);
   prof_end(SPEC_PROF_VERIFY, st);
   if (e != cudaSuccess) return e;
+  // walk: as many CTAs per sequence as fill the GPU once (1..8), at least
+  // enough for the draw's chunk table
+  int sms = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, 0);
+  if (e != cudaSuccess) return e;
+  int w = 1;
+  while (w < kMaxW && (int64_t)P.s.B * w * 2 <= sms) w *= 2;
+  for (;;) {
+    const int sl = ((P.s.V + w - 1) / w + 7) / 8 * 8;
+    if ((sl + kCH - 1) / kCH <= kMaxTiles || w == kMaxW) {
+      P.wC = w;
+      P.wslice = sl;
+      break;
+    }
+    w *= 2;
+  }
+  if ((P.wslice + kCH - 1) / kCH > kMaxTiles) return cudaErrorInvalidConfiguration;
+  cudaLaunchAttribute wattr[1];
+  wattr[0].id = cudaLaunchAttributeClusterDimension;
+  wattr[0].val.clusterDim.x = P.wC;
+  wattr[0].val.clusterDim.y = 1;
+  wattr[0].val.clusterDim.z = 1;
   cudaLaunchConfig_t wc = {};
   wc.blockDim = dim3(kWalkThreads);
-  wc.gridDim = dim3((unsigned)(P.s.B * P.C));
+  wc.gridDim = dim3((unsigned)(P.s.B * P.wC));
   wc.stream = st;
-  wc.attrs = attr;
+  wc.attrs = wattr;
   wc.numAttrs = 1;
   return cudaLaunchKernelEx(&wc, stream_walk<TT, TD, QK>, P);
 }

@@ -1,8 +1,9 @@
 // Tree attention mask (EAGLE-2 notes §4.2, verification input and its mask):
 // a drafted token sees only itself and its ancestors; for a chain this is the
-// lower-triangular causal mask.  Parents precede children, so row i of the
-// mask is row parent(i) plus the diagonal bit, and the rows can be built in
-// node order with all threads of the CTA sweeping the columns.
+// lower-triangular causal mask.  One CTA per sequence: the parent array goes
+// to shared memory, the N x N block is zeroed, then one thread per row walks
+// the row's ancestor chain (parents precede children; a link that does not
+// point to an earlier node ends the chain) and sets those bytes.
 //
 // Also: the device side of spec_philox_uniforms.
 #include "common.cuh"
@@ -14,27 +15,25 @@ namespace {
 __global__ void __launch_bounds__(256) tree_mask_kernel(const int32_t* __restrict__ parent, int N,
                                                         uint8_t* __restrict__ mask,
                                                         uint64_t* __restrict__ bits) {
+  __shared__ int par[SPEC_MAX_TREE_NODES];
   const int b = blockIdx.x;
-  const int32_t* par = parent + (int64_t)b * N;
-  if (mask) {
-    uint8_t* m = mask + (int64_t)b * N * N;
-    for (int i = 0; i < N; ++i) {
-      const int p = par[i];
-      const bool ok = (p >= 0 && p < i);
-      uint8_t* row = m + (int64_t)i * N;
-      const uint8_t* prow = m + (int64_t)(ok ? p : 0) * N;
-      for (int j = threadIdx.x; j < N; j += blockDim.x)
-        row[j] = (j == i) ? 1 : (ok && j < i ? prow[j] : 0);
-      __syncthreads();  // row i is read when its children are built
+  for (int i = threadIdx.x; i < N; i += blockDim.x) par[i] = parent[(int64_t)b * N + i];
+  uint8_t* m = mask ? mask + (int64_t)b * N * N : nullptr;
+  if (m)
+    for (int k = threadIdx.x; k < N * N; k += blockDim.x) m[k] = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < N; i += blockDim.x) {
+    uint64_t w = 0;
+    if (m) m[(int64_t)i * N + i] = 1;
+    if (i < 64) w = 1ull << i;
+    int cur = i, a = par[i];
+    while (a >= 0 && a < cur) {
+      if (m) m[(int64_t)i * N + a] = 1;
+      if (a < 64) w |= 1ull << a;
+      cur = a;
+      a = par[a];
     }
-  }
-  if (bits && threadIdx.x == 0) {
-    uint64_t* o = bits + (int64_t)b * N;
-    for (int i = 0; i < N; ++i) {
-      const int p = par[i];
-      const uint64_t up = (p >= 0 && p < i) ? o[p] : 0ull;
-      o[i] = up | (1ull << i);
-    }
+    if (bits) bits[(int64_t)b * N + i] = w;
   }
 }
 
