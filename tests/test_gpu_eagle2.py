@@ -140,6 +140,22 @@ def test_expand_rerank_ties_and_certain_tokens():
     _compare(w, draft, _run(w, draft), list(range(w.B)))
 
 
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float32])
+def test_expand_rerank_ties_aligned_rows(dt):
+    # aligned rows (V % 8 == 0, the bound-and-rescan path): logits on a 1/4
+    # grid give exact ties among the top few (ranked by index); rows of small
+    # integers tie thousands of logits at the top (more candidates than the
+    # rescan keeps: the general top-k takes the row)
+    w = synth.workload("eagle2", B=3, V=32000, depth=3, topk=10, width=4,
+                       total=20, seed=7, draft_dtype=dt)
+    R = 1 + (w.depth - 1) * w.width
+    g = torch.Generator(device="cpu").manual_seed(1)
+    d = torch.round(torch.randn(w.B, R, w.V, generator=g) * 2.5 * 4) / 4
+    d[2] = torch.randint(-3, 3, (R, w.V), generator=g).float()
+    draft = d.to(dt).cuda()
+    _compare(w, draft, _run(w, draft), list(range(w.B)))
+
+
 def test_eagle2_full_pipeline_sampled():
     # B=128, V=128256 bf16: expand + rerank + mask, then tree verification at
     # T = 0.8 with target = draft row + noise, compared on sampled sequences
