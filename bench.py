@@ -127,7 +127,7 @@ class Work:
             # top-k pass (top-k / top-p sampling) or the full-row pipeline
             self.kernel_name = ("argmax_partial" if w.temperature == 0 else
                                 "topk_rows" if (w.top_k > 0 or w.top_p < 1)
-                                else "unit_pipe")
+                                else "unit_stream")
             tb = self.target.element_size()
             self.kernel_bytes = B * (K + 1) * V * tb
             if w.temperature > 0:
@@ -151,7 +151,7 @@ class Work:
                            self.parent]
             self.prof_kind = _lib.SPEC_PROF_VERIFY
             self.kernel_name = ("topk_rows" if (w.top_k > 0 or w.top_p < 1)
-                                else "unit_pipe")
+                                else "unit_stream")
             self.kernel_bytes = B * (N + 1) * V * (
                 self.target.element_size() + self.draft.element_size())
             self.launches_per_step = 3  # mask, row verification, walk
@@ -183,7 +183,7 @@ class Work:
                                     device=device))
             self.inputs = [self.draft, self.target]
             self.prof_kind = _lib.SPEC_PROF_VERIFY
-            self.kernel_name = "unit_pipe"
+            self.kernel_name = "unit_stream"
             qrows = int((self.tree[2] >= 0).sum().item())
             self.kernel_bytes = (B * (M + 1) + qrows) * V * 2
             self.expand_bytes = B * self.R * V * 2

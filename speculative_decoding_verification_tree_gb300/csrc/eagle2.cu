@@ -30,20 +30,10 @@ namespace {
 constexpr int kSelThreads = 512;
 constexpr int kMaxCand = SPEC_EAGLE2_MAX_CANDIDATES;  // per sequence (host-checked)
 
-// One CTA per draft row: the row's `topk` most probable tokens and their
+// One CTA per draft row: the row's `topk` most probable tokens (bound-and-
+// rescan streaming top-k shared with the top-k sampling path) and their
 // log-probabilities log q = (z kt - log2 sum 2^(z kt)) ln 2 at temperature T
-// (kt = log2(e) / T).  Aligned rows take one streaming pass in which every
-// thread keeps its running maximum and the row's log-sum-exp; the k-th
-// largest thread maximum is a lower bound on the k-th largest logit, so only
-// the threads whose maximum reaches it rescan their own logits (recently
-// read, from L2) and the candidates (every logit at or above the bound) are
-// ranked exactly by (logit desc, index asc).  Rows where that leaves fewer
-// than k or more than kCandCap candidates (ties, NaN, -inf) take the
-// general streaming top-k shared with the top-k sampling path.
-constexpr int kCandCap = 256;
-constexpr int kFlagCap = 64;  // threads whose logits are rescanned
-constexpr int kRowBatch = 4;  // 16-byte groups in flight per thread
-
+// (kt = log2(e) / T).
 template <typename T, bool kVec>
 __global__ void __launch_bounds__(topk::kThreads) eagle2_rows(const T* __restrict__ x, int V,
                                                               int k, float kt,
@@ -54,148 +44,9 @@ __global__ void __launch_bounds__(topk::kThreads) eagle2_rows(const T* __restric
   __shared__ float val[SPEC_EAGLE2_MAX_TOPK];
   __shared__ int cnt;
   __shared__ float lse;
-  __shared__ uint32_t hist[256];
-  __shared__ uint32_t s_tau;
-  __shared__ int s_nc, s_nf;
-  __shared__ float red_m[topk::kWarps], red_z[topk::kWarps];
   const int64_t row = blockIdx.x;
-  const T* rp = x + row * (int64_t)V;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  topk::Cand* cbuf = reinterpret_cast<topk::Cand*>(smraw);
-  bool fallback = !kVec;
-  if constexpr (kVec) {
-    constexpr int kU = sizeof(T) == 2 ? 1 : 2;  // uint4 per 8-logit group
-    constexpr int kNT = topk::kThreads;
-    const int G = V / 8;
-    const uint4* base = reinterpret_cast<const uint4*>(rp);
-    float mx = neg_inf();
-    MaxSum ms{neg_inf(), 0.f};
-    auto unpack = [&](const uint4 (&r)[kU], float (&v)[8]) {
-      if constexpr (sizeof(T) == 2) {
-        v[0] = bf16_lo(r[0].x); v[1] = bf16_hi(r[0].x); v[2] = bf16_lo(r[0].y); v[3] = bf16_hi(r[0].y);
-        v[4] = bf16_lo(r[0].z); v[5] = bf16_hi(r[0].z); v[6] = bf16_lo(r[0].w); v[7] = bf16_hi(r[0].w);
-      } else {
-        v[0] = __uint_as_float(r[0].x); v[1] = __uint_as_float(r[0].y);
-        v[2] = __uint_as_float(r[0].z); v[3] = __uint_as_float(r[0].w);
-        v[4] = __uint_as_float(r[kU - 1].x); v[5] = __uint_as_float(r[kU - 1].y);
-        v[6] = __uint_as_float(r[kU - 1].z); v[7] = __uint_as_float(r[kU - 1].w);
-      }
-    };
-    for (int g0 = tid; g0 < G; g0 += kNT * kRowBatch) {
-      uint4 r[kRowBatch][kU];
-#pragma unroll
-      for (int bI = 0; bI < kRowBatch; ++bI) {
-        const int g = g0 + bI * kNT;
-        if (g < G) {
-#pragma unroll
-          for (int u = 0; u < kU; ++u) r[bI][u] = topk::ldg_stream16(base + (int64_t)g * kU + u);
-        }
-      }
-#pragma unroll
-      for (int bI = 0; bI < kRowBatch; ++bI) {
-        if (g0 + bI * kNT < G) {
-          float v[8];
-          unpack(r[bI], v);
-          const float gm = fmaxf(fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3])),
-                                 fmaxf(fmaxf(v[4], v[5]), fmaxf(v[6], v[7])));
-          mx = fmaxf(mx, gm);
-          const float mt = __fmul_rn(gm, kt);
-          if (mt > ms.m) {
-            ms.z *= ex2(ms.m - mt);
-            ms.m = mt;
-          }
-          if (ms.m != neg_inf()) {
-            float z = 0.f;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) z += ex2(fmaf(v[j], kt, -ms.m));
-            ms.z += z;
-          }
-        }
-      }
-    }
-    // log-sum-exp of the row
-    ms = warp_ms(ms);
-    if (lane == 0) {
-      red_m[warp] = ms.m;
-      red_z[warp] = ms.z;
-    }
-    // bound: k-th largest thread maximum (order keys; radix select by warp 0)
-    const uint32_t mykey = topk::fkey(mx);
-    cbuf[tid] = topk::Cand{mykey, tid};
-    if (tid == 0) {
-      s_nc = 0;
-      s_nf = 0;
-    }
-    __syncthreads();
-    if (warp == 0) {
-      uint32_t kth = 0u;
-      topk::warp_select(cbuf, kNT, k, lane, hist, &kth);
-      if (lane == 0) {
-        s_tau = kth;
-        MaxSum A{red_m[0], red_z[0]};
-        for (int w = 1; w < topk::kWarps; ++w) A = ms_combine(A, MaxSum{red_m[w], red_z[w]});
-        lse = A.m + log2f(A.z);
-      }
-    }
-    __syncthreads();
-    const uint32_t tau = s_tau;
-    topk::Cand* cand = cbuf + kNT;  // after the bound's scratch
-    int* flagged = reinterpret_cast<int*>(cand + kCandCap);
-    if (mykey >= tau) {  // this thread holds a logit at or above the bound
-      const int pos = atomicAdd(&s_nf, 1);
-      if (pos < kFlagCap) flagged[pos] = tid;
-    }
-    __syncthreads();
-    const int nf = s_nf;
-    if (nf <= kFlagCap) {
-      // the flagged threads' groups, rescanned by the whole CTA
-      const int gpt = (G + kNT - 1) / kNT;
-#pragma unroll 2
-      for (int w = tid; w < nf * gpt; w += kNT) {
-        const int f = w / gpt;
-        const int g = flagged[f] + (w - f * gpt) * kNT;
-        if (g < G) {
-          uint4 r[kU];
-#pragma unroll
-          for (int u = 0; u < kU; ++u) r[u] = topk::ldg_stream16(base + (int64_t)g * kU + u);
-          float v[8];
-          unpack(r, v);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint32_t kj = topk::fkey(v[j]);
-            if (kj >= tau) {
-              const int pos = atomicAdd(&s_nc, 1);
-              if (pos < kCandCap) cand[pos] = topk::Cand{kj, g * 8 + j};
-            }
-          }
-        }
-      }
-    }
-    __syncthreads();
-    const int nc = s_nc;
-    fallback = (nf > kFlagCap || nc < k || nc > kCandCap || tau == 0u);
-    if (!fallback) {
-      // exact ranking of the candidates: logit desc, index asc
-      for (int i = tid; i < nc; i += kNT) {
-        const topk::Cand c = cand[i];
-        int rk = 0;
-        for (int j2 = 0; j2 < nc; ++j2) {
-          const topk::Cand d = cand[j2];
-          rk += topk::before(d.key, d.idx, c.key, c.idx) ? 1 : 0;
-        }
-        if (rk < k) {
-          idx[rk] = c.idx;
-          val[rk] = topk::funkey(c.key);
-        }
-      }
-      if (tid == 0) cnt = k;
-    }
-    __syncthreads();
-  }
-  if (fallback) {
-    topk::row_topk<T, kVec>(rp, V, k, kt, reinterpret_cast<topk::Cand*>(smraw), idx, val, &cnt,
-                            &lse);
-  }
+  topk::row_topk_fast<T, kVec>(x + row * (int64_t)V, V, k, kt,
+                               reinterpret_cast<topk::Cand*>(smraw), idx, val, &cnt, &lse);
   const int i = threadIdx.x;
   if (i < k) {
     Eagle2Cand* o = out + row * SPEC_EAGLE2_MAX_TOPK;

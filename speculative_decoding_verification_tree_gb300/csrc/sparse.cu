@@ -44,7 +44,7 @@ __global__ void __launch_bounds__(topk::kThreads) topk_rows(VerifyShape s, Verif
   const int n = s.n, V = s.V;
   if (i < rows) {
     const TT* rp = reinterpret_cast<const TT*>(a.target) + i * (int64_t)V;
-    topk::row_topk<TT, kVecT>(rp, V, k, 1.f, smem, o.idx + i * kK, o.val + i * kK, o.cnt + i,
+    topk::row_topk_fast<TT, kVecT>(rp, V, k, 1.f, smem, o.idx + i * kK, o.val + i * kK, o.cnt + i,
                               nullptr);
     return;
   }
@@ -59,7 +59,7 @@ __global__ void __launch_bounds__(topk::kThreads) topk_rows(VerifyShape s, Verif
     return;
   }
   const TD* rp = reinterpret_cast<const TD*>(a.draft) + ((int64_t)b * s.R + q) * V;
-  topk::row_topk<TD, kVecD>(rp, V, k, 1.f, smem, o.idx + i * kK, o.val + i * kK, o.cnt + i,
+  topk::row_topk_fast<TD, kVecD>(rp, V, k, 1.f, smem, o.idx + i * kK, o.val + i * kK, o.cnt + i,
                             nullptr);
 }
 

@@ -332,6 +332,158 @@ __device__ void row_topk(const T* __restrict__ rp, int V, int k, float kt, Cand*
   __syncthreads();
 }
 
+// Streaming top-k, bound-and-rescan form (aligned rows).  One pass in which
+// every thread keeps its running maximum (and, if lse is wanted, the row's
+// log-sum-exp); the k-th largest thread maximum is a lower bound on the k-th
+// largest logit, so only the threads whose maximum reaches it have logits at
+// or above it: the CTA rescans just those threads' logits (recently read,
+// from L2) and ranks the candidates exactly by (logit desc, index asc).
+// Rows where that leaves fewer than k or more than kCandCap candidates (many
+// ties at the bound, NaN, -inf) take row_topk.  Same outputs as row_topk.
+constexpr int kCandCap = 1024;
+constexpr int kRowBatch = 4;  // 16-byte groups in flight per thread
+
+template <typename T, bool kVec>
+__device__ void row_topk_fast(const T* __restrict__ rp, int V, int k, float kt, Cand* smem,
+                              int32_t* out_idx, float* out_val, int* out_n, float* lse) {
+  __shared__ uint32_t hist[256];
+  __shared__ uint32_t s_tau;
+  __shared__ int s_nc, s_nf;
+  __shared__ float red_m[kWarps], red_z[kWarps];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  bool fallback = !kVec;
+  if constexpr (kVec) {
+    constexpr int kU = sizeof(T) == 2 ? 1 : 2;  // uint4 per 8-logit group
+    constexpr int kNT = kThreads;
+    const int G = V / 8;
+    const uint4* base = reinterpret_cast<const uint4*>(rp);
+    float mx = neg_inf();
+    MaxSum ms{neg_inf(), 0.f};
+    auto unpack = [&](const uint4 (&r)[kU], float (&v)[8]) {
+      if constexpr (sizeof(T) == 2) {
+        v[0] = bf16_lo(r[0].x); v[1] = bf16_hi(r[0].x); v[2] = bf16_lo(r[0].y); v[3] = bf16_hi(r[0].y);
+        v[4] = bf16_lo(r[0].z); v[5] = bf16_hi(r[0].z); v[6] = bf16_lo(r[0].w); v[7] = bf16_hi(r[0].w);
+      } else {
+        v[0] = __uint_as_float(r[0].x); v[1] = __uint_as_float(r[0].y);
+        v[2] = __uint_as_float(r[0].z); v[3] = __uint_as_float(r[0].w);
+        v[4] = __uint_as_float(r[kU - 1].x); v[5] = __uint_as_float(r[kU - 1].y);
+        v[6] = __uint_as_float(r[kU - 1].z); v[7] = __uint_as_float(r[kU - 1].w);
+      }
+    };
+    for (int g0 = tid; g0 < G; g0 += kNT * kRowBatch) {
+      uint4 r[kRowBatch][kU];
+#pragma unroll
+      for (int bI = 0; bI < kRowBatch; ++bI) {
+        const int g = g0 + bI * kNT;
+        if (g < G) {
+#pragma unroll
+          for (int u = 0; u < kU; ++u) r[bI][u] = ldg_stream16(base + (int64_t)g * kU + u);
+        }
+      }
+#pragma unroll
+      for (int bI = 0; bI < kRowBatch; ++bI) {
+        if (g0 + bI * kNT < G) {
+          float v[8];
+          unpack(r[bI], v);
+          const float gm = fmaxf(fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3])),
+                                 fmaxf(fmaxf(v[4], v[5]), fmaxf(v[6], v[7])));
+          mx = fmaxf(mx, gm);
+          if (lse) {
+            const float mt = __fmul_rn(gm, kt);
+            if (mt > ms.m) {
+              ms.z *= ex2(ms.m - mt);
+              ms.m = mt;
+            }
+            if (ms.m != neg_inf()) {
+              float z = 0.f;
+#pragma unroll
+              for (int j = 0; j < 8; ++j) z += ex2(fmaf(v[j], kt, -ms.m));
+              ms.z += z;
+            }
+          }
+        }
+      }
+    }
+    if (lse) {
+      ms = warp_ms(ms);
+      if (lane == 0) {
+        red_m[warp] = ms.m;
+        red_z[warp] = ms.z;
+      }
+    }
+    // bound: k-th largest thread maximum (order keys; radix select by warp 0)
+    const uint32_t mykey = fkey(mx);
+    smem[tid] = Cand{mykey, tid};
+    if (tid == 0) {
+      s_nc = 0;
+      s_nf = 0;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      uint32_t kth = 0u;
+      warp_select(smem, kNT, k, lane, hist, &kth);
+      if (lane == 0) {
+        s_tau = kth;
+        if (lse) {
+          MaxSum A{red_m[0], red_z[0]};
+          for (int w = 1; w < kWarps; ++w) A = ms_combine(A, MaxSum{red_m[w], red_z[w]});
+          *lse = A.m + log2f(A.z);
+        }
+      }
+    }
+    __syncthreads();
+    const uint32_t tau = s_tau;
+    int* flagged = reinterpret_cast<int*>(smem + kNT);
+    Cand* cand = smem + 2 * kNT;
+    if (mykey >= tau) flagged[atomicAdd(&s_nf, 1)] = tid;  // at most kNT entries
+    __syncthreads();
+    const int nf = s_nf;
+    // the flagged threads' groups, rescanned by the whole CTA
+    const int gpt = (G + kNT - 1) / kNT;
+#pragma unroll 2
+    for (int w = tid; w < nf * gpt; w += kNT) {
+      const int f = w / gpt;
+      const int g = flagged[f] + (w - f * gpt) * kNT;
+      if (g < G) {
+        uint4 r[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) r[u] = ldg_stream16(base + (int64_t)g * kU + u);
+        float v[8];
+        unpack(r, v);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t kj = fkey(v[j]);
+          if (kj >= tau) {
+            const int pos = atomicAdd(&s_nc, 1);
+            if (pos < kCandCap) cand[pos] = Cand{kj, g * 8 + j};
+          }
+        }
+      }
+    }
+    __syncthreads();
+    const int nc = s_nc;
+    fallback = (nc < k || nc > kCandCap || tau == 0u);
+    if (!fallback) {
+      // exact ranking of the candidates: logit desc, index asc
+      for (int i = tid; i < nc; i += kNT) {
+        const Cand c = cand[i];
+        int rk = 0;
+        for (int j2 = 0; j2 < nc; ++j2) {
+          const Cand d = cand[j2];
+          rk += before(d.key, d.idx, c.key, c.idx) ? 1 : 0;
+        }
+        if (rk < k) {
+          out_idx[rk] = c.idx;
+          out_val[rk] = funkey(c.key);
+        }
+      }
+      if (tid == 0) *out_n = k;
+    }
+    __syncthreads();
+  }
+  if (fallback) row_topk<T, kVec>(rp, V, k, kt, smem, out_idx, out_val, out_n, lse);
+}
+
 }  // namespace
 }  // namespace topk
 }  // namespace sv
