@@ -1059,6 +1059,8 @@ inline bool geometry(int V, int tsz, int dsz, int* C, int* slice, int* nch, int*
 
 template <typename TT, typename TD, int QK>
 cudaError_t launch_t(StreamParams P, cudaStream_t st) {
+  // the shared-memory barrier arrays hold kMaxNS stages and kMaxC ranks
+  if (P.stages < 2 || P.stages > kMaxNS || P.C < 1 || P.C > kMaxC) return cudaErrorInvalidValue;
   auto kern = unit_stream<TT, TD, QK>;
   const size_t dyn = (size_t)P.stages * 2 * kCH * (sizeof(TT) + sizeof(TD));
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
