@@ -287,6 +287,30 @@ __device__ __forceinline__ float q_of(float raw, float kt, float invT, float neg
   else return ex2(fmaf(lg2(raw), invT, negLq));
 }
 
+// Online sum of 2^(x_i s - m) over a thread's logits with a lazy reference m:
+// the exponentials use the current m, which moves up (rescaling the sum) only
+// when a group's sum would pass 2^60, so the common path has no dependency on
+// the group's maximum; z stays below 2^64 per 16 groups, far from overflow.
+// (m, z) then combine like a (max, sum) pair; m = -inf until a finite logit.
+__device__ __forceinline__ void lazy_sum(const float (&x)[8], float s, float& m, float& z) {
+  float zc = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) zc += ex2(fmaf(x[i], s, -m));
+  if (!(zc <= 0x1p60f)) {  // a new maximum (or the first finite logit, or NaN)
+    const float cm = fmaxf(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])),
+                           fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7])));
+    const float mn = fmaxf(m, __fmul_rn(cm, s));
+    zc = 0.f;
+    if (mn != neg_inf()) {
+      if (m != neg_inf()) z *= ex2(m - mn);
+      m = mn;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) zc += ex2(fmaf(x[i], s, -m));
+    }
+  }
+  z += zc;
+}
+
 // Test of child k of a row (u = its accept uniform): accepted iff
 // u < (r(x) / W) / (q(x) / D) with r = max(0, p - Cc q) (p when Cc = 0), W its
 // mass and D the draft mass left after the rejected siblings; a token already
@@ -478,111 +502,115 @@ __global__ void __launch_bounds__(kThreads, 1) unit_stream(StreamParams P) {
       const int q_next = (j + 1 < nrow) ? a.qres[cid + (int64_t)(j + 1) * ncl] : -1;
       const int64_t ua = cid + (int64_t)j * ncl, ub = ua - ncl;
 
-      // 1. statistics of row j - 1 (and residual mass of row j - 2)
-      if (j >= 1) {
-        const int xs = (j - 1) & 3;
-        wait_cluster(sm, &sm.xbar[xs], (uint32_t)(((j - 1) >> 2) & 1), a.status);
-        if (hB) {
-          const float4 v = (lane < C) ? sm.xslot[xs][lane][0]
-                                      : make_float4(neg_inf(), 0.f, neg_inf(), 0.f);
-          MaxSum A{v.x, v.y}, Bq{v.z, v.w};
-          float z1 = (lane < C) ? v.w : 0.f;
-#pragma unroll
-          for (int o = kMaxC / 2; o > 0; o >>= 1) {
-            A = ms_combine(A, MaxSum{__shfl_xor_sync(0xffffffffu, A.m, o),
-                                     __shfl_xor_sync(0xffffffffu, A.z, o)});
-            if (QK == Q_PROBS_T1) {
-              z1 += __shfl_xor_sync(0xffffffffu, z1, o);
-            } else {
-              Bq = ms_combine(Bq, MaxSum{__shfl_xor_sync(0xffffffffu, Bq.m, o),
-                                         __shfl_xor_sync(0xffffffffu, Bq.z, o)});
+      // Steps 1-3: the previous row-time's exchange and the decisions it allows.
+      auto row_start = [&]() {
+        // 1. statistics of row j - 1 (and residual mass of row j - 2)
+        if (j >= 1) {
+          const int xs = (j - 1) & 3;
+          wait_cluster(sm, &sm.xbar[xs], (uint32_t)(((j - 1) >> 2) & 1), a.status);
+          if (hB) {
+            const float4 v = (lane < C) ? sm.xslot[xs][lane][0]
+                                        : make_float4(neg_inf(), 0.f, neg_inf(), 0.f);
+            MaxSum A{v.x, v.y}, Bq{v.z, v.w};
+            float z1 = (lane < C) ? v.w : 0.f;
+  #pragma unroll
+            for (int o = kMaxC / 2; o > 0; o >>= 1) {
+              A = ms_combine(A, MaxSum{__shfl_xor_sync(0xffffffffu, A.m, o),
+                                       __shfl_xor_sync(0xffffffffu, A.z, o)});
+              if (QK == Q_PROBS_T1) {
+                z1 += __shfl_xor_sync(0xffffffffu, z1, o);
+              } else {
+                Bq = ms_combine(Bq, MaxSum{__shfl_xor_sync(0xffffffffu, Bq.m, o),
+                                           __shfl_xor_sync(0xffffffffu, Bq.z, o)});
+              }
+            }
+            A.m = __shfl_sync(0xffffffffu, A.m, 0);
+            A.z = __shfl_sync(0xffffffffu, A.z, 0);
+            Lp = A.m + log2f(A.z);
+            zp_tot = A.z;
+            Lq = 0.f;
+            invZq = 0.f;
+            zq_tot = 0.f;
+            if (qb >= 0) {
+              if (QK == Q_PROBS_T1) {
+                zq_tot = __shfl_sync(0xffffffffu, z1, 0);
+                invZq = 1.f / zq_tot;
+              } else {
+                Bq.m = __shfl_sync(0xffffffffu, Bq.m, 0);
+                Bq.z = __shfl_sync(0xffffffffu, Bq.z, 0);
+                Lq = Bq.m + log2f(Bq.z);
+                zq_tot = Bq.z;
+              }
             }
           }
-          A.m = __shfl_sync(0xffffffffu, A.m, 0);
-          A.z = __shfl_sync(0xffffffffu, A.z, 0);
-          Lp = A.m + log2f(A.z);
-          zp_tot = A.z;
-          Lq = 0.f;
-          invZq = 0.f;
-          zq_tot = 0.f;
-          if (qb >= 0) {
-            if (QK == Q_PROBS_T1) {
-              zq_tot = __shfl_sync(0xffffffffu, z1, 0);
-              invZq = 1.f / zq_tot;
-            } else {
-              Bq.m = __shfl_sync(0xffffffffu, Bq.m, 0);
-              Bq.z = __shfl_sync(0xffffffffu, Bq.z, 0);
-              Lq = Bq.m + log2f(Bq.z);
-              zq_tot = Bq.z;
-            }
+        }
+
+        // 2. decisions of row j - 2 that need its residual mass R (thread 0)
+        if (j >= 2 && tid == 0) {
+          const int rr = j - 2;
+          const int64_t ur = ub - ncl;
+          const RowState& S = sm.rs[rr & 1];
+          const Meta& M = sm.rec[rr % 3];
+          RowOut st{};
+          st.child = -1;
+          st.k = 0;
+          st.Cc = 0.f;
+          st.W = 1.f;
+          st.D = 1.f;
+          st.Cn = 0.f;  // a leaf draws from p
+          st.Lp = S.Lp;
+          st.Lq = S.Lq;
+          st.invZq = S.invZq;
+          st.bits = S.bits | M.bad;
+          if (S.accepted >= 0) {
+            st.child = S.accepted;
+          } else if (S.pending) {  // child 0 rejected: Cn = 1, whose mass is R
+            const float4(*rx)[2] = sm.xslot[(rr + 1) & 3];
+            float R = 0.f;
+            for (int i = 0; i < C; ++i) R += rx[i][1].x;
+            st.Cn = 1.f;
+            siblings<QK>(M, P.kidcap, st, -1.f, R, false, kt, invT, V);
           }
-        }
-      }
-
-      // 2. decisions of row j - 2 that need its residual mass R (thread 0)
-      if (j >= 2 && tid == 0) {
-        const int rr = j - 2;
-        const int64_t ur = ub - ncl;
-        const RowState& S = sm.rs[rr & 1];
-        const Meta& M = sm.rec[rr % 3];
-        RowOut st{};
-        st.child = -1;
-        st.k = 0;
-        st.Cc = 0.f;
-        st.W = 1.f;
-        st.D = 1.f;
-        st.Cn = 0.f;  // a leaf draws from p
-        st.Lp = S.Lp;
-        st.Lq = S.Lq;
-        st.invZq = S.invZq;
-        st.bits = S.bits | M.bad;
-        if (S.accepted >= 0) {
-          st.child = S.accepted;
-        } else if (S.pending) {  // child 0 rejected: Cn = 1, whose mass is R
-          const float4(*rx)[2] = sm.xslot[(rr + 1) & 3];
-          float R = 0.f;
-          for (int i = 0; i < C; ++i) R += rx[i][1].x;
-          st.Cn = 1.f;
-          siblings<QK>(M, P.kidcap, st, -1.f, R, false, kt, invT, V);
-        }
-        if (rank == 0) {
-          a.rowout[ur] = st;
-          flag_status(a.status, st.bits);
-        }
-        mbar_arrive(&sm.recfree[rr % 3]);
-      }
-
-      // 3. first decision of row j - 1 (needs only its normalisers); every
-      // thread takes it (no broadcast needed), thread 0 records it
-      if (hB) {
-        const int rb = (j - 1) % 3;
-        wait_cta(sm, &sm.mrec[rb], (uint32_t)(((j - 1) / 3) & 1), a.status);
-        const Meta& M = sm.rec[rb];
-        const RowState S0{Lp, Lq, invZq, -1, 0, 0u};
-        uint32_t bits = 0;
-        int acc0 = -1;
-        if (M.nk > 0 && child_test<QK>(M, P.kidcap, 0, 0.f, 1.f, 1.f, S0, kt, invT, V, &bits))
-          acc0 = M.kid[0].node;
-        if (tid == 0) {
           if (rank == 0) {
-            if (!(zp_tot > 0.f) || isnan(zp_tot)) bits |= SPEC_STATUS_NAN;
-            if (qb >= 0 && (!(zq_tot > 0.f) || isnan(zq_tot))) bits |= SPEC_STATUS_NAN;
+            a.rowout[ur] = st;
+            flag_status(a.status, st.bits);
           }
-          RowState& S = sm.rs[(j - 1) & 1];
-          S.Lp = Lp;
-          S.Lq = Lq;
-          S.invZq = invZq;
-          S.accepted = acc0;
-          S.pending = (M.nk > 0 && acc0 < 0) ? 1 : 0;
-          S.bits = bits;
+          mbar_arrive(&sm.recfree[rr % 3]);
         }
-      }
+
+        // 3. first decision of row j - 1 (needs only its normalisers); every
+        // thread takes it (no broadcast needed), thread 0 records it
+        if (hB) {
+          const int rb = (j - 1) % 3;
+          wait_cta(sm, &sm.mrec[rb], (uint32_t)(((j - 1) / 3) & 1), a.status);
+          const Meta& M = sm.rec[rb];
+          const RowState S0{Lp, Lq, invZq, -1, 0, 0u};
+          uint32_t bits = 0;
+          int acc0 = -1;
+          if (M.nk > 0 && child_test<QK>(M, P.kidcap, 0, 0.f, 1.f, 1.f, S0, kt, invT, V, &bits))
+            acc0 = M.kid[0].node;
+          if (tid == 0) {
+            if (rank == 0) {
+              if (!(zp_tot > 0.f) || isnan(zp_tot)) bits |= SPEC_STATUS_NAN;
+              if (qb >= 0 && (!(zq_tot > 0.f) || isnan(zq_tot))) bits |= SPEC_STATUS_NAN;
+            }
+            RowState& S = sm.rs[(j - 1) & 1];
+            S.Lp = Lp;
+            S.Lq = Lq;
+            S.invZq = invZq;
+            S.accepted = acc0;
+            S.pending = (M.nk > 0 && acc0 < 0) ? 1 : 0;
+            S.bits = bits;
+          }
+        }
+
+      };
 
       // 4. one row-time of chunks: pass A of row j, pass B of row j - 1
+      row_start();
       if (j > nrow) break;
       float m = neg_inf(), z = 0.f, mq = neg_inf(), zq = 0.f;
       float acc_a = 0.f, acc_r = 0.f;
-      const float negLp = -Lp, negLq = -Lq;
       for (int c = 0; c < nch; ++c) {
         wait_cta(sm, &sm.full[stg], (uint32_t)(round & 1), a.status);
         const int e = c * kCH + tid * kEPT;
@@ -591,39 +619,23 @@ __global__ void __launch_bounds__(kThreads, 1) unit_stream(StreamParams P) {
             const unsigned char* sa = stage(stg, 0);
             float x[8];
             load8<TT>(reinterpret_cast<const TT*>(sa) + tid * kEPT, x);
-            float cm = fmaxf(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])),
-                             fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7])));
-            const float mn = fmaxf(m, __fmul_rn(cm, kt));
-            if (mn != neg_inf()) {
-              float zz = (m == neg_inf()) ? 0.f : z * ex2(m - mn);
-#pragma unroll
-              for (int i = 0; i < 8; ++i) zz += ex2(fmaf(x[i], kt, -mn));
-              z = zz;
-              m = mn;
-            }
+            lazy_sum(x, kt, m, z);
             if (qa >= 0) {
               float y[8];
               load8<TD>(reinterpret_cast<const TD*>(sa + kTB) + tid * kEPT, y);
               if constexpr (QK == Q_PROBS_T1) {
                 zq += ((y[0] + y[1]) + (y[2] + y[3])) + ((y[4] + y[5]) + (y[6] + y[7]));
+              } else if constexpr (QK == Q_LOGITS) {
+                lazy_sum(y, kt, mq, zq);
               } else {
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                  y[i] = (QK == Q_LOGITS) ? __fmul_rn(y[i], kt) : __fmul_rn(lg2(y[i]), invT);
-                const float cq = fmaxf(fmaxf(fmaxf(y[0], y[1]), fmaxf(y[2], y[3])),
-                                       fmaxf(fmaxf(y[4], y[5]), fmaxf(y[6], y[7])));
-                const float mnq = fmaxf(mq, cq);
-                if (mnq != neg_inf()) {
-                  float zz = (mq == neg_inf()) ? 0.f : zq * ex2(mq - mnq);
-#pragma unroll
-                  for (int i = 0; i < 8; ++i) zz += ex2(y[i] - mnq);
-                  zq = zz;
-                  mq = mnq;
-                }
+                for (int i = 0; i < 8; ++i) y[i] = lg2(y[i]);
+                lazy_sum(y, invT, mq, zq);
               }
             }
           }
           if (qb >= 0) {
+            const float negLp = -Lp, negLq = -Lq;
             const unsigned char* sb = stage(stg, 1);
             float x[8], y[8];
             load8<TT>(reinterpret_cast<const TT*>(sb) + tid * kEPT, x);
