@@ -45,7 +45,7 @@ namespace {  // internal to each translation unit that instantiates it
 
 constexpr int kCW = 16;             // consumer warps
 constexpr int kCT = kCW * 32;       // consumer threads
-constexpr int kThreads = kCT + 32;  // + one producer warp
+constexpr int kThreads = kCT + 64;  // + a producer warp and a control warp
 constexpr int kEPT = 8;             // logits per consumer thread per chunk
 constexpr int kCH = kCT * kEPT;     // logits per chunk (4096)
 constexpr int kMaxC = 4;
@@ -490,7 +490,8 @@ __global__ void __launch_bounds__(kThreads, 1) unit_stream(StreamParams P) {
       }
     }
   } else {
-    // ----------------------------------------------------------- consumers
+    // ------------------------------------------- consumers and control warp
+    const bool ctl = warp == kCW + 1;
     int stg = 0, round = 0;
     int sxq = 0;                        // continuation exchanges so far
     float Lp = 0.f, Lq = 0.f, invZq = 0.f;  // normalisers of the pass-B row
@@ -545,8 +546,8 @@ __global__ void __launch_bounds__(kThreads, 1) unit_stream(StreamParams P) {
           }
         }
 
-        // 2. decisions of row j - 2 that need its residual mass R (thread 0)
-        if (j >= 2 && tid == 0) {
+        // 2. decisions of row j - 2 that need its residual mass R (control)
+        if (j >= 2 && ctl && lane == 0) {
           const int rr = j - 2;
           const int64_t ur = ub - ncl;
           const RowState& S = sm.rs[rr & 1];
@@ -578,9 +579,8 @@ __global__ void __launch_bounds__(kThreads, 1) unit_stream(StreamParams P) {
           mbar_arrive(&sm.recfree[rr % 3]);
         }
 
-        // 3. first decision of row j - 1 (needs only its normalisers); every
-        // thread takes it (no broadcast needed), thread 0 records it
-        if (hB) {
+        // 3. first decision of row j - 1 (needs only its normalisers; control)
+        if (hB && ctl && lane == 0) {
           const int rb = (j - 1) % 3;
           wait_cta(sm, &sm.mrec[rb], (uint32_t)(((j - 1) / 3) & 1), a.status);
           const Meta& M = sm.rec[rb];
@@ -589,26 +589,30 @@ __global__ void __launch_bounds__(kThreads, 1) unit_stream(StreamParams P) {
           int acc0 = -1;
           if (M.nk > 0 && child_test<QK>(M, P.kidcap, 0, 0.f, 1.f, 1.f, S0, kt, invT, V, &bits))
             acc0 = M.kid[0].node;
-          if (tid == 0) {
-            if (rank == 0) {
-              if (!(zp_tot > 0.f) || isnan(zp_tot)) bits |= SPEC_STATUS_NAN;
-              if (qb >= 0 && (!(zq_tot > 0.f) || isnan(zq_tot))) bits |= SPEC_STATUS_NAN;
-            }
-            RowState& S = sm.rs[(j - 1) & 1];
-            S.Lp = Lp;
-            S.Lq = Lq;
-            S.invZq = invZq;
-            S.accepted = acc0;
-            S.pending = (M.nk > 0 && acc0 < 0) ? 1 : 0;
-            S.bits = bits;
+          if (rank == 0) {
+            if (!(zp_tot > 0.f) || isnan(zp_tot)) bits |= SPEC_STATUS_NAN;
+            if (qb >= 0 && (!(zq_tot > 0.f) || isnan(zq_tot))) bits |= SPEC_STATUS_NAN;
           }
+          RowState& S = sm.rs[(j - 1) & 1];
+          S.Lp = Lp;
+          S.Lq = Lq;
+          S.invZq = invZq;
+          S.accepted = acc0;
+          S.pending = (M.nk > 0 && acc0 < 0) ? 1 : 0;
+          S.bits = bits;
         }
 
       };
 
-      // 4. one row-time of chunks: pass A of row j, pass B of row j - 1
+      // 4. one row-time of chunks: pass A of row j, pass B of row j - 1 (the
+      // control warp only takes the decisions)
       row_start();
       if (j > nrow) break;
+      if (ctl) {
+        q_prev = qa;
+        q_cur = q_next;
+        continue;
+      }
       float m = neg_inf(), z = 0.f, mq = neg_inf(), zq = 0.f;
       float acc_a = 0.f, acc_r = 0.f;
       for (int c = 0; c < nch; ++c) {
