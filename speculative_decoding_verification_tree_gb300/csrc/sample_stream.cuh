@@ -736,6 +736,7 @@ constexpr int kWalkWarps = kWalkThreads / 32;
 constexpr int kMaxW = 8;  // CTAs per sequence in the walk
 
 struct WalkSmem {
+  int child[SPEC_MAX_TREE_NODES + 1];  // each row's outcome (RowOut::child)
   float wsum[kMaxTiles][kWalkWarps];  // per (chunk, warp) masses of the draw
   float red[kWalkWarps];
   float xs[2][kMaxW];                 // cluster exchange slots (by parity)
@@ -760,6 +761,7 @@ __global__ void __launch_bounds__(kWalkThreads) stream_walk(StreamParams P) {
   const int r0 = (int)rank * P.wslice;
   const int len = max(0, min(P.wslice, V - r0));
   const int nch = (len + kCH - 1) / kCH;
+  for (int r = tid; r <= n; r += kWalkThreads) ws.child[r] = a.rowout[u0 + r].child;
   if (rank == 0) {
     for (int r = tid; r <= n; r += kWalkThreads) {
       const int64_t row = u0 + r;
@@ -860,21 +862,23 @@ __global__ void __launch_bounds__(kWalkThreads) stream_walk(StreamParams P) {
   for (;;) {
     if (tid == 0) {
       int rr = ws.rr, plen = ws.len;
-      RowOut st = a.rowout[u0 + rr];
-      if (ws.act == 1) st = ws.st;  // continuing a pending row
+      RowOut st;
+      bool have = ws.act == 1;  // continuing a pending row
+      if (have) st = ws.st;
       int act = 0;
       for (;;) {
-        if (st.child >= 0 && st.child < n && plen < n) {
-          const int j = st.child;
+        const int ch = have ? st.child : ws.child[rr];
+        if (ch >= 0 && ch < n && plen < n) {
           if (rank == 0) {
-            if (!s.chain) a.path_nodes[(int64_t)b * n + plen] = j;
-            a.out_tokens[u0 + plen] = a.node_tokens[(int64_t)b * n + j];
+            if (!s.chain) a.path_nodes[(int64_t)b * n + plen] = ch;
+            a.out_tokens[u0 + plen] = a.node_tokens[(int64_t)b * n + ch];
           }
           ++plen;
-          rr = j + 1;
-          st = a.rowout[u0 + rr];
+          rr = ch + 1;
+          have = false;
           continue;
         }
+        if (!have) st = a.rowout[u0 + rr];  // the row where the walk stops or waits
         act = (st.child == -2) ? 1 : 2;
         break;
       }
