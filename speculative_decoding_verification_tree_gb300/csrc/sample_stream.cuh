@@ -1111,13 +1111,14 @@ cudaError_t launch_t(StreamParams P, cudaStream_t st) {
   e = cudaLaunchKernelEx(&cfg, kern, P);
   prof_end(SPEC_PROF_VERIFY, st);
   if (e != cudaSuccess) return e;
-  // walk: as many CTAs per sequence as fill the GPU once (1..8), at least
-  // enough for the draw's chunk table
+  // walk: as many CTAs per sequence (1..4) as fit the GPU at two CTAs per SM
+  // (more made the cluster barriers cost more than the passes gain), at
+  // least enough for the draw's chunk table (up to 8)
   int sms = 0;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, 0);
   if (e != cudaSuccess) return e;
   int w = 1;
-  while (w < kMaxW && (int64_t)P.s.B * w * 2 <= sms) w *= 2;
+  while (w < 4 && (int64_t)P.s.B * w * 2 <= 2 * sms) w *= 2;
   for (;;) {
     const int sl = ((P.s.V + w - 1) / w + 7) / 8 * 8;
     if ((sl + kCH - 1) / kCH <= kMaxTiles || w == kMaxW) {
