@@ -171,6 +171,8 @@ struct Smem {
   float4 wst[2][kCW];         // per-warp statistics (double-buffered by row-time)
   float2 wab[2][kCW];         // per-warp alpha / residual
   RowState rs[2];
+  uint64_t dec[2];            // control warp -> consumers: needR of the pass-B row
+  int needR[2];
   int dead;                   // a bounded wait gave up: skip the remaining waits
 };
 
@@ -434,6 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1) unit_stream(StreamParams P) {
       mbar_init(&sm.recfree[i], 1);
     }
     for (int i = 0; i < 4; ++i) mbar_init(&sm.xbar[i], 1);
+    for (int i = 0; i < 2; ++i) mbar_init(&sm.dec[i], 1);
     fence_mbar_init();
   }
   cluster_sync();  // every CTA's barriers exist before the first st.async
@@ -546,6 +549,33 @@ __global__ void __launch_bounds__(kThreads, 1) unit_stream(StreamParams P) {
           }
         }
 
+        // 3. first decision of row j - 1 (needs only its normalisers; control)
+        if (hB && ctl && lane == 0) {
+          const int rb = (j - 1) % 3;
+          wait_cta(sm, &sm.mrec[rb], (uint32_t)(((j - 1) / 3) & 1), a.status);
+          const Meta& M = sm.rec[rb];
+          const RowState S0{Lp, Lq, invZq, -1, 0, 0u};
+          uint32_t bits = 0;
+          int acc0 = -1;
+          if (M.nk > 0 && child_test<QK>(M, P.kidcap, 0, 0.f, 1.f, 1.f, S0, kt, invT, V, &bits))
+            acc0 = M.kid[0].node;
+          if (rank == 0) {
+            if (!(zp_tot > 0.f) || isnan(zp_tot)) bits |= SPEC_STATUS_NAN;
+            if (qb >= 0 && (!(zq_tot > 0.f) || isnan(zq_tot))) bits |= SPEC_STATUS_NAN;
+          }
+          RowState& S = sm.rs[(j - 1) & 1];
+          S.Lp = Lp;
+          S.Lq = Lq;
+          S.invZq = invZq;
+          S.accepted = acc0;
+          S.pending = (M.nk > 0 && acc0 < 0) ? 1 : 0;
+          S.bits = bits;
+          // pass B needs R only for a second child's test
+          sm.needR[(j - 1) & 1] = (M.nk >= 2 && acc0 < 0) ? 1 : 0;
+          mbar_arrive(&sm.dec[(j - 1) & 1]);
+        }
+
+
         // 2. decisions of row j - 2 that need its residual mass R (control)
         if (j >= 2 && ctl && lane == 0) {
           const int rr = j - 2;
@@ -579,29 +609,6 @@ __global__ void __launch_bounds__(kThreads, 1) unit_stream(StreamParams P) {
           mbar_arrive(&sm.recfree[rr % 3]);
         }
 
-        // 3. first decision of row j - 1 (needs only its normalisers; control)
-        if (hB && ctl && lane == 0) {
-          const int rb = (j - 1) % 3;
-          wait_cta(sm, &sm.mrec[rb], (uint32_t)(((j - 1) / 3) & 1), a.status);
-          const Meta& M = sm.rec[rb];
-          const RowState S0{Lp, Lq, invZq, -1, 0, 0u};
-          uint32_t bits = 0;
-          int acc0 = -1;
-          if (M.nk > 0 && child_test<QK>(M, P.kidcap, 0, 0.f, 1.f, 1.f, S0, kt, invT, V, &bits))
-            acc0 = M.kid[0].node;
-          if (rank == 0) {
-            if (!(zp_tot > 0.f) || isnan(zp_tot)) bits |= SPEC_STATUS_NAN;
-            if (qb >= 0 && (!(zq_tot > 0.f) || isnan(zq_tot))) bits |= SPEC_STATUS_NAN;
-          }
-          RowState& S = sm.rs[(j - 1) & 1];
-          S.Lp = Lp;
-          S.Lq = Lq;
-          S.invZq = invZq;
-          S.accepted = acc0;
-          S.pending = (M.nk > 0 && acc0 < 0) ? 1 : 0;
-          S.bits = bits;
-        }
-
       };
 
       // 4. one row-time of chunks: pass A of row j, pass B of row j - 1 (the
@@ -612,6 +619,11 @@ __global__ void __launch_bounds__(kThreads, 1) unit_stream(StreamParams P) {
         q_prev = qa;
         q_cur = q_next;
         continue;
+      }
+      bool needR = false;
+      if (qb >= 0) {
+        wait_cta(sm, &sm.dec[(j - 1) & 1], (uint32_t)(((j - 1) >> 1) & 1), a.status);
+        needR = sm.needR[(j - 1) & 1] != 0;
       }
       float m = neg_inf(), z = 0.f, mq = neg_inf(), zq = 0.f;
       float acc_a = 0.f, acc_r = 0.f;
@@ -644,15 +656,26 @@ __global__ void __launch_bounds__(kThreads, 1) unit_stream(StreamParams P) {
             float x[8], y[8];
             load8<TT>(reinterpret_cast<const TT*>(sb) + tid * kEPT, x);
             load8<TD>(reinterpret_cast<const TD*>(sb + kTB) + tid * kEPT, y);
-            float lr = 0.f;
+            if (needR) {
+              float lr = 0.f;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float p = ex2(fmaf(x[i], kt, negLp));
-              const float mn = fminf(p, q_of<QK>(y[i], kt, invT, negLq, invZq));
-              acc_a += mn;
-              lr += p - mn;
+              for (int i = 0; i < 8; ++i) {
+                const float p = ex2(fmaf(x[i], kt, negLp));
+                const float mn = fminf(p, q_of<QK>(y[i], kt, invT, negLq, invZq));
+                acc_a += mn;
+                lr += p - mn;
+              }
+              acc_r += lr;
+            } else if constexpr (QK == Q_LOGITS) {
+              // min(p, q) = 2^min(log2 p, log2 q): one exponential
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                acc_a += ex2(fminf(fmaf(x[i], kt, negLp), fmaf(y[i], kt, negLq)));
+            } else {
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                acc_a += fminf(ex2(fmaf(x[i], kt, negLp)), q_of<QK>(y[i], kt, invT, negLq, invZq));
             }
-            acc_r += lr;
           }
         }
         __syncwarp();
