@@ -127,7 +127,12 @@ size_t spec_workspace_bytes(int op, int B, int n, int V);
  *     every k (also after the first rejection); at temperature 0 the
  *     indicator 1[x_k == argmax_k].
  * B >= 0 (0 = nothing to do), 0 <= K <= SPEC_MAX_TREE_NODES,
- * 1 <= V <= SPEC_MAX_VOCAB.
+ * 1 <= V <= SPEC_MAX_VOCAB.  Sampling over the full vocabulary streams rows
+ * whose pointers are 16-byte aligned with V % 8 == 0 up to V = 524288; other
+ * rows (odd lengths, unaligned pointers) up to about 200 K float32 or 400 K
+ * bfloat16 logits per row pair; beyond that the call returns
+ * SPEC_ERR_UNSUPPORTED before launching anything.  The same holds for
+ * spec_verify_tree.
  */
 int spec_verify_chain(const void* target_logits, const void* draft,
                       const int32_t* draft_tokens, int B, int K, int V,

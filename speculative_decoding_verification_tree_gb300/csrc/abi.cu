@@ -79,6 +79,7 @@ int run_verify(const VerifyShape& s, VerifyArgs& a, void* ws, size_t ws_bytes, c
   a.topk_val = (float*)(base + w.off_tval);
   a.topk_cnt = (int32_t*)(base + w.off_tcnt);
   a.rowout = (RowOut*)(base + w.off_out);
+  if (a.prm.temperature != 0.f && !sampled_supported(s, a)) return SPEC_ERR_UNSUPPORTED;
   cudaError_t e = cudaMemsetAsync(a.status, 0, sizeof(uint32_t), st);
   if (e != cudaSuccess) return SPEC_ERR_CUDA;
   if (s.B == 0) return SPEC_OK;

@@ -127,6 +127,7 @@ void prof_end(int kind, cudaStream_t st);
 
 cudaError_t launch_greedy(const VerifyShape& s, const VerifyArgs& a, cudaStream_t st);
 cudaError_t launch_sampled(const VerifyShape& s, const VerifyArgs& a, cudaStream_t st);
+bool sampled_supported(const VerifyShape& s, const VerifyArgs& a);
 cudaError_t launch_tree_mask(const int32_t* parent, int B, int N, uint8_t* mask,
                              uint64_t* bits, cudaStream_t st);
 cudaError_t launch_philox(uint64_t seed, uint32_t offset, const int32_t* b, const int32_t* i,

@@ -670,15 +670,31 @@ cudaError_t launch_units(const UnitParams& P, int C, cudaStream_t st) {
 
 // Cluster size and slice for a row of V logits: the smallest cluster whose
 // per-CTA slices fit the shared-memory budget.
-void full_geometry(int V, int bytes_per_elem, int* C, int* slice) {
-  const int budget = 100 * 1024;
-  int c = 1;
-  for (; c < kMaxCluster; c *= 2) {
+bool full_geometry(int V, int bytes_per_elem, int* C, int* slice) {
+  const int budget = 200 * 1024;  // dynamic shared memory of one CTA
+  for (int c = 1; c <= kMaxCluster; c *= 2) {
     const int sl = ((V + c - 1) / c + kSliceQuant - 1) / kSliceQuant * kSliceQuant;
-    if ((int64_t)sl * bytes_per_elem <= budget) break;
+    if ((int64_t)sl * bytes_per_elem <= budget) {
+      *C = c;
+      *slice = sl;
+      return true;
+    }
   }
-  *C = c;
-  *slice = ((V + c - 1) / c + kSliceQuant - 1) / kSliceQuant * kSliceQuant;
+  return false;
+}
+
+// Full-vocabulary sampled verification can run: the streaming kernel takes
+// 16-byte aligned rows, the general kernel any row whose slice fits one
+// CTA's shared memory in a cluster of up to 8.
+bool sampled_supported(const VerifyShape& s, const VerifyArgs& a) {
+  if (truncation_k(&a.prm, s.V) > 0) return true;
+  const int tsz = a.dt_target == SPEC_BF16 ? 2 : 4;
+  const int dsz = a.dt_draft == SPEC_BF16 ? 2 : 4;
+  const bool al_t = ((uintptr_t)a.target % 16 == 0) && ((int64_t)s.V * tsz % 16 == 0);
+  const bool al_d = (a.draft == nullptr) || (((uintptr_t)a.draft % 16 == 0) && ((int64_t)s.V * dsz % 16 == 0));
+  int c, sl, nch, ns;
+  if (al_t && al_d && stream_geometry(s.V, tsz, dsz, &c, &sl, &nch, &ns)) return true;
+  return full_geometry(s.V, tsz + dsz, &c, &sl);
 }
 
 cudaError_t launch_sampled(const VerifyShape& s, const VerifyArgs& a, cudaStream_t st) {
@@ -693,8 +709,8 @@ cudaError_t launch_sampled(const VerifyShape& s, const VerifyArgs& a, cudaStream
   P.a = a;
   const int tsz = a.dt_target == SPEC_BF16 ? 2 : 4;
   const int dsz = a.dt_draft == SPEC_BF16 ? 2 : 4;
-  int C, slice;
-  full_geometry(s.V, tsz + dsz, &C, &slice);
+  int C = 1, slice = 0;
+  const bool full_ok = full_geometry(s.V, tsz + dsz, &C, &slice);
   P.slice = slice;
   const bool al_t = ((uintptr_t)a.target % 16 == 0) && ((int64_t)s.V * tsz % 16 == 0);
   const bool al_d = (a.draft == nullptr) || (((uintptr_t)a.draft % 16 == 0) && ((int64_t)s.V * dsz % 16 == 0));
@@ -717,6 +733,7 @@ cudaError_t launch_sampled(const VerifyShape& s, const VerifyArgs& a, cudaStream
     Q.rec_bytes = meta_rec_bytes(s.chain);
     return (a.dt_target == SPEC_BF16) ? launch_stream_bf16(Q, st) : launch_stream_f32(Q, st);
   }
+  if (!full_ok) return cudaErrorNotSupported;
   prof_begin(SPEC_PROF_VERIFY, st);
 #define SV_DISPATCH(TT, TD)                                     \
   if (qk == Q_LOGITS) e = launch_units<TT, TD, Q_LOGITS>(P, C, st); \

@@ -88,6 +88,9 @@ def test_chain_argument_errors(lib):
         lib.SPEC_ERR_UNSUPPORTED
     assert _chain(lib, V=5000, prm=_prm(lib, top_k=2000)) == \
         lib.SPEC_ERR_UNSUPPORTED
+    # an odd row length too long for the general kernel's shared memory
+    big = lib.raw("spec_workspace_bytes", lib.SPEC_OP_CHAIN, 2, 3, 700001)
+    assert _chain(lib, V=700001, ws_bytes=big) == lib.SPEC_ERR_UNSUPPORTED
     assert _chain(lib, ws=None) == lib.SPEC_ERR_WORKSPACE
     assert _chain(lib, ws=ctypes.c_void_p(0x7f0000000010)) == \
         lib.SPEC_ERR_WORKSPACE

@@ -62,6 +62,17 @@ def test_chain_vocab_sizes(V, dt):
     assert ex <= 1
 
 
+@pytest.mark.parametrize("V,dt", [(300000, "bf16"), (150001, "f32")])
+def test_chain_large_vocab(V, dt):
+    # V = 300000 (aligned): the streaming kernel with 4-CTA clusters;
+    # V = 150001 (odd row length): the general kernel, 8-CTA clusters
+    tdt = torch.float32 if dt == "f32" else torch.bfloat16
+    w = synth.workload("chain_sample", B=3, K=2, V=V, target_dtype=tdt,
+                       draft_dtype=tdt, seed=V % 1000)
+    gpu, ref = run(w)
+    assert compare_chain(gpu, ref) <= 1
+
+
 @pytest.mark.parametrize("T", [1.0, 0.6])
 def test_chain_probs_draft(T):
     w = synth.workload("chain_sample", B=8, K=4, V=5000, draft_kind="probs",

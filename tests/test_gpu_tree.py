@@ -109,6 +109,14 @@ def test_static_tree_small_vocab(V):
     assert ex <= 1
 
 
+def test_static_tree_large_vocab():
+    # aligned V = 300000: 4-CTA clusters in the streaming kernel and the walk
+    w = synth.workload("tree_static", B=2, V=300000, seed=8)
+    ins = synth.tree_inputs(w, "cuda")
+    gpu, ref = run_tree(w, *ins)
+    assert compare_tree(gpu, ref) <= 1
+
+
 def test_static_tree_low_acceptance_many_sibling_passes():
     # noisy draft: most first children are rejected, siblings are tried
     w = synth.workload("tree_static", B=12, V=2000, draft_noise=3.0, seed=5)
