@@ -16,7 +16,7 @@ inline size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 // Workspace of a verification call: [status | row_child | row_token | argmax parts]
 struct VerifyWs {
   size_t off_child, off_token, off_parts, off_alpha, off_meta, off_qres;
-  size_t off_tidx, off_tval, off_tcnt, off_out, total;
+  size_t off_tidx, off_tval, off_tcnt, off_out, off_qlist, total;
 };
 VerifyWs verify_ws(int B, int n, int V, bool chain) {
   const size_t rows = (size_t)B * (n + 1);
@@ -31,7 +31,8 @@ VerifyWs verify_ws(int B, int n, int V, bool chain) {
   w.off_tval = w.off_tidx + up(2 * rows * SPEC_MAX_TOP_K * sizeof(int32_t));
   w.off_tcnt = w.off_tval + up(2 * rows * SPEC_MAX_TOP_K * sizeof(float));
   w.off_out = w.off_tcnt + up(2 * rows * sizeof(int32_t));
-  w.total = w.off_out + up(rows * sizeof(RowOut));
+  w.off_qlist = w.off_out + up(rows * sizeof(RowOut));
+  w.total = w.off_qlist + up(rows * sizeof(int32_t));
   return w;
 }
 struct Eagle2Ws {
@@ -79,8 +80,10 @@ int run_verify(const VerifyShape& s, VerifyArgs& a, void* ws, size_t ws_bytes, c
   a.topk_val = (float*)(base + w.off_tval);
   a.topk_cnt = (int32_t*)(base + w.off_tcnt);
   a.rowout = (RowOut*)(base + w.off_out);
+  a.qlist = (int32_t*)(base + w.off_qlist);
+  a.qcount = (int32_t*)(base + 4);  // beside the status word, zeroed with it
   if (a.prm.temperature != 0.f && !sampled_supported(s, a)) return SPEC_ERR_UNSUPPORTED;
-  cudaError_t e = cudaMemsetAsync(a.status, 0, sizeof(uint32_t), st);
+  cudaError_t e = cudaMemsetAsync(a.status, 0, 2 * sizeof(uint32_t), st);
   if (e != cudaSuccess) return SPEC_ERR_CUDA;
   if (s.B == 0) return SPEC_OK;
   if (a.prm.temperature == 0.f) return cuda_rc(launch_greedy(s, a, st));

@@ -76,6 +76,8 @@ struct VerifyArgs {
   float* topk_val;      //   (target rows, then draft rows)
   int32_t* topk_cnt;    // [2 * rows]
   RowOut* rowout;       // [rows] row outcomes of the streaming verifier
+  int32_t* qlist;       // [rows] rows that have a draft row (the streaming kernel's work)
+  int32_t* qcount;      //   their number (zeroed with the status word)
 };
 
 // Tokens a truncating sampling transform keeps per row: min(top_k, V), with

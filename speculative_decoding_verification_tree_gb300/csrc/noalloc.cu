@@ -43,9 +43,9 @@ constexpr size_t kAlphaBytes = (size_t)SPEC_NOALLOC_MAX_ROWS * kAlphaSlots * siz
 constexpr size_t kMetaBytes = (size_t)SPEC_NOALLOC_MAX_ROWS * 48;  // chain row records
 constexpr size_t kOutBytes = (size_t)SPEC_NOALLOC_MAX_ROWS * sizeof(RowOut);
 constexpr size_t kScratchBytes =
-    kStatusBytes + 3 * kRowBytes + kPartBytes + kAlphaBytes + kMetaBytes + kOutBytes;
+    kStatusBytes + 4 * kRowBytes + kPartBytes + kAlphaBytes + kMetaBytes + kOutBytes;
 
-// The scratch itself (~1.7 MiB per device).  In host code this name is only
+// The scratch itself (~1.75 MiB per device).  In host code this name is only
 // a stand-in; its device address comes from cudaGetSymbolAddress below.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
@@ -124,10 +124,13 @@ extern "C" int spec_verify_chain_noalloc(const void* target_logits, const void* 
   a.meta = (unsigned char*)(p + kStatusBytes + 2 * kRowBytes + kPartBytes + kAlphaBytes);
   a.qres = (int32_t*)(p + kStatusBytes + 2 * kRowBytes + kPartBytes + kAlphaBytes + kMetaBytes);
   a.rowout = (RowOut*)(p + kStatusBytes + 3 * kRowBytes + kPartBytes + kAlphaBytes + kMetaBytes);
+  a.qlist = (int32_t*)(p + kStatusBytes + 3 * kRowBytes + kPartBytes + kAlphaBytes + kMetaBytes +
+                       kOutBytes);
+  a.qcount = (int32_t*)(p + 4);  // beside the status word, zeroed with it
   if (meta_rec_bytes(true) != 48) return SPEC_ERR_CUDA;  // chain row record size
   // the status word must start at zero; everything else is written before it
   // is read within the call
-  if (cudaMemsetAsync(a.status, 0, sizeof(uint32_t), st) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (cudaMemsetAsync(a.status, 0, 2 * sizeof(uint32_t), st) != cudaSuccess) return SPEC_ERR_CUDA;
   if (B == 0) return SPEC_OK;
   const cudaError_t e = greedy ? launch_greedy(s, a, st) : launch_sampled(s, a, st);
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;

@@ -151,6 +151,22 @@ __global__ void __launch_bounds__(256) row_meta(VerifyShape s, VerifyArgs a, int
     h->bad = bad;
     h->u_draw = philox_uniform(a.prm.seed, a.prm.philox_offset, (uint32_t)b, (uint32_t)r, 1u);
     a.qres[unit] = qr;
+    if (a.qlist) {
+      if (qr >= 0) {  // the streaming kernel's work: rows that have a draft row
+        a.qlist[atomicAdd(a.qcount, 1)] = (int32_t)unit;
+      } else {
+        // a row without a draft row has no children and no acceptance mass;
+        // the walk finds its normaliser only if it draws there (Lp = NaN)
+        RowOut o{};
+        o.child = -1;
+        o.W = 1.f;
+        o.D = 1.f;
+        o.Lp = __int_as_float(0x7fc00000);
+        o.bits = bad;
+        a.rowout[unit] = o;
+        flag_status(a.status, bad);
+      }
+    }
   }
 }
 
@@ -407,7 +423,13 @@ __global__ void __launch_bounds__(kThreads, 1) unit_stream(StreamParams P) {
   const int C = P.C;
   const int cid = blockIdx.x / C;
   const int ncl = P.nclusters;
-  const int64_t nunits = s.rows();
+  const int64_t nunits = *reinterpret_cast<volatile const int32_t*>(a.qcount);  // rows with a draft row
+  // when every row has a draft row the list is all rows: keep row order
+  const bool ident = nunits == s.rows();
+  auto unit_of = [&](int j) -> int64_t {
+    const int64_t i = cid + (int64_t)j * ncl;
+    return ident ? i : (int64_t)a.qlist[i];
+  };
   const int V = s.V, n = s.n;
   const int r0 = (int)rank * P.slice;
   const int len = max(0, min(P.slice, V - r0));
@@ -448,12 +470,17 @@ __global__ void __launch_bounds__(kThreads, 1) unit_stream(StreamParams P) {
       asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_a));
       asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol_b));
       int stg = 0, round = 0;
-      int q_cur = a.qres[cid], q_prev = -1;
+      // this cluster's rows: qlist[cid + j * ncl]; unit ids and draft rows
+      // are read two and one rows ahead of their use
+      int64_t u_cur = unit_of(0), u_prev = -1;
+      int64_t u_nxt = (1 < nrow) ? unit_of(1) : -1;
+      int q_cur = a.qres[u_cur], q_prev = -1;
       for (int j = 0; j <= nrow; ++j) {
         const bool hA = j < nrow, hB = j >= 1;
-        const int64_t ua = cid + (int64_t)j * ncl, ub = ua - ncl;
+        const int64_t ua = u_cur, ub = u_prev;
         const int qa = hA ? q_cur : -1, qb = hB ? q_prev : -1;
-        const int q_next = (j + 1 < nrow) ? a.qres[ua + ncl] : -1;
+        const int64_t u_nn = (j + 2 < nrow) ? unit_of(j + 2) : -1;
+        const int q_next = (u_nxt >= 0) ? a.qres[u_nxt] : -1;
         if (hA) {  // row j's record: read at its first decision and its last
           const int rb = j % 3;
           if (j >= 3) wait_cta(sm, &sm.recfree[rb], (uint32_t)(((j / 3) - 1) & 1), a.status);
@@ -461,9 +488,9 @@ __global__ void __launch_bounds__(kThreads, 1) unit_stream(StreamParams P) {
           bulk_g2s(&sm.rec[rb], a.meta + ua * (int64_t)P.rec_bytes, (uint32_t)P.rec_bytes,
                    &sm.mrec[rb]);
         }
-        const TT* ta = tgt + ua * (int64_t)V + r0;
+        const TT* ta = hA ? tgt + ua * (int64_t)V + r0 : nullptr;
         const TD* da = qa >= 0 ? draft_row(ua, qa) + r0 : nullptr;
-        const TT* tb = tgt + ub * (int64_t)V + r0;
+        const TT* tb = hB ? tgt + ub * (int64_t)V + r0 : nullptr;
         const TD* db = qb >= 0 ? draft_row(ub, qb) + r0 : nullptr;
         for (int c = 0; c < nch; ++c) {
           if (round > 0) wait_cta(sm, &sm.empty[stg], (uint32_t)((round - 1) & 1), a.status);
@@ -490,6 +517,9 @@ __global__ void __launch_bounds__(kThreads, 1) unit_stream(StreamParams P) {
         }
         q_prev = qa;
         q_cur = q_next;
+        u_prev = ua;
+        u_cur = u_nxt;
+        u_nxt = u_nn;
       }
     }
   } else {
@@ -499,12 +529,14 @@ __global__ void __launch_bounds__(kThreads, 1) unit_stream(StreamParams P) {
     int sxq = 0;                        // continuation exchanges so far
     float Lp = 0.f, Lq = 0.f, invZq = 0.f;  // normalisers of the pass-B row
     float zp_tot = 0.f, zq_tot = 0.f;
-    int q_cur = nrow > 0 ? a.qres[cid] : -1, q_prev = -1;
+    int64_t u_cur = nrow > 0 ? unit_of(0) : -1, u_prev = -1, u_prev2 = -1;
+    int q_cur = nrow > 0 ? a.qres[u_cur] : -1, q_prev = -1;
     for (int j = 0; nrow > 0 && j <= nrow + 1; ++j) {
       const bool hA = j < nrow, hB = j >= 1 && j <= nrow;
       const int qa = hA ? q_cur : -1, qb = hB ? q_prev : -1;
-      const int q_next = (j + 1 < nrow) ? a.qres[cid + (int64_t)(j + 1) * ncl] : -1;
-      const int64_t ua = cid + (int64_t)j * ncl, ub = ua - ncl;
+      const int64_t u_next = (j + 1 < nrow) ? unit_of(j + 1) : -1;
+      const int q_next = (u_next >= 0) ? a.qres[u_next] : -1;
+      const int64_t ua = u_cur, ub = u_prev, ur2 = u_prev2;
 
       // Steps 1-3: the previous row-time's exchange and the decisions it allows.
       auto row_start = [&]() {
@@ -579,7 +611,7 @@ __global__ void __launch_bounds__(kThreads, 1) unit_stream(StreamParams P) {
         // 2. decisions of row j - 2 that need its residual mass R (control)
         if (j >= 2 && ctl && lane == 0) {
           const int rr = j - 2;
-          const int64_t ur = ub - ncl;
+          const int64_t ur = ur2;
           const RowState& S = sm.rs[rr & 1];
           const Meta& M = sm.rec[rr % 3];
           RowOut st{};
@@ -618,6 +650,9 @@ __global__ void __launch_bounds__(kThreads, 1) unit_stream(StreamParams P) {
       if (ctl) {
         q_prev = qa;
         q_cur = q_next;
+        u_prev2 = u_prev;
+        u_prev = u_cur;
+        u_cur = u_next;
         continue;
       }
       bool needR = false;
@@ -740,6 +775,9 @@ __global__ void __launch_bounds__(kThreads, 1) unit_stream(StreamParams P) {
       }
       q_prev = qa;
       q_cur = q_next;
+      u_prev2 = u_prev;
+      u_prev = u_cur;
+      u_cur = u_next;
     }
   }
   cluster_sync();  // no CTA leaves while a peer may still push to it
@@ -763,6 +801,7 @@ struct WalkSmem {
   float wsum[kMaxTiles][kWalkWarps];  // per (chunk, warp) masses of the draw
   float red[kWalkWarps];
   float xs[2][kMaxW];                 // cluster exchange slots (by parity)
+  float xm[2][kMaxW];                 //   (maxima of a normaliser exchange)
   RowOut st;                          // walk state (thread 0 writes)
   int act;                            // 0 done, 1 pass, 2 draw
   int rr, len, rsel, tile, wsel;
@@ -875,6 +914,48 @@ __global__ void __launch_bounds__(kWalkThreads) stream_walk(StreamParams P) {
     return reduce_exchange(acc);
   };
 
+  // Base-2 log normaliser of target row u (a row the streaming kernel did
+  // not process): online sums over the CTA's slice, (max, sum) exchanged.
+  auto lse_pass = [&](int64_t u) -> float {
+    const TT* tr = reinterpret_cast<const TT*>(a.target) + u * (int64_t)V + r0;
+    float m = neg_inf(), z = 0.f;
+    for (int c = 0; c < nch; ++c) {
+      const int e = c * kCH + tid * kEPT;
+      if (e < len) {
+        Raw8<TT> xt;
+        ldg_raw<TT>(tr + e, xt);
+        float x[8];
+        unpack8(xt, x);
+        lazy_sum(x, kt, m, z);
+      }
+    }
+    MaxSum A = warp_ms(MaxSum{m, z});
+    if (lane == 0) {
+      ws.red[warp] = A.m;
+      ws.wsum[0][warp] = A.z;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      MaxSum B{(lane < kWalkWarps) ? ws.red[lane] : neg_inf(),
+               (lane < kWalkWarps) ? ws.wsum[0][lane] : 0.f};
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1)
+        B = ms_combine(B, MaxSum{__shfl_xor_sync(0xffffffffu, B.m, o),
+                                 __shfl_xor_sync(0xffffffffu, B.z, o)});
+      if (lane < C) {
+        const uint32_t dm = mapa(smem_u32(&ws.xm[xe & 1][rank]), (uint32_t)lane);
+        const uint32_t dz = mapa(smem_u32(&ws.xs[xe & 1][rank]), (uint32_t)lane);
+        asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dm), "f"(B.m) : "memory");
+        asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dz), "f"(B.z) : "memory");
+      }
+    }
+    cluster_sync();
+    MaxSum T{ws.xm[xe & 1][0], ws.xs[xe & 1][0]};
+    for (int i = 1; i < C; ++i) T = ms_combine(T, MaxSum{ws.xm[xe & 1][i], ws.xs[xe & 1][i]});
+    ++xe;
+    return T.m + log2f(T.z);
+  };
+
   // walk (thread 0 of every CTA, identical decisions)
   if (tid == 0) {
     ws.rr = 0;
@@ -927,6 +1008,7 @@ __global__ void __launch_bounds__(kWalkThreads) stream_walk(StreamParams P) {
       continue;
     }
     // draw at row ur from max(0, p - Cn q), else from max(0, p - Cc q)
+    if (isnan(st.Lp)) st.Lp = lse_pass(ur);  // a row without a draft row
     float Cx = st.Cn;
     float tot = pass(ur, qr, Cx, st, true);
     if (!(tot > 0.f) && Cx != 0.f) {
