@@ -58,13 +58,13 @@ def _args():
 
 # DRAM traffic per launch of the profiled kernel, from one ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum of a smaller batch, scaled
-# to the workload's rows), keyed by workload, with a hash of the sources the
+# to the rows the kernel processes), keyed by workload, with a hash of the sources the
 # kernel is built from at capture time.  Reported as null once they changed.
 _STREAM_SRC = ("sample_stream.cuh", "sample_stream_bf16.cu",
                "sample_stream_f32.cu", "common.cuh", "kernels.h")
 TRAFFIC = {
     # unit_stream, tree_static at B=16: 759.77 MB read + 3.70 MB written, 976 rows
-    "tree_static": {"bytes_per_row": 763.47e6 / 976, "src": _STREAM_SRC,
+    "tree_static": {"bytes_per_unit": 763.47e6 / 976, "src": _STREAM_SRC,
                     "hash": "ca2e2218f16009bc"},
 }
 
@@ -85,11 +85,11 @@ def _src_hash(files):
     return h.hexdigest()[:16]
 
 
-def _traffic(name, rows):
+def _traffic(name, units):
     t = TRAFFIC.get(name)
     if not t or t["hash"] != _src_hash(t["src"]):
         return None
-    return int(t["bytes_per_row"] * rows)
+    return int(t["bytes_per_unit"] * units)
 
 
 def _peaks():
@@ -120,6 +120,7 @@ class Work:
             self.target, self.draft, self.toks = synth.chain_inputs(w, device)
             B, K, V = w.B, w.K, w.V
             self.rows = B * K
+            self.kernel_units = self.rows
             self.ws = api.workspace(_lib.SPEC_OP_CHAIN, B, K, V, device)
             self.out = (torch.empty(B, dtype=torch.int32, device=device),
                         torch.empty(B, K + 1, dtype=torch.int32, device=device),
@@ -144,6 +145,7 @@ class Work:
             B, N, V = w.B, self.toks.shape[1], w.V
             self.N = N
             self.rows = B * (N + 1)
+            self.kernel_units = self.rows
             self.ws = api.workspace(_lib.SPEC_OP_TREE, B, N, V, device)
             self.out = (torch.empty(B, dtype=torch.int32, device=device),
                         torch.empty(B, N, dtype=torch.int32, device=device),
@@ -166,6 +168,10 @@ class Work:
             self.N = M
             self.R = self.draft.shape[1]
             self.ews = api.workspace(_lib.SPEC_OP_EAGLE2, B, self.R, V, device)
+            # each draft row's log2 normaliser: written by the expand, read
+            # by the verification (which then skips summing the draft rows)
+            self.lse = torch.empty(B, self.R, dtype=torch.float32,
+                                   device=device)
             self.tree = (torch.empty(B, M, dtype=torch.int32, device=device),
                          torch.empty(B, M, dtype=torch.int32, device=device),
                          torch.empty(B, M + 1, dtype=torch.int32,
@@ -188,8 +194,12 @@ class Work:
             self.inputs = [self.draft, self.target]
             self.prof_kind = _lib.SPEC_PROF_VERIFY
             self.kernel_name = "unit_stream"
+            # unit_stream reads the target and draft row of every node that
+            # has a draft row; a target row without one is read by the walk,
+            # and only when the accepted path ends there
             qrows = int((self.tree[2] >= 0).sum().item())
-            self.kernel_bytes = (B * (M + 1) + qrows) * V * 2
+            self.kernel_units = qrows
+            self.kernel_bytes = qrows * V * (2 + 2)
             self.expand_bytes = B * self.R * V * 2
             self.launches_per_step = 5  # rows, select, mask, verify, walk
         else:
@@ -199,7 +209,8 @@ class Work:
         w = self.w
         self.api.spec_eagle2_expand_rerank(
             draft, temperature=w.temperature, depth=w.depth, topk=w.topk,
-            width=w.width, total=w.total, out=self.tree, ws=self.ews)
+            width=w.width, total=w.total, out=self.tree, ws=self.ews,
+            draft_lse=self.lse)
 
     def step(self, inputs=None):
         """Enqueue one step on the current stream."""
@@ -217,7 +228,7 @@ class Work:
             api.spec_verify_tree(x[1], x[0], qrow, tok, par,
                                  temperature=w.temperature,
                                  seed=w.decision_seed, out=self.out,
-                                 ws=self.ws)
+                                 ws=self.ws, draft_lse=self.lse)
         else:
             from speculative_decoding_verification_tree_gb300.api import (
                 _ptr, _stream)
@@ -489,7 +500,7 @@ def main():
         roof = {"bound": "hbm", "achieved": round(achieved, 1),
                 "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4),
-                "traffic": _traffic(args.workload, work.rows),
+                "traffic": _traffic(args.workload, work.kernel_units),
                 "kernel": work.kernel_name,
                 "bytes_per_launch": work.kernel_bytes,
                 "avg_launch_ms": round(kern_ms, 5),

@@ -100,6 +100,14 @@ typedef struct spec_params {
   uint64_t seed;          /* Philox key                                    */
   uint32_t philox_offset; /* fourth Philox counter word                    */
   uint32_t flags;         /* reserved, must be 0                           */
+  /* Optional device array [B, R] float32 (NULL = unused): the log2
+     normaliser log2 sum_v 2^(z_v log2(e) / temperature) of each draft row.
+     spec_eagle2_expand_rerank writes it (the expand already sums every
+     draft row); spec_verify_tree then reads it instead of summing the draft
+     rows again, which is valid only for logit drafts at the same
+     temperature, without top-k / top-p (else SPEC_ERR_ARG; ignored at
+     temperature 0).  Must be NULL for spec_verify_chain. */
+  float* draft_lse;
 } spec_params_t;
 
 /*
@@ -165,6 +173,9 @@ int spec_verify_chain(const void* target_logits, const void* draft,
  * accept_mass [B, N+1] float32 (out): alpha per tree row (NaN where the row
  *     has no draft row; at temperature 0: 1 if a child matches the argmax,
  *     0 if none does, NaN for a row without children).
+ * prm->draft_lse (optional, [B, R]): the draft rows' log2 normalisers, as
+ *     spec_eagle2_expand_rerank writes them; the caller vouches that they
+ *     belong to these rows at this temperature.
  */
 int spec_verify_tree(const void* target_logits, const void* draft,
                      const int32_t* q_row, const int32_t* node_tokens,
@@ -204,6 +215,8 @@ int spec_tree_mask(const int32_t* parent, int B, int N, uint8_t* mask,
  * q_row [B, total+1] (draft row of each tree row or -1; row 0 -> 0),
  * value [B, total] float32 (sum of log q along the path),
  * mask [B, total, total] uint8 (may be NULL) as spec_tree_mask.
+ * prm->draft_lse (optional out, [B, R] float32): each draft row's log2
+ *     normaliser at this temperature, for spec_verify_tree.
  * Limits: 1 <= topk <= SPEC_EAGLE2_MAX_TOPK, width <= topk * width of the
  * layer above, total <= number of candidates, total <= SPEC_MAX_TREE_NODES.
  */

@@ -49,7 +49,7 @@ SPEC_OP_EAGLE2 = 3
 
 
 class SpecParams(ctypes.Structure):
-    """Mirror of spec_params_t (32 bytes)."""
+    """Mirror of spec_params_t (40 bytes)."""
     _fields_ = [
         ("temperature", ctypes.c_float),
         ("top_k", ctypes.c_int32),
@@ -58,10 +58,11 @@ class SpecParams(ctypes.Structure):
         ("seed", ctypes.c_uint64),
         ("philox_offset", ctypes.c_uint32),
         ("flags", ctypes.c_uint32),
+        ("draft_lse", ctypes.c_void_p),
     ]
 
 
-assert ctypes.sizeof(SpecParams) == 32
+assert ctypes.sizeof(SpecParams) == 40
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int

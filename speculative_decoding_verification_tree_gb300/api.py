@@ -43,10 +43,14 @@ def _stream(stream):
 
 
 def params(temperature=1.0, top_k=0, top_p=1.0, draft_kind="logits", seed=0,
-           offset=0) -> SpecParams:
+           offset=0, draft_lse=None) -> SpecParams:
+    if draft_lse is not None:
+        if draft_lse.dtype != torch.float32 or not draft_lse.is_contiguous():
+            raise ValueError("draft_lse must be a contiguous float32 tensor")
     return SpecParams(float(temperature), int(top_k), float(top_p),
                       _KIND[draft_kind], int(seed) & (2**64 - 1),
-                      int(offset) & 0xFFFFFFFF, 0)
+                      int(offset) & 0xFFFFFFFF, 0,
+                      None if draft_lse is None else draft_lse.data_ptr())
 
 
 def spec_workspace_bytes(op: int, B: int, n: int, V: int) -> int:
@@ -86,10 +90,13 @@ def spec_verify_chain(target, draft, draft_tokens, *, temperature=1.0,
 
 def spec_verify_tree(target, draft, q_row, node_tokens, parent, *,
                      temperature=1.0, top_k=0, top_p=1.0, draft_kind="logits",
-                     seed=0, offset=0, out=None, ws=None, stream=None):
+                     seed=0, offset=0, out=None, ws=None, stream=None,
+                     draft_lse=None):
     """target [B, N+1, V]; draft [B, R, V]; q_row [B, N+1]; node_tokens and
-    parent [B, N].  Returns (path_len [B], path_nodes [B, N],
-    tokens [B, N+1], accept_mass [B, N+1])."""
+    parent [B, N]; draft_lse [B, R] float32 (optional): the draft rows' log2
+    normalisers at this temperature, as spec_eagle2_expand_rerank writes
+    them.  Returns (path_len [B], path_nodes [B, N], tokens [B, N+1],
+    accept_mass [B, N+1])."""
     B, N1, V = target.shape
     N = N1 - 1
     R = 0 if draft is None else draft.shape[1]
@@ -101,7 +108,8 @@ def spec_verify_tree(target, draft, q_row, node_tokens, parent, *,
                torch.empty(B, N + 1, dtype=torch.float32, device=dev))
     if ws is None:
         ws = workspace(_lib.SPEC_OP_TREE, B, N, V, dev)
-    prm = params(temperature, top_k, top_p, draft_kind, seed, offset)
+    prm = params(temperature, top_k, top_p, draft_kind, seed, offset,
+                 draft_lse)
     _lib.call("spec_verify_tree", _ptr(target), _ptr(draft), _ptr(q_row),
               _ptr(node_tokens), _ptr(parent), B, N, R, V, _dt(target),
               _dt(draft), ctypes.byref(prm), _ptr(out[0]), _ptr(out[1]),
@@ -124,9 +132,10 @@ def spec_tree_mask(parent, *, bits=False, mask=True, stream=None):
 
 def spec_eagle2_expand_rerank(draft_logits, *, temperature, depth=6, topk=10,
                               width=10, total=60, mask=True, out=None,
-                              ws=None, stream=None):
+                              ws=None, stream=None, draft_lse=None):
     """draft_logits [B, 1 + (depth-1)*width, V].  Returns (node_tokens,
-    parent, q_row, value, mask)."""
+    parent, q_row, value, mask).  draft_lse [B, R] float32 (optional) is
+    filled with each draft row's log2 normaliser, for spec_verify_tree."""
     B, R, V = draft_logits.shape
     dev = draft_logits.device
     if out is None:
@@ -138,7 +147,9 @@ def spec_eagle2_expand_rerank(draft_logits, *, temperature, depth=6, topk=10,
                if mask else None)
     if ws is None:
         ws = workspace(_lib.SPEC_OP_EAGLE2, B, R, V, dev)
-    prm = params(temperature)
+    if draft_lse is not None and tuple(draft_lse.shape) != (B, R):
+        raise ValueError("draft_lse must have shape [B, R]")
+    prm = params(temperature, draft_lse=draft_lse)
     _lib.call("spec_eagle2_expand_rerank", _ptr(draft_logits), B, V,
               _dt(draft_logits), depth, topk, width, total, ctypes.byref(prm),
               _ptr(out[0]), _ptr(out[1]), _ptr(out[2]), _ptr(out[3]),

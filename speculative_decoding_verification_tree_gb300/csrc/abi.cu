@@ -115,6 +115,7 @@ int spec_verify_chain(const void* target_logits, const void* draft, const int32_
   if (V > SPEC_MAX_VOCAB || K > SPEC_MAX_TREE_NODES) return SPEC_ERR_SHAPE;
   int rc = check_params(prm, V);
   if (rc != SPEC_OK) return rc;
+  if (prm->draft_lse) return SPEC_ERR_ARG;
   if (!dtype_ok(dtype_target)) return SPEC_ERR_DTYPE;
   const bool greedy = prm->temperature == 0.f;
   if (!greedy && K > 0 && !dtype_ok(dtype_draft)) return SPEC_ERR_DTYPE;
@@ -146,6 +147,10 @@ int spec_verify_tree(const void* target_logits, const void* draft, const int32_t
   if (V > SPEC_MAX_VOCAB || N > SPEC_MAX_TREE_NODES) return SPEC_ERR_SHAPE;
   int rc = check_params(prm, V);
   if (rc != SPEC_OK) return rc;
+  // given draft normalisers stand for softmax(z / T) of logit rows only
+  if (prm->draft_lse && prm->temperature > 0.f &&
+      (prm->draft_kind != SPEC_DRAFT_LOGITS || truncation_k(prm, V) > 0))
+    return SPEC_ERR_ARG;
   if (!dtype_ok(dtype_target)) return SPEC_ERR_DTYPE;
   const bool greedy = prm->temperature == 0.f;
   if (!greedy && R > 0 && !dtype_ok(dtype_draft)) return SPEC_ERR_DTYPE;
@@ -164,6 +169,7 @@ int spec_verify_tree(const void* target_logits, const void* draft, const int32_t
   a.dt_target = dtype_target;
   a.dt_draft = dtype_ok(dtype_draft) ? dtype_draft : SPEC_F32;
   a.prm = *prm;
+  if (greedy) a.prm.draft_lse = nullptr;
   a.count = path_len;
   a.path_nodes = path_nodes;
   a.out_tokens = out_tokens;
@@ -209,6 +215,7 @@ int spec_eagle2_expand_rerank(const void* draft_logits, int B, int V, int dtype,
   if (B == 0) return SPEC_OK;
   return cuda_rc(launch_eagle2(draft_logits, B, V, dtype, depth, topk, width, total,
                                prm->temperature, node_tokens, parent, q_row, value, mask,
+                               prm->draft_lse,
                                (Eagle2Cand*)((char*)workspace + w.off_cand), status, st));
 }
 

@@ -33,11 +33,12 @@ constexpr int kMaxCand = SPEC_EAGLE2_MAX_CANDIDATES;  // per sequence (host-chec
 // One CTA per draft row: the row's `topk` most probable tokens (bound-and-
 // rescan streaming top-k shared with the top-k sampling path) and their
 // log-probabilities log q = (z kt - log2 sum 2^(z kt)) ln 2 at temperature T
-// (kt = log2(e) / T).
+// (kt = log2(e) / T); the row's log2 normaliser goes to lse_out if given.
 template <typename T, bool kVec>
 __global__ void __launch_bounds__(topk::kThreads) eagle2_rows(const T* __restrict__ x, int V,
                                                               int k, float kt,
                                                               Eagle2Cand* __restrict__ out,
+                                                              float* __restrict__ lse_out,
                                                               uint32_t* status) {
   extern __shared__ __align__(16) unsigned char smraw[];
   __shared__ int32_t idx[SPEC_EAGLE2_MAX_TOPK];
@@ -55,6 +56,7 @@ __global__ void __launch_bounds__(topk::kThreads) eagle2_rows(const T* __restric
     if (i == 0 && (cnt < k || !(lse > neg_inf()) || isnan(lse)))
       flag_status(status, SPEC_STATUS_NAN);
   }
+  if (lse_out && i == 0) lse_out[row] = lse;
 }
 
 struct SelNode {
@@ -157,7 +159,8 @@ __global__ void __launch_bounds__(kSelThreads) eagle2_select(const Eagle2Cand* _
 cudaError_t launch_eagle2(const void* draft, int B, int V, int dtype, int depth, int topk,
                           int width, int total, float temperature, int32_t* node_tokens,
                           int32_t* parent, int32_t* q_row, float* value, uint8_t* mask,
-                          Eagle2Cand* cand, uint32_t* status, cudaStream_t st) {
+                          float* draft_lse, Eagle2Cand* cand, uint32_t* status,
+                          cudaStream_t st) {
   const int R = 1 + (depth - 1) * width;
   const float kt = kLog2e / temperature;
   const int64_t rows = (int64_t)B * R;
@@ -169,7 +172,7 @@ cudaError_t launch_eagle2(const void* draft, int B, int V, int dtype, int depth,
     cudaError_t err =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)rsm);
     if (err != cudaSuccess) return err;
-    kern<<<(unsigned)rows, topk::kThreads, rsm, st>>>(src, V, topk, kt, cand, status);
+    kern<<<(unsigned)rows, topk::kThreads, rsm, st>>>(src, V, topk, kt, cand, draft_lse, status);
     return cudaGetLastError();
   };
   prof_begin(SPEC_PROF_EXPAND, st);

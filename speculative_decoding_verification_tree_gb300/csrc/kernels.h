@@ -143,6 +143,7 @@ struct Eagle2Cand {
 cudaError_t launch_eagle2(const void* draft, int B, int V, int dtype, int depth, int topk,
                           int width, int total, float temperature, int32_t* node_tokens,
                           int32_t* parent, int32_t* q_row, float* value, uint8_t* mask,
-                          Eagle2Cand* cand, uint32_t* status, cudaStream_t st);
+                          float* draft_lse, Eagle2Cand* cand, uint32_t* status,
+                          cudaStream_t st);
 
 }  // namespace sv

@@ -86,7 +86,7 @@ extern "C" int spec_verify_chain_noalloc(const void* target_logits, const void* 
   if (rows * arg_splits(V) > SPEC_NOALLOC_MAX_PARTS) return SPEC_ERR_SHAPE;
   if (!prm) return SPEC_ERR_ARG;
   if (!(prm->temperature >= 0.f) || !std::isfinite(prm->temperature)) return SPEC_ERR_ARG;
-  if (prm->flags != 0 || prm->top_k < 0) return SPEC_ERR_ARG;
+  if (prm->flags != 0 || prm->top_k < 0 || prm->draft_lse) return SPEC_ERR_ARG;
   if (prm->draft_kind != SPEC_DRAFT_LOGITS && prm->draft_kind != SPEC_DRAFT_PROBS)
     return SPEC_ERR_DTYPE;
   if (!(prm->top_p > 0.f && prm->top_p <= 1.f)) return SPEC_ERR_ARG;

@@ -305,15 +305,50 @@ __device__ __forceinline__ float q_of(float raw, float kt, float invT, float neg
   else return ex2(fmaf(lg2(raw), invT, negLq));
 }
 
+// Packed fp32 pairs (two IEEE round-to-nearest operations per instruction).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  float2 d;
+  asm("{.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  float2 d;
+  asm("{.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 ex2x2(float2 t) { return make_float2(ex2(t.x), ex2(t.y)); }
+
 // Online sum of 2^(x_i s - m) over a thread's logits with a lazy reference m:
 // the exponentials use the current m, which moves up (rescaling the sum) only
 // when a group's sum would pass 2^60, so the common path has no dependency on
 // the group's maximum; z stays below 2^64 per 16 groups, far from overflow.
 // (m, z) then combine like a (max, sum) pair; m = -inf until a finite logit.
 __device__ __forceinline__ void lazy_sum(const float (&x)[8], float s, float& m, float& z) {
-  float zc = 0.f;
+  float2 zc2 = make_float2(0.f, 0.f);
+  {
+    const float2 s2 = make_float2(s, s), nm2 = make_float2(-m, -m);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) zc += ex2(fmaf(x[i], s, -m));
+    for (int i = 0; i < 8; i += 2)
+      zc2 = fadd2(zc2, ex2x2(ffma2(make_float2(x[i], x[i + 1]), s2, nm2)));
+  }
+  float zc = zc2.x + zc2.y;
   if (!(zc <= 0x1p60f)) {  // a new maximum (or the first finite logit, or NaN)
     const float cm = fmaxf(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])),
                            fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7])));
@@ -442,6 +477,9 @@ __global__ void __launch_bounds__(kThreads, 1) unit_stream(StreamParams P) {
   auto stage = [&](int st, int half) { return dyn + (size_t)st * 2 * kHalf + half * kHalf; };
   const TT* tgt = reinterpret_cast<const TT*>(a.target);
   const TD* drf = reinterpret_cast<const TD*>(a.draft);
+  // the caller's draft-row normalisers (logit drafts only): pass A then
+  // reads the target row alone and the draft row is read once, in pass B
+  const float* qlse = QK == Q_LOGITS ? a.prm.draft_lse : nullptr;
   auto draft_row = [&](int64_t u, int q) -> const TD* {
     const int64_t b = u / (n + 1);
     return drf + ((int64_t)b * s.R + q) * V;
@@ -489,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1) unit_stream(StreamParams P) {
                    &sm.mrec[rb]);
         }
         const TT* ta = hA ? tgt + ua * (int64_t)V + r0 : nullptr;
-        const TD* da = qa >= 0 ? draft_row(ua, qa) + r0 : nullptr;
+        const TD* da = (qa >= 0 && !qlse) ? draft_row(ua, qa) + r0 : nullptr;
         const TT* tb = hB ? tgt + ub * (int64_t)V + r0 : nullptr;
         const TD* db = qb >= 0 ? draft_row(ub, qb) + r0 : nullptr;
         for (int c = 0; c < nch; ++c) {
@@ -526,17 +564,19 @@ __global__ void __launch_bounds__(kThreads, 1) unit_stream(StreamParams P) {
     // ------------------------------------------- consumers and control warp
     const bool ctl = warp == kCW + 1;
     int stg = 0, round = 0;
-    int sxq = 0;                        // continuation exchanges so far
     float Lp = 0.f, Lq = 0.f, invZq = 0.f;  // normalisers of the pass-B row
     float zp_tot = 0.f, zq_tot = 0.f;
     int64_t u_cur = nrow > 0 ? unit_of(0) : -1, u_prev = -1, u_prev2 = -1;
     int q_cur = nrow > 0 ? a.qres[u_cur] : -1, q_prev = -1;
+    float lq_carry = 0.f;
     for (int j = 0; nrow > 0 && j <= nrow + 1; ++j) {
       const bool hA = j < nrow, hB = j >= 1 && j <= nrow;
       const int qa = hA ? q_cur : -1, qb = hB ? q_prev : -1;
       const int64_t u_next = (j + 1 < nrow) ? unit_of(j + 1) : -1;
       const int q_next = (u_next >= 0) ? a.qres[u_next] : -1;
-      const int64_t ua = u_cur, ub = u_prev, ur2 = u_prev2;
+      const int64_t ub = u_prev, ur2 = u_prev2;
+      const float lq_b = lq_carry;  // row j - 1's given normaliser
+      lq_carry = (qlse && qa >= 0) ? __ldg(qlse + (u_cur / (n + 1)) * s.R + qa) : 0.f;
 
       // Steps 1-3: the previous row-time's exchange and the decisions it allows.
       auto row_start = [&]() {
@@ -576,6 +616,10 @@ __global__ void __launch_bounds__(kThreads, 1) unit_stream(StreamParams P) {
                 Bq.z = __shfl_sync(0xffffffffu, Bq.z, 0);
                 Lq = Bq.m + log2f(Bq.z);
                 zq_tot = Bq.z;
+                if (qlse) {  // given: finite unless the row is empty or not a number
+                  Lq = lq_b;
+                  zq_tot = (fabsf(lq_b) < 0x1p126f) ? 1.f : 0.f;
+                }
               }
             }
           }
@@ -661,7 +705,8 @@ __global__ void __launch_bounds__(kThreads, 1) unit_stream(StreamParams P) {
         needR = sm.needR[(j - 1) & 1] != 0;
       }
       float m = neg_inf(), z = 0.f, mq = neg_inf(), zq = 0.f;
-      float acc_a = 0.f, acc_r = 0.f;
+      float2 acc_a2 = make_float2(0.f, 0.f), acc_r2 = make_float2(0.f, 0.f), zq2 = make_float2(0.f, 0.f);
+      const float2 kt2 = make_float2(kt, kt);
       for (int c = 0; c < nch; ++c) {
         wait_cta(sm, &sm.full[stg], (uint32_t)(round & 1), a.status);
         const int e = c * kCH + tid * kEPT;
@@ -671,11 +716,12 @@ __global__ void __launch_bounds__(kThreads, 1) unit_stream(StreamParams P) {
             float x[8];
             load8<TT>(reinterpret_cast<const TT*>(sa) + tid * kEPT, x);
             lazy_sum(x, kt, m, z);
-            if (qa >= 0) {
+            if (qa >= 0 && !qlse) {
               float y[8];
               load8<TD>(reinterpret_cast<const TD*>(sa + kTB) + tid * kEPT, y);
               if constexpr (QK == Q_PROBS_T1) {
-                zq += ((y[0] + y[1]) + (y[2] + y[3])) + ((y[4] + y[5]) + (y[6] + y[7]));
+                zq2 = fadd2(zq2, fadd2(fadd2(make_float2(y[0], y[1]), make_float2(y[2], y[3])),
+                                       fadd2(make_float2(y[4], y[5]), make_float2(y[6], y[7]))));
               } else if constexpr (QK == Q_LOGITS) {
                 lazy_sum(y, kt, mq, zq);
               } else {
@@ -691,25 +737,40 @@ __global__ void __launch_bounds__(kThreads, 1) unit_stream(StreamParams P) {
             float x[8], y[8];
             load8<TT>(reinterpret_cast<const TT*>(sb) + tid * kEPT, x);
             load8<TD>(reinterpret_cast<const TD*>(sb + kTB) + tid * kEPT, y);
+            const float2 nLp2 = make_float2(negLp, negLp), nLq2 = make_float2(negLq, negLq);
+            auto q2_of = [&](int i) -> float2 {
+              if constexpr (QK == Q_LOGITS)
+                return ex2x2(ffma2(make_float2(y[i], y[i + 1]), kt2, nLq2));
+              else if constexpr (QK == Q_PROBS_T1)
+                return fmul2(make_float2(y[i], y[i + 1]), make_float2(invZq, invZq));
+              else
+                return make_float2(q_of<QK>(y[i], kt, invT, negLq, invZq),
+                                   q_of<QK>(y[i + 1], kt, invT, negLq, invZq));
+            };
             if (needR) {
-              float lr = 0.f;
 #pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                const float p = ex2(fmaf(x[i], kt, negLp));
-                const float mn = fminf(p, q_of<QK>(y[i], kt, invT, negLq, invZq));
-                acc_a += mn;
-                lr += p - mn;
+              for (int i = 0; i < 8; i += 2) {
+                const float2 p = ex2x2(ffma2(make_float2(x[i], x[i + 1]), kt2, nLp2));
+                const float2 q = q2_of(i);
+                const float2 mn = make_float2(fminf(p.x, q.x), fminf(p.y, q.y));
+                acc_a2 = fadd2(acc_a2, mn);
+                acc_r2 = fadd2(acc_r2, ffma2(mn, make_float2(-1.f, -1.f), p));
               }
-              acc_r += lr;
             } else if constexpr (QK == Q_LOGITS) {
               // min(p, q) = 2^min(log2 p, log2 q): one exponential
 #pragma unroll
-              for (int i = 0; i < 8; ++i)
-                acc_a += ex2(fminf(fmaf(x[i], kt, negLp), fmaf(y[i], kt, negLq)));
+              for (int i = 0; i < 8; i += 2) {
+                const float2 lp = ffma2(make_float2(x[i], x[i + 1]), kt2, nLp2);
+                const float2 lq = ffma2(make_float2(y[i], y[i + 1]), kt2, nLq2);
+                acc_a2 = fadd2(acc_a2, ex2x2(make_float2(fminf(lp.x, lq.x), fminf(lp.y, lq.y))));
+              }
             } else {
 #pragma unroll
-              for (int i = 0; i < 8; ++i)
-                acc_a += fminf(ex2(fmaf(x[i], kt, negLp)), q_of<QK>(y[i], kt, invT, negLq, invZq));
+              for (int i = 0; i < 8; i += 2) {
+                const float2 p = ex2x2(ffma2(make_float2(x[i], x[i + 1]), kt2, nLp2));
+                const float2 q = q2_of(i);
+                acc_a2 = fadd2(acc_a2, make_float2(fminf(p.x, q.x), fminf(p.y, q.y)));
+              }
             }
           }
         }
@@ -722,6 +783,8 @@ __global__ void __launch_bounds__(kThreads, 1) unit_stream(StreamParams P) {
       }
 
       // 5. CTA reductions; alpha partial of row j - 1; exchange
+      const float acc_a = acc_a2.x + acc_a2.y, acc_r = acc_r2.x + acc_r2.y;
+      if constexpr (QK == Q_PROBS_T1) zq += zq2.x + zq2.y;
       {
         const int pb = j & 1;
         const MaxSum A = warp_ms(MaxSum{m, z});

@@ -36,8 +36,9 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_params_struct_layout(lib):
     P = lib.SpecParams
-    assert ctypes.sizeof(P) == 32
+    assert ctypes.sizeof(P) == 40
     assert P.seed.offset == 16 and P.philox_offset.offset == 24
+    assert P.draft_lse.offset == 32
 
 
 def test_workspace_sizes(lib):
@@ -83,6 +84,8 @@ def test_chain_argument_errors(lib):
     assert _chain(lib, prm=_prm(lib, top_k=-2)) == lib.SPEC_ERR_ARG
     assert _chain(lib, prm=_prm(lib, draft_kind=3)) == lib.SPEC_ERR_DTYPE
     assert _chain(lib, prm=_prm(lib, flags=1)) == lib.SPEC_ERR_ARG
+    # given draft normalisers are a tree-verification input only
+    assert _chain(lib, prm=_prm(lib, draft_lse=FAKE.value)) == lib.SPEC_ERR_ARG
     # top-p alone keeps up to V tokens: fine for V <= 128, not beyond
     assert _chain(lib, V=1000, prm=_prm(lib, top_p=0.9)) == \
         lib.SPEC_ERR_UNSUPPORTED
@@ -109,6 +112,12 @@ def test_tree_and_mask_argument_errors(lib):
     assert f("spec_verify_tree", FAKE, FAKE, None, FAKE, FAKE, 1, 3, 4, 10,
              0, 0, ctypes.byref(prm), FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 20,
              None) == lib.SPEC_ERR_ARG
+    # given draft normalisers: logit drafts without truncation only
+    for kw in (dict(draft_kind=1), dict(top_k=5), dict(top_p=0.5)):
+        p = _prm(lib, draft_lse=FAKE.value, **kw)
+        assert f("spec_verify_tree", FAKE, FAKE, FAKE, FAKE, FAKE, 1, 3, 4,
+                 100, 0, 0, ctypes.byref(p), FAKE, FAKE, FAKE, FAKE, FAKE,
+                 1 << 20, None) == lib.SPEC_ERR_ARG, kw
     assert f("spec_tree_mask", FAKE, 1, 65, None, FAKE, None) == \
         lib.SPEC_ERR_SHAPE
     assert f("spec_tree_mask", FAKE, 1, 5, None, None, None) == \

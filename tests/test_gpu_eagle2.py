@@ -178,3 +178,36 @@ def test_eagle2_full_pipeline_sampled():
     compare_tree(out, ref, seqs=seqs)
     plen = out[0].cpu().numpy()
     assert plen.mean() > 0.5  # the synthetic target tracks the draft
+
+
+@pytest.mark.parametrize("V,dt,B", [(32000, torch.bfloat16, 12),
+                                    (128256, torch.bfloat16, 128),
+                                    (4099, torch.float32, 6)])
+def test_eagle2_verify_with_expand_normalisers(V, dt, B):
+    # the expand writes each draft row's log2 normaliser; tree verification
+    # then leaves the draft rows out of its first pass (aligned rows) or
+    # ignores them (the general kernel) and must still match the oracle
+    w = synth.workload("eagle2", B=B, V=V, draft_dtype=dt, seed=V + 11)
+    draft = synth.eagle2_draft(w, "cuda")
+    R = draft.shape[1]
+    lse = torch.full((B, R), float("nan"), dtype=torch.float32, device="cuda")
+    tok, par, qrow, val, mask = api().spec_eagle2_expand_rerank(
+        draft, temperature=w.temperature, draft_lse=lse)
+    torch.cuda.synchronize()
+    # q = 2^(z log2(e) / T - lse) is a distribution (float64 recomputation)
+    kt = np.log2(np.e) / w.temperature
+    L = lse.cpu().numpy().astype(np.float64)
+    for b, r in [(0, 0), (B - 1, R - 1), (B // 2, R // 2)]:
+        z = np64(draft[b, r])
+        assert abs(np.exp2(z * kt - L[b, r]).sum() - 1.0) < 3e-5, (b, r)
+    target = synth.eagle2_target(w, draft, qrow, "cuda")
+    out = api().spec_verify_tree(target, draft, qrow, tok, par,
+                                 temperature=w.temperature,
+                                 seed=w.decision_seed, draft_lse=lse)
+    torch.cuda.synchronize()
+    seqs = list(range(B)) if B <= 12 else [1, 64, 126]
+    ref = verify_tree(np64(target[seqs]), np64(draft[seqs]),
+                      qrow[seqs].cpu().numpy(), tok[seqs].cpu().numpy(),
+                      par[seqs].cpu().numpy(), temperature=w.temperature,
+                      seed=w.decision_seed, batch_ids=seqs)
+    compare_tree(out, ref, seqs=seqs)
