@@ -64,10 +64,27 @@ struct SelNode {
   int tok, dep, id, par, row;
 };
 
-__device__ __forceinline__ bool sel_before(const SelNode& a, const SelNode& b) {
-  if (a.val != b.val) return a.val > b.val;
-  if (a.dep != b.dep) return a.dep < b.dep;
-  return a.id < b.id;
+// Rank order of candidates: value descending, then depth, then candidate id
+// ascending.  One 64-bit key per candidate whose ascending order is that
+// order: the value's bits made monotone (-0 counts as +0; NaN values were
+// made -inf), complemented, above depth (< 2^16) and id (< 2^16).
+__device__ __forceinline__ uint64_t sel_key(float v, int dep, int id) {
+  const uint32_t u = __float_as_uint(v + 0.f);
+  const uint32_t up = (u & 0x80000000u) ? ~u : (u | 0x80000000u);  // grows with v
+  return ((uint64_t)~up << 32) | ((uint64_t)(uint32_t)dep << 16) | (uint32_t)id;
+}
+
+// Number of keys in k[0, n) below `me` (4 independent counters).
+__device__ __forceinline__ int count_below(const uint64_t* k, int n, uint64_t me) {
+  int c0 = 0, c1 = 0, c2 = 0, c3 = 0, j = 0;
+  for (; j + 4 <= n; j += 4) {
+    c0 += k[j] < me;
+    c1 += k[j + 1] < me;
+    c2 += k[j + 2] < me;
+    c3 += k[j + 3] < me;
+  }
+  for (; j < n; ++j) c0 += k[j] < me;
+  return (c0 + c1) + (c2 + c3);
 }
 
 __global__ void __launch_bounds__(kSelThreads) eagle2_select(const Eagle2Cand* __restrict__ cand,
@@ -76,7 +93,8 @@ __global__ void __launch_bounds__(kSelThreads) eagle2_select(const Eagle2Cand* _
                                                              int32_t* parent, int32_t* q_row,
                                                              float* value, uint32_t* status) {
   extern __shared__ unsigned char smraw[];
-  SelNode* nd = reinterpret_cast<SelNode*>(smraw);
+  uint64_t* key = reinterpret_cast<uint64_t*>(smraw);
+  SelNode* nd = reinterpret_cast<SelNode*>(key + kMaxCand);
   int* rank = reinterpret_cast<int*>(nd + kMaxCand);
   __shared__ int kept[SPEC_EAGLE2_MAX_WIDTH];
   __shared__ int s_n, s_prev0, s_prevn;
@@ -87,6 +105,7 @@ __global__ void __launch_bounds__(kSelThreads) eagle2_select(const Eagle2Cand* _
     const Eagle2Cand e = cb[c];
     const float v = isnan(e.logq) ? neg_inf() : e.logq;
     nd[c] = SelNode{v, e.token, 1, c, -1, -1};
+    key[c] = sel_key(v, 1, c);
   }
   if (tid == 0) {
     s_n = topk;
@@ -99,8 +118,7 @@ __global__ void __launch_bounds__(kSelThreads) eagle2_select(const Eagle2Cand* _
     if (d == depth) break;
     // keep the `width` best of layer d (rank by counting within the layer)
     for (int i = tid; i < ln; i += blockDim.x) {
-      int rk = 0;
-      for (int j = 0; j < ln; ++j) rk += sel_before(nd[l0 + j], nd[l0 + i]) ? 1 : 0;
+      const int rk = count_below(key + l0, ln, key[l0 + i]);
       if (rk < width) {
         kept[rk] = l0 + i;
         nd[l0 + i].row = 1 + (d - 1) * width + rk;
@@ -116,7 +134,9 @@ __global__ void __launch_bounds__(kSelThreads) eagle2_select(const Eagle2Cand* _
       const int rw = nd[pi].row;
       const Eagle2Cand e = cb[(int64_t)rw * SPEC_EAGLE2_MAX_TOPK + c];
       const float lq = isnan(e.logq) ? neg_inf() : e.logq;
-      nd[base + t] = SelNode{nd[pi].val + lq, e.token, d + 1, r * topk + c, pi, -1};
+      const float v = nd[pi].val + lq;
+      nd[base + t] = SelNode{v, e.token, d + 1, r * topk + c, pi, -1};
+      key[base + t] = sel_key(v, d + 1, r * topk + c);
     }
     __syncthreads();
     if (tid == 0) {
@@ -128,12 +148,7 @@ __global__ void __launch_bounds__(kSelThreads) eagle2_select(const Eagle2Cand* _
   }
   const int n = s_n;
   // rerank every candidate
-  for (int i = tid; i < n; i += blockDim.x) {
-    int rk = 0;
-    const SelNode me = nd[i];
-    for (int j = 0; j < n; ++j) rk += sel_before(nd[j], me) ? 1 : 0;
-    rank[i] = rk;
-  }
+  for (int i = tid; i < n; i += blockDim.x) rank[i] = count_below(key, n, key[i]);
   __syncthreads();
   if (tid == 0) q_row[(int64_t)b * (total + 1)] = 0;
   uint32_t bad = 0;
@@ -186,7 +201,7 @@ cudaError_t launch_eagle2(const void* draft, int B, int V, int dtype, int depth,
   }
   prof_end(SPEC_PROF_EXPAND, st);
   if (e != cudaSuccess) return e;
-  const size_t smem = (size_t)kMaxCand * (sizeof(SelNode) + sizeof(int));
+  const size_t smem = (size_t)kMaxCand * (sizeof(uint64_t) + sizeof(SelNode) + sizeof(int));
   e = cudaFuncSetAttribute(eagle2_select, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   eagle2_select<<<B, kSelThreads, smem, st>>>(cand, R, depth, topk, width, total, node_tokens,
