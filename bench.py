@@ -58,14 +58,20 @@ def _args():
 
 # DRAM traffic per launch of the profiled kernel, from one ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum of a smaller batch, scaled
-# to the rows the kernel processes), keyed by workload, with a hash of the sources the
-# kernel is built from at capture time.  Reported as null once they changed.
+# to the rows the kernel processes), keyed by workload, with a hash of the
+# sources the kernel is built from at capture time.  Reported as null once
+# they changed.
 _STREAM_SRC = ("sample_stream.cuh", "sample_stream_bf16.cu",
                "sample_stream_f32.cu", "common.cuh", "kernels.h")
 TRAFFIC = {
-    # unit_stream, tree_static at B=16: 759.77 MB read + 3.70 MB written, 976 rows
-    "tree_static": {"bytes_per_unit": 763.47e6 / 976, "src": _STREAM_SRC,
-                    "hash": "ca2e2218f16009bc"},
+    # unit_stream, tree_static at B=16: 760.16 MB read + 3.53 MB written,
+    # 976 rows
+    "tree_static": {"bytes_per_unit": 763.69e6 / 976, "src": _STREAM_SRC,
+                    "hash": "6a139c25b796bfaa"},
+    # unit_stream, eagle2 at B=32: 402.37 MB read + 3.69 MB written, 782
+    # rows with a draft row
+    "eagle2": {"bytes_per_unit": 406.06e6 / 782, "src": _STREAM_SRC,
+               "hash": "6a139c25b796bfaa"},
 }
 
 
@@ -137,7 +143,11 @@ class Work:
             self.kernel_bytes = B * (K + 1) * V * tb
             if w.temperature > 0:
                 self.kernel_bytes += B * K * V * self.draft.element_size()
-            self.launches_per_step = 2
+            # argmax + finalize; top-k rows, records, units, walk; or
+            # records, streaming verification, walk
+            self.launches_per_step = (2 if w.temperature == 0 else
+                                      4 if (w.top_k > 0 or w.top_p < 1)
+                                      else 3)
         elif name == "tree_static":
             self.kind = "tree"
             (self.target, self.draft, self.q_row, self.toks,
@@ -160,7 +170,10 @@ class Work:
                                 else "unit_stream")
             self.kernel_bytes = B * (N + 1) * V * (
                 self.target.element_size() + self.draft.element_size())
-            self.launches_per_step = 3  # mask, row verification, walk
+            # mask, row records, row verification, walk (top-k / top-p:
+            # mask, top-k rows, records, units, walk)
+            self.launches_per_step = (5 if (w.top_k > 0 or w.top_p < 1)
+                                      else 4)
         elif name == "eagle2":
             self.kind = "eagle2"
             self.draft = synth.eagle2_draft(w, device)
@@ -201,7 +214,8 @@ class Work:
             self.kernel_units = qrows
             self.kernel_bytes = qrows * V * (2 + 2)
             self.expand_bytes = B * self.R * V * 2
-            self.launches_per_step = 5  # rows, select, mask, verify, walk
+            # expand rows, select, mask, row records, verification, walk
+            self.launches_per_step = 6
         else:
             raise SystemExit(f"workload {name} is not wired into the bench")
 
