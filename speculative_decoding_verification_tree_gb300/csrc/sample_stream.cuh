@@ -860,6 +860,7 @@ constexpr int kWalkWarps = kWalkThreads / 32;
 constexpr int kMaxW = 8;  // CTAs per sequence in the walk
 
 struct WalkSmem {
+  Meta rec;                           // record of the row the walk is at
   int child[SPEC_MAX_TREE_NODES + 1];  // each row's outcome (RowOut::child)
   float wsum[kMaxTiles][kWalkWarps];  // per (chunk, warp) masses of the draw
   float red[kWalkWarps];
@@ -868,6 +869,7 @@ struct WalkSmem {
   RowOut st;                          // walk state (thread 0 writes)
   int act;                            // 0 done, 1 pass, 2 draw
   int rr, len, rsel, tile, wsel;
+  int rec_row;                        // row whose record is in `rec` (-1: none)
   float t;
 };
 
@@ -1024,6 +1026,7 @@ __global__ void __launch_bounds__(kWalkThreads) stream_walk(StreamParams P) {
     ws.rr = 0;
     ws.len = 0;
     ws.act = 0;
+    ws.rec_row = -1;
   }
   __syncthreads();
   for (;;) {
@@ -1057,7 +1060,14 @@ __global__ void __launch_bounds__(kWalkThreads) stream_walk(StreamParams P) {
     __syncthreads();
     const int act = ws.act;
     const int64_t ur = u0 + ws.rr;
-    const Meta* M = reinterpret_cast<const Meta*>(a.meta + ur * (int64_t)P.rec_bytes);
+    if (ws.rr != ws.rec_row) {  // the row's record into shared memory, once
+      const uint4* src = reinterpret_cast<const uint4*>(a.meta + ur * (int64_t)P.rec_bytes);
+      uint4* dst = reinterpret_cast<uint4*>(&ws.rec);
+      for (int i = tid; i < P.rec_bytes / 16; i += kWalkThreads) dst[i] = src[i];
+      __syncthreads();
+      if (tid == 0) ws.rec_row = ws.rr;
+    }
+    const Meta* M = &ws.rec;
     const int qr = M->qr;
     RowOut st = ws.st;
     if (act == 1) {

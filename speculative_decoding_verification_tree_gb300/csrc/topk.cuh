@@ -341,7 +341,7 @@ __device__ void row_topk(const T* __restrict__ rp, int V, int k, float kt, Cand*
 // Rows where that leaves fewer than k or more than kCandCap candidates (many
 // ties at the bound, NaN, -inf) take row_topk.  Same outputs as row_topk.
 constexpr int kCandCap = 1024;
-constexpr int kRowBatch = 4;  // 16-byte groups in flight per thread
+constexpr int kRowBatch = 8;  // 16-byte groups in flight per thread
 
 template <typename T, bool kVec>
 __device__ void row_topk_fast(const T* __restrict__ rp, int V, int k, float kt, Cand* smem,
