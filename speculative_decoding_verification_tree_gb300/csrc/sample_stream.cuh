@@ -198,8 +198,11 @@ __device__ __forceinline__ float resid_w(float p, float q, float C) {
 
 // Waits that give up after ~1 s, flag SPEC_STATUS_TIMEOUT and make every
 // later wait of the CTA return at once, so a broken peer cannot hang the GPU.
+// A phase that is already complete returns after one test, before the flag
+// (a shared-memory load) is read.
 __device__ __forceinline__ void wait_cta(Smem& sm, uint64_t* bar, uint32_t parity,
                                          uint32_t* status) {
+  if (mbar_try_wait(bar, parity)) return;
   if (*(volatile int*)&sm.dead) return;
   if (!mbar_wait_bounded(bar, parity)) {
     sm.dead = 1;
@@ -208,6 +211,7 @@ __device__ __forceinline__ void wait_cta(Smem& sm, uint64_t* bar, uint32_t parit
 }
 __device__ __forceinline__ void wait_cluster(Smem& sm, uint64_t* bar, uint32_t parity,
                                              uint32_t* status) {
+  if (mbar_try_wait_cluster(bar, parity)) return;
   if (*(volatile int*)&sm.dead) return;
   if (!mbar_wait_cluster_bounded(bar, parity)) {
     sm.dead = 1;
