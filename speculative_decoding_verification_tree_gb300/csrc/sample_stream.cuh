@@ -35,6 +35,7 @@
 #pragma once
 
 #include <climits>
+#include <type_traits>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -711,80 +712,98 @@ __global__ void __launch_bounds__(kThreads, 1) unit_stream(StreamParams P) {
       float m = neg_inf(), z = 0.f, mq = neg_inf(), zq = 0.f;
       float2 acc_a2 = make_float2(0.f, 0.f), acc_r2 = make_float2(0.f, 0.f), zq2 = make_float2(0.f, 0.f);
       const float2 kt2 = make_float2(kt, kt);
-      for (int c = 0; c < nch; ++c) {
-        wait_cta(sm, &sm.full[stg], (uint32_t)(round & 1), a.status);
-        const int e = c * kCH + tid * kEPT;
-        if (e < len) {  // len is a multiple of 8: the thread's 8 logits are all valid
-          if (hA) {
-            const unsigned char* sa = stage(stg, 0);
-            float x[8];
-            load8<TT>(reinterpret_cast<const TT*>(sa) + tid * kEPT, x);
-            lazy_sum(x, kt, m, z);
-            if (qa >= 0 && !qlse) {
-              float y[8];
-              load8<TD>(reinterpret_cast<const TD*>(sa + kTB) + tid * kEPT, y);
-              if constexpr (QK == Q_PROBS_T1) {
-                zq2 = fadd2(zq2, fadd2(fadd2(make_float2(y[0], y[1]), make_float2(y[2], y[3])),
-                                       fadd2(make_float2(y[4], y[5]), make_float2(y[6], y[7]))));
+      // The chunk loop, one instantiation per combination of the row-time's
+      // uniform choices (pass A present and whether it sums the draft row,
+      // pass B present and whether it needs the residual mass), so that the
+      // loop body tests none of them.
+      auto chunk_loop = [&](auto fA, auto fQ, auto fB, auto fR) {
+        constexpr bool kA = decltype(fA)::value, kQ = decltype(fQ)::value;
+        constexpr bool kB = decltype(fB)::value, kR = decltype(fR)::value;
+        for (int c = 0; c < nch; ++c) {
+          wait_cta(sm, &sm.full[stg], (uint32_t)(round & 1), a.status);
+          const int e = c * kCH + tid * kEPT;
+          if (e < len) {  // len is a multiple of 8: the thread's 8 logits are all valid
+            if constexpr (kA) {
+              const unsigned char* sa = stage(stg, 0);
+              float x[8];
+              load8<TT>(reinterpret_cast<const TT*>(sa) + tid * kEPT, x);
+              lazy_sum(x, kt, m, z);
+              if constexpr (kQ) {
+                float y[8];
+                load8<TD>(reinterpret_cast<const TD*>(sa + kTB) + tid * kEPT, y);
+                if constexpr (QK == Q_PROBS_T1) {
+                  zq2 = fadd2(zq2, fadd2(fadd2(make_float2(y[0], y[1]), make_float2(y[2], y[3])),
+                                         fadd2(make_float2(y[4], y[5]), make_float2(y[6], y[7]))));
+                } else if constexpr (QK == Q_LOGITS) {
+                  lazy_sum(y, kt, mq, zq);
+                } else {
+  #pragma unroll
+                  for (int i = 0; i < 8; ++i) y[i] = lg2(y[i]);
+                  lazy_sum(y, invT, mq, zq);
+                }
+              }
+            }
+            if constexpr (kB) {
+              const float negLp = -Lp, negLq = -Lq;
+              const unsigned char* sb = stage(stg, 1);
+              float x[8], y[8];
+              load8<TT>(reinterpret_cast<const TT*>(sb) + tid * kEPT, x);
+              load8<TD>(reinterpret_cast<const TD*>(sb + kTB) + tid * kEPT, y);
+              const float2 nLp2 = make_float2(negLp, negLp), nLq2 = make_float2(negLq, negLq);
+              auto q2_of = [&](int i) -> float2 {
+                if constexpr (QK == Q_LOGITS)
+                  return ex2x2(ffma2(make_float2(y[i], y[i + 1]), kt2, nLq2));
+                else if constexpr (QK == Q_PROBS_T1)
+                  return fmul2(make_float2(y[i], y[i + 1]), make_float2(invZq, invZq));
+                else
+                  return make_float2(q_of<QK>(y[i], kt, invT, negLq, invZq),
+                                     q_of<QK>(y[i + 1], kt, invT, negLq, invZq));
+              };
+              if constexpr (kR) {
+  #pragma unroll
+                for (int i = 0; i < 8; i += 2) {
+                  const float2 p = ex2x2(ffma2(make_float2(x[i], x[i + 1]), kt2, nLp2));
+                  const float2 q = q2_of(i);
+                  const float2 mn = make_float2(fminf(p.x, q.x), fminf(p.y, q.y));
+                  acc_a2 = fadd2(acc_a2, mn);
+                  acc_r2 = fadd2(acc_r2, ffma2(mn, make_float2(-1.f, -1.f), p));
+                }
               } else if constexpr (QK == Q_LOGITS) {
-                lazy_sum(y, kt, mq, zq);
+                // min(p, q) = 2^min(log2 p, log2 q): one exponential
+  #pragma unroll
+                for (int i = 0; i < 8; i += 2) {
+                  const float2 lp = ffma2(make_float2(x[i], x[i + 1]), kt2, nLp2);
+                  const float2 lq = ffma2(make_float2(y[i], y[i + 1]), kt2, nLq2);
+                  acc_a2 = fadd2(acc_a2, ex2x2(make_float2(fminf(lp.x, lq.x), fminf(lp.y, lq.y))));
+                }
               } else {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) y[i] = lg2(y[i]);
-                lazy_sum(y, invT, mq, zq);
+  #pragma unroll
+                for (int i = 0; i < 8; i += 2) {
+                  const float2 p = ex2x2(ffma2(make_float2(x[i], x[i + 1]), kt2, nLp2));
+                  const float2 q = q2_of(i);
+                  acc_a2 = fadd2(acc_a2, make_float2(fminf(p.x, q.x), fminf(p.y, q.y)));
+                }
               }
             }
           }
-          if (qb >= 0) {
-            const float negLp = -Lp, negLq = -Lq;
-            const unsigned char* sb = stage(stg, 1);
-            float x[8], y[8];
-            load8<TT>(reinterpret_cast<const TT*>(sb) + tid * kEPT, x);
-            load8<TD>(reinterpret_cast<const TD*>(sb + kTB) + tid * kEPT, y);
-            const float2 nLp2 = make_float2(negLp, negLp), nLq2 = make_float2(negLq, negLq);
-            auto q2_of = [&](int i) -> float2 {
-              if constexpr (QK == Q_LOGITS)
-                return ex2x2(ffma2(make_float2(y[i], y[i + 1]), kt2, nLq2));
-              else if constexpr (QK == Q_PROBS_T1)
-                return fmul2(make_float2(y[i], y[i + 1]), make_float2(invZq, invZq));
-              else
-                return make_float2(q_of<QK>(y[i], kt, invT, negLq, invZq),
-                                   q_of<QK>(y[i + 1], kt, invT, negLq, invZq));
-            };
-            if (needR) {
-#pragma unroll
-              for (int i = 0; i < 8; i += 2) {
-                const float2 p = ex2x2(ffma2(make_float2(x[i], x[i + 1]), kt2, nLp2));
-                const float2 q = q2_of(i);
-                const float2 mn = make_float2(fminf(p.x, q.x), fminf(p.y, q.y));
-                acc_a2 = fadd2(acc_a2, mn);
-                acc_r2 = fadd2(acc_r2, ffma2(mn, make_float2(-1.f, -1.f), p));
-              }
-            } else if constexpr (QK == Q_LOGITS) {
-              // min(p, q) = 2^min(log2 p, log2 q): one exponential
-#pragma unroll
-              for (int i = 0; i < 8; i += 2) {
-                const float2 lp = ffma2(make_float2(x[i], x[i + 1]), kt2, nLp2);
-                const float2 lq = ffma2(make_float2(y[i], y[i + 1]), kt2, nLq2);
-                acc_a2 = fadd2(acc_a2, ex2x2(make_float2(fminf(lp.x, lq.x), fminf(lp.y, lq.y))));
-              }
-            } else {
-#pragma unroll
-              for (int i = 0; i < 8; i += 2) {
-                const float2 p = ex2x2(ffma2(make_float2(x[i], x[i + 1]), kt2, nLp2));
-                const float2 q = q2_of(i);
-                acc_a2 = fadd2(acc_a2, make_float2(fminf(p.x, q.x), fminf(p.y, q.y)));
-              }
-            }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.empty[stg]);
+          if (++stg == NS) {
+            stg = 0;
+            ++round;
           }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.empty[stg]);
-        if (++stg == NS) {
-          stg = 0;
-          ++round;
-        }
-      }
+      };
+      using Yes = std::true_type;
+      using No = std::false_type;
+      auto with_b = [&](auto fA, auto fQ) {
+        if (qb < 0) chunk_loop(fA, fQ, No{}, No{});
+        else if (needR) chunk_loop(fA, fQ, Yes{}, Yes{});
+        else chunk_loop(fA, fQ, Yes{}, No{});
+      };
+      if (!hA) with_b(No{}, No{});
+      else if (qa >= 0 && !qlse) with_b(Yes{}, Yes{});
+      else with_b(Yes{}, No{});
 
       // 5. CTA reductions; alpha partial of row j - 1; exchange
       const float acc_a = acc_a2.x + acc_a2.y, acc_r = acc_r2.x + acc_r2.y;
