@@ -43,7 +43,7 @@ def _args():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default=DEFAULT_WORKLOAD,
                    choices=["tree_static", "greedy", "eagle2", "chain_topk",
-                            "chain_sample"])
+                            "chain_sample", "kv_commit"])
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -435,6 +435,8 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
 
+    if args.workload == "kv_commit":
+        return kv_main(args, world, rank, local)
     if args.impl == "reference":
         return reference_arm(args, world, rank)
 
@@ -597,6 +599,239 @@ def dtype_name(w):
     if w.temperature == 0:
         return n[w.target_dtype]
     return f"{n[w.target_dtype]}+{n[w.draft_dtype]} (f32 accumulate)"
+
+
+# ------------------------------------------------------- KV-cache commit
+# A 32-layer model's KV cache (K and V, 8 KV heads of 128 bf16 values),
+# head-major [64, B, 8, S, 128], B = 32 sequences with 2048..4095 committed
+# positions each; after verification of the 60-node static tree, each
+# sequence keeps the path to a random node (none with probability 0.2).
+# 64 seeded path sets cycle, so the rows a step touches are not left in L2
+# by the previous steps (about 1.3 GB over the cycle).
+KV = dict(L=32, H=8, D=128, B=32, N=60, pre_lo=2048, pre_hi=4096, sets=64)
+KV_METRIC = "KV-cache commit bytes moved/s (read + write)"
+
+
+def kv_paths(seed=11):
+    """Path sets: prefix [P, B], length [P, B], nodes [P, B, N] (int32)."""
+    import numpy as np
+    import synth
+    parent = synth.static_tree(synth.workload("tree_static")).numpy()
+    N, B, P = KV["N"], KV["B"], KV["sets"]
+    rng = np.random.default_rng(seed)
+    pre = rng.integers(KV["pre_lo"], KV["pre_hi"], size=(P, B)).astype(np.int32)
+    lens = np.zeros((P, B), dtype=np.int32)
+    nodes = np.full((P, B, N), -1, dtype=np.int32)
+    for k in range(P):
+        for b in range(B):
+            if rng.random() < 0.2:
+                continue
+            j, chain = int(rng.integers(0, N)), []
+            while j >= 0:
+                chain.append(j)
+                j = int(parent[j])
+            chain.reverse()
+            lens[k, b] = len(chain)
+            nodes[k, b, :len(chain)] = chain
+    return pre, lens, nodes
+
+
+def kv_moved_bytes(lens, nodes):
+    """Bytes read + written per path set: 2 x row x planes per moved
+    position (a path position already in place moves nothing)."""
+    import numpy as np
+    row = KV["D"] * 2 * 2 * KV["L"] * KV["H"]  # bf16 rows over all planes
+    idx = np.arange(nodes.shape[-1])
+    moved = ((nodes != idx) & (idx < lens[..., None])).sum(axis=-1)
+    return moved.sum(axis=-1) * row * 2
+
+
+def kv_oracle_rate(pre, lens, nodes, seconds):
+    """The oracle on one sequence at a time (prefix cut to 64 positions so
+    that the host copy of the cache stays small): bytes moved per second."""
+    import numpy as np
+    from oracle.kv import kv_commit
+    N = KV["N"]
+    cache = np.zeros((1, 64 + N, 2 * KV["L"] * KV["H"] * KV["D"]), np.int16)
+    done, t0, i = 0, time.perf_counter(), 0
+    P, B = lens.shape
+    while True:
+        k, b = (i // B) % P, i % B
+        kv_commit(cache, [64], lens[k, b:b + 1], nodes[k, b:b + 1])
+        done += int(kv_moved_bytes(lens[k, b:b + 1][None],
+                                   nodes[k, b:b + 1][None])[0])
+        i += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            return done / el / 1e9, i, el
+
+
+def kv_main(args, world, rank, local):
+    pre, lens, nodes = kv_paths()
+    moved = kv_moved_bytes(lens, nodes)
+    sample = ("sequences one by one through the oracle (numpy), prefix cut "
+              "to 64 positions, {n} sequences in {el:.1f} s")
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        steps = args.steps or 3
+        for _ in range(args.warmup):
+            kv_oracle_rate(pre, lens, nodes, 2.0)
+        tot_b = tot_t = 0.0
+        n_all = 0
+        for _ in range(steps):
+            r, n, el = kv_oracle_rate(pre, lens, nodes, 10.0)
+            tot_b += r * el
+            tot_t += el
+            n_all += n
+        v = tot_b / tot_t
+        print(json.dumps({
+            "impl": "reference", "metric": KV_METRIC, "value": round(v, 4),
+            "unit": "GB/s", "n_gpus": world, "steps": steps,
+            "warmup": args.warmup, "ms_per_step": round(tot_t / steps * 1e3, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16 (bytes)", "data": "synthetic",
+            "config": {"workload": "kv_commit", "B": KV["B"]},
+            "cpu_baseline": {"kind": "oracle", "cores": 1, "value": round(v, 4),
+                             "unit": "GB/s",
+                             "sample": sample.format(n=n_all, el=tot_t)},
+            "e2e": {"value": round(v, 4), "unit": "GB/s",
+                    "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+              flush=True)
+        return
+    import ctypes
+    import torch
+    import __graft_entry__ as g
+    g.build()
+    from speculative_decoding_verification_tree_gb300 import _lib, api
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    L2, H, D, B, N = 2 * KV["L"], KV["H"], KV["D"], KV["B"], KV["N"]
+    S = KV["pre_hi"] + N
+    cache = torch.zeros(L2, B, H, S, D, dtype=torch.bfloat16, device=dev)
+    es = 2
+    layout = (L2, H, H * S * D * es, B * H * S * D * es, S * D * es, D * es)
+    d_pre = torch.tensor(pre, device=dev)
+    d_len = torch.tensor(lens, device=dev)
+    d_nodes = torch.tensor(nodes, device=dev)
+    new_len = torch.empty(B, dtype=torch.int32, device=dev)
+    P = KV["sets"]
+
+    def step(k, ins=None):
+        p_, l_, n_ = ins if ins is not None else (d_pre[k], d_len[k],
+                                                   d_nodes[k])
+        api.spec_kv_commit(cache, p_, l_, n_, layout=layout,
+                           row_bytes=D * es, N=N, new_len=new_len)
+
+    steps = args.steps or 3200
+    warm = max(3, args.warmup)
+    for k in range(warm):
+        step(k % P)
+    torch.cuda.synchronize()
+    clocks = Clocks(local)
+    clocks.start()
+    time.sleep(0.3)
+    h = _lib.load()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    h.spec_profile_enable(1)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for k in range(steps):
+        step(k % P)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    tot, nl = ctypes.c_double(0), ctypes.c_int(0)
+    rc = h.spec_profile_read(_lib.SPEC_PROF_KV, ctypes.byref(tot),
+                             ctypes.byref(nl))
+    h.spec_profile_enable(0)
+    if ms < 1000.0 and not args.no_extend:
+        t_end = time.time() + 1.0
+        while time.time() < t_end:
+            for k in range(50):
+                step(k % P)
+            torch.cuda.synchronize()
+    clocks.stop()
+    ms = max_over_ranks(dist, ms, dev)
+    bytes_run = float(sum(moved[k % P] for k in range(steps)))
+    value = bytes_run * world / (ms / 1e3) / 1e9
+    peak, peak_kind = _peaks()
+    roof = None
+    if nl.value:
+        kern_ms = tot.value / nl.value
+        per_launch = bytes_run / steps
+        achieved = per_launch / (kern_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "traffic": None, "kernel": "kv_move",
+                "bytes_per_launch": int(per_launch),
+                "avg_launch_ms": round(kern_ms, 5), "peak_source": peak_kind,
+                "profile_rc": rc}
+    e2e = None
+    if not args.no_e2e:
+        h_pre = torch.tensor(pre).pin_memory()
+        h_len = torch.tensor(lens).pin_memory()
+        h_nodes = torch.tensor(nodes).pin_memory()
+        h_out = torch.empty(B, dtype=torch.int32).pin_memory()
+        x_pre = torch.empty(B, dtype=torch.int32, device=dev)
+        x_len = torch.empty(B, dtype=torch.int32, device=dev)
+        x_nodes = torch.empty(B, N, dtype=torch.int32, device=dev)
+        n_e2e = 200
+
+        def e2e_step(k):
+            x_pre.copy_(h_pre[k], non_blocking=True)
+            x_len.copy_(h_len[k], non_blocking=True)
+            x_nodes.copy_(h_nodes[k], non_blocking=True)
+            step(k, (x_pre, x_len, x_nodes))
+            h_out.copy_(new_len, non_blocking=True)
+        e2e_step(0)
+        torch.cuda.synchronize()
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record()
+        for k in range(n_e2e):
+            e2e_step(k % P)
+        a1.record()
+        torch.cuda.synchronize()
+        ems = max_over_ranks(dist, a0.elapsed_time(a1), dev)
+        eb = float(sum(moved[k % P] for k in range(n_e2e)))
+        e2e = {"value": round(eb * world / (ems / 1e3) / 1e9, 2),
+               "unit": "GB/s", "h2d_bytes_per_step": B * (N + 2) * 4,
+               "d2h_bytes_per_step": B * 4, "steps": n_e2e,
+               "ms_per_step": round(ems / n_e2e, 4)}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        r, n, el = kv_oracle_rate(pre, lens, nodes, min(args.cpu_seconds, 10))
+        cpu = {"value": round(r, 4), "unit": "GB/s", "cores": 1,
+               "kind": "oracle", "sample": sample.format(n=n, el=el)}
+    if rank == 0:
+        print(json.dumps({
+            "metric": KV_METRIC, "value": round(value, 2), "unit": "GB/s",
+            "n_gpus": world, "steps": steps, "warmup": warm,
+            "ms_per_step": round(ms / steps, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (bytes)",
+            "data": "synthetic (seeded paths of the 60-node static tree)",
+            "config": {"workload": "kv_commit", "B": B, "layers": KV["L"],
+                       "kv_heads": H, "head_dim": D,
+                       "layout": "head-major [2L, B, H, S, D]",
+                       "positions": S, "path_sets": P,
+                       "moved_positions_per_step": round(
+                           float(moved.mean()) / (2 * D * es * L2 * H), 2),
+                       "parallelism": f"replicas x{world} (sequences split)",
+                       "l2": "64 path sets cycle over a "
+                             f"{cache.numel() * es / 1e9:.1f} GB cache"},
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "clocks": clocks.summary(), "gpu_launches": 2 * steps}),
+              flush=True)
+    if dist:
+        dist.destroy_process_group()
 
 
 def reference_arm(args, world, rank):

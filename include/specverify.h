@@ -89,7 +89,7 @@ extern "C" {
 #define SPEC_OP_TREE 2
 #define SPEC_OP_EAGLE2 3
 
-/* Sampling parameters (plain data, 32 bytes). */
+/* Sampling parameters (plain data, 40 bytes). */
 typedef struct spec_params {
   float temperature;      /* > 0: sampling rule; == 0: greedy argmax rule  */
   int32_t top_k;          /* 0 = off; keeps min(top_k, V) tokens           */
@@ -234,6 +234,44 @@ int spec_eagle2_expand_rerank(const void* draft_logits, int B, int V,
 int spec_get_status(const void* workspace, uint32_t* status, void* stream);
 
 /*
+ * KV-cache commit after verification ("KV cache rollback" and step 4 of the
+ * Vietnamese speculative-decoding page; "El baile de caché KV" of the
+ * Spanish page).  The verification pass wrote the drafted positions' KV
+ * entries after each sequence's committed prefix; this keeps those of the
+ * accepted drafts, in path order, and sets the logical lengths.  The token
+ * drawn after the path has no entry yet (the next forward pass writes it).
+ *
+ * Chain (path_nodes == NULL): the accepted drafts are the first path_len[b]
+ *     positions after the prefix, already in place; nothing moves.
+ * Tree: drafted node j's entry is at position prefix_len[b] + j; the path
+ *     path_nodes[b, 0 .. path_len[b]) (node indices, strictly increasing, as
+ *     spec_verify_tree returns them) moves to positions prefix_len[b] + i.
+ *     The move runs in place in path order, which is safe because
+ *     path_nodes[b, i] >= i.
+ * new_len[b] (out) = prefix_len[b] + path_len[b], or -1 if the path is
+ *     invalid (path_len outside [0, N], a node outside [0, N) or not above
+ *     the previous one); such a sequence is left unchanged.
+ * Positions past the new length keep whatever they held.
+ *
+ * Layout: the entry of sequence b at position s is, for every plane
+ * (p1 < n1, p2 < n2), the row_bytes bytes at
+ *     kv + b*stride_b + p1*stride_1 + p2*stride_2 + s*stride_pos   (bytes),
+ * which describes head-major caches ([L*2, B, H, S, D]: n1 = 2L, n2 = H),
+ * position-major ones ([B, S, L*2*H*D]: n1 = n2 = 1) and the like.  The
+ * caller guarantees that the addressed rows of positions up to
+ * prefix_len[b] + N lie in its allocation and do not overlap one another.
+ * Device arrays: prefix_len [B], path_nodes [B, N] (or NULL), path_len [B],
+ * new_len [B].  Errors: SPEC_ERR_SHAPE for negative sizes or a negative
+ * stride; SPEC_ERR_ARG for a NULL prefix_len, path_len or new_len, or a NULL
+ * kv for a tree (when B > 0; a chain does not touch kv).
+ */
+int spec_kv_commit(void* kv, int B, int n1, int n2, int64_t stride_b,
+                   int64_t stride_1, int64_t stride_2, int64_t stride_pos,
+                   int row_bytes, const int32_t* prefix_len,
+                   const int32_t* path_nodes, const int32_t* path_len, int N,
+                   int32_t* new_len, void* stream);
+
+/*
  * The uniforms the kernels draw: out[i] = u(b[i], idx[i], slot[i]) for the
  * given seed and offset (all arrays device, length n).  Lets callers and
  * tests check the device generator bit for bit.
@@ -253,7 +291,8 @@ const char* spec_error_string(int code);
  * milliseconds and number of launches of one kernel kind:
  *   SPEC_PROF_ARGMAX    greedy argmax streaming kernel,
  *   SPEC_PROF_VERIFY    sampled row-verification kernel,
- *   SPEC_PROF_EXPAND    EAGLE-2 draft-row top-k kernel.
+ *   SPEC_PROF_EXPAND    EAGLE-2 draft-row top-k kernel,
+ *   SPEC_PROF_KV        KV-cache commit move kernel.
  * Returns SPEC_ERR_SHAPE if pairs were dropped.  Not thread-safe.
  */
 /*
@@ -285,6 +324,7 @@ int spec_verify_chain_noalloc(const void* target_logits, const void* draft,
 #define SPEC_PROF_ARGMAX 0
 #define SPEC_PROF_VERIFY 1
 #define SPEC_PROF_EXPAND 2
+#define SPEC_PROF_KV 3
 int spec_profile_enable(int on);
 int spec_profile_read(int kind, double* total_ms, int* launches);
 

@@ -51,6 +51,10 @@ PINS = {
     "eagle2.expand_rerank": "brute force over all candidates with sorted(); "
     "connectivity invariant",
     "analysis": "E[tokens], speedup and op-count values printed on the pages",
+    "kv.kv_commit": "the rollback exercise of the Spanish page (prefix 10, "
+    "5 drafts, rejection at the third); the logical-length rule of the "
+    "Vietnamese page; in-place path-order copy equals the alias-free gather; "
+    "the committed entries of a tree are the tokens verify_tree emits",
     "residual inverse-CDF at large V": "parity unpinned beyond the oracle "
     "itself (no page example); guarded by small-V Monte-Carlo",
 }

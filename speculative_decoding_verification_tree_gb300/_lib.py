@@ -87,6 +87,9 @@ _SIGNATURES = {
     "spec_verify_chain_noalloc": (_I, [_P, _P, _P, _I, _I, _I, _I, _I,
                                        ctypes.POINTER(SpecParams), _P, _P, _P,
                                        _P]),
+    "spec_kv_commit": (_I, [_P, _I, _I, _I, ctypes.c_int64, ctypes.c_int64,
+                            ctypes.c_int64, ctypes.c_int64, _I, _P, _P, _P, _I,
+                            _P, _P]),
     "spec_profile_enable": (_I, [_I]),
     "spec_profile_read": (_I, [_I, ctypes.POINTER(ctypes.c_double),
                                ctypes.POINTER(ctypes.c_int)]),
@@ -95,6 +98,7 @@ _SIGNATURES = {
 SPEC_PROF_ARGMAX = 0
 SPEC_PROF_VERIFY = 1
 SPEC_PROF_EXPAND = 2
+SPEC_PROF_KV = 3
 
 EXPORTED = tuple(_SIGNATURES)
 

@@ -157,6 +157,23 @@ def spec_eagle2_expand_rerank(draft_logits, *, temperature, depth=6, topk=10,
     return out
 
 
+def spec_kv_commit(kv, prefix_len, path_len, path_nodes=None, *, layout,
+                   row_bytes, N, new_len=None, stream=None):
+    """Keep the accepted drafts' KV entries (see the C declaration).
+    kv: the cache tensor (its storage is addressed in bytes); layout: the
+    byte strides (n1, n2, stride_b, stride_1, stride_2, stride_pos);
+    prefix_len, path_len [B] int32; path_nodes [B, N] int32 or None (chain).
+    Returns new_len [B] int32."""
+    B = prefix_len.numel()
+    if new_len is None:
+        new_len = torch.empty(B, dtype=torch.int32, device=prefix_len.device)
+    n1, n2, sb, s1, s2, sp = layout
+    _lib.call("spec_kv_commit", _ptr(kv), B, n1, n2, sb, s1, s2, sp,
+              row_bytes, _ptr(prefix_len), _ptr(path_nodes), _ptr(path_len),
+              N, _ptr(new_len), _stream(stream))
+    return new_len
+
+
 def spec_get_status(ws, stream=None) -> int:
     v = ctypes.c_uint32(0)
     _lib.call("spec_get_status", _ptr(ws), ctypes.byref(v), _stream(stream))

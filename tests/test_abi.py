@@ -144,6 +144,24 @@ def test_eagle2_argument_errors(lib):
     assert call(ws_bytes=8) == lib.SPEC_ERR_WORKSPACE
 
 
+def test_kv_commit_argument_errors(lib):
+    f = lib.raw
+
+    def call(B=2, n1=1, n2=1, sb=256, s1=0, s2=0, sp=16, row=16, kv=FAKE,
+             pre=FAKE, nodes=FAKE, plen=FAKE, N=4, out=FAKE):
+        return f("spec_kv_commit", kv, B, n1, n2, sb, s1, s2, sp, row, pre,
+                 nodes, plen, N, out, None)
+    assert call(B=-1) == lib.SPEC_ERR_SHAPE
+    assert call(N=-1) == lib.SPEC_ERR_SHAPE
+    assert call(row=-16) == lib.SPEC_ERR_SHAPE
+    assert call(sp=-16) == lib.SPEC_ERR_SHAPE
+    assert call(pre=None) == lib.SPEC_ERR_ARG
+    assert call(plen=None) == lib.SPEC_ERR_ARG
+    assert call(out=None) == lib.SPEC_ERR_ARG
+    assert call(kv=None) == lib.SPEC_ERR_ARG          # a tree moves entries
+    assert call(B=0, kv=None, pre=None, plen=None, out=None) == lib.SPEC_OK
+
+
 def test_error_strings(lib):
     h = lib.load()
     for code in range(-6, 1):
