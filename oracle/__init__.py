@@ -55,6 +55,12 @@ PINS = {
     "5 drafts, rejection at the third); the logical-length rule of the "
     "Vietnamese page; in-place path-order copy equals the alias-free gather; "
     "the committed entries of a tree are the tokens verify_tree emits",
+    "stats.accept_stats": "hand-worked tree and chain example "
+    "(tests/golden/accept_stats_example.txt); tested set equal to a "
+    "step-by-step simulation of the decisions over every outcome of small "
+    "trees; truncated-geometric lengths and E[tokens] of an i.i.d. chain; a "
+    "calibrated drafter on the diagonal; first- and second-sibling rates of "
+    "verify_tree equal to their exact values",
     "residual inverse-CDF at large V": "parity unpinned beyond the oracle "
     "itself (no page example); guarded by small-V Monte-Carlo",
 }
