@@ -43,7 +43,7 @@ def _args():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default=DEFAULT_WORKLOAD,
                    choices=["tree_static", "greedy", "eagle2", "chain_topk",
-                            "chain_sample", "kv_commit"])
+                            "chain_sample", "kv_commit", "accept_stats"])
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -72,6 +72,10 @@ TRAFFIC = {
     # rows with a draft row
     "eagle2": {"bytes_per_unit": 405.30e6 / 782, "src": _STREAM_SRC,
                "hash": "c09a95dec008f0fa"},
+    # accept_stats_warp at B=65536 rounds: 47.46 MB read + 9.7 KB written
+    "accept_stats": {"bytes_per_unit": 47.47e6 / 65536,
+                     "src": ("accept_stats.cu", "common.cuh", "kernels.h"),
+                     "hash": "7c0188394f47a332"},
 }
 
 
@@ -437,6 +441,8 @@ def main():
 
     if args.workload == "kv_commit":
         return kv_main(args, world, rank, local)
+    if args.workload == "accept_stats":
+        return stats_main(args, world, rank, local)
     if args.impl == "reference":
         return reference_arm(args, world, rank)
 
@@ -829,6 +835,231 @@ def kv_main(args, world, rank, local):
                              f"{cache.numel() * es / 1e9:.1f} GB cache"},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
             "clocks": clocks.summary(), "gpu_launches": 2 * steps}),
+              flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------ acceptance records
+# The outcomes of verifying the 60-node static tree, B = 32 rounds per call
+# (one verification step's batch; --B sets another): each round's path goes
+# to a random node (none with probability 0.15), the drafter's confidence in
+# each node's token is uniform on [0, 1], 20 confidence bins.  Seeded input
+# sets cycle (64 at B = 32).
+ST = dict(B=32, N=60, nbins=20, sets=64)
+ST_METRIC = "verification rounds recorded/s (acceptance records)"
+
+
+def stats_sets(B):
+    """Input sets that cycle: 64 at the default batch, fewer for large
+    batches (at least 4, and the cycle stays larger than L2)."""
+    return max(4, min(ST["sets"], (1 << 20) // max(B, 1)))
+
+
+def stats_inputs(B, seed=13):
+    """count [P, B], parent [P, B, N], path [P, B, N] int32; conf [P, B, N]
+    float32."""
+    import numpy as np
+    import synth
+    tree = synth.static_tree(synth.workload("tree_static")).numpy()
+    N, P = ST["N"], stats_sets(B)
+    # root path of every node
+    tab = np.full((N, N), -1, dtype=np.int32)
+    tlen = np.zeros(N, dtype=np.int32)
+    for j in range(N):
+        chain, v = [], j
+        while v >= 0:
+            chain.append(v)
+            v = int(tree[v])
+        tab[j, :len(chain)] = chain[::-1]
+        tlen[j] = len(chain)
+    rng = np.random.default_rng(seed)
+    target = rng.integers(0, N, size=(P, B))
+    none = rng.random((P, B)) < 0.15
+    count = np.where(none, 0, tlen[target]).astype(np.int32)
+    path = np.where(none[..., None], -1, tab[target]).astype(np.int32)
+    parent = np.ascontiguousarray(
+        np.broadcast_to(tree, (P, B, N)).astype(np.int32))
+    conf = rng.random((P, B, N)).astype(np.float32)
+    return count, parent, path, conf
+
+
+def stats_bytes(count, B):
+    """Algorithmic bytes of one call: each round's count, parent row,
+    confidence row and path prefix read once (records are < 1 KB)."""
+    N = ST["N"]
+    return B * (4 + 8 * N) + 4 * int(count.sum())
+
+
+def stats_oracle_rate(count, parent, path, conf, seconds):
+    from oracle.stats import accept_stats
+    done, t0, k = 0, time.perf_counter(), 0
+    P = count.shape[0]
+    while True:
+        accept_stats(count[k % P], parent[k % P], path[k % P], conf[k % P],
+                     ST["N"], ST["nbins"])
+        done += count.shape[1]
+        k += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            return done / el, done, el
+
+
+def stats_main(args, world, rank, local):
+    B = args.B or ST["B"]
+    count, parent, path, conf = stats_inputs(B)
+    P, N, nb = count.shape[0], ST["N"], ST["nbins"]
+    sample = "rounds through the oracle (numpy / Python), {n} rounds in {el:.1f} s"
+    cfg = {"workload": "accept_stats", "B": B, "nodes": N, "nbins": nb,
+           "tree": "60-node static tree (4,12,16,14,8,6)", "input_sets": P,
+           "l2": f"{P} input sets cycle "
+                 f"({P * stats_bytes(count[0], B) / 1e6:.1f} MB)"}
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        steps = args.steps or 3
+        for _ in range(args.warmup):
+            stats_oracle_rate(count, parent, path, conf, 1.0)
+        done = el = 0.0
+        for _ in range(steps):
+            _, d, e = stats_oracle_rate(count, parent, path, conf, 10.0)
+            done += d
+            el += e
+        v = done / el
+        print(json.dumps({
+            "impl": "reference", "metric": ST_METRIC, "value": round(v, 1),
+            "unit": "rounds/s", "n_gpus": world, "steps": steps,
+            "warmup": args.warmup, "ms_per_step": round(el / steps * 1e3, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "int64 (counts) + f64 (sums)", "data": "synthetic",
+            "config": cfg,
+            "cpu_baseline": {"kind": "oracle", "cores": 1, "value": round(v, 1),
+                             "unit": "rounds/s",
+                             "sample": sample.format(n=int(done), el=el)},
+            "e2e": {"value": round(v, 1), "unit": "rounds/s",
+                    "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+              flush=True)
+        return
+    import ctypes
+    import torch
+    import __graft_entry__ as g
+    g.build()
+    from speculative_decoding_verification_tree_gb300 import _lib, api
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    d_count = torch.from_numpy(count).to(dev)
+    d_parent = torch.from_numpy(parent).to(dev)
+    d_path = torch.from_numpy(path).to(dev)
+    d_conf = torch.from_numpy(conf).to(dev)
+    rec = api.accept_stats_records(N, nb, dev)
+
+    def step(k, ins=None):
+        c, p_, q_, f_ = ins if ins is not None else (
+            d_count[k], d_parent[k], d_path[k], d_conf[k])
+        api.spec_accept_stats(c, p_, q_, f_, n=N, nbins=nb, out=rec)
+
+    steps = args.steps or 2000
+    warm = max(3, args.warmup)
+    for k in range(warm):
+        step(k % P)
+    torch.cuda.synchronize()
+    clocks = Clocks(local)
+    clocks.start()
+    time.sleep(0.3)
+    h = _lib.load()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    h.spec_profile_enable(1)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for k in range(steps):
+        step(k % P)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    tot, nl = ctypes.c_double(0), ctypes.c_int(0)
+    rc = h.spec_profile_read(_lib.SPEC_PROF_STATS, ctypes.byref(tot),
+                             ctypes.byref(nl))
+    h.spec_profile_enable(0)
+    if ms < 1000.0 and not args.no_extend:
+        t_end = time.time() + 1.0
+        while time.time() < t_end:
+            for k in range(50):
+                step(k % P)
+            torch.cuda.synchronize()
+    clocks.stop()
+    ms = max_over_ranks(dist, ms, dev)
+    value = B * steps * world / (ms / 1e3)
+    peak, peak_kind = _peaks()
+    roof = None
+    if nl.value:
+        kern_ms = tot.value / nl.value
+        per_launch = sum(stats_bytes(count[k % P], B)
+                         for k in range(steps)) / steps
+        achieved = per_launch / (kern_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                "unit": "GB/s", "frac": round(achieved / peak, 5),
+                "traffic": _traffic("accept_stats", B),
+                "kernel": "accept_stats_warp" if N <= 64 else
+                          "accept_stats_cta",
+                "bytes_per_launch": int(per_launch),
+                "avg_launch_ms": round(kern_ms, 5), "peak_source": peak_kind,
+                "profile_rc": rc}
+    e2e = None
+    if not args.no_e2e:
+        h_in = [torch.from_numpy(a).pin_memory()
+                for a in (count, parent, path, conf)]
+        x_in = [torch.empty_like(a[0], device=dev) for a in h_in]
+        h_out = {f: torch.empty_like(t, device="cpu").pin_memory()
+                 for f, t in rec.items()}
+        n_e2e = 500
+
+        def e2e_step(k):
+            for x, hh in zip(x_in, h_in):
+                x.copy_(hh[k], non_blocking=True)
+            step(k, x_in)
+            for f, t in rec.items():
+                h_out[f].copy_(t, non_blocking=True)
+        e2e_step(0)
+        torch.cuda.synchronize()
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record()
+        for k in range(n_e2e):
+            e2e_step(k % P)
+        a1.record()
+        torch.cuda.synchronize()
+        ems = max_over_ranks(dist, a0.elapsed_time(a1), dev)
+        e2e = {"value": round(B * n_e2e * world / (ems / 1e3), 1),
+               "unit": "rounds/s",
+               "h2d_bytes_per_step": sum(a[0].numel() * a.element_size()
+                                         for a in h_in),
+               "d2h_bytes_per_step": sum(t.numel() * t.element_size()
+                                         for t in rec.values()),
+               "steps": n_e2e, "ms_per_step": round(ems / n_e2e, 4)}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        r, n, el = stats_oracle_rate(count, parent, path, conf,
+                                     min(args.cpu_seconds, 10))
+        cpu = {"value": round(r, 1), "unit": "rounds/s", "cores": 1,
+               "kind": "oracle", "sample": sample.format(n=n, el=el)}
+    if rank == 0:
+        cfg["parallelism"] = f"replicas x{world} (rounds split)"
+        print(json.dumps({
+            "metric": ST_METRIC, "value": round(value, 1), "unit": "rounds/s",
+            "n_gpus": world, "steps": steps, "warmup": warm,
+            "ms_per_step": round(ms / steps, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "int32 in; int64 counts, f64 confidence sums",
+            "data": "synthetic (seeded paths of the 60-node static tree)",
+            "config": cfg, "roofline": roof, "cpu_baseline": cpu,
+            "e2e": e2e, "clocks": clocks.summary(), "gpu_launches": steps}),
               flush=True)
     if dist:
         dist.destroy_process_group()

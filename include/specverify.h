@@ -272,6 +272,68 @@ int spec_kv_commit(void* kv, int B, int n1, int n2, int64_t stride_b,
                    int32_t* new_len, void* stream);
 
 /*
+ * Acceptance records over verification outcomes, accumulated across calls:
+ * the distribution of the accepted length per round, not only its mean
+ * ("064 · 投机解码", section 五), the acceptance rate of drafted tokens by
+ * position in the draft tree and by depth (EAGLE-2 notes §3.1, Fig. 5), and
+ * by interval of the draft model's confidence in its token (§3.2, Fig. 6).
+ *
+ * A round is one sequence's verification.  A drafted token is TESTED iff its
+ * parent is the root or on the accepted path and no sibling with a lower node
+ * index was accepted (the tree rule tries siblings in node order); it is
+ * ACCEPTED iff it is on the path.  (When the draft distribution runs out of
+ * mass the rule stops trying siblings early; the outcome does not show this
+ * and such siblings count as tested.)  Depth: 1 for a child of the root,
+ * else the parent's depth + 1.
+ *
+ * Chain (parent == path_nodes == NULL): count[b] = accepted drafts of
+ *     spec_verify_chain; token k is tested iff k <= count[b], accepted iff
+ *     k < count[b]; its depth is k + 1.
+ * Tree: count[b] = path_len[b], path_nodes [B, n] and parent [B, n] as
+ *     spec_verify_tree takes and returns them.
+ * confidence [B, n] (float32, or NULL for no calibration record): the draft
+ *     model's probability of each drafted token.  It is clamped to [0, 1] and
+ *     counted in bin floor(c * nbins) (float32 product; 1.0 in the last bin);
+ *     NaN is not binned.
+ *
+ * Records (device arrays owned by the caller, ADDED to, never cleared; any
+ * pointer may be NULL to skip that record):
+ *   len_hist [n + 1]     rounds by accepted length (chain count / path_len)
+ *   node_tested [n], node_accepted [n]      by node index (chain: position)
+ *   depth_tested [n], depth_accepted [n]    index = depth - 1
+ *   calib_tested [nbins], calib_accepted [nbins], calib_conf_sum [nbins]
+ *                        (double: sum of the clamped confidences)
+ *   invalid [1]          rounds that are not a root path of their tree
+ *                        (count outside [0, n], a path node out of range or
+ *                        not a child of the previous one, a parent array
+ *                        not pointing to earlier nodes); they add nothing
+ *                        else.
+ * Integer records are exact; calib_conf_sum is summed in double in no fixed
+ * order.  Calls on one record that overlap on the GPU still add correctly
+ * (device atomics).
+ * Errors: SPEC_ERR_ARG for a NULL count or out, or exactly one of parent /
+ * path_nodes NULL; SPEC_ERR_SHAPE for B < 0, n outside [1,
+ * SPEC_MAX_TREE_NODES], or nbins outside [1, SPEC_STATS_MAX_BINS] when
+ * confidence is given.  B == 0 does nothing.
+ */
+#define SPEC_STATS_MAX_BINS 1024
+typedef struct {
+  int64_t* len_hist;
+  int64_t* node_tested;
+  int64_t* node_accepted;
+  int64_t* depth_tested;
+  int64_t* depth_accepted;
+  int64_t* calib_tested;
+  int64_t* calib_accepted;
+  double* calib_conf_sum;
+  int64_t* invalid;
+} spec_accept_stats_t;
+int spec_accept_stats(const int32_t* count, const int32_t* parent,
+                      const int32_t* path_nodes, const float* confidence,
+                      int B, int n, int nbins, const spec_accept_stats_t* out,
+                      void* stream);
+
+/*
  * The uniforms the kernels draw: out[i] = u(b[i], idx[i], slot[i]) for the
  * given seed and offset (all arrays device, length n).  Lets callers and
  * tests check the device generator bit for bit.
@@ -283,18 +345,6 @@ int spec_philox_uniforms(uint64_t seed, uint32_t offset, const int32_t* b,
 /* Human-readable name of a return code. */
 const char* spec_error_string(int code);
 
-/*
- * Kernel timing for benchmarks.  spec_profile_enable(1) clears the record and
- * makes every later call bracket its dominant kernel with a pair of CUDA
- * events recorded on the caller's stream (at most 16384 pairs); 0 turns it
- * off.  spec_profile_read waits for the recorded events and returns the total
- * milliseconds and number of launches of one kernel kind:
- *   SPEC_PROF_ARGMAX    greedy argmax streaming kernel,
- *   SPEC_PROF_VERIFY    sampled row-verification kernel,
- *   SPEC_PROF_EXPAND    EAGLE-2 draft-row top-k kernel,
- *   SPEC_PROF_KV        KV-cache commit move kernel.
- * Returns SPEC_ERR_SHAPE if pairs were dropped.  Not thread-safe.
- */
 /*
  * Chain verification without a workspace, for callers that cannot allocate
  * device memory (an engine plugin handed only its input and output buffers,
@@ -321,10 +371,24 @@ int spec_verify_chain_noalloc(const void* target_logits, const void* draft,
                               int32_t* out_tokens, float* accept_mass,
                               void* stream);
 
+/*
+ * Kernel timing for benchmarks.  spec_profile_enable(1) clears the record and
+ * makes every later call bracket its dominant kernel with a pair of CUDA
+ * events recorded on the caller's stream (at most 16384 pairs); 0 turns it
+ * off.  spec_profile_read waits for the recorded events and returns the total
+ * milliseconds and number of launches of one kernel kind:
+ *   SPEC_PROF_ARGMAX    greedy argmax streaming kernel,
+ *   SPEC_PROF_VERIFY    sampled row-verification kernel,
+ *   SPEC_PROF_EXPAND    EAGLE-2 draft-row top-k kernel,
+ *   SPEC_PROF_KV        KV-cache commit move kernel,
+ *   SPEC_PROF_STATS     acceptance-records kernel.
+ * Returns SPEC_ERR_SHAPE if pairs were dropped.  Not thread-safe.
+ */
 #define SPEC_PROF_ARGMAX 0
 #define SPEC_PROF_VERIFY 1
 #define SPEC_PROF_EXPAND 2
 #define SPEC_PROF_KV 3
+#define SPEC_PROF_STATS 4
 int spec_profile_enable(int on);
 int spec_profile_read(int kind, double* total_ms, int* launches);
 

@@ -64,6 +64,16 @@ class SpecParams(ctypes.Structure):
 
 assert ctypes.sizeof(SpecParams) == 40
 
+SPEC_STATS_MAX_BINS = 1024
+STATS_FIELDS = ("len_hist", "node_tested", "node_accepted", "depth_tested",
+                "depth_accepted", "calib_tested", "calib_accepted",
+                "calib_conf_sum", "invalid")
+
+
+class SpecAcceptStats(ctypes.Structure):
+    """Mirror of spec_accept_stats_t (nine device pointers)."""
+    _fields_ = [(f, ctypes.c_void_p) for f in STATS_FIELDS]
+
 _P = ctypes.c_void_p
 _I = ctypes.c_int
 _SZ = ctypes.c_size_t
@@ -90,6 +100,8 @@ _SIGNATURES = {
     "spec_kv_commit": (_I, [_P, _I, _I, _I, ctypes.c_int64, ctypes.c_int64,
                             ctypes.c_int64, ctypes.c_int64, _I, _P, _P, _P, _I,
                             _P, _P]),
+    "spec_accept_stats": (_I, [_P, _P, _P, _P, _I, _I, _I,
+                               ctypes.POINTER(SpecAcceptStats), _P]),
     "spec_profile_enable": (_I, [_I]),
     "spec_profile_read": (_I, [_I, ctypes.POINTER(ctypes.c_double),
                                ctypes.POINTER(ctypes.c_int)]),
@@ -99,6 +111,7 @@ SPEC_PROF_ARGMAX = 0
 SPEC_PROF_VERIFY = 1
 SPEC_PROF_EXPAND = 2
 SPEC_PROF_KV = 3
+SPEC_PROF_STATS = 4
 
 EXPORTED = tuple(_SIGNATURES)
 

@@ -174,6 +174,35 @@ def spec_kv_commit(kv, prefix_len, path_len, path_nodes=None, *, layout,
     return new_len
 
 
+def accept_stats_records(n, nbins=20, device=None):
+    """Zeroed records for spec_accept_stats (a dict of device tensors)."""
+    dev = device or torch.cuda.current_device()
+    z = lambda k, dt=torch.int64: torch.zeros(k, dtype=dt, device=dev)
+    return {"len_hist": z(n + 1), "node_tested": z(n), "node_accepted": z(n),
+            "depth_tested": z(n), "depth_accepted": z(n),
+            "calib_tested": z(nbins), "calib_accepted": z(nbins),
+            "calib_conf_sum": z(nbins, torch.float64), "invalid": z(1)}
+
+
+def spec_accept_stats(count, parent=None, path_nodes=None, confidence=None,
+                      *, n, nbins=20, out=None, stream=None):
+    """Add one batch of verification outcomes to the acceptance records.
+    count [B] int32 (chain accepted counts or tree path_len); parent and
+    path_nodes [B, n] int32 for a tree (None for a chain); confidence [B, n]
+    float32 or None.  out: the records (accept_stats_records), added to and
+    returned; entries may be None to skip them."""
+    B = count.numel()
+    if out is None:
+        out = accept_stats_records(n, nbins, count.device)
+    rec = _lib.SpecAcceptStats(*[
+        None if out.get(f) is None else _ptr(out[f]).value
+        for f in _lib.STATS_FIELDS])
+    _lib.call("spec_accept_stats", _ptr(count), _ptr(parent),
+              _ptr(path_nodes), _ptr(confidence), B, n, nbins,
+              ctypes.byref(rec), _stream(stream))
+    return out
+
+
 def spec_get_status(ws, stream=None) -> int:
     v = ctypes.c_uint32(0)
     _lib.call("spec_get_status", _ptr(ws), ctypes.byref(v), _stream(stream))

@@ -167,3 +167,26 @@ def test_error_strings(lib):
     for code in range(-6, 1):
         assert h.spec_error_string(code)
     assert h.spec_error_string(-99) == b"unknown error"
+
+
+def test_accept_stats_argument_errors(lib):
+    f = lib.raw
+    rec = lib.SpecAcceptStats()
+    assert ctypes.sizeof(rec) == 9 * 8
+
+    def call(count=FAKE, parent=FAKE, path=FAKE, conf=FAKE, B=2, n=4,
+             nbins=10, out=ctypes.byref(rec)):
+        return f("spec_accept_stats", count, parent, path, conf, B, n, nbins,
+                 out, None)
+    assert call(count=None) == lib.SPEC_ERR_ARG
+    assert call(out=None) == lib.SPEC_ERR_ARG
+    assert call(parent=None) == lib.SPEC_ERR_ARG      # one of the pair
+    assert call(path=None) == lib.SPEC_ERR_ARG
+    assert call(B=-1) == lib.SPEC_ERR_SHAPE
+    assert call(n=0) == lib.SPEC_ERR_SHAPE
+    assert call(n=1025) == lib.SPEC_ERR_SHAPE
+    assert call(nbins=0) == lib.SPEC_ERR_SHAPE
+    assert call(nbins=lib.SPEC_STATS_MAX_BINS + 1) == lib.SPEC_ERR_SHAPE
+    # without confidences the bin count is not used; B = 0 does nothing
+    assert call(conf=None, nbins=0, B=0) == lib.SPEC_OK
+    assert call(parent=None, path=None, B=0) == lib.SPEC_OK
