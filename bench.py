@@ -64,14 +64,14 @@ def _args():
 _STREAM_SRC = ("sample_stream.cuh", "sample_stream_bf16.cu",
                "sample_stream_f32.cu", "common.cuh", "kernels.h")
 TRAFFIC = {
-    # unit_stream, tree_static at B=16: 759.84 MB read + 3.27 MB written,
+    # unit_stream, tree_static at B=16: 760.13 MB read + 3.39 MB written,
     # 976 rows
-    "tree_static": {"bytes_per_unit": 763.10e6 / 976, "src": _STREAM_SRC,
-                    "hash": "c09a95dec008f0fa"},
-    # unit_stream, eagle2 at B=32: 402.31 MB read + 2.99 MB written, 782
+    "tree_static": {"bytes_per_unit": 763.52e6 / 976, "src": _STREAM_SRC,
+                    "hash": "4e178ce601756105"},
+    # unit_stream, eagle2 at B=32: 402.31 MB read + 3.61 MB written, 782
     # rows with a draft row
-    "eagle2": {"bytes_per_unit": 405.30e6 / 782, "src": _STREAM_SRC,
-               "hash": "c09a95dec008f0fa"},
+    "eagle2": {"bytes_per_unit": 405.93e6 / 782, "src": _STREAM_SRC,
+               "hash": "4e178ce601756105"},
     # accept_stats_warp at B=65536 rounds: 47.46 MB read + 9.7 KB written
     "accept_stats": {"bytes_per_unit": 47.47e6 / 65536,
                      "src": ("accept_stats.cu", "common.cuh", "kernels.h"),
