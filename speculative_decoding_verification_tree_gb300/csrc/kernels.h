@@ -119,7 +119,10 @@ struct StreamParams {
   int wC;         // CTAs per sequence in the walk (its own vocabulary split)
   int wslice;     // vocabulary elements per walk CTA
 };
-bool stream_geometry(int V, int tsz, int dsz, int* C, int* slice, int* nch, int* stages);
+// rows, sms, passA (bytes per logit that pass A reads): when given, rows
+// that fill every SM and whose pass-A bytes fit L2 take one CTA each.
+bool stream_geometry(int V, int tsz, int dsz, int* C, int* slice, int* nch, int* stages,
+                     int64_t rows = 0, int sms = 0, int passA = 0);
 cudaError_t launch_stream_bf16(StreamParams P, cudaStream_t st);
 cudaError_t launch_stream_f32(StreamParams P, cudaStream_t st);
 

@@ -722,8 +722,15 @@ cudaError_t launch_sampled(const VerifyShape& s, const VerifyArgs& a, cudaStream
   cudaError_t e = cudaSuccess;
   // bandwidth path: persistent streaming clusters (16-byte aligned rows)
   StreamParams Q{};
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return cudaErrorInvalidDevice;
+  // pass A reads the draft row too unless its normaliser is given
+  const int passA = tsz + ((qk == Q_LOGITS && a.prm.draft_lse) ? 0 : dsz);
   if (P.bulk && a.meta && a.qres && a.rowout &&
-      stream_geometry(s.V, tsz, dsz, &Q.C, &Q.slice, &Q.nch, &Q.stages)) {
+      stream_geometry(s.V, tsz, dsz, &Q.C, &Q.slice, &Q.nch, &Q.stages, s.rows(), sms,
+                      passA)) {
     Q.s = s;
     Q.a = a;
     Q.qk = qk;

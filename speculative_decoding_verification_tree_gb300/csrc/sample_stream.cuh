@@ -1256,16 +1256,31 @@ __global__ void __launch_bounds__(kWalkThreads) stream_walk(StreamParams P) {
   cluster_sync();  // no CTA leaves while a peer may still write to it
 }
 
+// L2 that the pass-B re-reads may count on: a cluster's pass A of row j and
+// pass B of row j - 1 are one row-time apart, so every cluster keeps one
+// row's pass-A bytes (its slices) in L2 until they are read again.  With
+// 152 single-CTA clusters a static-tree row (2 + 4 bytes per logit at V =
+// 128256) would keep 117 MB in flight and pass B fell out of L2 (the
+// kernel took 0.397 ms against 0.253 ms with clusters of 2); an EAGLE-2
+// row whose draft normaliser is given keeps only the target row, 39 MB.
+constexpr int64_t kL2Keep = 64LL << 20;
+
 // Geometry for rows of V logits with element sizes tsz (target), dsz (draft):
-// the smallest cluster (from 2) whose slices fit the walk's chunk table, and
-// as many ring stages as fit kRing.  False when the streaming kernel does not
-// apply (V not a multiple of 8, or rows too long).
-inline bool geometry(int V, int tsz, int dsz, int* C, int* slice, int* nch, int* stages) {
+// the smallest cluster whose slices fit the walk's chunk table, and as many
+// ring stages as fit kRing.  One CTA per row (no cluster exchange, twice the
+// logits per row-time) when there are at least as many rows as SMs and the
+// rows' pass-A bytes (passA per logit) in flight fit kL2Keep; otherwise
+// clusters of 2 or more.  False when the streaming kernel does not apply (V
+// not a multiple of 8, or rows too long).
+inline bool geometry(int V, int tsz, int dsz, int* C, int* slice, int* nch, int* stages,
+                     int64_t rows = 0, int sms = 0, int passA = 0) {
   if (V <= 0 || V % 8 != 0) return false;
   const int64_t stage = 2LL * kCH * (tsz + dsz);
   const int ns = (int)(kRing / stage);
   if (ns < 2) return false;
-  for (int c = 2; c <= kMaxC; c *= 2) {
+  const bool single = sms > 0 && passA > 0 && rows >= sms &&
+                      (int64_t)sms * V * passA <= kL2Keep;
+  for (int c = single ? 1 : 2; c <= kMaxC; c *= 2) {
     const int sl = ((V + c - 1) / c + 7) / 8 * 8;
     const int nc = (sl + kCH - 1) / kCH;
     if (nc > kMaxTiles) continue;

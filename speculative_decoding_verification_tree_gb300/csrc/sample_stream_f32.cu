@@ -9,8 +9,9 @@ cudaError_t launch_stream_f32(StreamParams P, cudaStream_t st) {
   return stream::launch_dt<float, float>(P, st);
 }
 
-bool stream_geometry(int V, int tsz, int dsz, int* C, int* slice, int* nch, int* stages) {
-  return stream::geometry(V, tsz, dsz, C, slice, nch, stages);
+bool stream_geometry(int V, int tsz, int dsz, int* C, int* slice, int* nch, int* stages,
+                     int64_t rows, int sms, int passA) {
+  return stream::geometry(V, tsz, dsz, C, slice, nch, stages, rows, sms, passA);
 }
 
 }  // namespace sv
