@@ -21,7 +21,7 @@ Synthetic harness (the draft forward between layers is outside this path):
 ``draft`` holds every draft row up front, row 0 for the root and row
 1 + (d-1)*W + r for the r-th kept node of layer d (d = 1 .. L-1).
 
-Readings (listed in the design doc): confidence = q after the temperature
+Readings taken where the pages are silent: confidence = q after the temperature
 transform; children of a row are its ``topk`` most probable tokens (ties to the
 lower index); layer keep and rerank order by (value desc, depth asc, candidate
 id asc) with candidate id = (layer, parent rank, child rank).

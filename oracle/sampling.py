@@ -6,7 +6,7 @@ Every helper that does arithmetic on distributions is written with plain numpy
 operations that also work on ``dtype=object`` arrays of ``fractions.Fraction``,
 so the exactness tests can run the very same code in exact arithmetic.
 
-Readings taken where the pages are silent (listed again in the design doc):
+Readings taken where the pages are silent:
 
 * Transform order is temperature -> top-k -> top-p, renormalising after each
   truncation; top-k ties go to the lower token index; top-p keeps the shortest
