@@ -61,6 +61,11 @@ PINS = {
     "trees; truncated-geometric lengths and E[tokens] of an i.i.d. chain; a "
     "calibrated drafter on the diagonal; first- and second-sibling rates of "
     "verify_tree equal to their exact values",
+    "attention.tree_attention": "torch scaled_dot_product_attention "
+    "(float64) with the mask written out per position, grouped-query heads "
+    "included; the chain case equals causal attention; a root child without "
+    "prefix returns its own value; other branches and the prefix order do "
+    "not change a node's output",
     "residual inverse-CDF at large V": "parity unpinned beyond the oracle "
     "itself (no page example); guarded by small-V Monte-Carlo",
 }
