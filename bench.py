@@ -43,7 +43,8 @@ def _args():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default=DEFAULT_WORKLOAD,
                    choices=["tree_static", "greedy", "eagle2", "chain_topk",
-                            "chain_sample", "kv_commit", "accept_stats"])
+                            "chain_sample", "kv_commit", "accept_stats",
+                            "tree_attention"])
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -443,6 +444,8 @@ def main():
         return kv_main(args, world, rank, local)
     if args.workload == "accept_stats":
         return stats_main(args, world, rank, local)
+    if args.workload == "tree_attention":
+        return attn_main(args, world, rank, local)
     if args.impl == "reference":
         return reference_arm(args, world, rank)
 
@@ -1058,6 +1061,229 @@ def stats_main(args, world, rank, local):
             "scaling": "weak", "vs_baseline": None,
             "dtype": "int32 in; int64 counts, f64 confidence sums",
             "data": "synthetic (seeded paths of the 60-node static tree)",
+            "config": cfg, "roofline": roof, "cpu_baseline": cpu,
+            "e2e": e2e, "clocks": clocks.summary(), "gpu_launches": steps}),
+              flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------ tree attention
+# One attention layer of the verification pass of a Llama-3-8B-shaped target
+# (32 query heads over 8 key/value heads, head dim 128, bf16): B = 32
+# sequences with committed prefixes of 2048..4095 positions, the 60-node
+# static tree drafted after each.  The caches (2 x 272 MB) exceed L2.
+AT = dict(B=32, Hq=32, Hkv=8, D=128, pre_lo=2048, pre_hi=4096)
+AT_METRIC = "tree-attention verified draft tokens/s (one layer)"
+
+
+def attn_inputs(B, seed=31):
+    import numpy as np
+    import synth
+    tree = synth.static_tree(synth.workload("tree_static")).numpy()
+    rng = np.random.default_rng(seed)
+    prefix = rng.integers(AT["pre_lo"], AT["pre_hi"], size=B).astype(np.int32)
+    return tree, prefix
+
+
+def attn_work(prefix, N):
+    """Algorithmic bytes (each key / value row of the range once, q, out)
+    and FLOPs (QK and PV over every key of the range) of one call."""
+    H, Hq, D = AT["Hkv"], AT["Hq"], AT["D"]
+    keys = int(prefix.sum()) + len(prefix) * N
+    nbytes = keys * H * D * 2 * 2 + 2 * len(prefix) * N * Hq * D * 2
+    flops = 4 * keys * N * Hq * D
+    return nbytes, flops
+
+
+def attn_oracle_rate(tree, prefix, seconds):
+    """The oracle on one sequence at a time (prefix cut to 256 positions so
+    that a sample finishes): draft tokens per second."""
+    import numpy as np
+    from oracle.attention import tree_attention
+    rng = np.random.default_rng(0)
+    N, Hq, H, D = tree.size, AT["Hq"], AT["Hkv"], AT["D"]
+    P = 256
+    q = rng.normal(size=(1, N, Hq, D))
+    k = rng.normal(size=(1, H, P + N, D))
+    v = rng.normal(size=(1, H, P + N, D))
+    done, t0 = 0, time.perf_counter()
+    while True:
+        tree_attention(q, k, v, [P], tree[None], D ** -0.5)
+        done += N
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            return done / el, done, el
+
+
+def attn_main(args, world, rank, local):
+    B = args.B or AT["B"]
+    tree, prefix = attn_inputs(B)
+    N = tree.size
+    sample = ("sequences of the oracle (numpy float64) with the prefix cut to "
+              "256 positions, {n} draft tokens in {el:.1f} s")
+    cfg = {"workload": "tree_attention", "B": B, "nodes": N, "q_heads": AT["Hq"],
+           "kv_heads": AT["Hkv"], "head_dim": AT["D"],
+           "prefix": f"{AT['pre_lo']}..{AT['pre_hi'] - 1}",
+           "tree": "60-node static tree (4,12,16,14,8,6)",
+           "l2": "K and V caches (2 x 272 MB at B=32) exceed L2"}
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        steps = args.steps or 3
+        for _ in range(args.warmup):
+            attn_oracle_rate(tree, prefix, 1.0)
+        done = el = 0.0
+        for _ in range(steps):
+            _, d, e = attn_oracle_rate(tree, prefix, 10.0)
+            done += d
+            el += e
+        v = done / el
+        print(json.dumps({
+            "impl": "reference", "metric": AT_METRIC, "value": round(v, 2),
+            "unit": "tokens/s", "n_gpus": world, "steps": steps,
+            "warmup": args.warmup, "ms_per_step": round(el / steps * 1e3, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic", "config": cfg,
+            "cpu_baseline": {"kind": "oracle", "cores": 1, "value": round(v, 2),
+                             "unit": "tokens/s",
+                             "sample": sample.format(n=int(done), el=el)},
+            "e2e": {"value": round(v, 2), "unit": "tokens/s",
+                    "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+              flush=True)
+        return
+    import ctypes
+    import numpy as np
+    import torch
+    import __graft_entry__ as g
+    g.build()
+    from oracle.tree import tree_mask
+    from speculative_decoding_verification_tree_gb300 import _lib, api
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    Hq, H, D = AT["Hq"], AT["Hkv"], AT["D"]
+    S = AT["pre_hi"] + 64
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(37)
+    q = torch.randn(B, N, Hq, D, generator=gen, device=dev).bfloat16()
+    kc = torch.randn(B, H, S, D, generator=gen, device=dev).bfloat16()
+    vc = torch.randn(B, H, S, D, generator=gen, device=dev).bfloat16()
+    parent = np.tile(tree, (B, 1))
+    bits = torch.from_numpy(tree_mask(parent)[1].view(np.int64)).to(dev)
+    pre = torch.from_numpy(prefix).to(dev)
+    out = torch.empty_like(q)
+
+    def step(ins=None):
+        q_, p_, b_ = ins if ins is not None else (q, pre, bits)
+        api.spec_tree_attention(q_, kc, vc, p_, b_, out=out)
+
+    steps = args.steps or 300
+    warm = max(3, args.warmup)
+    for _ in range(warm):
+        step()
+    torch.cuda.synchronize()
+    clocks = Clocks(local)
+    clocks.start()
+    time.sleep(0.3)
+    h = _lib.load()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    h.spec_profile_enable(1)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    tot, nl = ctypes.c_double(0), ctypes.c_int(0)
+    rc = h.spec_profile_read(_lib.SPEC_PROF_ATTN, ctypes.byref(tot),
+                             ctypes.byref(nl))
+    h.spec_profile_enable(0)
+    if ms < 1000.0 and not args.no_extend:
+        t_end = time.time() + 1.0
+        while time.time() < t_end:
+            for _ in range(20):
+                step()
+            torch.cuda.synchronize()
+    clocks.stop()
+    ms = max_over_ranks(dist, ms, dev)
+    value = B * N * steps * world / (ms / 1e3)
+    nbytes, flops = attn_work(prefix, N)
+    peak, peak_kind = _peaks()
+    roof = None
+    if nl.value:
+        kern_ms = tot.value / nl.value
+        achieved = nbytes / (kern_ms / 1e3) / 1e9
+        tf = flops / (kern_ms / 1e3) / 1e12
+        try:
+            with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+                tpk = float(json.load(f)["bf16_tflops"])
+        except (OSError, KeyError, ValueError):
+            tpk = 1900.0
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "traffic": None, "kernel": "tree_attn_kernel",
+                "bytes_per_launch": int(nbytes),
+                "avg_launch_ms": round(kern_ms, 5), "peak_source": peak_kind,
+                "tensor": {"achieved_tflops": round(tf, 1),
+                           "peak_tflops": tpk, "frac": round(tf / tpk, 4),
+                           "flops_per_launch": int(flops),
+                           "path": "mma.sync m16n8k16 bf16"},
+                "profile_rc": rc}
+    e2e = None
+    if not args.no_e2e:
+        h_q = q.cpu().pin_memory()
+        h_pre = pre.cpu().pin_memory()
+        h_bits = bits.cpu().pin_memory()
+        h_out = torch.empty_like(out, device="cpu").pin_memory()
+        x_q, x_pre, x_bits = (torch.empty_like(q), torch.empty_like(pre),
+                              torch.empty_like(bits))
+        n_e2e = 100
+
+        def e2e_step():
+            x_q.copy_(h_q, non_blocking=True)
+            x_pre.copy_(h_pre, non_blocking=True)
+            x_bits.copy_(h_bits, non_blocking=True)
+            step((x_q, x_pre, x_bits))
+            h_out.copy_(out, non_blocking=True)
+        e2e_step()
+        torch.cuda.synchronize()
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record()
+        for _ in range(n_e2e):
+            e2e_step()
+        a1.record()
+        torch.cuda.synchronize()
+        ems = max_over_ranks(dist, a0.elapsed_time(a1), dev)
+        e2e = {"value": round(B * N * n_e2e * world / (ems / 1e3), 1),
+               "unit": "tokens/s",
+               "h2d_bytes_per_step": q.numel() * 2 + B * 4 + B * N * 8,
+               "d2h_bytes_per_step": out.numel() * 2,
+               "steps": n_e2e, "ms_per_step": round(ems / n_e2e, 4),
+               "note": "the K/V caches stay resident (they are the model's "
+                       "state, not a per-step input)"}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        r, n, el = attn_oracle_rate(tree, prefix, min(args.cpu_seconds, 10))
+        cpu = {"value": round(r, 2), "unit": "tokens/s", "cores": 1,
+               "kind": "oracle", "sample": sample.format(n=n, el=el)}
+    if rank == 0:
+        cfg["parallelism"] = f"replicas x{world} (sequences split)"
+        print(json.dumps({
+            "metric": AT_METRIC, "value": round(value, 1), "unit": "tokens/s",
+            "n_gpus": world, "steps": steps, "warmup": warm,
+            "ms_per_step": round(ms / steps, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16 (f32 softmax and accumulation)",
+            "data": "synthetic (seeded N(0,1) q, k, v; static tree)",
             "config": cfg, "roofline": roof, "cpu_baseline": cpu,
             "e2e": e2e, "clocks": clocks.summary(), "gpu_launches": steps}),
               flush=True)

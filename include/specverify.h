@@ -334,6 +334,37 @@ int spec_accept_stats(const int32_t* count, const int32_t* parent,
                       void* stream);
 
 /*
+ * Attention of the verification pass over a draft tree (EAGLE-2 notes §4.2:
+ * the selected draft tokens are flattened and verified in one forward pass,
+ * each seeing only the committed prefix, its ancestors and itself; the
+ * Spanish lesson's Medusa section uses the same tree attention).  For
+ * sequence b with prefix length P = prefix_len[b] and drafted node i:
+ *
+ *   o[b,i,h] = sum_s softmax_s(scale * q[b,i,h] . k[b,h/G,s]) v[b,h/G,s]
+ *   over s < P, and s = P + j for every bit j set in mask_bits[b, i]
+ *
+ * (G = Hq / Hkv query heads per key/value head).  The drafted tokens' keys
+ * and values are already in the cache at positions P .. P + N - 1 in node
+ * order; mask_bits is spec_tree_mask's 64-bit output (bit j of row i:
+ * j is an ancestor of i, or i itself).
+ *
+ * Layout (device, bf16 stored as uint16, row-major, contiguous):
+ *   q [B, N, Hq, D], out [B, N, Hq, D] (written), k_cache and v_cache
+ *   [B, Hkv, S, D], prefix_len [B] int32, mask_bits [B, N] uint64.
+ * Softmax and accumulation in float32; the output is rounded to bf16.
+ * prefix_len is clamped to [0, S - N].
+ * Errors: SPEC_ERR_SHAPE unless 1 <= N <= 64, Hq % Hkv == 0 and S >= N;
+ * SPEC_ERR_UNSUPPORTED unless D == 128; SPEC_ERR_ARG for scale <= 0 or not
+ * finite, a NULL pointer (B > 0), caches not 16-byte aligned or q / out
+ * not 4-byte aligned.  B == 0 does nothing.
+ */
+int spec_tree_attention(const void* q, const void* k_cache,
+                        const void* v_cache, const int32_t* prefix_len,
+                        const uint64_t* mask_bits, int B, int N, int Hq,
+                        int Hkv, int D, int S, float scale, void* out,
+                        void* stream);
+
+/*
  * The uniforms the kernels draw: out[i] = u(b[i], idx[i], slot[i]) for the
  * given seed and offset (all arrays device, length n).  Lets callers and
  * tests check the device generator bit for bit.
@@ -381,7 +412,8 @@ int spec_verify_chain_noalloc(const void* target_logits, const void* draft,
  *   SPEC_PROF_VERIFY    sampled row-verification kernel,
  *   SPEC_PROF_EXPAND    EAGLE-2 draft-row top-k kernel,
  *   SPEC_PROF_KV        KV-cache commit move kernel,
- *   SPEC_PROF_STATS     acceptance-records kernel.
+ *   SPEC_PROF_STATS     acceptance-records kernel,
+ *   SPEC_PROF_ATTN      tree-attention kernel.
  * Returns SPEC_ERR_SHAPE if pairs were dropped.  Not thread-safe.
  */
 #define SPEC_PROF_ARGMAX 0
@@ -389,6 +421,7 @@ int spec_verify_chain_noalloc(const void* target_logits, const void* draft,
 #define SPEC_PROF_EXPAND 2
 #define SPEC_PROF_KV 3
 #define SPEC_PROF_STATS 4
+#define SPEC_PROF_ATTN 5
 int spec_profile_enable(int on);
 int spec_profile_read(int kind, double* total_ms, int* launches);
 

@@ -102,6 +102,8 @@ _SIGNATURES = {
                             _P, _P]),
     "spec_accept_stats": (_I, [_P, _P, _P, _P, _I, _I, _I,
                                ctypes.POINTER(SpecAcceptStats), _P]),
+    "spec_tree_attention": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
+                                 ctypes.c_float, _P, _P]),
     "spec_profile_enable": (_I, [_I]),
     "spec_profile_read": (_I, [_I, ctypes.POINTER(ctypes.c_double),
                                ctypes.POINTER(ctypes.c_int)]),
@@ -112,6 +114,7 @@ SPEC_PROF_VERIFY = 1
 SPEC_PROF_EXPAND = 2
 SPEC_PROF_KV = 3
 SPEC_PROF_STATS = 4
+SPEC_PROF_ATTN = 5
 
 EXPORTED = tuple(_SIGNATURES)
 

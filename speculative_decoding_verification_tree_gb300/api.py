@@ -203,6 +203,26 @@ def spec_accept_stats(count, parent=None, path_nodes=None, confidence=None,
     return out
 
 
+def spec_tree_attention(q, k_cache, v_cache, prefix_len, mask_bits, *,
+                        scale=None, out=None, stream=None):
+    """q [B, N, Hq, D] bf16; k_cache, v_cache [B, Hkv, S, D] bf16;
+    prefix_len [B] int32; mask_bits [B, N] int64 (uint64 bit patterns from
+    spec_tree_mask).  Returns out [B, N, Hq, D] bf16."""
+    B, N, Hq, D = q.shape
+    _, Hkv, S, _ = k_cache.shape
+    for t in (q, k_cache, v_cache):
+        if t.dtype != torch.bfloat16:
+            raise ValueError("q, k_cache and v_cache must be bfloat16")
+    if out is None:
+        out = torch.empty_like(q)
+    if scale is None:
+        scale = D ** -0.5
+    _lib.call("spec_tree_attention", _ptr(q), _ptr(k_cache), _ptr(v_cache),
+              _ptr(prefix_len), _ptr(mask_bits), B, N, Hq, Hkv, D, S,
+              float(scale), _ptr(out), _stream(stream))
+    return out
+
+
 def spec_get_status(ws, stream=None) -> int:
     v = ctypes.c_uint32(0)
     _lib.call("spec_get_status", _ptr(ws), ctypes.byref(v), _stream(stream))

@@ -190,3 +190,23 @@ def test_accept_stats_argument_errors(lib):
     # without confidences the bin count is not used; B = 0 does nothing
     assert call(conf=None, nbins=0, B=0) == lib.SPEC_OK
     assert call(parent=None, path=None, B=0) == lib.SPEC_OK
+
+
+def test_tree_attention_argument_errors(lib):
+    f = lib.raw
+
+    def call(B=2, N=8, Hq=8, Hkv=2, D=128, S=64, scale=0.1, q=FAKE, k=FAKE,
+             v=FAKE, out=FAKE):
+        return f("spec_tree_attention", q, k, v, FAKE, FAKE, B, N, Hq, Hkv, D,
+                 S, ctypes.c_float(scale), out, None)
+    assert call(N=0) == lib.SPEC_ERR_SHAPE
+    assert call(N=65) == lib.SPEC_ERR_SHAPE
+    assert call(Hq=6, Hkv=4) == lib.SPEC_ERR_SHAPE
+    assert call(S=4) == lib.SPEC_ERR_SHAPE
+    assert call(B=-1) == lib.SPEC_ERR_SHAPE
+    assert call(D=64) == lib.SPEC_ERR_UNSUPPORTED
+    assert call(scale=0.0) == lib.SPEC_ERR_ARG
+    assert call(scale=float("inf")) == lib.SPEC_ERR_ARG
+    assert call(q=None) == lib.SPEC_ERR_ARG
+    assert call(k=ctypes.c_void_p(0x7f0000000008)) == lib.SPEC_ERR_ARG
+    assert call(B=0, q=None, out=None) == lib.SPEC_OK
