@@ -107,6 +107,8 @@ __global__ void __launch_bounds__(kK) sparse_units(VerifyShape s, VerifyArgs a, 
   __shared__ float pk[kK], qk[kK];          // probabilities, list order
   __shared__ int ptok_v[kK];                // support of p in vocabulary order
   __shared__ float pv_v[kK], qv_v[kK];      // p and q at those tokens
+  __shared__ float tvs[kK], dvs[kK];        // candidate values (target, draft)
+  __shared__ int32_t tis[kK], dis[kK];      // candidate tokens
   __shared__ int s_np, s_nq;
   const int64_t u = blockIdx.x;
   const int64_t rows = s.rows();
@@ -122,23 +124,34 @@ __global__ void __launch_bounds__(kK) sparse_units(VerifyShape s, VerifyArgs a, 
   const float* dv = o.val + (rows + u) * kK;
   const int32_t* di = o.idx + (rows + u) * kK;
   const bool has_q = M->qr >= 0 && cq > 0;
+  // the candidate lists into shared memory (one element per thread: at most
+  // kK each), so that the serial steps below read no global memory
+  if (tid < ct) {
+    tvs[tid] = tv[tid];
+    tis[tid] = ti[tid];
+  }
+  if (tid < cq) {
+    dvs[tid] = dv[tid];
+    dis[tid] = di[tid];
+  }
+  __syncthreads();
   if (tid == 0) {
     uint32_t bad = M->bad;
     if (ct <= 0) bad |= SPEC_STATUS_NAN;
-    s_np = transform_list(tv, ct, false, kt, invT, a.prm.top_p, pk);
-    s_nq = has_q ? transform_list(dv, cq, probs, kt, invT, a.prm.top_p, qk) : 0;
+    s_np = transform_list(tvs, ct, false, kt, invT, a.prm.top_p, pk);
+    s_nq = has_q ? transform_list(dvs, cq, probs, kt, invT, a.prm.top_p, qk) : 0;
     if (bad) flag_status(a.status, bad);
   }
   __syncthreads();
   const int np = s_np, nq = s_nq;
   // support of p in vocabulary order (tokens are distinct: rank by counting)
   if (tid < np) {
-    const int t = ti[tid];
+    const int t = tis[tid];
     int rk = 0;
-    for (int j = 0; j < np; ++j) rk += (ti[j] < t) ? 1 : 0;
+    for (int j = 0; j < np; ++j) rk += (tis[j] < t) ? 1 : 0;
     float qa = 0.f;
     for (int j = 0; j < nq; ++j)
-      if (di[j] == t) qa = qk[j];
+      if (dis[j] == t) qa = qk[j];
     ptok_v[rk] = t;
     pv_v[rk] = pk[tid];
     qv_v[rk] = qa;
@@ -158,7 +171,7 @@ __global__ void __launch_bounds__(kK) sparse_units(VerifyShape s, VerifyArgs a, 
   };
   auto q_at = [&](int x) -> float {
     for (int j = 0; j < nq; ++j)
-      if (di[j] == x) return qk[j];
+      if (dis[j] == x) return qk[j];
     return 0.f;
   };
   // acceptance mass over the common support
