@@ -37,6 +37,13 @@ def _dt(t):
     return _DT[t.dtype]
 
 
+def _want(t, dtype, shape, name):
+    """Dtype and shape check of an argument (the C ABI sees only pointers)."""
+    if t.dtype != dtype or tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must be {dtype} of shape {tuple(shape)}, "
+                         f"got {t.dtype} {tuple(t.shape)}")
+
+
 def _stream(stream):
     s = stream if stream is not None else torch.cuda.current_stream()
     return ctypes.c_void_p(s.cuda_stream)
@@ -192,6 +199,15 @@ def spec_accept_stats(count, parent=None, path_nodes=None, confidence=None,
     float32 or None.  out: the records (accept_stats_records), added to and
     returned; entries may be None to skip them."""
     B = count.numel()
+    _want(count, torch.int32, (B,), "count")
+    if (parent is None) != (path_nodes is None):
+        raise ValueError("parent and path_nodes go together (tree) or are "
+                         "both None (chain)")
+    if parent is not None:
+        _want(parent, torch.int32, (B, n), "parent")
+        _want(path_nodes, torch.int32, (B, n), "path_nodes")
+    if confidence is not None:
+        _want(confidence, torch.float32, (B, n), "confidence")
     if out is None:
         out = accept_stats_records(n, nbins, count.device)
     rec = _lib.SpecAcceptStats(*[
@@ -210,9 +226,11 @@ def spec_tree_attention(q, k_cache, v_cache, prefix_len, mask_bits, *,
     spec_tree_mask).  Returns out [B, N, Hq, D] bf16."""
     B, N, Hq, D = q.shape
     _, Hkv, S, _ = k_cache.shape
-    for t in (q, k_cache, v_cache):
-        if t.dtype != torch.bfloat16:
-            raise ValueError("q, k_cache and v_cache must be bfloat16")
+    _want(q, torch.bfloat16, (B, N, Hq, D), "q")
+    _want(k_cache, torch.bfloat16, (B, Hkv, S, D), "k_cache")
+    _want(v_cache, torch.bfloat16, (B, Hkv, S, D), "v_cache")
+    _want(prefix_len, torch.int32, (B,), "prefix_len")
+    _want(mask_bits, torch.int64, (B, N), "mask_bits")
     if out is None:
         out = torch.empty_like(q)
     if scale is None:
