@@ -35,9 +35,10 @@ pinned by tests in ``tests/test_oracle_*.py`` except where marked
 """
 
 PINS = {
-    "philox.philox4x32_10": "structural (bijection per key, round function vs "
-    "big-integer arithmetic) + uniformity chi-square; no external known-answer "
-    "vector -- parity unpinned against a third-party KAT",
+    "philox.philox4x32_10": "equal to an independent library implementation "
+    "(Triton's tl.philox, ten rounds, run as a black box in its CPU "
+    "interpreter) on extreme and random keys and counters; structural "
+    "(bijection per key) + uniformity chi-square",
     "sampling.transform": "brute force vs stable sort on V<=64; softmax closed "
     "forms",
     "sampling.residual / accept_prob": "worked examples of the Leviathan "
