@@ -67,6 +67,8 @@ PINS = {
     "included; the chain case equals causal attention; a root child without "
     "prefix returns its own value; other branches and the prefix order do "
     "not change a node's output",
-    "residual inverse-CDF at large V": "parity unpinned beyond the oracle "
-    "itself (no page example); guarded by small-V Monte-Carlo",
+    "residual inverse-CDF at large V": "equal to the draw in exact integer "
+    "arithmetic (weights scaled by a common power of two, 24-bit dyadic "
+    "uniforms) on residual rows at V = 128256, wherever no near tie is "
+    "reported",
 }

@@ -265,3 +265,47 @@ def test_philox_round_matches_multiword_product():
         prod1 = divmod(philox.M1 * c[2], 2**32)
         assert out == (prod1[0] ^ c[1] ^ k[0], prod1[1],
                        prod0[0] ^ c[3] ^ k[1], prod0[1])
+
+
+def _exact_inverse_cdf(w, u):
+    """Smallest y with sum_{x<=y} w(x) > u * sum(w), in exact arithmetic:
+    float64 weights are scaled to integers by a common power of two, and u
+    is a 24-bit dyadic (k / 2^24), so every comparison is between integers."""
+    import math
+    w = np.asarray(w, dtype=np.float64)
+    fr = [math.frexp(float(x)) for x in w]          # x = m * 2^e, 0.5<=m<1
+    emin = min(e for m, e in fr if m != 0.0) - 53
+    ints = [int(m * (1 << 53)) << (e - 53 - emin) if m != 0.0 else 0
+            for m, e in fr]
+    total = sum(ints)
+    k = int(round(u * (1 << 24)))
+    assert k / (1 << 24) == u
+    acc = 0
+    for y, v in enumerate(ints):
+        acc += v
+        if (acc << 24) > k * total:
+            return y
+    return None
+
+
+@pytest.mark.slow
+def test_inverse_cdf_large_vocab_against_exact_arithmetic():
+    # residual rows at V = 128256 (the workloads' vocabulary): the oracle's
+    # float64 draw equals the exact one wherever it reports no near tie (the
+    # 1e-5 band is about one token's mass here, so about a third are skipped)
+    rng = np.random.default_rng(31)
+    V = 128256
+    checked = 0
+    for row in range(5):
+        zt = rng.normal(0, 2.0, V)
+        zq = zt + rng.normal(0, 0.8, V)
+        p, _ = transform_logits(zt, 1.0)
+        q, _ = transform_logits(zq, 1.0)
+        r, _ = residual(p, q)
+        for u in rng.integers(0, 1 << 24, size=8) / float(1 << 24):
+            y, near = inverse_cdf(r, float(u))
+            if near:
+                continue
+            assert y == _exact_inverse_cdf(r, float(u))
+            checked += 1
+    assert checked >= 15
