@@ -311,8 +311,10 @@ int spec_kv_commit(void* kv, int B, int n1, int n2, int64_t stride_b,
  * Integer records are exact; calib_conf_sum is summed in double in no fixed
  * order.  Calls on one record that overlap on the GPU still add correctly
  * (device atomics).
- * Errors: SPEC_ERR_ARG for a NULL count or out, or exactly one of parent /
- * path_nodes NULL; SPEC_ERR_SHAPE for B < 0, n outside [1,
+ * Errors: SPEC_ERR_ARG for a NULL count or out, exactly one of parent /
+ * path_nodes NULL, or (B > 0) an array not aligned to its element size (4
+ * bytes for the inputs, 8 for the records); SPEC_ERR_SHAPE for B < 0, n
+ * outside [1,
  * SPEC_MAX_TREE_NODES], or nbins outside [1, SPEC_STATS_MAX_BINS] when
  * confidence is given.  B == 0 does nothing.
  */
@@ -355,8 +357,9 @@ int spec_accept_stats(const int32_t* count, const int32_t* parent,
  * prefix_len is clamped to [0, S - N].
  * Errors: SPEC_ERR_SHAPE unless 1 <= N <= 64, Hq % Hkv == 0 and S >= N;
  * SPEC_ERR_UNSUPPORTED unless D == 128; SPEC_ERR_ARG for scale <= 0 or not
- * finite, a NULL pointer (B > 0), caches not 16-byte aligned or q / out
- * not 4-byte aligned.  B == 0 does nothing.
+ * finite, a NULL pointer (B > 0), caches not 16-byte aligned, q, out or
+ * prefix_len not 4-byte aligned, or mask_bits not 8-byte aligned.  B == 0
+ * does nothing.
  */
 int spec_tree_attention(const void* q, const void* k_cache,
                         const void* v_cache, const int32_t* prefix_len,

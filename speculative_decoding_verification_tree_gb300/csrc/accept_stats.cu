@@ -331,6 +331,16 @@ extern "C" int spec_accept_stats(const int32_t* count, const int32_t* parent,
   const bool calib = confidence != nullptr;
   if (calib && (nbins < 1 || nbins > SPEC_STATS_MAX_BINS)) return SPEC_ERR_SHAPE;
   if (B == 0) return SPEC_OK;
+  // element alignment of every array (a misaligned pointer is an argument
+  // error here, not a fault on the device)
+  const uintptr_t a4 = (uintptr_t)count | (uintptr_t)parent | (uintptr_t)path_nodes |
+                       (uintptr_t)confidence;
+  const uintptr_t a8 = (uintptr_t)out->len_hist | (uintptr_t)out->node_tested |
+                       (uintptr_t)out->node_accepted | (uintptr_t)out->depth_tested |
+                       (uintptr_t)out->depth_accepted | (uintptr_t)out->calib_tested |
+                       (uintptr_t)out->calib_accepted | (uintptr_t)out->calib_conf_sum |
+                       (uintptr_t)out->invalid;
+  if (a4 % 4 != 0 || a8 % 8 != 0) return SPEC_ERR_ARG;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SPEC_ERR_CUDA;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)

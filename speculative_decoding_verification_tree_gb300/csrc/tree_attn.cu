@@ -285,7 +285,8 @@ extern "C" int spec_tree_attention(const void* q, const void* k_cache, const voi
   if (B == 0) return SPEC_OK;
   if (!q || !k_cache || !v_cache || !prefix_len || !mask_bits || !out) return SPEC_ERR_ARG;
   if (((uintptr_t)k_cache | (uintptr_t)v_cache) % 16 != 0 ||
-      ((uintptr_t)q | (uintptr_t)out) % 4 != 0)
+      ((uintptr_t)q | (uintptr_t)out | (uintptr_t)prefix_len) % 4 != 0 ||
+      (uintptr_t)mask_bits % 8 != 0)
     return SPEC_ERR_ARG;
   const int R = N * (Hq / Hkv);
   const dim3 grid((unsigned)((R + kARows - 1) / kARows), (unsigned)Hkv, (unsigned)B);

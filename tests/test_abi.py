@@ -190,6 +190,13 @@ def test_accept_stats_argument_errors(lib):
     # without confidences the bin count is not used; B = 0 does nothing
     assert call(conf=None, nbins=0, B=0) == lib.SPEC_OK
     assert call(parent=None, path=None, B=0) == lib.SPEC_OK
+    # misaligned arrays are argument errors, caught before any launch
+    odd = ctypes.c_void_p(0x7f0000000002)
+    assert call(count=odd) == lib.SPEC_ERR_ARG
+    assert call(conf=odd) == lib.SPEC_ERR_ARG
+    rec.len_hist = 0x7f0000000004
+    assert call() == lib.SPEC_ERR_ARG
+    rec.len_hist = None
 
 
 def test_tree_attention_argument_errors(lib):
@@ -209,4 +216,7 @@ def test_tree_attention_argument_errors(lib):
     assert call(scale=float("inf")) == lib.SPEC_ERR_ARG
     assert call(q=None) == lib.SPEC_ERR_ARG
     assert call(k=ctypes.c_void_p(0x7f0000000008)) == lib.SPEC_ERR_ARG
+    assert f("spec_tree_attention", FAKE, FAKE, FAKE, FAKE,
+             ctypes.c_void_p(0x7f0000000004), 2, 8, 8, 2, 128, 64,
+             ctypes.c_float(0.1), FAKE, None) == lib.SPEC_ERR_ARG
     assert call(B=0, q=None, out=None) == lib.SPEC_OK
