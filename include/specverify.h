@@ -314,9 +314,8 @@ int spec_kv_commit(void* kv, int B, int n1, int n2, int64_t stride_b,
  * Errors: SPEC_ERR_ARG for a NULL count or out, exactly one of parent /
  * path_nodes NULL, or (B > 0) an array not aligned to its element size (4
  * bytes for the inputs, 8 for the records); SPEC_ERR_SHAPE for B < 0, n
- * outside [1,
- * SPEC_MAX_TREE_NODES], or nbins outside [1, SPEC_STATS_MAX_BINS] when
- * confidence is given.  B == 0 does nothing.
+ * outside [1, SPEC_MAX_TREE_NODES], or nbins outside [1,
+ * SPEC_STATS_MAX_BINS] when confidence is given.  B == 0 does nothing.
  */
 #define SPEC_STATS_MAX_BINS 1024
 typedef struct {
