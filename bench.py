@@ -60,19 +60,19 @@ def _args():
 # DRAM traffic per launch of the profiled kernel, from one ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum of a smaller batch, scaled
 # to the rows the kernel processes), keyed by workload, with a hash of the
-# sources the kernel is built from at capture time.  Reported as null once
-# they changed.
+# sources the kernel is built from at capture time (and of the header
+# definitions they use).  Reported as null once they changed.
 _STREAM_SRC = ("sample_stream.cuh", "sample_stream_bf16.cu",
                "sample_stream_f32.cu", "common.cuh", "kernels.h")
 TRAFFIC = {
     # unit_stream, tree_static at B=16 (clusters of 2): 760.44 MB read +
     # 3.38 MB written, 976 rows
     "tree_static": {"bytes_per_unit": 763.82e6 / 976, "src": _STREAM_SRC,
-                    "hash": "e294d57f90fb6e45"},
+                    "hash": "c751e29930420a52"},
     # unit_stream, eagle2 at B=32 (one CTA per row): 403.52 MB read + 3.28 MB
     # written, 782 rows with a draft row
     "eagle2": {"bytes_per_unit": 406.80e6 / 782, "src": _STREAM_SRC,
-               "hash": "e294d57f90fb6e45"},
+               "hash": "c751e29930420a52"},
     # accept_stats_warp at B=65536 rounds: 47.46 MB read + 9.7 KB written
     "accept_stats": {"bytes_per_unit": 47.47e6 / 65536,
                      "src": ("accept_stats.cu", "common.cuh", "kernels.h"),
@@ -81,18 +81,36 @@ TRAFFIC = {
 
 
 def _src_hash(files):
+    """Hash of a kernel's sources and of the parts of the public header they
+    use (the #define constants and typedef structs they name), so that
+    declarations and comments added for other entry points do not count as
+    a change of this kernel."""
     import hashlib
+    import re
     d = os.path.join(ROOT, "speculative_decoding_verification_tree_gb300",
                      "csrc")
     h = hashlib.sha256()
+    texts = []
     for f in files:
         try:
             with open(os.path.join(d, f), "rb") as fh:
-                h.update(f.encode() + b"\0" + fh.read())
+                data = fh.read()
+            h.update(f.encode() + b"\0" + data)
+            texts.append(data.decode("utf-8", "replace"))
         except OSError:
             h.update(f.encode() + b"\0missing")
-    with open(os.path.join(ROOT, "include", "specverify.h"), "rb") as fh:
-        h.update(fh.read())
+    with open(os.path.join(ROOT, "include", "specverify.h"),
+              encoding="utf-8") as fh:
+        hdr = re.sub(r"/\*.*?\*/", "", fh.read(), flags=re.S)
+    used = set(re.findall(r"\b(?:SPEC_[A-Z0-9_]+|spec_\w+_t)\b",
+                          "".join(texts)))
+    for m in re.finditer(r"#define\s+(\w+)[^\n]*", hdr):
+        if m.group(1) in used:
+            h.update(m.group(0).encode())
+    for m in re.finditer(r"typedef\s+struct\s*\{.*?\}\s*(\w+)\s*;", hdr,
+                         flags=re.S):
+        if m.group(1) in used:
+            h.update(m.group(0).encode())
     return h.hexdigest()[:16]
 
 
