@@ -10,10 +10,9 @@
 //
 // What it does instead: the scratch the verification kernels need (status
 // word, per-row outcomes and records, argmax and acceptance-mass partials)
-// lives in one
-// file-scope __device__
-// array of fixed size, which every GPU that loads this library holds until
-// the process exits.  Nothing is allocated per call.
+// lives in one file-scope __device__ array of fixed size, which every GPU
+// that loads this library holds until the process exits.  Nothing is
+// allocated per call.
 //
 // Rules for callers:
 //  * The first call on each device looks up the array's device address
