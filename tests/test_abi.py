@@ -220,3 +220,22 @@ def test_tree_attention_argument_errors(lib):
              ctypes.c_void_p(0x7f0000000004), 2, 8, 8, 2, 128, 64,
              ctypes.c_float(0.1), FAKE, None) == lib.SPEC_ERR_ARG
     assert call(B=0, q=None, out=None) == lib.SPEC_OK
+
+
+@pytest.mark.parametrize("lang,std", [("c", "c99"), ("c++", "c++11")])
+def test_header_compiles_for_plain_c_and_cpp_callers(tmp_path, lang, std):
+    # the boundary is a C ABI: the header must stand alone in C and C++
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc" if lang == "c" else "g++")
+    if cc is None:
+        pytest.skip("no host compiler")
+    src = tmp_path / ("use.c" if lang == "c" else "use.cpp")
+    src.write_text('#include "specverify.h"\n'
+                   "int main(void) { spec_params_t p; spec_accept_stats_t r;\n"
+                   "  (void)p; (void)r; return SPEC_OK; }\n")
+    r = subprocess.run([cc, f"-std={std}", "-Wall", "-Wextra", "-pedantic",
+                        "-Werror", "-I", os.path.join(ROOT, "include"),
+                        "-fsyntax-only", str(src)], capture_output=True,
+                       text=True)
+    assert r.returncode == 0, r.stderr
