@@ -354,7 +354,8 @@ int spec_accept_stats(const int32_t* count, const int32_t* parent,
  *   [B, Hkv, S, D], prefix_len [B] int32, mask_bits [B, N] uint64.
  * Softmax and accumulation in float32; the output is rounded to bf16.
  * prefix_len is clamped to [0, S - N].
- * Errors: SPEC_ERR_SHAPE unless 1 <= N <= 64, Hq % Hkv == 0 and S >= N;
+ * Errors: SPEC_ERR_SHAPE unless 1 <= N <= 64, Hq % Hkv == 0, S >= N and
+ * B, Hkv <= 65535;
  * SPEC_ERR_UNSUPPORTED unless D == 128; SPEC_ERR_ARG for scale <= 0 or not
  * finite, a NULL pointer (B > 0), caches not 16-byte aligned, q, out or
  * prefix_len not 4-byte aligned, or mask_bits not 8-byte aligned.  B == 0

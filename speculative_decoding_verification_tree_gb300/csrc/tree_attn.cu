@@ -278,7 +278,9 @@ extern "C" int spec_tree_attention(const void* q, const void* k_cache, const voi
                                    const int32_t* prefix_len, const uint64_t* mask_bits, int B,
                                    int N, int Hq, int Hkv, int D, int S, float scale, void* out,
                                    void* stream) {
-  if (B < 0 || N < 1 || N > 64 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || S < N)
+  // B and Hkv index grid dimensions z and y (at most 65535 each)
+  if (B < 0 || B > 65535 || N < 1 || N > 64 || Hq < 1 || Hkv < 1 || Hkv > 65535 ||
+      Hq % Hkv != 0 || S < N)
     return SPEC_ERR_SHAPE;
   if (D != kAD) return SPEC_ERR_UNSUPPORTED;
   if (!(scale > 0.f) || !(scale < 3.4e38f)) return SPEC_ERR_ARG;

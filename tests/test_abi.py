@@ -211,6 +211,7 @@ def test_tree_attention_argument_errors(lib):
     assert call(Hq=6, Hkv=4) == lib.SPEC_ERR_SHAPE
     assert call(S=4) == lib.SPEC_ERR_SHAPE
     assert call(B=-1) == lib.SPEC_ERR_SHAPE
+    assert call(B=65536) == lib.SPEC_ERR_SHAPE
     assert call(D=64) == lib.SPEC_ERR_UNSUPPORTED
     assert call(scale=0.0) == lib.SPEC_ERR_ARG
     assert call(scale=float("inf")) == lib.SPEC_ERR_ARG
