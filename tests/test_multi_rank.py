@@ -68,3 +68,69 @@ def test_reference_arm_only_rank0_reports(capsys):
         steps, warmup, workload = 1, 0, "chain_sample"
     assert bench.reference_arm(A(), 2, 1) is None
     assert capsys.readouterr().out == ""
+
+
+def _records_worker(rank, world, port, out_dir):
+    """Each rank records its own share of the rounds (oracle side), then
+    the records are summed across ranks with an all-reduce."""
+    sys.path.insert(0, ROOT)
+    from oracle import stats
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        count, parent, path, conf, n, nb = _rounds_for_records()
+        mine = slice(rank, None, world)           # rounds split over ranks
+        st = stats.accept_stats(count[mine], parent[mine], path[mine],
+                                conf[mine], n, nb)
+        out = {}
+        for f in ("len_hist", "node_tested", "node_accepted", "depth_tested",
+                  "depth_accepted", "calib_tested", "calib_accepted"):
+            t = torch.from_numpy(getattr(st, f).copy())
+            dist.all_reduce(t)
+            out[f] = t.tolist()
+        t = torch.tensor([st.invalid], dtype=torch.int64)
+        dist.all_reduce(t)
+        out["invalid"] = int(t.item())
+        with open(os.path.join(out_dir, f"rec{rank}.json"), "w") as fh:
+            json.dump(out, fh)
+    finally:
+        dist.destroy_process_group()
+
+
+def _rounds_for_records():
+    import numpy as np
+    rng = np.random.default_rng(5)
+    B, n, nb = 41, 12, 6
+    parent = np.array([[-1 if j == 0 or rng.random() < 0.3 else
+                        int(rng.integers(0, j)) for j in range(n)]
+                       for _ in range(B)], dtype=np.int32)
+    count = np.zeros(B, dtype=np.int32)
+    path = np.full((B, n), -1, dtype=np.int32)
+    for b in range(B):
+        j, chain = int(rng.integers(0, n)), []
+        while j >= 0:
+            chain.append(j)
+            j = int(parent[b, j])
+        count[b] = len(chain)
+        path[b, :len(chain)] = chain[::-1]
+    count[3] = n + 2                                # one invalid round
+    conf = rng.random((B, n)).astype(np.float32)
+    return count, parent, path, conf, n, nb
+
+
+def test_acceptance_records_of_replicas_add_up_gloo(tmp_path):
+    # replicas verify disjoint rounds; their acceptance records combine by a
+    # sum (all-reduce) into exactly the records of all rounds together
+    sys.path.insert(0, ROOT)
+    from oracle import stats
+    world = 2
+    mp.spawn(_records_worker, args=(world, _free_port(), str(tmp_path)),
+             nprocs=world, join=True)
+    count, parent, path, conf, n, nb = _rounds_for_records()
+    whole = stats.accept_stats(count, parent, path, conf, n, nb)
+    for r in range(world):
+        got = json.load(open(tmp_path / f"rec{r}.json"))
+        for f, v in got.items():
+            want = whole.invalid if f == "invalid" else getattr(whole, f).tolist()
+            assert v == want, f
