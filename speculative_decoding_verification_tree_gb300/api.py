@@ -210,6 +210,13 @@ def spec_accept_stats(count, parent=None, path_nodes=None, confidence=None,
         _want(confidence, torch.float32, (B, n), "confidence")
     if out is None:
         out = accept_stats_records(n, nbins, count.device)
+    sizes = {"len_hist": n + 1, "node_tested": n, "node_accepted": n,
+             "depth_tested": n, "depth_accepted": n, "calib_tested": nbins,
+             "calib_accepted": nbins, "calib_conf_sum": nbins, "invalid": 1}
+    for f, k in sizes.items():  # the kernel writes int64 / float64 records
+        if out.get(f) is not None:
+            _want(out[f], torch.float64 if f == "calib_conf_sum"
+                  else torch.int64, (k,), f)
     rec = _lib.SpecAcceptStats(*[
         None if out.get(f) is None else _ptr(out[f]).value
         for f in _lib.STATS_FIELDS])
@@ -233,6 +240,7 @@ def spec_tree_attention(q, k_cache, v_cache, prefix_len, mask_bits, *,
     _want(mask_bits, torch.int64, (B, N), "mask_bits")
     if out is None:
         out = torch.empty_like(q)
+    _want(out, torch.bfloat16, (B, N, Hq, D), "out")
     if scale is None:
         scale = D ** -0.5
     _lib.call("spec_tree_attention", _ptr(q), _ptr(k_cache), _ptr(v_cache),

@@ -3,7 +3,6 @@ wrapper in api.py passes exactly the arguments its C signature declares, in
 a form ctypes accepts, and rejects malformed tensors before any call."""
 
 import ctypes
-import types
 
 import pytest
 import torch
@@ -105,4 +104,17 @@ def test_wrappers_reject_malformed_tensors(captured):
         api.spec_tree_attention(q.float(), kv, kv,
                                 torch.zeros(1, dtype=torch.int32),
                                 torch.zeros(1, 2, dtype=torch.int64))
+    with pytest.raises(ValueError):  # 32-bit records would be overrun
+        api.spec_accept_stats(torch.zeros(3, dtype=torch.int32), n=4,
+                              out={"len_hist": torch.zeros(5,
+                                                           dtype=torch.int32)})
+    with pytest.raises(ValueError):  # records sized for another n
+        api.spec_accept_stats(torch.zeros(3, dtype=torch.int32), n=4,
+                              out={"node_tested": torch.zeros(
+                                  5, dtype=torch.int64)})
+    with pytest.raises(ValueError):  # output of the wrong shape
+        api.spec_tree_attention(q, kv, kv, torch.zeros(1, dtype=torch.int32),
+                                torch.zeros(1, 2, dtype=torch.int64),
+                                out=torch.zeros(1, 2, 2, 64,
+                                                dtype=torch.bfloat16))
     assert captured == []
