@@ -85,6 +85,9 @@ def spec_verify_chain(target, draft, draft_tokens, *, temperature=1.0,
         out = (torch.empty(B, dtype=torch.int32, device=dev),
                torch.empty(B, K + 1, dtype=torch.int32, device=dev),
                torch.empty(B, K, dtype=torch.float32, device=dev))
+    _want(out[0], torch.int32, (B,), "accepted")
+    _want(out[1], torch.int32, (B, K + 1), "tokens")
+    _want(out[2], torch.float32, (B, K), "accept_mass")
     if ws is None:
         ws = workspace(_lib.SPEC_OP_CHAIN, B, K, V, dev)
     prm = params(temperature, top_k, top_p, draft_kind, seed, offset)
@@ -113,6 +116,10 @@ def spec_verify_tree(target, draft, q_row, node_tokens, parent, *,
                torch.empty(B, N, dtype=torch.int32, device=dev),
                torch.empty(B, N + 1, dtype=torch.int32, device=dev),
                torch.empty(B, N + 1, dtype=torch.float32, device=dev))
+    _want(out[0], torch.int32, (B,), "path_len")
+    _want(out[1], torch.int32, (B, N), "path_nodes")
+    _want(out[2], torch.int32, (B, N + 1), "tokens")
+    _want(out[3], torch.float32, (B, N + 1), "accept_mass")
     if ws is None:
         ws = workspace(_lib.SPEC_OP_TREE, B, N, V, dev)
     prm = params(temperature, top_k, top_p, draft_kind, seed, offset,
@@ -154,6 +161,12 @@ def spec_eagle2_expand_rerank(draft_logits, *, temperature, depth=6, topk=10,
                if mask else None)
     if ws is None:
         ws = workspace(_lib.SPEC_OP_EAGLE2, B, R, V, dev)
+    _want(out[0], torch.int32, (B, total), "node_tokens")
+    _want(out[1], torch.int32, (B, total), "parent")
+    _want(out[2], torch.int32, (B, total + 1), "q_row")
+    _want(out[3], torch.float32, (B, total), "value")
+    if out[4] is not None:
+        _want(out[4], torch.uint8, (B, total, total), "mask")
     if draft_lse is not None and tuple(draft_lse.shape) != (B, R):
         raise ValueError("draft_lse must have shape [B, R]")
     prm = params(temperature, draft_lse=draft_lse)
@@ -174,6 +187,7 @@ def spec_kv_commit(kv, prefix_len, path_len, path_nodes=None, *, layout,
     B = prefix_len.numel()
     if new_len is None:
         new_len = torch.empty(B, dtype=torch.int32, device=prefix_len.device)
+    _want(new_len, torch.int32, (B,), "new_len")
     n1, n2, sb, s1, s2, sp = layout
     _lib.call("spec_kv_commit", _ptr(kv), B, n1, n2, sb, s1, s2, sp,
               row_bytes, _ptr(prefix_len), _ptr(path_nodes), _ptr(path_len),
