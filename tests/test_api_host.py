@@ -118,3 +118,31 @@ def test_wrappers_reject_malformed_tensors(captured):
                                 out=torch.zeros(1, 2, 2, 64,
                                                 dtype=torch.bfloat16))
     assert captured == []
+
+
+def test_verification_wrappers_reject_wrong_outputs(captured):
+    B, K, V = 2, 3, 64
+    t, d = torch.zeros(B, K + 1, V), torch.zeros(B, K, V)
+    tok = torch.zeros(B, K, dtype=torch.int32)
+    bad = (torch.empty(B, dtype=torch.int64),          # accepted as int64
+           torch.empty(B, K + 1, dtype=torch.int32),
+           torch.empty(B, K))
+    with pytest.raises(ValueError):
+        api.spec_verify_chain(t, d, tok, out=bad)
+    N = 5
+    short = (torch.empty(B, dtype=torch.int32),
+             torch.empty(B, N, dtype=torch.int32),
+             torch.empty(B, N, dtype=torch.int32),      # one token short
+             torch.empty(B, N + 1))
+    with pytest.raises(ValueError):
+        api.spec_verify_tree(torch.zeros(B, N + 1, V), torch.zeros(B, N + 1, V),
+                             torch.zeros(B, N + 1, dtype=torch.int32),
+                             torch.zeros(B, N, dtype=torch.int32),
+                             torch.zeros(B, N, dtype=torch.int32), out=short)
+    with pytest.raises(ValueError):
+        api.spec_kv_commit(torch.zeros(8, dtype=torch.uint8),
+                           torch.zeros(B, dtype=torch.int32),
+                           torch.zeros(B, dtype=torch.int32), None,
+                           layout=(1, 1, 0, 0, 0, 16), row_bytes=16, N=4,
+                           new_len=torch.zeros(B, dtype=torch.int64))
+    assert captured == []
