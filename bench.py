@@ -54,7 +54,21 @@ def _args():
     p.add_argument("--no-extend", action="store_true",
                    help="do not keep the load running for the clock sampler "
                         "after a short timed region (profiler runs)")
+    p.add_argument("--no-configs", action="store_true",
+                   help="time the chosen workload only (by default the "
+                        "tree_static line also times the other "
+                        "verification workloads under its `configs` key)")
     return p.parse_args()
+
+
+# Verification workloads timed beside the headline one (each is one of the
+# pages' configurations; see synth.workload).
+OTHER_CONFIGS = ("greedy", "eagle2", "chain_topk", "chain_sample")
+L2_BYTES = 129 * 2**20  # GB300 L2 (about 129 MB)
+
+
+def metric_of(w):
+    return f"verified draft rows/s at V={w.V}"
 
 
 # DRAM traffic per launch of the profiled kernel, from one ncu capture
@@ -68,11 +82,11 @@ TRAFFIC = {
     # unit_stream, tree_static at B=16 (clusters of 2): 760.44 MB read +
     # 3.38 MB written, 976 rows
     "tree_static": {"bytes_per_unit": 763.82e6 / 976, "src": _STREAM_SRC,
-                    "hash": "c751e29930420a52"},
+                    "hash": "7ea3859da293773b"},
     # unit_stream, eagle2 at B=32 (one CTA per row): 403.52 MB read + 3.28 MB
     # written, 782 rows with a draft row
     "eagle2": {"bytes_per_unit": 406.80e6 / 782, "src": _STREAM_SRC,
-               "hash": "c751e29930420a52"},
+               "hash": "7ea3859da293773b"},
     # accept_stats_warp at B=65536 rounds: 47.46 MB read + 9.7 KB written
     "accept_stats": {"bytes_per_unit": 47.47e6 / 65536,
                      "src": ("accept_stats.cu", "common.cuh", "kernels.h"),
@@ -107,9 +121,10 @@ def _src_hash(files):
     for m in re.finditer(r"#define\s+(\w+)[^\n]*", hdr):
         if m.group(1) in used:
             h.update(m.group(0).encode())
-    for m in re.finditer(r"typedef\s+struct\s*\{.*?\}\s*(\w+)\s*;", hdr,
-                         flags=re.S):
-        if m.group(1) in used:
+    # typedef struct {...} name; and typedef struct tag {...} name;
+    for m in re.finditer(r"typedef\s+struct\s*(\w+)?\s*\{.*?\}\s*(\w+)\s*;",
+                         hdr, flags=re.S):
+        if m.group(2) in used or (m.group(1) and m.group(1) in used):
             h.update(m.group(0).encode())
     return h.hexdigest()[:16]
 
@@ -242,6 +257,11 @@ class Work:
         else:
             raise SystemExit(f"workload {name} is not wired into the bench")
 
+    def input_bytes(self):
+        """Bytes of the step's device inputs (decides the L2 flush)."""
+        return sum(x.numel() * x.element_size() for x in self.inputs
+                   if x is not None)
+
     def _expand(self, draft):
         w = self.w
         self.api.spec_eagle2_expand_rerank(
@@ -370,26 +390,27 @@ def oracle_step(w, host, seqs):
         d = host["draft"][seqs].float().numpy().astype(np.float64)
         tr = expand_rerank(d, temperature=w.temperature, depth=w.depth,
                            topk=w.topk, width=w.width, total=w.total)
-        verify_tree(t, d, tr.q_row, tr.node_tokens, tr.parent,
-                    temperature=w.temperature, seed=w.decision_seed,
-                    batch_ids=seqs)
-        return len(seqs) * (w.total + 1)
+        ref = verify_tree(t, d, tr.q_row, tr.node_tokens, tr.parent,
+                          temperature=w.temperature, seed=w.decision_seed,
+                          batch_ids=seqs)
+        return len(seqs) * (w.total + 1), (tr, ref)
     if w.name in ("greedy", "chain_topk", "chain_sample"):
         d = None if host["draft"] is None else \
             host["draft"][seqs].float().numpy().astype(np.float64)
-        verify_chain(t, d, host["toks"][seqs].numpy(),
-                     temperature=w.temperature, top_k=w.top_k, top_p=w.top_p,
-                     draft_kind=w.draft_kind, seed=w.decision_seed,
-                     batch_ids=seqs)
-        return len(seqs) * w.K
+        ref = verify_chain(t, d, host["toks"][seqs].numpy(),
+                           temperature=w.temperature, top_k=w.top_k,
+                           top_p=w.top_p, draft_kind=w.draft_kind,
+                           seed=w.decision_seed, batch_ids=seqs)
+        return len(seqs) * w.K, ref
     d = host["draft"][seqs].float().numpy().astype(np.float64)
     par = host["parent"][seqs].numpy()
     tree_mask(par)
-    verify_tree(t, d, host["q_row"][seqs].numpy(), host["toks"][seqs].numpy(),
-                par, temperature=w.temperature, top_k=w.top_k, top_p=w.top_p,
-                draft_kind=w.draft_kind, seed=w.decision_seed,
-                batch_ids=seqs)
-    return len(seqs) * (par.shape[1] + 1)
+    ref = verify_tree(t, d, host["q_row"][seqs].numpy(),
+                      host["toks"][seqs].numpy(), par,
+                      temperature=w.temperature, top_k=w.top_k,
+                      top_p=w.top_p, draft_kind=w.draft_kind,
+                      seed=w.decision_seed, batch_ids=seqs)
+    return len(seqs) * (par.shape[1] + 1), ref
 
 
 def host_inputs(name, nseq=8):
@@ -417,18 +438,66 @@ def host_inputs(name, nseq=8):
     return w, {"target": t, "draft": d, "q_row": q, "toks": k, "parent": p}
 
 
-def time_oracle(name, seconds, host=None):
+def time_oracle(name, seconds, host=None, results=None):
     """Oracle rows/s on a bounded sample: sequences one by one until
-    `seconds` of CPU work."""
+    `seconds` of CPU work.  `results` (a list) receives (b, oracle result)
+    per sequence."""
     w, host = host_inputs(name) if host is None else host
     rows, t0, b = 0, time.perf_counter(), 0
     while True:
-        rows += oracle_step(w, host, [b % w.B])
+        r, ref = oracle_step(w, host, [b % w.B])
+        rows += r
+        if results is not None:
+            results.append((b % w.B, ref))
         b += 1
         el = time.perf_counter() - t0
         if el >= seconds or b >= w.B:
             break
     return rows / el, b, el
+
+
+def parity_counts(work, results):
+    """Compare the GPU outputs of the timed step with the oracle results of
+    the sampled sequences: compared element by element (exact, or a final
+    draw inside the 1e-5 CDF band), excluded as near ties (an accept test
+    within 1e-5 of its threshold), and mismatches (must be 0)."""
+    import numpy as np
+    out = [o.cpu().numpy() for o in work.out]
+    c = {"sequences": 0, "compared": 0, "exact": 0, "near_tie_excluded": 0,
+         "cdf_band": 0, "mismatch": 0}
+    for b, ref in results:
+        c["sequences"] += 1
+        if work.kind == "eagle2":
+            tr, ref = ref
+            tree = [t.cpu().numpy() for t in work.tree]
+            if not (np.array_equal(tree[0][b], tr.node_tokens[0]) and
+                    np.array_equal(tree[1][b], tr.parent[0])):
+                c["mismatch"] += 1  # reranked tree differs
+                continue
+        if ref.near_tie[0]:
+            c["near_tie_excluded"] += 1
+            continue
+        c["compared"] += 1
+        if work.kind == "chain":
+            n = int(ref.accepted[0])
+            same = int(out[0][b]) == n
+            tok = out[1][b]
+        else:
+            n = int(ref.path_len[0])
+            same = (int(out[0][b]) == n and
+                    np.array_equal(out[1][b], ref.path_nodes[0]))
+            tok = out[2][b]
+        same = (same and np.array_equal(tok[:n], ref.tokens[0][:n]) and
+                np.array_equal(tok[n + 1:], ref.tokens[0][n + 1:]))
+        if not same:
+            c["mismatch"] += 1
+        elif tok[n] == ref.tokens[0][n]:
+            c["exact"] += 1
+        elif ref.sample_near is not None and ref.sample_near[0]:
+            c["cdf_band"] += 1
+        else:
+            c["mismatch"] += 1
+    return c
 
 
 def cpu_sample_text(name, nseq, el):
@@ -452,11 +521,127 @@ def job_rate(units_per_rank, steps, world, ms):
     return units_per_rank * steps * world / (ms / 1e3)
 
 
+def spawn_ranks(args):
+    """`--gpus N` outside torchrun: launch N local ranks (one per GPU)
+    through torch.distributed.run on 127.0.0.1 and return their exit code;
+    rank 0 prints the line."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={args.gpus}", "--master-addr", "127.0.0.1",
+           "--master-port", str(port), os.path.abspath(__file__),
+           *sys.argv[1:]]
+    return subprocess.call(cmd)
+
+
+def time_steps(torch, work, steps, flush=None):
+    """Enqueue `steps` steps and return the summed device time (ms) of the
+    steps alone.  With `flush` (a buffer larger than L2) every step is
+    preceded by a write of the whole buffer, outside the timed events, so
+    each step starts with the inputs out of L2."""
+    if flush is None:
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev0.record()
+        for _ in range(steps):
+            work.step()
+        ev1.record()
+        torch.cuda.synchronize()
+        return ev0.elapsed_time(ev1)
+    evs = []
+    for _ in range(steps):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        work.step()
+        e1.record()
+        evs.append((e0, e1))
+    torch.cuda.synchronize()
+    return sum(e0.elapsed_time(e1) for e0, e1 in evs)
+
+
+def kernel_time(h, kind):
+    """(average launch ms, launches, rc) of one profiled kernel kind."""
+    import ctypes
+    tot, nl = ctypes.c_double(0), ctypes.c_int(0)
+    rc = h.spec_profile_read(kind, ctypes.byref(tot), ctypes.byref(nl))
+    return (tot.value / nl.value if nl.value else None), nl.value, rc
+
+
+def l2_note(work):
+    return ("inputs exceed L2 (no flush)" if work.input_bytes() > L2_BYTES
+            else "L2 flushed before every timed step (2 x L2 written "
+                 "outside the timed events)")
+
+
+def run_config(torch, h, lib, name, dev, steps, peak, peak_kind):
+    """Time one more verification workload; returns its summary (step time,
+    dominant kernel and its fraction of the HBM roofline)."""
+    work = Work(name, dev)
+    flush = None
+    if work.input_bytes() <= L2_BYTES:
+        flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    for _ in range(5):
+        work.step()
+    torch.cuda.synchronize()
+    h.spec_profile_enable(1)
+    ms = time_steps(torch, work, steps, flush)
+    kern_ms, nl, rc = kernel_time(h, work.prof_kind)
+    other = {}
+    if work.kind == "eagle2":
+        ems, n2, _ = kernel_time(h, lib.SPEC_PROF_EXPAND)
+        if n2:
+            other["eagle2_rows"] = {
+                "avg_launch_ms": round(ems, 5),
+                "bytes_per_launch": work.expand_bytes,
+                "frac": round(work.expand_bytes / (ems / 1e3) / 1e9 / peak,
+                              4)}
+    h.spec_profile_enable(0)
+    w = work.w
+    d = {"metric": metric_of(w), "unit": UNIT,
+         "value": round(work.rows * steps / (ms / 1e3), 1),
+         "ms_per_step": round(ms / steps, 5), "steps": steps,
+         "B": w.B, "drafts_per_seq": w.K, "V": w.V,
+         "temperature": w.temperature, "dtype": dtype_name(w),
+         "l2": l2_note(work), "kernel": work.kernel_name,
+         "avg_launch_ms": None if kern_ms is None else round(kern_ms, 5),
+         "bytes_per_launch": work.kernel_bytes, "profile_rc": rc,
+         "gpu_launches": work.launches_per_step * steps}
+    if kern_ms:
+        gbs = work.kernel_bytes / (kern_ms / 1e3) / 1e9
+        d.update({"achieved_gbs": round(gbs, 1), "peak_gbs": peak,
+                  "peak_source": peak_kind, "frac": round(gbs / peak, 4)})
+    if work.kind == "eagle2":
+        step_bytes = work.kernel_bytes + work.expand_bytes
+        d["step_frac"] = round(step_bytes / (ms / steps / 1e3) / 1e9 / peak,
+                               4)
+        d["other_kernels"] = other
+    d["tokens_per_s"] = round(work.emitted_tokens() * steps / (ms / 1e3), 1)
+    del work, flush
+    torch.cuda.empty_cache()
+    return d
+
+
+def workload_config(name, w, world):
+    return {"workload": name, "B": w.B, "drafts_per_seq": w.K, "V": w.V,
+            "temperature": w.temperature, "top_k": w.top_k,
+            "top_p": w.top_p,
+            "parallelism": f"replicas x{world} (sequences split)"}
+
+
 def main():
     args = _args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        return spawn_ranks(args)
+    if args.gpus != world:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world}: launch "
+                         "one rank per GPU (or leave WORLD_SIZE unset)")
 
     if args.workload == "kv_commit":
         return kv_main(args, world, rank, local)
@@ -481,6 +666,9 @@ def main():
     work = Work(args.workload, dev, args.B)
     steps = args.steps or (3000 if args.workload != "eagle2" else 800)
     warm = max(3, args.warmup)
+    flush = None
+    if work.input_bytes() <= L2_BYTES:
+        flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
     for _ in range(warm):
         work.step()
     torch.cuda.synchronize()
@@ -493,28 +681,15 @@ def main():
         dist.barrier()
     torch.cuda.synchronize()
     h.spec_profile_enable(1)
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    ev0.record()
-    for _ in range(steps):
-        work.step()
-    ev1.record()
-    torch.cuda.synchronize()
+    ms = time_steps(torch, work, steps, flush)
     if dist:
         dist.barrier()
-    ms = ev0.elapsed_time(ev1)
-    import ctypes
-    tot = ctypes.c_double(0)
-    nl = ctypes.c_int(0)
-    rc = h.spec_profile_read(work.prof_kind, ctypes.byref(tot),
-                             ctypes.byref(nl))
+    kern_ms, nl, rc = kernel_time(h, work.prof_kind)
+    peak, peak_kind = _peaks()
     other = {}
     if work.kind == "eagle2":
-        t2, n2 = ctypes.c_double(0), ctypes.c_int(0)
-        h.spec_profile_read(_lib.SPEC_PROF_EXPAND, ctypes.byref(t2),
-                            ctypes.byref(n2))
-        if n2.value:
-            ems_k = t2.value / n2.value
+        ems_k, n2, _ = kernel_time(h, _lib.SPEC_PROF_EXPAND)
+        if n2:
             other["eagle2_rows"] = {
                 "avg_launch_ms": round(ems_k, 5),
                 "bytes_per_launch": work.expand_bytes,
@@ -535,8 +710,6 @@ def main():
     value = job_rate(work.rows, steps, world, ms)
     tokens_per_step = work.emitted_tokens()
 
-    peak, peak_kind = _peaks()
-    kern_ms = (tot.value / nl.value) if nl.value else None
     roof = None
     if kern_ms:
         achieved = work.kernel_bytes / (kern_ms / 1e3) / 1e9
@@ -586,34 +759,63 @@ def main():
                "d2h_bytes_per_step": d2h, "steps": n_e2e,
                "ms_per_step": round(ems / n_e2e, 4)}
 
-    cpu = None
+    cpu = parity = None
     if rank == 0 and world == 1 and not args.no_cpu:
+        results = []
         rps, nseq, el = time_oracle(args.workload, args.cpu_seconds,
-                                    work.host_copy())
+                                    work.host_copy(), results)
         cpu = {"value": round(rps, 2), "unit": UNIT, "cores": 1,
                "kind": "oracle",
                "sample": cpu_sample_text(args.workload, nseq, el)}
+        # the same sequences' GPU outputs against the oracle's
+        parity = parity_counts(work, results)
+        parity["rule"] = ("decisions exact except an accept test within "
+                          "1e-5 of its threshold (excluded, counted); a "
+                          "final draw may differ only inside the 1e-5 CDF "
+                          "band (counted)")
 
-    w = work.w
+    rows_per_step, launches, l2 = work.rows, work.launches_per_step, \
+        l2_note(work)
+    configs = None
+    if (args.workload == DEFAULT_WORKLOAD and args.B is None and
+            not args.no_configs):
+        w0 = work.w
+        del work, flush
+        torch.cuda.empty_cache()
+        configs = {}
+        cclk = Clocks(local)
+        cclk.start()
+        for name in OTHER_CONFIGS:
+            n = {"greedy": 1000, "eagle2": 300, "chain_topk": 500,
+                 "chain_sample": 500}[name]
+            if args.steps is not None:  # short runs (profiler captures)
+                n = max(10, min(n, args.steps))
+            configs[name] = run_config(torch, h, _lib, name, dev, n, peak,
+                                       peak_kind)
+        cclk.stop()
+        configs["clocks"] = cclk.summary()
+        w = w0
+    else:
+        w = work.w
     if rank == 0:
+        cfg = workload_config(args.workload, w, world)
+        cfg["rows_per_step"] = rows_per_step
+        cfg["l2"] = l2
         line = {
-            "metric": METRIC, "value": round(value, 1), "unit": UNIT,
+            "metric": metric_of(w), "value": round(value, 1), "unit": UNIT,
             "n_gpus": world, "steps": steps, "warmup": warm,
             "ms_per_step": round(ms_step, 5), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": dtype_name(w),
             "data": "synthetic (seeded; shapes and distributions of the "
                     "pages' workloads)",
-            "config": {"workload": args.workload, "B": w.B,
-                       "drafts_per_seq": w.K, "V": w.V,
-                       "temperature": w.temperature,
-                       "rows_per_step": work.rows,
-                       "parallelism": f"replicas x{world} (sequences split)",
-                       "l2": "inputs exceed L2 (no flush)"},
+            "config": cfg,
             "tokens_per_s": round(tokens_per_step * steps * world
                                   / (ms / 1e3), 1),
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "parity": parity,
             "clocks": clocks.summary(),
-            "gpu_launches": work.launches_per_step * steps,
+            "gpu_launches": launches * steps,
+            "configs": configs,
         }
         print(json.dumps(line), flush=True)
     if dist:
@@ -1314,7 +1516,7 @@ def reference_arm(args, world, rank):
         return
     steps = args.steps or 3
     w, host = host_inputs(args.workload)
-    per_step = max(1.0, min(20.0, 150.0 / (steps + args.warmup)))
+    per_step = max(0.2, min(args.cpu_seconds, 150.0 / (steps + args.warmup)))
     for _ in range(args.warmup):
         time_oracle(args.workload, per_step, (w, host))
     rows, el = 0, 0.0
@@ -1325,12 +1527,15 @@ def reference_arm(args, world, rank):
         el += e
         nseq += n
     value = rows / el
-    line = {"impl": "reference", "metric": METRIC, "value": round(value, 2),
+    import synth
+    wf = synth.workload(args.workload)  # the workload our arm times
+    line = {"impl": "reference", "metric": metric_of(wf),
+            "value": round(value, 2),
             "unit": UNIT, "n_gpus": world, "steps": steps,
             "warmup": args.warmup, "ms_per_step": round(el / steps * 1e3, 2),
             "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload, "B": w.B, "V": w.V},
+            "config": workload_config(args.workload, wf, world),
             "cpu_baseline": {"kind": "oracle", "cores": 1,
                              "sample": cpu_sample_text(args.workload, nseq,
                                                        el),

@@ -383,8 +383,12 @@ const char* spec_error_string(int code);
  * Chain verification without a workspace, for callers that cannot allocate
  * device memory (an engine plugin handed only its input and output buffers,
  * or a decode loop where cudaMalloc is not allowed).  No counterpart on the
- * pages: it computes exactly what spec_verify_chain computes (same arguments
- * minus the workspace) and differs only in where its scratch lives.
+ * pages: for the calls it serves it computes what spec_verify_chain computes
+ * (same arguments minus the workspace) and differs only in where its scratch
+ * lives.  Not served: sampling with top-k / top-p truncation (temperature
+ * > 0 with top_k > 0 or top_p < 1) and rows the streaming kernels cannot
+ * take, both SPEC_ERR_UNSUPPORTED; given draft normalisers (draft_lse),
+ * SPEC_ERR_ARG.  Its status bits are read with spec_get_status_noalloc.
  *
  * The scratch is one fixed array inside the library (about 1.7 MiB) that
  * every GPU which loads the library holds until the process exits.  The first
@@ -404,6 +408,14 @@ int spec_verify_chain_noalloc(const void* target_logits, const void* draft,
                               const spec_params_t* prm, int32_t* accepted,
                               int32_t* out_tokens, float* accept_mass,
                               void* stream);
+
+/*
+ * Status bits (SPEC_STATUS_*) of the last spec_verify_chain_noalloc call on
+ * the current device: copies the status word out of the library's fixed
+ * array into the host word *status and waits for `stream`.  Like the call
+ * itself it allocates nothing; SPEC_ERR_ARG if status is NULL.
+ */
+int spec_get_status_noalloc(uint32_t* status, void* stream);
 
 /*
  * Kernel timing for benchmarks.  spec_profile_enable(1) clears the record and

@@ -97,6 +97,7 @@ _SIGNATURES = {
     "spec_verify_chain_noalloc": (_I, [_P, _P, _P, _I, _I, _I, _I, _I,
                                        ctypes.POINTER(SpecParams), _P, _P, _P,
                                        _P]),
+    "spec_get_status_noalloc": (_I, [ctypes.POINTER(ctypes.c_uint32), _P]),
     "spec_kv_commit": (_I, [_P, _I, _I, _I, ctypes.c_int64, ctypes.c_int64,
                             ctypes.c_int64, ctypes.c_int64, _I, _P, _P, _P, _I,
                             _P, _P]),

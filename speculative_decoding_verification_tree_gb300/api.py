@@ -8,6 +8,7 @@ libspecverify.so.
 
 from __future__ import annotations
 
+import contextlib
 import ctypes
 
 import torch
@@ -45,8 +46,32 @@ def _want(t, dtype, shape, name):
 
 
 def _stream(stream):
+    """The caller's stream, else torch's current stream of the current
+    device (the wrappers make the tensors' device current first)."""
     s = stream if stream is not None else torch.cuda.current_stream()
     return ctypes.c_void_p(s.cuda_stream)
+
+
+def _device(primary, *others, stream=None):
+    """The device of `primary`.  Every other tensor given (inputs, outputs,
+    workspace) and the stream must be on it: the library launches on the
+    current device and would otherwise touch another GPU's memory."""
+    dev = primary.device
+    for t in others:
+        if t is not None and t.device != dev:
+            raise ValueError(f"all tensors must be on {dev}; got one on "
+                             f"{t.device}")
+    if stream is not None and dev.type == "cuda" and stream.device != dev:
+        raise ValueError(f"stream is on {stream.device}, tensors on {dev}")
+    return dev
+
+
+def _on(dev):
+    """Make `dev` the current CUDA device for the call (launch device and
+    current stream follow it)."""
+    if dev.type == "cuda":
+        return torch.cuda.device(dev)
+    return contextlib.nullcontext()  # host-side tests with CPU tensors
 
 
 def params(temperature=1.0, top_k=0, top_p=1.0, draft_kind="logits", seed=0,
@@ -90,11 +115,13 @@ def spec_verify_chain(target, draft, draft_tokens, *, temperature=1.0,
     _want(out[2], torch.float32, (B, K), "accept_mass")
     if ws is None:
         ws = workspace(_lib.SPEC_OP_CHAIN, B, K, V, dev)
+    _device(target, draft, draft_tokens, *out, ws, stream=stream)
     prm = params(temperature, top_k, top_p, draft_kind, seed, offset)
-    _lib.call("spec_verify_chain", _ptr(target), _ptr(draft),
-              _ptr(draft_tokens), B, K, V, _dt(target), _dt(draft),
-              ctypes.byref(prm), _ptr(out[0]), _ptr(out[1]), _ptr(out[2]),
-              _ptr(ws), ws.numel(), _stream(stream))
+    with _on(dev):
+        _lib.call("spec_verify_chain", _ptr(target), _ptr(draft),
+                  _ptr(draft_tokens), B, K, V, _dt(target), _dt(draft),
+                  ctypes.byref(prm), _ptr(out[0]), _ptr(out[1]),
+                  _ptr(out[2]), _ptr(ws), ws.numel(), _stream(stream))
     return out
 
 
@@ -122,13 +149,16 @@ def spec_verify_tree(target, draft, q_row, node_tokens, parent, *,
     _want(out[3], torch.float32, (B, N + 1), "accept_mass")
     if ws is None:
         ws = workspace(_lib.SPEC_OP_TREE, B, N, V, dev)
+    _device(target, draft, q_row, node_tokens, parent, draft_lse, *out, ws,
+            stream=stream)
     prm = params(temperature, top_k, top_p, draft_kind, seed, offset,
                  draft_lse)
-    _lib.call("spec_verify_tree", _ptr(target), _ptr(draft), _ptr(q_row),
-              _ptr(node_tokens), _ptr(parent), B, N, R, V, _dt(target),
-              _dt(draft), ctypes.byref(prm), _ptr(out[0]), _ptr(out[1]),
-              _ptr(out[2]), _ptr(out[3]), _ptr(ws), ws.numel(),
-              _stream(stream))
+    with _on(dev):
+        _lib.call("spec_verify_tree", _ptr(target), _ptr(draft), _ptr(q_row),
+                  _ptr(node_tokens), _ptr(parent), B, N, R, V, _dt(target),
+                  _dt(draft), ctypes.byref(prm), _ptr(out[0]), _ptr(out[1]),
+                  _ptr(out[2]), _ptr(out[3]), _ptr(ws), ws.numel(),
+                  _stream(stream))
     return out
 
 
@@ -136,11 +166,12 @@ def spec_tree_mask(parent, *, bits=False, mask=True, stream=None):
     """parent [B, N] int32 -> (mask [B, N, N] uint8 or None,
     bits [B, N] int64 (uint64 bit patterns) or None)."""
     B, N = parent.shape
-    dev = parent.device
+    dev = _device(parent, stream=stream)
     m = torch.empty(B, N, N, dtype=torch.uint8, device=dev) if mask else None
     bt = torch.empty(B, N, dtype=torch.int64, device=dev) if bits else None
-    _lib.call("spec_tree_mask", _ptr(parent), B, N, _ptr(m), _ptr(bt),
-              _stream(stream))
+    with _on(dev):
+        _lib.call("spec_tree_mask", _ptr(parent), B, N, _ptr(m), _ptr(bt),
+                  _stream(stream))
     return m, bt
 
 
@@ -169,11 +200,14 @@ def spec_eagle2_expand_rerank(draft_logits, *, temperature, depth=6, topk=10,
         _want(out[4], torch.uint8, (B, total, total), "mask")
     if draft_lse is not None and tuple(draft_lse.shape) != (B, R):
         raise ValueError("draft_lse must have shape [B, R]")
+    _device(draft_logits, *out, ws, draft_lse, stream=stream)
     prm = params(temperature, draft_lse=draft_lse)
-    _lib.call("spec_eagle2_expand_rerank", _ptr(draft_logits), B, V,
-              _dt(draft_logits), depth, topk, width, total, ctypes.byref(prm),
-              _ptr(out[0]), _ptr(out[1]), _ptr(out[2]), _ptr(out[3]),
-              _ptr(out[4]), _ptr(ws), ws.numel(), _stream(stream))
+    with _on(dev):
+        _lib.call("spec_eagle2_expand_rerank", _ptr(draft_logits), B, V,
+                  _dt(draft_logits), depth, topk, width, total,
+                  ctypes.byref(prm), _ptr(out[0]), _ptr(out[1]),
+                  _ptr(out[2]), _ptr(out[3]), _ptr(out[4]), _ptr(ws),
+                  ws.numel(), _stream(stream))
     return out
 
 
@@ -188,10 +222,13 @@ def spec_kv_commit(kv, prefix_len, path_len, path_nodes=None, *, layout,
     if new_len is None:
         new_len = torch.empty(B, dtype=torch.int32, device=prefix_len.device)
     _want(new_len, torch.int32, (B,), "new_len")
+    dev = _device(kv, prefix_len, path_len, path_nodes, new_len,
+                  stream=stream)
     n1, n2, sb, s1, s2, sp = layout
-    _lib.call("spec_kv_commit", _ptr(kv), B, n1, n2, sb, s1, s2, sp,
-              row_bytes, _ptr(prefix_len), _ptr(path_nodes), _ptr(path_len),
-              N, _ptr(new_len), _stream(stream))
+    with _on(dev):
+        _lib.call("spec_kv_commit", _ptr(kv), B, n1, n2, sb, s1, s2, sp,
+                  row_bytes, _ptr(prefix_len), _ptr(path_nodes),
+                  _ptr(path_len), N, _ptr(new_len), _stream(stream))
     return new_len
 
 
@@ -231,12 +268,15 @@ def spec_accept_stats(count, parent=None, path_nodes=None, confidence=None,
         if out.get(f) is not None:
             _want(out[f], torch.float64 if f == "calib_conf_sum"
                   else torch.int64, (k,), f)
+    dev = _device(count, parent, path_nodes, confidence,
+                  *[out.get(f) for f in _lib.STATS_FIELDS], stream=stream)
     rec = _lib.SpecAcceptStats(*[
         None if out.get(f) is None else _ptr(out[f]).value
         for f in _lib.STATS_FIELDS])
-    _lib.call("spec_accept_stats", _ptr(count), _ptr(parent),
-              _ptr(path_nodes), _ptr(confidence), B, n, nbins,
-              ctypes.byref(rec), _stream(stream))
+    with _on(dev):
+        _lib.call("spec_accept_stats", _ptr(count), _ptr(parent),
+                  _ptr(path_nodes), _ptr(confidence), B, n, nbins,
+                  ctypes.byref(rec), _stream(stream))
     return out
 
 
@@ -257,22 +297,29 @@ def spec_tree_attention(q, k_cache, v_cache, prefix_len, mask_bits, *,
     _want(out, torch.bfloat16, (B, N, Hq, D), "out")
     if scale is None:
         scale = D ** -0.5
-    _lib.call("spec_tree_attention", _ptr(q), _ptr(k_cache), _ptr(v_cache),
-              _ptr(prefix_len), _ptr(mask_bits), B, N, Hq, Hkv, D, S,
-              float(scale), _ptr(out), _stream(stream))
+    dev = _device(q, k_cache, v_cache, prefix_len, mask_bits, out,
+                  stream=stream)
+    with _on(dev):
+        _lib.call("spec_tree_attention", _ptr(q), _ptr(k_cache),
+                  _ptr(v_cache), _ptr(prefix_len), _ptr(mask_bits), B, N, Hq,
+                  Hkv, D, S, float(scale), _ptr(out), _stream(stream))
     return out
 
 
 def spec_get_status(ws, stream=None) -> int:
     v = ctypes.c_uint32(0)
-    _lib.call("spec_get_status", _ptr(ws), ctypes.byref(v), _stream(stream))
+    with _on(_device(ws, stream=stream)):
+        _lib.call("spec_get_status", _ptr(ws), ctypes.byref(v),
+                  _stream(stream))
     return int(v.value)
 
 
 def spec_philox_uniforms(seed, offset, b, idx, slot, stream=None):
     n = b.numel()
-    out = torch.empty(n, dtype=torch.float32, device=b.device)
-    _lib.call("spec_philox_uniforms", int(seed) & (2**64 - 1),
-              int(offset) & 0xFFFFFFFF, _ptr(b), _ptr(idx), _ptr(slot), n,
-              _ptr(out), _stream(stream))
+    dev = _device(b, idx, slot, stream=stream)
+    out = torch.empty(n, dtype=torch.float32, device=dev)
+    with _on(dev):
+        _lib.call("spec_philox_uniforms", int(seed) & (2**64 - 1),
+                  int(offset) & 0xFFFFFFFF, _ptr(b), _ptr(idx), _ptr(slot), n,
+                  _ptr(out), _stream(stream))
     return out

@@ -19,13 +19,18 @@
 //    (cudaGetSymbolAddress) with that device current; make that first call
 //    before any stream capture.
 //  * Every call on a device shares the one array and leaves the last call's
-//    contents in it; the status word is cleared at the start of each call.
+//    contents in it; the status word is cleared at the start of each call
+//    and read back with spec_get_status_noalloc after it.
 //    Calls whose work overlaps on the GPU (other streams, other host threads
 //    on the same device) race on the array and must be serialised by the
 //    caller.
 //  * Sizes: B * (K + 1) <= SPEC_NOALLOC_MAX_ROWS rows and
 //    B * (K + 1) * ceil(V / 16384) <= SPEC_NOALLOC_MAX_PARTS argmax partials;
 //    larger requests are rejected with SPEC_ERR_SHAPE before any GPU work.
+//  * Not served (SPEC_ERR_UNSUPPORTED): sampling with top-k / top-p
+//    truncation (its candidate lists need scratch beyond the array), and
+//    rows the streaming kernels cannot take (see sampled_supported).  Given
+//    draft normalisers (draft_lse) are rejected with SPEC_ERR_ARG.
 #include <cmath>
 #include <mutex>
 
@@ -99,11 +104,6 @@ extern "C" int spec_verify_chain_noalloc(const void* target_logits, const void* 
     if (K > 0 && (!draft_tokens || !accept_mass)) return SPEC_ERR_ARG;
     if (!greedy && K > 0 && !draft) return SPEC_ERR_ARG;
   }
-  void* base = nullptr;
-  int rc = scratch_address(&base);
-  if (rc != SPEC_OK) return rc;
-  cudaStream_t st = (cudaStream_t)stream;
-  char* p = (char*)base;
   VerifyShape s{B, K, K, V, true};
   VerifyArgs a{};
   a.target = target_logits;
@@ -115,6 +115,14 @@ extern "C" int spec_verify_chain_noalloc(const void* target_logits, const void* 
   a.count = accepted;
   a.out_tokens = out_tokens;
   a.mass = accept_mass;
+  // the same refusal as the workspace entry point, before the status word
+  // of the previous call is cleared
+  if (!greedy && !sampled_supported(s, a)) return SPEC_ERR_UNSUPPORTED;
+  void* base = nullptr;
+  int rc = scratch_address(&base);
+  if (rc != SPEC_OK) return rc;
+  cudaStream_t st = (cudaStream_t)stream;
+  char* p = (char*)base;
   a.status = (uint32_t*)p;
   a.row_child = (int32_t*)(p + kStatusBytes);
   a.row_token = (int32_t*)(p + kStatusBytes + kRowBytes);
@@ -133,4 +141,16 @@ extern "C" int spec_verify_chain_noalloc(const void* target_logits, const void* 
   if (B == 0) return SPEC_OK;
   const cudaError_t e = greedy ? launch_greedy(s, a, st) : launch_sampled(s, a, st);
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+extern "C" int spec_get_status_noalloc(uint32_t* status, void* stream) {
+  if (!status) return SPEC_ERR_ARG;
+  void* base = nullptr;
+  const int rc = scratch_address(&base);
+  if (rc != SPEC_OK) return rc;
+  cudaStream_t st = (cudaStream_t)stream;
+  // the status word is the first word of the array
+  if (cudaMemcpyAsync(status, base, sizeof(uint32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  return cudaStreamSynchronize(st) == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }

@@ -1,6 +1,14 @@
-"""Helpers for GPU-vs-oracle parity tests (not collected by pytest)."""
+"""Helpers for GPU-vs-oracle parity tests (not collected by pytest).
+
+The compare functions return a Parity record of what they compared and
+append it to REPORT; tests/conftest.py prints REPORT at the end of the
+session, so near-tie exclusions are counted and reported, never silent."""
 
 from __future__ import annotations
+
+import dataclasses
+import math
+import os
 
 import numpy as np
 import torch
@@ -44,6 +52,46 @@ def draw_in_band(weights, u, y):
     return lo - CDF_BAND <= u <= hi + CDF_BAND
 
 
+@dataclasses.dataclass
+class Parity:
+    """Outcome of one GPU-vs-oracle comparison over `sequences` sequences:
+    `compared` were checked element by element, `near_tie_excluded` were
+    left out because an accept test on the path lies within 1e-5 of its
+    threshold (or a top-p cut sits at a near tie), and `cdf_band` of the
+    compared ones drew a final token that is the float32 neighbour of the
+    oracle's draw inside the CDF band.  `exact` = compared - cdf_band."""
+    test: str
+    sequences: int
+    compared: int
+    near_tie_excluded: int
+    cdf_band: int
+
+    @property
+    def exact(self):
+        return self.compared - self.cdf_band
+
+    def as_dict(self):
+        d = dataclasses.asdict(self)
+        d["exact"] = self.exact
+        return d
+
+
+REPORT: list = []
+
+
+def _record(seqs, compared, excluded, band, max_excluded):
+    test = os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0]
+    n = len(seqs)
+    p = Parity(test, n, compared, excluded, band)
+    REPORT.append(p)
+    # a comparison must compare something, and exclusions stay under the
+    # bound (default: a tenth of the sequences, at least one)
+    bound = max(1, math.ceil(n / 10)) if max_excluded is None else max_excluded
+    assert compared >= 1, p
+    assert excluded <= bound, (p, bound)
+    return p
+
+
 def _check_final(ref, i, got, want):
     """Final (replacement / bonus) token: equal, or a float32 neighbour of a
     boundary draw.  Returns 1 if the band was needed."""
@@ -55,14 +103,17 @@ def _check_final(ref, i, got, want):
     return 1
 
 
-def compare_chain(gpu, ref, *, greedy=False, check_mass=True, seqs=None):
+def compare_chain(gpu, ref, *, greedy=False, check_mass=True, seqs=None,
+                  max_excluded=None):
     """gpu = (accepted, tokens, mass) tensors; ref = oracle ChainResult.
-    Returns the number of sequences excluded as near ties (an accept test on
-    the path within 1e-5 of its threshold, or a top-p cut)."""
+    Returns the Parity record (sequences compared, excluded as near ties --
+    an accept test on the path within 1e-5 of its threshold, or a top-p cut
+    -- and final draws inside the CDF band); asserts that at least one
+    sequence was compared and that exclusions stay under `max_excluded`."""
     acc, tok, mass = (x.cpu().numpy() for x in gpu)
     B = ref.accepted.shape[0]
-    seqs = range(B) if seqs is None else seqs
-    excluded = 0
+    seqs = list(range(B) if seqs is None else seqs)
+    excluded = band = 0
     for i, b in enumerate(seqs):
         if ref.near_tie[i]:
             excluded += 1
@@ -74,22 +125,24 @@ def compare_chain(gpu, ref, *, greedy=False, check_mass=True, seqs=None):
         if greedy:
             assert tok[b, n] == ref.tokens[i, n], b
         else:
-            _check_final(ref, i, int(tok[b, n]), int(ref.tokens[i, n]))
+            band += _check_final(ref, i, int(tok[b, n]), int(ref.tokens[i, n]))
     if check_mass:
-        m = mass[list(seqs)]
+        m = mass[seqs]
         if greedy:
             assert np.array_equal(m, ref.mass.astype(np.float32))
         else:
             np.testing.assert_allclose(m, ref.mass, rtol=MASS_RTOL,
                                        atol=MASS_ATOL)
-    return excluded
+    return _record(seqs, len(seqs) - excluded, excluded, band, max_excluded)
 
 
-def compare_tree(gpu, ref, *, greedy=False, seqs=None):
+def compare_tree(gpu, ref, *, greedy=False, seqs=None, max_excluded=None):
+    """gpu = (path_len, path_nodes, tokens, mass); ref = oracle TreeResult.
+    Returns the Parity record, with the same assertions as compare_chain."""
     plen, pnodes, tok, mass = (x.cpu().numpy() for x in gpu)
     B = ref.path_len.shape[0]
-    seqs = range(B) if seqs is None else seqs
-    excluded = 0
+    seqs = list(range(B) if seqs is None else seqs)
+    excluded = band = 0
     for i, b in enumerate(seqs):
         if ref.near_tie[i]:
             excluded += 1
@@ -102,8 +155,8 @@ def compare_tree(gpu, ref, *, greedy=False, seqs=None):
         if greedy:
             assert tok[b, n] == ref.tokens[i, n], b
         else:
-            _check_final(ref, i, int(tok[b, n]), int(ref.tokens[i, n]))
-    m = mass[list(seqs)]
+            band += _check_final(ref, i, int(tok[b, n]), int(ref.tokens[i, n]))
+    m = mass[seqs]
     nan_g, nan_r = np.isnan(m), np.isnan(ref.mass)
     assert np.array_equal(nan_g, nan_r)
     if greedy:
@@ -111,4 +164,4 @@ def compare_tree(gpu, ref, *, greedy=False, seqs=None):
     else:
         np.testing.assert_allclose(m[~nan_g], ref.mass[~nan_r],
                                    rtol=MASS_RTOL, atol=MASS_ATOL)
-    return excluded
+    return _record(seqs, len(seqs) - excluded, excluded, band, max_excluded)

@@ -146,3 +146,50 @@ def test_verification_wrappers_reject_wrong_outputs(captured):
                            layout=(1, 1, 0, 0, 0, 16), row_bytes=16, N=4,
                            new_len=torch.zeros(B, dtype=torch.int64))
     assert captured == []
+
+
+def test_wrappers_reject_tensors_on_another_device(captured):
+    """Every tensor of a call (inputs, outputs, workspace) must be on the
+    primary input's device: the library launches on that device and would
+    otherwise dereference another device's memory.  A tensor on the meta
+    device stands in for one on another GPU."""
+    B, K, V = 2, 3, 64
+    t = torch.zeros(B, K + 1, V)
+    d = torch.zeros(B, K, V)
+    tok = torch.zeros(B, K, dtype=torch.int32)
+    other = lambda *s, dtype=torch.float32: torch.empty(*s, dtype=dtype,
+                                                        device="meta")
+    with pytest.raises(ValueError, match="same|must be on"):
+        api.spec_verify_chain(t, other(B, K, V), tok, temperature=1.0)
+    with pytest.raises(ValueError, match="must be on"):
+        api.spec_verify_chain(t, d, tok, temperature=1.0,
+                              out=(other(B, dtype=torch.int32),
+                                   torch.zeros(B, K + 1, dtype=torch.int32),
+                                   torch.zeros(B, K)))
+    with pytest.raises(ValueError, match="must be on"):
+        api.spec_verify_chain(t, d, tok, temperature=1.0,
+                              ws=other(256, dtype=torch.uint8))
+    N = 4
+    tt = torch.zeros(B, N + 1, V)
+    qr = torch.zeros(B, N + 1, dtype=torch.int32)
+    nt = torch.zeros(B, N, dtype=torch.int32)
+    par = torch.zeros(B, N, dtype=torch.int32)
+    with pytest.raises(ValueError, match="must be on"):
+        api.spec_verify_tree(tt, tt, qr, nt, other(B, N, dtype=torch.int32),
+                             temperature=1.0)
+    q = torch.zeros(B, N, 4, 128, dtype=torch.bfloat16)
+    kv = torch.zeros(B, 2, 16, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="must be on"):
+        api.spec_tree_attention(q, kv, other(B, 2, 16, 128,
+                                             dtype=torch.bfloat16),
+                                torch.zeros(B, dtype=torch.int32),
+                                torch.zeros(B, N, dtype=torch.int64))
+    with pytest.raises(ValueError, match="must be on"):
+        api.spec_accept_stats(torch.zeros(B, dtype=torch.int32), par,
+                              other(B, N, dtype=torch.int32), n=N)
+    with pytest.raises(ValueError, match="must be on"):
+        api.spec_kv_commit(torch.zeros(64, dtype=torch.uint8),
+                           torch.zeros(B, dtype=torch.int32),
+                           other(B, dtype=torch.int32), None,
+                           layout=(1, 1, 0, 0, 0, 16), row_bytes=16, N=N)
+    assert captured == []  # nothing reached the library

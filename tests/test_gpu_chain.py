@@ -58,8 +58,7 @@ def test_chain_vocab_sizes(V, dt):
     w = synth.workload("chain_sample", B=6, K=3, V=V, target_dtype=tdt,
                        draft_dtype=tdt, seed=77 + V)
     gpu, ref = run(w)
-    ex = compare_chain(gpu, ref)
-    assert ex <= 1
+    compare_chain(gpu, ref, max_excluded=1)
 
 
 @pytest.mark.parametrize("V,dt", [(300000, "bf16"), (150001, "f32")])
@@ -70,7 +69,7 @@ def test_chain_large_vocab(V, dt):
     w = synth.workload("chain_sample", B=3, K=2, V=V, target_dtype=tdt,
                        draft_dtype=tdt, seed=V % 1000)
     gpu, ref = run(w)
-    assert compare_chain(gpu, ref) <= 1
+    compare_chain(gpu, ref, max_excluded=1)
 
 
 @pytest.mark.parametrize("T", [1.0, 0.6])
@@ -128,6 +127,7 @@ def test_chain_batched_full_vocab_llama_size():
                        target_dtype=torch.bfloat16,
                        draft_dtype=torch.bfloat16, seed=11)
     target, draft, toks = synth.chain_inputs(w, "cuda")
-    seqs = [0, 7, 23, 47]
+    seqs = list(range(w.B))  # all 48 sequences
     gpu, ref = run(w, seqs=seqs, target=target, draft=draft, toks=toks)
-    compare_chain(gpu, ref, seqs=seqs)
+    p = compare_chain(gpu, ref, seqs=seqs, max_excluded=2)
+    assert p.exact >= w.B - 4, p

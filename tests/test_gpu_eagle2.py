@@ -163,7 +163,7 @@ def test_eagle2_full_pipeline_sampled():
     draft = synth.eagle2_draft(w, "cuda")
     tok, par, qrow, val, mask = api().spec_eagle2_expand_rerank(
         draft, temperature=w.temperature)
-    seqs = [0, 77, 127]
+    seqs = list(range(0, w.B, 8))  # 16 of the 128 sequences
     gpu = [x.cpu().numpy() for x in (tok, par, qrow, val, mask)]
     _compare(w, draft, gpu, seqs)
     target = synth.eagle2_target(w, draft, qrow, "cuda")
@@ -175,7 +175,8 @@ def test_eagle2_full_pipeline_sampled():
                       qrow[seqs].cpu().numpy(), tok[seqs].cpu().numpy(),
                       par[seqs].cpu().numpy(), temperature=w.temperature,
                       seed=w.decision_seed, batch_ids=seqs)
-    compare_tree(out, ref, seqs=seqs)
+    p = compare_tree(out, ref, seqs=seqs, max_excluded=2)
+    assert p.exact >= len(seqs) - 3, p
     plen = out[0].cpu().numpy()
     assert plen.mean() > 0.5  # the synthetic target tracks the draft
 

@@ -48,8 +48,7 @@ def test_topk_topp_workload_full():
     # B=64, K=5, V=32000 bf16, T=0.7, top-k 50, top-p 0.9 on both sides
     w = synth.workload("chain_topk")
     gpu, ref = run_chain(w)
-    ex = compare_chain(gpu, ref)
-    assert ex <= 3
+    compare_chain(gpu, ref, max_excluded=3)
     assert ref.status == 0
 
 
@@ -59,7 +58,7 @@ def test_topk_variants(k, p):
     w = synth.workload("chain_topk", B=24, K=3, V=3001, top_k=k, top_p=p,
                        seed=k * 10 + int(p * 10))
     gpu, ref = run_chain(w)
-    assert compare_chain(gpu, ref) <= 2
+    compare_chain(gpu, ref, max_excluded=2)
 
 
 def test_topp_only_small_vocab():
@@ -107,4 +106,4 @@ def test_topk_tree():
                       toks.cpu().numpy(), par.cpu().numpy(),
                       temperature=w.temperature, top_k=w.top_k, top_p=w.top_p,
                       seed=w.decision_seed)
-    assert compare_tree(gpu, ref) <= 1
+    compare_tree(gpu, ref, max_excluded=1)

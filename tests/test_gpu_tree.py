@@ -105,8 +105,7 @@ def test_static_tree_small_vocab(V):
     w = synth.workload("tree_static", B=8, V=V, seed=40 + V)
     ins = synth.tree_inputs(w, "cuda")
     gpu, ref = run_tree(w, *ins)
-    ex = compare_tree(gpu, ref)
-    assert ex <= 1
+    compare_tree(gpu, ref, max_excluded=1)
 
 
 def test_static_tree_large_vocab():
@@ -114,7 +113,7 @@ def test_static_tree_large_vocab():
     w = synth.workload("tree_static", B=2, V=300000, seed=8)
     ins = synth.tree_inputs(w, "cuda")
     gpu, ref = run_tree(w, *ins)
-    assert compare_tree(gpu, ref) <= 1
+    compare_tree(gpu, ref, max_excluded=1)
 
 
 def test_static_tree_low_acceptance_many_sibling_passes():
@@ -154,6 +153,8 @@ def test_static_tree_full_size_sampled():
     # B=32, 60 nodes, V=128256, bf16 target + float32 draft probabilities
     w = synth.workload("tree_static")
     ins = synth.tree_inputs(w, "cuda")
-    seqs = [0, 13, 31]
+    # every sequence of the batch against the oracle (about 40 s of CPU)
+    seqs = list(range(w.B))
     gpu, ref = run_tree(w, *ins, seqs=seqs)
-    compare_tree(gpu, ref, seqs=seqs)
+    p = compare_tree(gpu, ref, seqs=seqs, max_excluded=2)
+    assert p.exact >= w.B - 4, p

@@ -134,3 +134,38 @@ def test_acceptance_records_of_replicas_add_up_gloo(tmp_path):
         for f, v in got.items():
             want = whole.invalid if f == "invalid" else getattr(whole, f).tolist()
             assert v == want, f
+
+
+def _bench(args, env=None, timeout=240):
+    import subprocess
+    e = dict(os.environ)
+    for k in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR",
+              "MASTER_PORT"):
+        e.pop(k, None)
+    e.update(env or {})
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"),
+                           *args], capture_output=True, text=True, env=e,
+                          timeout=timeout, cwd=ROOT)
+
+
+def test_bench_gpus_flag_launches_its_ranks():
+    # outside torchrun, --gpus 2 launches two local ranks itself (the
+    # reference arm runs on the host cores, so this needs no GPU); rank 0
+    # prints the one line and reports both ranks
+    r = _bench(["--gpus", "2", "--impl", "reference", "--workload",
+                "chain_sample", "--steps", "1", "--warmup", "0",
+                "--cpu-seconds", "0.3"])
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2
+    assert d["config"]["workload"] == "chain_sample"
+
+
+def test_bench_refuses_gpus_that_differ_from_world_size():
+    r = _bench(["--gpus", "1", "--impl", "reference", "--workload",
+                "chain_sample"], env={"WORLD_SIZE": "2", "RANK": "0",
+                                      "LOCAL_RANK": "0"})
+    assert r.returncode != 0
+    assert "WORLD_SIZE" in (r.stderr + r.stdout)

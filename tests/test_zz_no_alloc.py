@@ -47,6 +47,25 @@ def test_noalloc_rejects_oversize_requests(lib):
     assert lib.raw("spec_verify_chain_noalloc", fake, fake, fake, 1000, 4,
                    16384 * 14, 1, 1, ctypes.byref(prm), fake, fake, fake,
                    None) == lib.SPEC_ERR_SHAPE
+    # sampling with top-k / top-p truncation needs candidate lists the
+    # fixed array does not hold
+    for top_k, top_p in ((50, 1.0), (0, 0.9), (50, 0.9)):
+        tprm = lib.SpecParams(0.7, top_k, top_p, 0, 0, 0, 0)
+        assert lib.raw("spec_verify_chain_noalloc", fake, fake, fake, 4, 4,
+                       32000, 1, 1, ctypes.byref(tprm), fake, fake, fake,
+                       None) == lib.SPEC_ERR_UNSUPPORTED
+    # unaligned float32 rows too long for one cluster's shared memory: the
+    # same SPEC_ERR_UNSUPPORTED as the workspace entry point, before any
+    # GPU work
+    assert lib.raw("spec_verify_chain_noalloc", fake, fake, fake, 1, 4,
+                   300001, 0, 0, ctypes.byref(prm), fake, fake, fake,
+                   None) == lib.SPEC_ERR_UNSUPPORTED
+    # given draft normalisers are refused
+    lprm = lib.SpecParams(1.0, 0, 1.0, 0, 0, 0, 0, 0x7f0000001000)
+    assert lib.raw("spec_verify_chain_noalloc", fake, fake, fake, 4, 4,
+                   32000, 1, 1, ctypes.byref(lprm), fake, fake, fake,
+                   None) == lib.SPEC_ERR_ARG
+    assert lib.raw("spec_get_status_noalloc", None, None) == lib.SPEC_ERR_ARG
 
 
 @pytest.mark.gpu
@@ -69,9 +88,10 @@ def test_noalloc_matches_workspace_entry_point_twice(lib, kind):
             w = synth.workload("greedy", B=64, K=8, V=128256, seed=seed)
         target, draft, toks = synth.chain_inputs(w, dev)
         B, K = toks.shape
+        ws = api.workspace(lib.SPEC_OP_CHAIN, B, K, w.V, dev)
         want = api.spec_verify_chain(target, draft, toks,
                                      temperature=w.temperature,
-                                     seed=w.decision_seed + call)
+                                     seed=w.decision_seed + call, ws=ws)
         out = (torch.full((B,), -7, dtype=torch.int32, device=dev),
                torch.full((B, K + 1), -7, dtype=torch.int32, device=dev),
                torch.full((B, K), -7.0, dtype=torch.float32, device=dev))
@@ -79,6 +99,11 @@ def test_noalloc_matches_workspace_entry_point_twice(lib, kind):
         rc = _noalloc(lib, target, draft, toks, prm, out, stream)
         assert rc == lib.SPEC_OK, rc
         torch.cuda.synchronize()
+        # the status words of both calls agree (and report nothing here)
+        st = ctypes.c_uint32(0xFFFFFFFF)
+        assert lib.raw("spec_get_status_noalloc", ctypes.byref(st),
+                       stream) == lib.SPEC_OK
+        assert st.value == api.spec_get_status(ws) == 0, st.value
         assert np.array_equal(out[0].cpu().numpy(), want[0].cpu().numpy())
         assert np.array_equal(out[1].cpu().numpy(), want[1].cpu().numpy())
         np.testing.assert_allclose(out[2].cpu().numpy(),
