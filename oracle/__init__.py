@@ -67,6 +67,14 @@ PINS = {
     "included; the chain case equals causal attention; a root child without "
     "prefix returns its own value; other branches and the prefix order do "
     "not change a node's output",
+    "lmhead.lm_head_logits / bf16_round": "bf16 rounding equal to torch's "
+    "float32 -> bfloat16 conversion (ties included); neighbours bracket the "
+    "value one bf16 unit apart; exact logits equal rational dot products; "
+    "the accumulation bound covers an explicit float32 summation in groups "
+    "of 16",
+    "lmhead.verify_tree_lmhead": "equals verify_tree on logits that are bf16 "
+    "values already (no rounding ties); a uniform between the two roundings' "
+    "acceptance ratios is a rounding tie, one outside is not",
     "residual inverse-CDF at large V": "equal to the draw in exact integer "
     "arithmetic (weights scaled by a common power of two, 24-bit dyadic "
     "uniforms) on residual rows at V = 128256, wherever no near tie is "
