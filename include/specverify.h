@@ -88,6 +88,8 @@ extern "C" {
 #define SPEC_OP_CHAIN 1
 #define SPEC_OP_TREE 2
 #define SPEC_OP_EAGLE2 3
+#define SPEC_OP_LMHEAD 4       /* spec_lm_head: B = rows M, n = 0           */
+#define SPEC_OP_TREE_LMHEAD 5  /* spec_verify_tree_lmhead: n = N            */
 
 /* Sampling parameters (plain data, 40 bytes). */
 typedef struct spec_params {
@@ -113,7 +115,8 @@ typedef struct spec_params {
 /*
  * Workspace size in bytes for one call of `op` (SPEC_OP_CHAIN with n = K,
  * SPEC_OP_TREE with n = N, SPEC_OP_EAGLE2 with n = number of draft rows per
- * sequence).  The workspace must be 256-byte aligned device memory; its
+ * sequence, SPEC_OP_LMHEAD with B = rows and n = 0, SPEC_OP_TREE_LMHEAD
+ * with n = N).  The workspace must be 256-byte aligned device memory; its
  * contents need no initialisation and are overwritten by every call.  Returns
  * 0 for invalid sizes.
  */
@@ -185,6 +188,51 @@ int spec_verify_tree(const void* target_logits, const void* draft,
                      int32_t* path_nodes, int32_t* out_tokens,
                      float* accept_mass, void* workspace, size_t ws_bytes,
                      void* stream);
+
+/*
+ * Target LM head of the verification pass (step 2 of the draft/verify loop
+ * of "投机解码与 EAGLE": one target forward over every drafted position; its
+ * last layer maps each position's final hidden state to logits).
+ *
+ * logits [M, V] bf16 (out) = hidden [M, H] bf16 x w_vocab^T, w_vocab [V, H]
+ *     bf16 (row-major, the layout of a linear layer's weight); products
+ *     accumulated in float32 on the tensor cores, rounded to bf16 (nearest,
+ *     ties to even).
+ * row_lse [M] float32 (out, may be NULL; needs temperature > 0): each row's
+ *     base-2 log normaliser log2 sum_v 2^(z_v log2(e) / temperature) of the
+ *     rounded logits, the first pass of verification taken in the GEMM's
+ *     epilogue.
+ * Requirements: H % 8 == 0 (rows of 16-byte multiples), hidden and w_vocab
+ * 16-byte aligned, else SPEC_ERR_UNSUPPORTED; M >= 0, 1 <= V <=
+ * SPEC_MAX_VOCAB.  Workspace: spec_workspace_bytes(SPEC_OP_LMHEAD, M, 0, V)
+ * (status word and per-tile statistics).  Status bits (SPEC_STATUS_TIMEOUT)
+ * via spec_get_status.
+ */
+int spec_lm_head(const void* hidden, const void* w_vocab, int M, int H, int V,
+                 float temperature, void* logits, float* row_lse,
+                 void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Tree verification with the target logits computed from the target's final
+ * hidden states by the LM head (spec_lm_head followed by spec_verify_tree,
+ * with the target rows' normalisers taken in the GEMM's epilogue so that
+ * verification reads each target row once).
+ *
+ * hidden [B, N+1, H] bf16: the target's final hidden state at each tree row;
+ * w_vocab [V, H] bf16; the other arguments as for spec_verify_tree (the
+ * target logits are bf16).  logits [B, N+1, V] bf16 (out, may be NULL): the
+ * computed target logits; NULL keeps them in the workspace.  Workspace:
+ * spec_workspace_bytes(SPEC_OP_TREE_LMHEAD, B, N, V).  Requirements and
+ * errors as for spec_lm_head and spec_verify_tree.
+ */
+int spec_verify_tree_lmhead(const void* hidden, const void* w_vocab, int H,
+                            const void* draft, const int32_t* q_row,
+                            const int32_t* node_tokens, const int32_t* parent,
+                            int B, int N, int R, int V, int dtype_draft,
+                            const spec_params_t* prm, int32_t* path_len,
+                            int32_t* path_nodes, int32_t* out_tokens,
+                            float* accept_mass, void* logits,
+                            void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * Tree attention mask (EAGLE-2 notes §4.2: each token sees only its
@@ -428,7 +476,8 @@ int spec_get_status_noalloc(uint32_t* status, void* stream);
  *   SPEC_PROF_EXPAND    EAGLE-2 draft-row top-k kernel,
  *   SPEC_PROF_KV        KV-cache commit move kernel,
  *   SPEC_PROF_STATS     acceptance-records kernel,
- *   SPEC_PROF_ATTN      tree-attention kernel.
+ *   SPEC_PROF_ATTN      tree-attention kernel,
+ *   SPEC_PROF_LMHEAD    LM-head GEMM kernel.
  * Returns SPEC_ERR_SHAPE if pairs were dropped.  Not thread-safe.
  */
 #define SPEC_PROF_ARGMAX 0
@@ -437,6 +486,7 @@ int spec_get_status_noalloc(uint32_t* status, void* stream);
 #define SPEC_PROF_KV 3
 #define SPEC_PROF_STATS 4
 #define SPEC_PROF_ATTN 5
+#define SPEC_PROF_LMHEAD 6
 int spec_profile_enable(int on);
 int spec_profile_read(int kind, double* total_ms, int* launches);
 

@@ -46,6 +46,8 @@ SPEC_STATUS_TIMEOUT = 128
 SPEC_OP_CHAIN = 1
 SPEC_OP_TREE = 2
 SPEC_OP_EAGLE2 = 3
+SPEC_OP_LMHEAD = 4
+SPEC_OP_TREE_LMHEAD = 5
 
 
 class SpecParams(ctypes.Structure):
@@ -87,6 +89,11 @@ _SIGNATURES = {
                               ctypes.POINTER(SpecParams), _P, _P, _P, _P, _P,
                               _SZ, _P]),
     "spec_tree_mask": (_I, [_P, _I, _I, _P, _P, _P]),
+    "spec_lm_head": (_I, [_P, _P, _I, _I, _I, ctypes.c_float, _P, _P, _P,
+                          _SZ, _P]),
+    "spec_verify_tree_lmhead": (_I, [_P, _P, _I, _P, _P, _P, _P, _I, _I, _I,
+                                     _I, _I, ctypes.POINTER(SpecParams), _P,
+                                     _P, _P, _P, _P, _P, _SZ, _P]),
     "spec_eagle2_expand_rerank": (_I, [_P, _I, _I, _I, _I, _I, _I, _I,
                                        ctypes.POINTER(SpecParams), _P, _P, _P,
                                        _P, _P, _P, _SZ, _P]),
@@ -116,6 +123,7 @@ SPEC_PROF_EXPAND = 2
 SPEC_PROF_KV = 3
 SPEC_PROF_STATS = 4
 SPEC_PROF_ATTN = 5
+SPEC_PROF_LMHEAD = 6
 
 EXPORTED = tuple(_SIGNATURES)
 

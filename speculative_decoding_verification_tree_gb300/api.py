@@ -162,6 +162,78 @@ def spec_verify_tree(target, draft, q_row, node_tokens, parent, *,
     return out
 
 
+def spec_lm_head(hidden, w_vocab, *, temperature=0.0, row_lse=False,
+                 out=None, ws=None, stream=None):
+    """Target logits = hidden [..., H] x w_vocab^T (w_vocab [V, H]), bf16.
+    Returns (logits [..., V] bf16, row_lse [...] float32 or None): with
+    row_lse=True (temperature > 0) also each row's base-2 log normaliser
+    log2 sum_v 2^(z_v log2(e) / temperature), taken in the GEMM epilogue."""
+    H = hidden.shape[-1]
+    V = w_vocab.shape[0]
+    lead = tuple(hidden.shape[:-1])
+    M = 1
+    for d in lead:
+        M *= d
+    _want(hidden, torch.bfloat16, lead + (H,), "hidden")
+    _want(w_vocab, torch.bfloat16, (V, H), "w_vocab")
+    dev = hidden.device
+    if out is None:
+        out = torch.empty(lead + (V,), dtype=torch.bfloat16, device=dev)
+    _want(out, torch.bfloat16, lead + (V,), "logits")
+    lse = (torch.empty(lead, dtype=torch.float32, device=dev)
+           if row_lse else None)
+    if ws is None:
+        ws = workspace(_lib.SPEC_OP_LMHEAD, M, 0, V, dev)
+    _device(hidden, w_vocab, out, lse, ws, stream=stream)
+    with _on(dev):
+        _lib.call("spec_lm_head", _ptr(hidden), _ptr(w_vocab), M, H, V,
+                  float(temperature), _ptr(out), _ptr(lse), _ptr(ws),
+                  ws.numel(), _stream(stream))
+    return out, lse
+
+
+def spec_verify_tree_lmhead(hidden, w_vocab, draft, q_row, node_tokens,
+                            parent, *, temperature=1.0, top_k=0, top_p=1.0,
+                            draft_kind="logits", seed=0, offset=0,
+                            logits=None, out=None, ws=None, stream=None,
+                            draft_lse=None):
+    """Tree verification whose target logits are hidden [B, N+1, H] x
+    w_vocab^T (bf16; see spec_verify_tree for the rest).  logits: an
+    optional [B, N+1, V] bf16 tensor that receives the computed logits.
+    Returns (path_len, path_nodes, tokens, accept_mass)."""
+    B, N1, H = hidden.shape
+    N = N1 - 1
+    V = w_vocab.shape[0]
+    R = 0 if draft is None else draft.shape[1]
+    dev = hidden.device
+    _want(hidden, torch.bfloat16, (B, N1, H), "hidden")
+    _want(w_vocab, torch.bfloat16, (V, H), "w_vocab")
+    if logits is not None:
+        _want(logits, torch.bfloat16, (B, N1, V), "logits")
+    if out is None:
+        out = (torch.empty(B, dtype=torch.int32, device=dev),
+               torch.empty(B, N, dtype=torch.int32, device=dev),
+               torch.empty(B, N + 1, dtype=torch.int32, device=dev),
+               torch.empty(B, N + 1, dtype=torch.float32, device=dev))
+    _want(out[0], torch.int32, (B,), "path_len")
+    _want(out[1], torch.int32, (B, N), "path_nodes")
+    _want(out[2], torch.int32, (B, N + 1), "tokens")
+    _want(out[3], torch.float32, (B, N + 1), "accept_mass")
+    if ws is None:
+        ws = workspace(_lib.SPEC_OP_TREE_LMHEAD, B, N, V, dev)
+    _device(hidden, w_vocab, draft, q_row, node_tokens, parent, logits,
+            draft_lse, *out, ws, stream=stream)
+    prm = params(temperature, top_k, top_p, draft_kind, seed, offset,
+                 draft_lse)
+    with _on(dev):
+        _lib.call("spec_verify_tree_lmhead", _ptr(hidden), _ptr(w_vocab), H,
+                  _ptr(draft), _ptr(q_row), _ptr(node_tokens), _ptr(parent),
+                  B, N, R, V, _dt(draft), ctypes.byref(prm), _ptr(out[0]),
+                  _ptr(out[1]), _ptr(out[2]), _ptr(out[3]), _ptr(logits),
+                  _ptr(ws), ws.numel(), _stream(stream))
+    return out
+
+
 def spec_tree_mask(parent, *, bits=False, mask=True, stream=None):
     """parent [B, N] int32 -> (mask [B, N, N] uint8 or None,
     bits [B, N] int64 (uint64 bit patterns) or None)."""

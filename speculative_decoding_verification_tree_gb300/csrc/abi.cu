@@ -64,7 +64,26 @@ int check_params(const spec_params_t* prm, int V) {
 
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA; }
 
-int run_verify(const VerifyShape& s, VerifyArgs& a, void* ws, size_t ws_bytes, cudaStream_t st) {
+// Workspace of the LM head: [status | per-tile statistics [M, V/256] float2]
+size_t lmhead_ws(int M, int V) {
+  return kAlign + up((size_t)M * lmhead_tiles_n(V) * 2 * sizeof(float));
+}
+// Tree verification through the LM head: [verify | logits | stats | lse]
+struct TreeLmWs {
+  size_t off_logits, off_stats, off_lse, total;
+};
+TreeLmWs tree_lm_ws(int B, int N, int V) {
+  const size_t rows = (size_t)B * (N + 1);
+  TreeLmWs w;
+  w.off_logits = verify_ws(B, N, V, false).total;
+  w.off_stats = w.off_logits + up(rows * (size_t)V * 2);
+  w.off_lse = w.off_stats + up(rows * lmhead_tiles_n(V) * 2 * sizeof(float));
+  w.total = w.off_lse + up(rows * sizeof(float));
+  return w;
+}
+
+// Points the call's scratch pieces into the caller's workspace.
+int bind_verify_ws(const VerifyShape& s, VerifyArgs& a, void* ws, size_t ws_bytes) {
   const VerifyWs w = verify_ws(s.B, s.n, s.V, s.chain);
   if (!ws || ((uintptr_t)ws % kAlign) != 0) return SPEC_ERR_WORKSPACE;
   if (ws_bytes < w.total) return SPEC_ERR_WORKSPACE;
@@ -82,12 +101,23 @@ int run_verify(const VerifyShape& s, VerifyArgs& a, void* ws, size_t ws_bytes, c
   a.rowout = (RowOut*)(base + w.off_out);
   a.qlist = (int32_t*)(base + w.off_qlist);
   a.qcount = (int32_t*)(base + 4);  // beside the status word, zeroed with it
-  if (a.prm.temperature != 0.f && !sampled_supported(s, a)) return SPEC_ERR_UNSUPPORTED;
-  cudaError_t e = cudaMemsetAsync(a.status, 0, 2 * sizeof(uint32_t), st);
-  if (e != cudaSuccess) return SPEC_ERR_CUDA;
+  return SPEC_OK;
+}
+
+// Launches of a bound verification call (status word already cleared).
+int launch_verify(const VerifyShape& s, const VerifyArgs& a, cudaStream_t st) {
   if (s.B == 0) return SPEC_OK;
   if (a.prm.temperature == 0.f) return cuda_rc(launch_greedy(s, a, st));
   return cuda_rc(launch_sampled(s, a, st));
+}
+
+int run_verify(const VerifyShape& s, VerifyArgs& a, void* ws, size_t ws_bytes, cudaStream_t st) {
+  int rc = bind_verify_ws(s, a, ws, ws_bytes);
+  if (rc != SPEC_OK) return rc;
+  if (a.prm.temperature != 0.f && !sampled_supported(s, a)) return SPEC_ERR_UNSUPPORTED;
+  cudaError_t e = cudaMemsetAsync(a.status, 0, 2 * sizeof(uint32_t), st);
+  if (e != cudaSuccess) return SPEC_ERR_CUDA;
+  return launch_verify(s, a, st);
 }
 
 }  // namespace
@@ -104,6 +134,11 @@ size_t spec_workspace_bytes(int op, int B, int n, int V) {
     return verify_ws(B, n, V, op == SPEC_OP_CHAIN).total;
   }
   if (op == SPEC_OP_EAGLE2) return eagle2_ws(B, n).total;
+  if (op == SPEC_OP_LMHEAD) return n == 0 ? lmhead_ws(B, V) : 0;
+  if (op == SPEC_OP_TREE_LMHEAD) {
+    if (n > SPEC_MAX_TREE_NODES) return 0;
+    return tree_lm_ws(B, n, V).total;
+  }
   return 0;
 }
 
@@ -175,6 +210,82 @@ int spec_verify_tree(const void* target_logits, const void* draft, const int32_t
   a.out_tokens = out_tokens;
   a.mass = accept_mass;
   return run_verify(s, a, workspace, ws_bytes, (cudaStream_t)stream);
+}
+
+int spec_lm_head(const void* hidden, const void* w_vocab, int M, int H, int V, float temperature,
+                 void* logits, float* row_lse, void* workspace, size_t ws_bytes, void* stream) {
+  if (M < 0 || H < 1 || V < 1 || V > SPEC_MAX_VOCAB) return SPEC_ERR_SHAPE;
+  if (!(temperature >= 0.f) || !std::isfinite(temperature)) return SPEC_ERR_ARG;
+  if (row_lse && !(temperature > 0.f)) return SPEC_ERR_ARG;
+  if (M > 0 && (!hidden || !w_vocab || !logits)) return SPEC_ERR_ARG;
+  if (M > 0 && !lmhead_supported(hidden, w_vocab, H)) return SPEC_ERR_UNSUPPORTED;
+  if (!workspace || ((uintptr_t)workspace % kAlign) != 0 || ws_bytes < lmhead_ws(M, V))
+    return SPEC_ERR_WORKSPACE;
+  cudaStream_t st = (cudaStream_t)stream;
+  uint32_t* status = (uint32_t*)workspace;
+  if (cudaMemsetAsync(status, 0, sizeof(uint32_t), st) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (M == 0) return SPEC_OK;
+  float2* stats = row_lse ? (float2*)((char*)workspace + kAlign) : nullptr;
+  return cuda_rc(launch_lmhead(hidden, w_vocab, M, H, V, temperature, (uint16_t*)logits, V, stats,
+                               row_lse, status, st));
+}
+
+int spec_verify_tree_lmhead(const void* hidden, const void* w_vocab, int H, const void* draft,
+                            const int32_t* q_row, const int32_t* node_tokens,
+                            const int32_t* parent, int B, int N, int R, int V, int dtype_draft,
+                            const spec_params_t* prm, int32_t* path_len, int32_t* path_nodes,
+                            int32_t* out_tokens, float* accept_mass, void* logits,
+                            void* workspace, size_t ws_bytes, void* stream) {
+  if (B < 0 || N < 0 || V < 1 || R < 0 || H < 1) return SPEC_ERR_SHAPE;
+  if (V > SPEC_MAX_VOCAB || N > SPEC_MAX_TREE_NODES) return SPEC_ERR_SHAPE;
+  int rc = check_params(prm, V);
+  if (rc != SPEC_OK) return rc;
+  if (prm->draft_lse && prm->temperature > 0.f &&
+      (prm->draft_kind != SPEC_DRAFT_LOGITS || truncation_k(prm, V) > 0))
+    return SPEC_ERR_ARG;
+  const bool greedy = prm->temperature == 0.f;
+  if (!greedy && R > 0 && !dtype_ok(dtype_draft)) return SPEC_ERR_DTYPE;
+  if (B > 0) {
+    if (!hidden || !w_vocab || !path_len || !out_tokens || !accept_mass) return SPEC_ERR_ARG;
+    if (N > 0 && (!node_tokens || !parent || !path_nodes)) return SPEC_ERR_ARG;
+    if (!greedy && (!q_row || (R > 0 && !draft))) return SPEC_ERR_ARG;
+    if (!lmhead_supported(hidden, w_vocab, H)) return SPEC_ERR_UNSUPPORTED;
+  }
+  const TreeLmWs lw = tree_lm_ws(B, N, V);
+  if (!workspace || ((uintptr_t)workspace % kAlign) != 0 || ws_bytes < lw.total)
+    return SPEC_ERR_WORKSPACE;
+  char* base = (char*)workspace;
+  uint16_t* lg = logits ? (uint16_t*)logits : (uint16_t*)(base + lw.off_logits);
+  VerifyShape s{B, N, R, V, false};
+  VerifyArgs a{};
+  a.target = lg;
+  a.draft = greedy ? nullptr : draft;
+  a.q_row = greedy ? nullptr : q_row;
+  a.node_tokens = node_tokens;
+  a.parent = parent;
+  a.dt_target = SPEC_BF16;
+  a.dt_draft = dtype_ok(dtype_draft) ? dtype_draft : SPEC_F32;
+  a.prm = *prm;
+  if (greedy) a.prm.draft_lse = nullptr;
+  a.count = path_len;
+  a.path_nodes = path_nodes;
+  a.out_tokens = out_tokens;
+  a.mass = accept_mass;
+  // the epilogue's normalisers serve the full-vocabulary sampled path
+  const bool stats = !greedy && truncation_k(prm, V) == 0;
+  a.tlse = stats ? (const float*)(base + lw.off_lse) : nullptr;
+  rc = bind_verify_ws(s, a, workspace, ws_bytes);
+  if (rc != SPEC_OK) return rc;
+  if (!greedy && !sampled_supported(s, a)) return SPEC_ERR_UNSUPPORTED;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemsetAsync(a.status, 0, 2 * sizeof(uint32_t), st) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (B == 0) return SPEC_OK;
+  const int M = B * (N + 1);
+  rc = cuda_rc(launch_lmhead(hidden, w_vocab, M, H, V, prm->temperature, lg, V,
+                             stats ? (float2*)(base + lw.off_stats) : nullptr,
+                             stats ? (float*)(base + lw.off_lse) : nullptr, a.status, st));
+  if (rc != SPEC_OK) return rc;
+  return launch_verify(s, a, st);
 }
 
 int spec_tree_mask(const int32_t* parent, int B, int N, uint8_t* mask, uint64_t* mask_bits,

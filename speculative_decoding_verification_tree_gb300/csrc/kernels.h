@@ -57,6 +57,9 @@ struct VerifyArgs {
   const int32_t* q_row;        // tree only
   const int32_t* node_tokens;  // chain: draft_tokens [B,K]; tree: [B,N]
   const int32_t* parent;       // tree only
+  const float* tlse;           // [rows] target rows' base-2 log normalisers
+                               // at the call's temperature, or null (the
+                               // streaming kernel then sums the rows itself)
   int dt_target, dt_draft;
   spec_params_t prm;
   // outputs
@@ -137,6 +140,15 @@ cudaError_t launch_tree_mask(const int32_t* parent, int B, int N, uint8_t* mask,
                              uint64_t* bits, cudaStream_t st);
 cudaError_t launch_philox(uint64_t seed, uint32_t offset, const int32_t* b, const int32_t* i,
                           const int32_t* slot, int n, float* out, cudaStream_t st);
+
+// Target LM head: logits [M, V] (bf16, row stride ldo) = hidden [M, H] x
+// W^T on tcgen05; with temperature > 0 and `stats`, also the per-row base-2
+// log normalisers at that temperature into `lse` [M] (stats: [M, V/256]).
+int lmhead_tiles_n(int V);
+bool lmhead_supported(const void* hidden, const void* w, int H);
+cudaError_t launch_lmhead(const void* hidden, const void* w, int M, int H, int V, float temperature,
+                          uint16_t* logits, int64_t ldo, float2* stats, float* lse,
+                          uint32_t* status, cudaStream_t st);
 
 // EAGLE-2 expand + rerank
 struct Eagle2Cand {

@@ -726,8 +726,9 @@ cudaError_t launch_sampled(const VerifyShape& s, const VerifyArgs& a, cudaStream
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return cudaErrorInvalidDevice;
-  // pass A reads the draft row too unless its normaliser is given
-  const int passA = tsz + ((qk == Q_LOGITS && a.prm.draft_lse) ? 0 : dsz);
+  // pass A reads the target row unless its normaliser is given (LM head
+  // epilogue), and the draft row unless its normaliser is given
+  const int passA = (a.tlse ? 0 : tsz) + ((qk == Q_LOGITS && a.prm.draft_lse) ? 0 : dsz);
   if (P.bulk && a.meta && a.qres && a.rowout &&
       stream_geometry(s.V, tsz, dsz, &Q.C, &Q.slice, &Q.nch, &Q.stages, s.rows(), sms,
                       passA)) {

@@ -485,6 +485,9 @@ __global__ void __launch_bounds__(kThreads, 1) unit_stream(StreamParams P) {
   // the caller's draft-row normalisers (logit drafts only): pass A then
   // reads the target row alone and the draft row is read once, in pass B
   const float* qlse = QK == Q_LOGITS ? a.prm.draft_lse : nullptr;
+  // the target rows' normalisers, when the LM head's epilogue computed them:
+  // pass A then leaves the target row out and pass B reads it once
+  const float* plse = a.tlse;
   auto draft_row = [&](int64_t u, int q) -> const TD* {
     const int64_t b = u / (n + 1);
     return drf + ((int64_t)b * s.R + q) * V;
@@ -531,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1) unit_stream(StreamParams P) {
           bulk_g2s(&sm.rec[rb], a.meta + ua * (int64_t)P.rec_bytes, (uint32_t)P.rec_bytes,
                    &sm.mrec[rb]);
         }
-        const TT* ta = hA ? tgt + ua * (int64_t)V + r0 : nullptr;
+        const TT* ta = (hA && !plse) ? tgt + ua * (int64_t)V + r0 : nullptr;
         const TD* da = (qa >= 0 && !qlse) ? draft_row(ua, qa) + r0 : nullptr;
         const TT* tb = hB ? tgt + ub * (int64_t)V + r0 : nullptr;
         const TD* db = qb >= 0 ? draft_row(ub, qb) + r0 : nullptr;
@@ -540,15 +543,14 @@ __global__ void __launch_bounds__(kThreads, 1) unit_stream(StreamParams P) {
           const int v = min(kCH, len - c * kCH);
           const uint32_t bt = (uint32_t)v * sizeof(TT), bd = (uint32_t)v * sizeof(TD);
           uint32_t bytes = 0;
-          if (hA) bytes += bt + (da ? bd : 0u);
+          if (ta) bytes += bt;
+          if (da) bytes += bd;
           if (db) bytes += bt + bd;
           mbar_expect_tx(&sm.full[stg], bytes);
           unsigned char* sa = stage(stg, 0);
           unsigned char* sb = stage(stg, 1);
-          if (hA) {
-            bulk_g2s_pol(sa, ta + c * kCH, bt, &sm.full[stg], pol_a);
-            if (da) bulk_g2s_pol(sa + kTB, da + c * kCH, bd, &sm.full[stg], pol_a);
-          }
+          if (ta) bulk_g2s_pol(sa, ta + c * kCH, bt, &sm.full[stg], pol_a);
+          if (da) bulk_g2s_pol(sa + kTB, da + c * kCH, bd, &sm.full[stg], pol_a);
           if (db) {
             bulk_g2s_pol(sb, tb + c * kCH, bt, &sm.full[stg], pol_b);
             bulk_g2s_pol(sb + kTB, db + c * kCH, bd, &sm.full[stg], pol_b);
@@ -573,15 +575,17 @@ __global__ void __launch_bounds__(kThreads, 1) unit_stream(StreamParams P) {
     float zp_tot = 0.f, zq_tot = 0.f;
     int64_t u_cur = nrow > 0 ? unit_of(0) : -1, u_prev = -1, u_prev2 = -1;
     int q_cur = nrow > 0 ? a.qres[u_cur] : -1, q_prev = -1;
-    float lq_carry = 0.f;
+    float lq_carry = 0.f, lp_carry = 0.f;
     for (int j = 0; nrow > 0 && j <= nrow + 1; ++j) {
       const bool hA = j < nrow, hB = j >= 1 && j <= nrow;
       const int qa = hA ? q_cur : -1, qb = hB ? q_prev : -1;
       const int64_t u_next = (j + 1 < nrow) ? unit_of(j + 1) : -1;
       const int q_next = (u_next >= 0) ? a.qres[u_next] : -1;
       const int64_t ub = u_prev, ur2 = u_prev2;
-      const float lq_b = lq_carry;  // row j - 1's given normaliser
+      const float lq_b = lq_carry;  // row j - 1's given normalisers
+      const float lp_b = lp_carry;
       lq_carry = (qlse && qa >= 0) ? __ldg(qlse + (u_cur / (n + 1)) * s.R + qa) : 0.f;
+      lp_carry = (plse && hA) ? __ldg(plse + u_cur) : 0.f;
 
       // Steps 1-3: the previous row-time's exchange and the decisions it allows.
       auto row_start = [&]() {
@@ -609,6 +613,10 @@ __global__ void __launch_bounds__(kThreads, 1) unit_stream(StreamParams P) {
             A.z = __shfl_sync(0xffffffffu, A.z, 0);
             Lp = A.m + log2f(A.z);
             zp_tot = A.z;
+            if (plse) {  // given: finite unless the row is empty or not a number
+              Lp = lp_b;
+              zp_tot = (fabsf(lp_b) < 0x1p126f) ? 1.f : 0.f;
+            }
             Lq = 0.f;
             invZq = 0.f;
             zq_tot = 0.f;
@@ -713,9 +721,9 @@ __global__ void __launch_bounds__(kThreads, 1) unit_stream(StreamParams P) {
       float2 acc_a2 = make_float2(0.f, 0.f), acc_r2 = make_float2(0.f, 0.f), zq2 = make_float2(0.f, 0.f);
       const float2 kt2 = make_float2(kt, kt);
       // The chunk loop, one instantiation per combination of the row-time's
-      // uniform choices (pass A present and whether it sums the draft row,
-      // pass B present and whether it needs the residual mass), so that the
-      // loop body tests none of them.
+      // uniform choices (whether pass A sums the target row and whether it
+      // sums the draft row, pass B present and whether it needs the residual
+      // mass), so that the loop body tests none of them.
       auto chunk_loop = [&](auto fA, auto fQ, auto fB, auto fR) {
         constexpr bool kA = decltype(fA)::value, kQ = decltype(fQ)::value;
         constexpr bool kB = decltype(fB)::value, kR = decltype(fR)::value;
@@ -728,19 +736,20 @@ __global__ void __launch_bounds__(kThreads, 1) unit_stream(StreamParams P) {
               float x[8];
               load8<TT>(reinterpret_cast<const TT*>(sa) + tid * kEPT, x);
               lazy_sum(x, kt, m, z);
-              if constexpr (kQ) {
-                float y[8];
-                load8<TD>(reinterpret_cast<const TD*>(sa + kTB) + tid * kEPT, y);
-                if constexpr (QK == Q_PROBS_T1) {
-                  zq2 = fadd2(zq2, fadd2(fadd2(make_float2(y[0], y[1]), make_float2(y[2], y[3])),
-                                         fadd2(make_float2(y[4], y[5]), make_float2(y[6], y[7]))));
-                } else if constexpr (QK == Q_LOGITS) {
-                  lazy_sum(y, kt, mq, zq);
-                } else {
+            }
+            if constexpr (kQ) {
+              const unsigned char* sa = stage(stg, 0);
+              float y[8];
+              load8<TD>(reinterpret_cast<const TD*>(sa + kTB) + tid * kEPT, y);
+              if constexpr (QK == Q_PROBS_T1) {
+                zq2 = fadd2(zq2, fadd2(fadd2(make_float2(y[0], y[1]), make_float2(y[2], y[3])),
+                                       fadd2(make_float2(y[4], y[5]), make_float2(y[6], y[7]))));
+              } else if constexpr (QK == Q_LOGITS) {
+                lazy_sum(y, kt, mq, zq);
+              } else {
   #pragma unroll
-                  for (int i = 0; i < 8; ++i) y[i] = lg2(y[i]);
-                  lazy_sum(y, invT, mq, zq);
-                }
+                for (int i = 0; i < 8; ++i) y[i] = lg2(y[i]);
+                lazy_sum(y, invT, mq, zq);
               }
             }
             if constexpr (kB) {
@@ -801,9 +810,13 @@ __global__ void __launch_bounds__(kThreads, 1) unit_stream(StreamParams P) {
         else if (needR) chunk_loop(fA, fQ, Yes{}, Yes{});
         else chunk_loop(fA, fQ, Yes{}, No{});
       };
-      if (!hA) with_b(No{}, No{});
-      else if (qa >= 0 && !qlse) with_b(Yes{}, Yes{});
-      else with_b(Yes{}, No{});
+      // pass A: the target row unless its normaliser is given, the draft
+      // row unless its normaliser is given (or the row has none)
+      const bool pA = hA && !plse, pQ = hA && qa >= 0 && !qlse;
+      if (pA && pQ) with_b(Yes{}, Yes{});
+      else if (pA) with_b(Yes{}, No{});
+      else if (pQ) with_b(No{}, Yes{});
+      else with_b(No{}, No{});
 
       // 5. CTA reductions; alpha partial of row j - 1; exchange
       const float acc_a = acc_a2.x + acc_a2.y, acc_r = acc_r2.x + acc_r2.y;
@@ -1278,7 +1291,7 @@ inline bool geometry(int V, int tsz, int dsz, int* C, int* slice, int* nch, int*
   const int64_t stage = 2LL * kCH * (tsz + dsz);
   const int ns = (int)(kRing / stage);
   if (ns < 2) return false;
-  const bool single = sms > 0 && passA > 0 && rows >= sms &&
+  const bool single = sms > 0 && rows >= sms &&
                       (int64_t)sms * V * passA <= kL2Keep;
   for (int c = single ? 1 : 2; c <= kMaxC; c *= 2) {
     const int sl = ((V + c - 1) / c + 7) / 8 * 8;

@@ -18,6 +18,11 @@ Workloads (sizes and distributions):
                 filled to level widths (4,12,16,14,8,6); target bf16 [B,61,V]
                 ~ N(0, 2^2); draft probs fp32 = softmax(target + N(0, 0.8^2));
                 T = 1; sibling tokens drawn without replacement from q.
+  lmhead_tree   the tree_static tree, batch and draft rule, with the target
+                logits coming from hidden states: hidden [B,61,H=4096] bf16
+                ~ N(0, 1), LM head W [V,H] bf16 ~ N(0, (2/sqrt(H))^2) (logits
+                of std about 2); the stand-in drafter perturbs the float32
+                product h W^T (torch matmul, input generation only).
   eagle2        B=128, V=128256 bf16; draft rows [B,51,V] ~ N(0, 2.5^2);
                 target row = its draft row + N(0, 1) (rows without a draft
                 row: fresh N(0, 2.5^2) + N(0, 1)); depth 6, 10 children, keep
@@ -56,6 +61,7 @@ class Workload:
     topk: int = 10
     width: int = 10
     total: int = 60
+    H: int = 0                 # hidden size (LM-head workloads)
 
 
 WORKLOADS = {
@@ -73,6 +79,11 @@ WORKLOADS = {
                             target_std=2.0, draft_noise=0.8, seed=1237,
                             branching=(4, 3, 2, 2, 1, 1),
                             widths=(4, 12, 16, 14, 8, 6)),
+    "lmhead_tree": Workload("lmhead_tree", 32, 60, V_LLAMA3, torch.bfloat16,
+                            torch.float32, 1.0, draft_kind="probs",
+                            target_std=2.0, draft_noise=0.8, seed=1239,
+                            branching=(4, 3, 2, 2, 1, 1),
+                            widths=(4, 12, 16, 14, 8, 6), H=4096),
     "eagle2": Workload("eagle2", 128, 60, V_LLAMA3, torch.bfloat16,
                        torch.bfloat16, 0.8, target_std=2.5, draft_noise=1.0,
                        seed=1238),
@@ -189,11 +200,40 @@ def tree_inputs(w: Workload, device="cpu", parent=None):
     tgt = _normal((B, N + 1, V), w.target_std, g, device)
     noisy = tgt + _normal((B, N + 1, V), w.draft_noise, g, device)
     target = tgt.to(w.target_dtype)
+    del tgt
+    draft, q_row, tokens, par = _tree_draft(w, noisy, parent, device)
+    return target, draft, q_row, tokens, par
+
+
+def lmhead_tree_inputs(w: Workload, device="cpu", parent=None):
+    """hidden [B,N+1,H] bf16, w_vocab [V,H] bf16, draft [B,N+1,V], q_row,
+    node_tokens [B,N], parent [B,N] (the static tree)."""
+    if parent is None:
+        parent = static_tree(w, device)
+    parent = parent.to(device)
+    N = parent.numel()
+    B, V, H = w.B, w.V, w.H
+    g = _gen(device, w.seed)
+    hidden = _normal((B, N + 1, H), 1.0, g, device).to(torch.bfloat16)
+    wv = _normal((V, H), w.target_std / H ** 0.5, g, device).to(
+        torch.bfloat16)
+    # the stand-in drafter sees a perturbed copy of the target's logits
+    noisy = torch.matmul(hidden.float(), wv.float().t())
+    noisy += _normal((B, N + 1, V), w.draft_noise, g, device)
+    draft, q_row, tokens, par = _tree_draft(w, noisy, parent, device)
+    return hidden, wv, draft, q_row, tokens, par
+
+
+def _tree_draft(w: Workload, noisy, parent, device):
+    """Draft rows from the drafter's logits, the identity q_row, sibling
+    tokens drawn without replacement from q, and the batch's parent rows."""
+    B, N1, V = noisy.shape
+    N = N1 - 1
     if w.draft_kind == "probs":
         draft = torch.softmax(noisy, dim=-1).to(w.draft_dtype)
     else:
         draft = noisy.to(w.draft_dtype)
-    del tgt, noisy
+    del noisy
     q_row = torch.arange(N + 1, dtype=torch.int32, device=device)
     q_row = q_row.unsqueeze(0).expand(B, N + 1).contiguous()
     # siblings drawn without replacement from the parent row's q
@@ -211,7 +251,7 @@ def tree_inputs(w: Workload, device="cpu", parent=None):
             draws = torch.topk(draft[:, r].float(), len(ks), dim=-1).indices
         tokens[:, ks] = draws.to(torch.int32)
     par = parent.unsqueeze(0).expand(B, N).contiguous()
-    return target, draft, q_row, tokens, par
+    return draft, q_row, tokens, par
 
 
 # ------------------------------------------------------------------ EAGLE-2

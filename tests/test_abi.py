@@ -223,6 +223,46 @@ def test_tree_attention_argument_errors(lib):
     assert call(B=0, q=None, out=None) == lib.SPEC_OK
 
 
+def test_lm_head_argument_errors(lib):
+    f = lib.raw
+    ws_ok = lib.raw("spec_workspace_bytes", lib.SPEC_OP_LMHEAD, 10, 0, 1000)
+    assert ws_ok > 10 * 4 * 8 and ws_ok % 256 == 0
+    assert f("spec_workspace_bytes", lib.SPEC_OP_LMHEAD, 10, 3, 1000) == 0
+    t = lib.raw("spec_workspace_bytes", lib.SPEC_OP_TREE_LMHEAD, 2, 5, 1000)
+    # the logits of every tree row are part of the workspace
+    assert t > lib.raw("spec_workspace_bytes", lib.SPEC_OP_TREE, 2, 5,
+                       1000) + 2 * 6 * 1000 * 2
+
+    def lm(M=10, H=64, V=1000, T=1.0, hidden=FAKE, w=FAKE, out=FAKE,
+           lse=None, ws=FAKE, nbytes=None):
+        return f("spec_lm_head", hidden, w, M, H, V, ctypes.c_float(T), out,
+                 lse, ws, ws_ok if nbytes is None else nbytes, None)
+    assert lm(M=-1) == lib.SPEC_ERR_SHAPE
+    assert lm(V=0) == lib.SPEC_ERR_SHAPE
+    assert lm(H=0) == lib.SPEC_ERR_SHAPE
+    assert lm(T=-1.0) == lib.SPEC_ERR_ARG
+    assert lm(T=0.0, lse=FAKE) == lib.SPEC_ERR_ARG  # normalisers need T > 0
+    assert lm(out=None) == lib.SPEC_ERR_ARG
+    assert lm(H=60) == lib.SPEC_ERR_UNSUPPORTED       # rows not 16-byte multiples
+    assert lm(w=ctypes.c_void_p(0x7f0000000008)) == lib.SPEC_ERR_UNSUPPORTED
+    assert lm(nbytes=ws_ok - 1) == lib.SPEC_ERR_WORKSPACE
+    assert lm(ws=ctypes.c_void_p(0x7f0000000010)) == lib.SPEC_ERR_WORKSPACE
+
+    prm = _prm(lib)
+
+    def tree(B=2, N=5, R=6, V=1000, H=64, hidden=FAKE, nbytes=None, p=prm):
+        return f("spec_verify_tree_lmhead", hidden, FAKE, H, FAKE, FAKE, FAKE,
+                 FAKE, B, N, R, V, 0, ctypes.byref(p), FAKE, FAKE, FAKE,
+                 FAKE, None, FAKE, t if nbytes is None else nbytes, None)
+    assert tree(B=-1) == lib.SPEC_ERR_SHAPE
+    assert tree(N=5000) == lib.SPEC_ERR_SHAPE
+    assert tree(H=12) == lib.SPEC_ERR_UNSUPPORTED
+    assert tree(hidden=None) == lib.SPEC_ERR_ARG
+    assert tree(nbytes=t - 256) == lib.SPEC_ERR_WORKSPACE
+    assert tree(p=_prm(lib, flags=1)) == lib.SPEC_ERR_ARG
+    assert tree(p=_prm(lib, top_k=500)) == lib.SPEC_ERR_UNSUPPORTED
+
+
 @pytest.mark.parametrize("lang,std", [("c", "c99"), ("c++", "c++11")])
 def test_header_compiles_for_plain_c_and_cpp_callers(tmp_path, lang, std):
     # the boundary is a C ABI: the header must stand alone in C and C++

@@ -55,9 +55,19 @@ def test_verify_wrappers_match_their_signatures(captured):
     api.spec_tree_mask(par, bits=True)
     api.spec_eagle2_expand_rerank(torch.zeros(B, 51, V, dtype=torch.bfloat16),
                                   temperature=0.8)
+    H = 64
+    api.spec_lm_head(torch.zeros(B, N + 1, H, dtype=torch.bfloat16),
+                     torch.zeros(V, H, dtype=torch.bfloat16), temperature=1.0,
+                     row_lse=True)
+    api.spec_verify_tree_lmhead(torch.zeros(B, N + 1, H, dtype=torch.bfloat16),
+                                torch.zeros(V, H, dtype=torch.bfloat16), dd,
+                                qr, nt, par, temperature=1.0,
+                                draft_kind="probs")
     assert [c[0] for c in captured] == ["spec_verify_chain", "spec_verify_tree",
                                         "spec_tree_mask",
-                                        "spec_eagle2_expand_rerank"]
+                                        "spec_eagle2_expand_rerank",
+                                        "spec_lm_head",
+                                        "spec_verify_tree_lmhead"]
 
 
 def test_post_verification_wrappers_match_their_signatures(captured):
