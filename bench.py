@@ -19,9 +19,14 @@ bounded sample of the same workload on the host cores.
 
 from __future__ import annotations
 
+import os
+
+# the CPU legs time the oracle on one thread (numpy's BLAS included)
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
 import argparse
 import json
-import os
 import statistics
 import subprocess
 import sys
@@ -43,8 +48,8 @@ def _args():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default=DEFAULT_WORKLOAD,
                    choices=["tree_static", "greedy", "eagle2", "chain_topk",
-                            "chain_sample", "kv_commit", "accept_stats",
-                            "tree_attention"])
+                            "chain_sample", "lmhead_tree", "kv_commit",
+                            "accept_stats", "tree_attention"])
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -63,7 +68,8 @@ def _args():
 
 # Verification workloads timed beside the headline one (each is one of the
 # pages' configurations; see synth.workload).
-OTHER_CONFIGS = ("greedy", "eagle2", "chain_topk", "chain_sample")
+OTHER_CONFIGS = ("greedy", "eagle2", "chain_topk", "chain_sample",
+                 "lmhead_tree")
 L2_BYTES = 129 * 2**20  # GB300 L2 (about 129 MB)
 
 
@@ -134,6 +140,52 @@ def _traffic(name, units):
     if not t or t["hash"] != _src_hash(t["src"]):
         return None
     return int(t["bytes_per_unit"] * units)
+
+
+def _tensor_peak():
+    """Dense bf16 tensor peak (TFLOP/s) for a kernel timed inside a long
+    step: the measured sustained figure, else the fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops_sustained"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1700.0, "fallback"
+
+
+def roofline_of(work, kern_ms, peak, peak_kind, rc, name):
+    """Roofline object of the step's dominant kernel."""
+    if work.bound == "tensor":
+        tpk, tkind = _tensor_peak()
+        tf = work.kernel_flops / (kern_ms / 1e3) / 1e12
+        return {"bound": "tensor", "achieved": round(tf, 1), "peak": tpk,
+                "unit": "TFLOP/s", "frac": round(tf / tpk, 4),
+                "traffic": _traffic(name, work.kernel_units),
+                "kernel": work.kernel_name,
+                "flops_per_launch": work.kernel_flops,
+                "bytes_per_launch": work.kernel_bytes,
+                "avg_launch_ms": round(kern_ms, 5),
+                "peak_source": f"{tkind} (bf16_tflops_sustained)",
+                "profile_rc": rc}
+    achieved = work.kernel_bytes / (kern_ms / 1e3) / 1e9
+    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+            "unit": "GB/s", "frac": round(achieved / peak, 4),
+            "traffic": _traffic(name, work.kernel_units),
+            "kernel": work.kernel_name,
+            "bytes_per_launch": work.kernel_bytes,
+            "avg_launch_ms": round(kern_ms, 5), "peak_source": peak_kind,
+            "profile_rc": rc}
+
+
+def verify_kernel(h, lib, work, peak):
+    """The verification kernel's share beside an LM-head GEMM."""
+    vms, nv, _ = kernel_time(h, lib.SPEC_PROF_VERIFY)
+    if not nv:
+        return {}
+    gbs = work.verify_bytes / (vms / 1e3) / 1e9
+    return {"unit_stream": {"avg_launch_ms": round(vms, 5),
+                            "bytes_per_launch": work.verify_bytes,
+                            "achieved_gbs": round(gbs, 1),
+                            "frac": round(gbs / peak, 4)}}
 
 
 def _peaks():
@@ -254,6 +306,35 @@ class Work:
             self.expand_bytes = B * self.R * V * 2
             # expand rows, select, mask, row records, verification, walk
             self.launches_per_step = 6
+        elif name == "lmhead_tree":
+            # the static tree with the target logits from the LM head
+            self.kind = "lmhead"
+            (self.hidden, self.wv, self.draft, self.q_row, self.toks,
+             self.parent) = synth.lmhead_tree_inputs(w, device)
+            B, N, V, H = w.B, self.toks.shape[1], w.V, w.H
+            self.N = N
+            self.rows = B * (N + 1)
+            self.kernel_units = self.rows
+            self.ws = api.workspace(_lib.SPEC_OP_TREE_LMHEAD, B, N, V, device)
+            self.out = (torch.empty(B, dtype=torch.int32, device=device),
+                        torch.empty(B, N, dtype=torch.int32, device=device),
+                        torch.empty(B, N + 1, dtype=torch.int32, device=device),
+                        torch.empty(B, N + 1, dtype=torch.float32,
+                                    device=device))
+            self.mask = torch.empty(B, N, N, dtype=torch.uint8, device=device)
+            self.inputs = [self.hidden, self.wv, self.draft, self.q_row,
+                           self.toks, self.parent]
+            self.resident = {1}  # the LM head's weights stay in HBM
+            self.prof_kind = _lib.SPEC_PROF_LMHEAD
+            self.kernel_name = "lmhead_gemm"
+            self.bound = "tensor"
+            self.kernel_flops = 2 * self.rows * H * V
+            # reads hidden and W, writes the bf16 logits
+            self.kernel_bytes = (self.rows * H + V * H + self.rows * V) * 2
+            # the verifier then reads the logits and draft rows once each
+            self.verify_bytes = self.rows * V * (2 + self.draft.element_size())
+            # mask, GEMM, normaliser merge, row records, verification, walk
+            self.launches_per_step = 6
         else:
             raise SystemExit(f"workload {name} is not wired into the bench")
 
@@ -286,6 +367,17 @@ class Work:
                                  temperature=w.temperature,
                                  seed=w.decision_seed, out=self.out,
                                  ws=self.ws, draft_lse=self.lse)
+        elif self.kind == "lmhead":
+            from speculative_decoding_verification_tree_gb300.api import (
+                _ptr, _stream)
+            B, N = self.w.B, self.N
+            self.lib.call("spec_tree_mask", _ptr(x[5]), B, N, _ptr(self.mask),
+                          None, _stream(None))
+            api.spec_verify_tree_lmhead(x[0], x[1], x[2], x[3], x[4], x[5],
+                                        temperature=w.temperature,
+                                        draft_kind=w.draft_kind,
+                                        seed=w.decision_seed, out=self.out,
+                                        ws=self.ws)
         else:
             from speculative_decoding_verification_tree_gb300.api import (
                 _ptr, _stream)
@@ -298,8 +390,14 @@ class Work:
                                  seed=w.decision_seed, out=self.out,
                                  ws=self.ws)
 
+    bound = "hbm"
+    resident = frozenset()
+
     def host_copy(self):
         """The step's inputs on the host, for the CPU oracle."""
+        if self.kind == "lmhead":
+            keys = ["hidden", "w", "draft", "q_row", "toks", "parent"]
+            return self.w, {k: x.cpu() for k, x in zip(keys, self.inputs)}
         if self.kind == "eagle2":
             return self.w, {"draft": self.draft.cpu(),
                             "target": self.target.cpu()}
@@ -385,6 +483,18 @@ def oracle_step(w, host, seqs):
     from oracle.chain import verify_chain
     from oracle.eagle2 import expand_rerank
     from oracle.tree import tree_mask, verify_tree
+    if w.name == "lmhead_tree":
+        from oracle.lmhead import verify_tree_lmhead
+        if "w64" not in host:  # the LM head in float64, converted once
+            host["w64"] = host["w"].float().numpy().astype(np.float64)
+        par = host["parent"][seqs].numpy()
+        res = verify_tree_lmhead(
+            host["hidden"][seqs].float().numpy().astype(np.float64),
+            host["w64"], host["draft"][seqs].float().numpy().astype(
+                np.float64), host["q_row"][seqs].numpy(),
+            host["toks"][seqs].numpy(), par, temperature=w.temperature,
+            draft_kind=w.draft_kind, seed=w.decision_seed, batch_ids=seqs)
+        return len(seqs) * (par.shape[1] + 1), res.ref
     t = host["target"][seqs].float().numpy().astype(np.float64)
     if w.name == "eagle2":
         d = host["draft"][seqs].float().numpy().astype(np.float64)
@@ -422,6 +532,10 @@ def host_inputs(name, nseq=8):
     if name in ("greedy", "chain_topk", "chain_sample"):
         t, d, k = synth.chain_inputs(w, "cpu")
         return w, {"target": t, "draft": d, "toks": k}
+    if name == "lmhead_tree":
+        hd, wv, d, q, k, p = synth.lmhead_tree_inputs(w, "cpu")
+        return w, {"hidden": hd, "w": wv, "draft": d, "q_row": q, "toks": k,
+                   "parent": p}
     if name == "eagle2":
         import torch
         d = synth.eagle2_draft(w, "cpu")
@@ -591,6 +705,9 @@ def run_config(torch, h, lib, name, dev, steps, peak, peak_kind):
     ms = time_steps(torch, work, steps, flush)
     kern_ms, nl, rc = kernel_time(h, work.prof_kind)
     other = {}
+    if work.kind == "lmhead":
+        other["unit_stream"] = verify_kernel(h, lib, work, peak).get(
+            "unit_stream")
     if work.kind == "eagle2":
         ems, n2, _ = kernel_time(h, lib.SPEC_PROF_EXPAND)
         if n2:
@@ -610,7 +727,13 @@ def run_config(torch, h, lib, name, dev, steps, peak, peak_kind):
          "avg_launch_ms": None if kern_ms is None else round(kern_ms, 5),
          "bytes_per_launch": work.kernel_bytes, "profile_rc": rc,
          "gpu_launches": work.launches_per_step * steps}
-    if kern_ms:
+    if kern_ms and work.bound == "tensor":
+        r = roofline_of(work, kern_ms, peak, peak_kind, rc, name)
+        d.update({"bound": "tensor", "achieved_tflops": r["achieved"],
+                  "peak_tflops": r["peak"], "peak_source": r["peak_source"],
+                  "frac": r["frac"], "flops_per_launch": work.kernel_flops})
+        d["other_kernels"] = verify_kernel(h, lib, work, peak)
+    elif kern_ms:
         gbs = work.kernel_bytes / (kern_ms / 1e3) / 1e9
         d.update({"achieved_gbs": round(gbs, 1), "peak_gbs": peak,
                   "peak_source": peak_kind, "frac": round(gbs / peak, 4)})
@@ -687,6 +810,8 @@ def main():
     kern_ms, nl, rc = kernel_time(h, work.prof_kind)
     peak, peak_kind = _peaks()
     other = {}
+    if work.kind == "lmhead":
+        other = verify_kernel(h, _lib, work, peak)
     if work.kind == "eagle2":
         ems_k, n2, _ = kernel_time(h, _lib.SPEC_PROF_EXPAND)
         if n2:
@@ -712,24 +837,18 @@ def main():
 
     roof = None
     if kern_ms:
-        achieved = work.kernel_bytes / (kern_ms / 1e3) / 1e9
-        roof = {"bound": "hbm", "achieved": round(achieved, 1),
-                "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4),
-                "traffic": _traffic(args.workload, work.kernel_units),
-                "kernel": work.kernel_name,
-                "bytes_per_launch": work.kernel_bytes,
-                "avg_launch_ms": round(kern_ms, 5),
-                "peak_source": peak_kind, "profile_rc": rc,
-                "other_kernels": other}
+        roof = roofline_of(work, kern_ms, peak, peak_kind, rc, args.workload)
+        roof["other_kernels"] = other
 
     # end to end through the public API from pinned host buffers
     e2e = None
     if not args.no_e2e:
-        host_in = [None if x is None else x.cpu().pin_memory()
-                   for x in work.inputs]
-        dev_in = [None if x is None else torch.empty_like(x)
-                  for x in work.inputs]
+        # inputs resident in HBM across steps (model weights) are not copied
+        host_in = [None if (x is None or i in work.resident) else
+                   x.cpu().pin_memory() for i, x in enumerate(work.inputs)]
+        dev_in = [x if i in work.resident else
+                  (None if x is None else torch.empty_like(x))
+                  for i, x in enumerate(work.inputs)]
         host_out = [o.cpu().pin_memory() for o in work.outputs()]
         h2d = sum(x.numel() * x.element_size() for x in host_in
                   if x is not None)
@@ -738,7 +857,7 @@ def main():
 
         def e2e_step():
             for d, s in zip(dev_in, host_in):
-                if d is not None:
+                if d is not None and s is not None:
                     d.copy_(s, non_blocking=True)
             work.step(dev_in)
             for d, s in zip(host_out, work.outputs()):
@@ -787,7 +906,7 @@ def main():
         cclk.start()
         for name in OTHER_CONFIGS:
             n = {"greedy": 1000, "eagle2": 300, "chain_topk": 500,
-                 "chain_sample": 500}[name]
+                 "chain_sample": 500, "lmhead_tree": 100}[name]
             if args.steps is not None:  # short runs (profiler captures)
                 n = max(10, min(n, args.steps))
             configs[name] = run_config(torch, h, _lib, name, dev, n, peak,

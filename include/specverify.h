@@ -404,10 +404,14 @@ int spec_accept_stats(const int32_t* count, const int32_t* parent,
  * prefix_len is clamped to [0, S - N].
  * Errors: SPEC_ERR_SHAPE unless 1 <= N <= 64, Hq % Hkv == 0, S >= N and
  * B, Hkv <= 65535;
- * SPEC_ERR_UNSUPPORTED unless D == 128; SPEC_ERR_ARG for scale <= 0 or not
- * finite, a NULL pointer (B > 0), caches not 16-byte aligned, q, out or
- * prefix_len not 4-byte aligned, or mask_bits not 8-byte aligned.  B == 0
- * does nothing.
+ * SPEC_ERR_UNSUPPORTED unless D == 128, or when q or out is not 16-byte
+ * aligned (rows are moved as 16-byte words); SPEC_ERR_ARG for scale <= 0 or
+ * not finite, a NULL pointer (B > 0), caches not 16-byte aligned, q, out or
+ * prefix_len not 4-byte aligned, or mask_bits not 8-byte aligned;
+ * SPEC_ERR_SHAPE when B * Hkv * S reaches 2^31 cache rows; SPEC_ERR_CUDA if
+ * the caches cannot be described to the copy engine.  B == 0 does nothing.
+ * Runs on the tensor cores (tcgen05): one CTA per 256 query rows of one
+ * (sequence, key/value head).
  */
 int spec_tree_attention(const void* q, const void* k_cache,
                         const void* v_cache, const int32_t* prefix_len,

@@ -11,62 +11,166 @@
 //
 // with grouped-query heads (query head h reads key/value head h / (Hq/Hkv)).
 //
-// Organisation (head dim 128, bf16, fp32 accumulation).  A CTA takes 64 query
-// rows of one (sequence, key/value head): the rows are (node, head in the
-// group) pairs, node-major, so the G query heads that share a key/value head
-// are served by one read of its keys and values.  Four warps of 16 rows each
-// run the FlashAttention-2 recurrence on tensor cores (mma.sync m16n8k16
-// bf16): S = Q K^T per 64-key tile from a double-buffered cp.async ring in
-// shared memory (K fragments by ldmatrix, V fragments by ldmatrix.trans), the
-// tree mask applied only in tiles that reach the drafted positions, an
-// online base-2 softmax in registers, and P V accumulated in registers.
+// Organisation (head dim 128, bf16 inputs, float32 accumulation) on the
+// fifth-generation tensor cores.  A CTA takes up to 256 query rows of one
+// (sequence, key/value head) -- the rows are (node, head in the group) pairs,
+// node-major, so the G query heads that share a key/value head are served by
+// one stream of its keys and values -- as two 128-row tiles:
+//   warp 0     TMA producer: 64-key blocks of K and V (128-byte swizzle) into
+//              a 3-stage shared-memory ring;
+//   warp 1     allocates TMEM and issues, per key block and tile t,
+//              S_t = Q_t K^T (tcgen05.mma M 128, N 64, K 128) and, once the
+//              softmax has written P_t, O_t += P_t V (M 128, N 128, K 64; V is
+//              the MN-major operand, read as stored);
+//   warps 2-9  softmax, one thread per query row (warp w reads TMEM lanes of
+//              quadrant w % 4): they stage Q once, then per block read S with
+//              tcgen05.ld, apply the scale and the tree mask, run the online
+//              base-2 softmax against a reference maximum that moves only when
+//              a row's maximum grows by more than 2^8 (then O_t is rescaled in
+//              TMEM), and write P as bf16 into 128-byte-swizzled shared memory
+//              for the next MMA; at the end O_t / l is rounded to bf16.
+// TMEM: S_t at columns 64 t, O_t at 128 + 128 t (384 of 512).  Every mbarrier
+// wait is bounded (SPEC_STATUS_TIMEOUT is not reported by this entry point,
+// which has no status word; a CTA that gives up stops waiting and still frees
+// its TMEM after waiting, bounded, for its own MMAs and copies).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 
 namespace sv {
 namespace {
 
-constexpr int kAD = 128;            // head dim
-constexpr int kAKeys = 64;          // keys per tile
-constexpr int kARows = 64;          // query rows per CTA (4 warps x 16)
-constexpr int kAThreads = 128;
-constexpr int kAPitch = kAD + 8;    // smem row pitch in bf16 (272 bytes: no bank conflicts)
-constexpr int kATile = kAKeys * kAPitch;  // bf16 elements per tile buffer
+constexpr int kAD = 128;   // head dim
+constexpr int kKB = 64;    // keys per block
+constexpr int kMT = 128;   // query rows per tile
+constexpr int kTiles = 2;  // tiles per CTA
+constexpr int kAStages = 3;
+constexpr int kQHalf = kMT * 64 * 2;     // 16 KB: 128 rows x 64 dims
+constexpr int kQTile = 2 * kQHalf;       // 32 KB
+constexpr int kKVHalf = kKB * 64 * 2;    // 8 KB: 64 keys x 64 dims
+constexpr int kKVTile = 2 * kKVHalf;     // 16 KB
+constexpr int kAStage = 2 * kKVTile;     // K then V: 32 KB
+constexpr int kPTile = kMT * kKB * 2;    // 16 KB: 128 rows x 64 keys
+constexpr int kOffKV = kTiles * kQTile;                  // 64 KB
+constexpr int kOffP = kOffKV + kAStages * kAStage;       // 160 KB
+constexpr int kOffBar = kOffP + kTiles * kPTile;         // 192 KB
+constexpr int kAThreads = 320;
+constexpr int kSoftThreads = 256;
+constexpr uint32_t kATmemCols = 512;
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-               "r"(src_bytes)
+struct __align__(8) AttnSmem {
+  uint64_t kvfull[kAStages], kvempty[kAStages];
+  uint64_t sfull[kTiles], pfull[kTiles], pdone[kTiles];
+  uint64_t qready, drain;
+  uint32_t tmem_base;
+  uint32_t dead;
+};
+constexpr size_t kASmemBytes = (size_t)kOffBar + sizeof(AttnSmem) + 1024;
+
+// S = Q K^T: M 128, N 64, bf16 K-major A and B, float32 D.
+constexpr uint32_t kIdescS = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kKB >> 3) << 17) |
+                             ((uint32_t)(kMT >> 4) << 24);
+// O += P V: M 128, N 128, A K-major, B MN-major (bit 16).
+constexpr uint32_t kIdescPV = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
+                              ((uint32_t)(kAD >> 3) << 17) | ((uint32_t)(kMT >> 4) << 24);
+
+__device__ __forceinline__ void await(AttnSmem& sm, uint64_t* bar, uint32_t parity) {
+  if (*(volatile uint32_t*)&sm.dead) return;
+  if (!mbar_wait_bounded(bar, parity)) *(volatile uint32_t*)&sm.dead = 1;
+}
+
+// K-major tile with 128-byte swizzle: rows of 64 bf16 (128 B), 8-row groups
+// 1024 B apart (start 1024-byte aligned; K steps add 32 B within a row).
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+// MN-major tile with 128-byte swizzle (V as stored: a key per 128-byte row of
+// 64 head dims): 64-dim column blocks kKVHalf apart (leading offset), 8-key
+// groups 1024 B apart (stride offset); K steps of 16 keys add 2048 B.
+__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(kKVHalf >> 4) << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+__device__ __forceinline__ void tma2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                      uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+      : "memory");
+}
+__device__ __forceinline__ void mma_f16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                        uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+// generic-proxy shared-memory writes made visible to the tensor cores
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+#define SV_R32(r)                                                                          \
+  "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),     \
+      "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),         \
+      "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),      \
+      "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),      \
+      "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),      \
+      "=r"(r[31])
+#define SV_W32(r)                                                                            \
+  "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),   \
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),     \
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),   \
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),   \
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+#define SV_REGS32                                                     \
+  "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18," \
+  "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}"
+
+__device__ __forceinline__ void tld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 " SV_REGS32 ", [%32];"
+               : SV_R32(r)
+               : "r"(taddr));
+}
+__device__ __forceinline__ void tst32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+               "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+               "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+               SV_W32(r)
                : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
+__device__ __forceinline__ void tld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                        uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                          uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-
-// D += A B, m16n8k16, bf16 inputs, fp32 accumulators.
-__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+__device__ __forceinline__ void tst_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // two floats -> bf16x2 (round to nearest even), lo in the low half
@@ -76,197 +180,286 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return r;
 }
 
-__global__ void __launch_bounds__(kAThreads, 3)
-    tree_attn_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ kc,
-                     const uint16_t* __restrict__ vc, const int32_t* __restrict__ prefix_len,
-                     const uint64_t* __restrict__ mask_bits, int N, int Hq, int Hkv, int S,
-                     float scale_log2, uint16_t* __restrict__ out) {
-  extern __shared__ __align__(16) uint16_t asmem[];
-  uint16_t* Ks = asmem;                // [2][64][kAPitch]
-  uint16_t* Vs = asmem + 2 * kATile;   // [2][64][kAPitch]
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int g = lane >> 2, t4 = lane & 3;
+// 16-byte chunk c (0..7) of row r inside a 128-byte-swizzled block
+__device__ __forceinline__ uint32_t swz(int r, int c) {
+  return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
+}
+
+__global__ void __launch_bounds__(kAThreads, 1)
+    tree_attn_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+                 const uint16_t* __restrict__ q, const int32_t* __restrict__ prefix_len,
+                 const uint64_t* __restrict__ mask_bits, int N, int Hq, int Hkv, int S,
+                 float scale_log2, uint16_t* __restrict__ out) {
+  extern __shared__ __align__(1024) unsigned char araw[];
+  const uint32_t raw = smem_u32(araw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  unsigned char* bp = araw + (base - raw);
+  AttnSmem& sm = *reinterpret_cast<AttnSmem*>(bp + kOffBar);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.z, kvh = blockIdx.y;
   const int G = Hq / Hkv, R = N * G;
-
+  const int row0 = blockIdx.x * (kTiles * kMT);
+  const int ntile = min(kTiles, (R - row0 + kMT - 1) / kMT);
   int P = prefix_len[b];
   P = P < 0 ? 0 : (P > S - N ? S - N : P);
-  const int L = P + N;  // keys of this sequence
-  const int64_t kvbase = ((int64_t)b * Hkv + kvh) * S * kAD;
+  const int L = P + N;
+  const int nblk = (L + kKB - 1) / kKB;
+  const int kvrow0 = (b * Hkv + kvh) * S;
 
-  // this thread's two rows (g and g + 8 of the warp's 16)
-  int node[2], hq[2];
-  bool valid[2];
-  uint64_t mb[2];
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int r = blockIdx.x * kARows + warp * 16 + g + 8 * h;
-    valid[h] = r < R;
-    node[h] = valid[h] ? r / G : 0;
-    hq[h] = kvh * G + (valid[h] ? r % G : 0);
-    mb[h] = valid[h] ? mask_bits[(int64_t)b * N + node[h]] : ~0ull;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kAStages; ++s) {
+      mbar_init(&sm.kvfull[s], 1);
+      mbar_init(&sm.kvempty[s], 1);
+    }
+    for (int t = 0; t < kTiles; ++t) {
+      mbar_init(&sm.sfull[t], 1);
+      mbar_init(&sm.pfull[t], kMT);
+      mbar_init(&sm.pdone[t], 1);
+    }
+    mbar_init(&sm.qready, kSoftThreads);
+    mbar_init(&sm.drain, 1);
+    sm.dead = 0;
+    fence_mbar_init();
   }
-  // Q fragments (A operand), 8 k-steps of 16 over the head dim
-  uint32_t qf[8][4];
-  {
-    const uint32_t* q0 =
-        reinterpret_cast<const uint32_t*>(q + (((int64_t)b * N + node[0]) * Hq + hq[0]) * kAD);
-    const uint32_t* q1 =
-        reinterpret_cast<const uint32_t*>(q + (((int64_t)b * N + node[1]) * Hq + hq[1]) * kAD);
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      const int c = kk * 8 + t4;  // 32-bit word: elements kk*16 + 2 t4, +1
-      qf[kk][0] = valid[0] ? q0[c] : 0u;
-      qf[kk][1] = valid[1] ? q1[c] : 0u;
-      qf[kk][2] = valid[0] ? q0[c + 4] : 0u;
-      qf[kk][3] = valid[1] ? q1[c + 4] : 0u;
-    }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&sm.tmem_base)),
+                 "r"(kATmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = sm.tmem_base;
 
-  float o[16][4];
-#pragma unroll
-  for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
-  float m[2] = {neg_inf(), neg_inf()}, l[2] = {0.f, 0.f};
-
-  // one tile of keys and values into buffer `buf` (keys past L are zeros)
-  auto load_tile = [&](int tile, int buf) {
-    const uint32_t kd = smem_u32(Ks + buf * kATile), vd = smem_u32(Vs + buf * kATile);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int c = tid + i * kAThreads;  // 16-byte chunk: key c / 16, column (c % 16) * 8
-      const int kr = c >> 4, col = (c & 15) * 8;
-      const int key = tile * kAKeys + kr;
-      const bool ok = key < L;
-      const int64_t src = kvbase + (int64_t)(ok ? key : 0) * kAD + col;
-      const uint32_t off = (uint32_t)((kr * kAPitch + col) * 2);
-      cp_async16(kd + off, kc + src, ok ? 16u : 0u);
-      cp_async16(vd + off, vc + src, ok ? 16u : 0u);
-    }
-    cp_async_commit();
-  };
-
-  const int ntile = (L + kAKeys - 1) / kAKeys;
-  load_tile(0, 0);
-  for (int tile = 0; tile < ntile; ++tile) {
-    const int buf = tile & 1;
-    if (tile + 1 < ntile) {
-      load_tile(tile + 1, buf ^ 1);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
-    __syncthreads();
-    const uint32_t kb = smem_u32(Ks + buf * kATile), vb = smem_u32(Vs + buf * kATile);
-
-    // S = Q K^T for 64 keys: 8 key groups of 8 (n) x 8 head-dim steps (k)
-    float s[8][4];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
-#pragma unroll
-      for (int k2 = 0; k2 < 4; ++k2) {
-        // matrices: (keys 8j.., dims 32 k2 + 8 mi), mi = lane / 8
-        const uint32_t addr =
-            kb + (uint32_t)(((j * 8 + (lane & 7)) * kAPitch + k2 * 32 + (lane >> 3) * 8) * 2);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(addr, b0, b1, b2, b3);
-        mma_bf16(s[j], qf[2 * k2], b0, b1);
-        mma_bf16(s[j], qf[2 * k2 + 1], b2, b3);
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      for (int j = 0; j < nblk; ++j) {
+        const int s = j % kAStages;
+        await(sm, &sm.kvempty[s], ((uint32_t)(j / kAStages) & 1u) ^ 1u);
+        mbar_expect_tx(&sm.kvfull[s], (uint32_t)kAStage);
+        const uint32_t st = base + kOffKV + (uint32_t)(s * kAStage);
+        const int y = kvrow0 + j * kKB;
+        tma2d(st, &map_k, 0, y, &sm.kvfull[s]);
+        tma2d(st + kKVHalf, &map_k, 64, y, &sm.kvfull[s]);
+        tma2d(st + kKVTile, &map_v, 0, y, &sm.kvfull[s]);
+        tma2d(st + kKVTile + kKVHalf, &map_v, 64, y, &sm.kvfull[s]);
+      }
+      // this CTA's last copy into each stage has landed before it exits
+      for (int s = 0; s < kAStages && s < nblk; ++s) {
+        const int fills = (nblk - s + kAStages - 1) / kAStages;
+        mbar_wait_bounded(&sm.kvfull[s], (uint32_t)(fills - 1) & 1u);
       }
     }
-    // scale to base 2; mask where the tile reaches the drafted positions
-    const int key0 = tile * kAKeys;
-    const bool masked = key0 + kAKeys > P;
-    float mx[2] = {neg_inf(), neg_inf()};
+  } else if (warp == 1) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      await(sm, &sm.qready, 0);
+      fence_after();
+      for (int j = 0; j < nblk; ++j) {
+        const int s = j % kAStages;
+        const uint32_t ph = (uint32_t)(j & 1);
+        await(sm, &sm.kvfull[s], (uint32_t)(j / kAStages) & 1u);
+        const uint32_t kst = base + kOffKV + (uint32_t)(s * kAStage);
+        const uint32_t vst = kst + kKVTile;
+        const int tail = L - j * kKB;  // keys of this block that exist
+        if (tail < kKB) {
+          // cache rows past the sequence's keys hold anything (NaN included);
+          // their P is 0, but 0 * NaN is not, so their V rows become zeros
+          unsigned char* vz = bp + kOffKV + s * kAStage + kKVTile;
+          for (int rr = tail; rr < kKB; ++rr)
+            for (int hb = 0; hb < 2; ++hb) {
+              uint4* z = reinterpret_cast<uint4*>(vz + hb * kKVHalf + rr * 128);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int h = e >> 1;
-        float v = s[j][e] * scale_log2;
-        if (masked) {
-          const int key = key0 + j * 8 + 2 * t4 + (e & 1);
-          const int tj = key - P;
-          const bool vis = key < P || (tj < N && ((mb[h] >> tj) & 1ull));
-          if (!vis) v = neg_inf();
+              for (int c = 0; c < 8; ++c) z[c] = make_uint4(0u, 0u, 0u, 0u);
+            }
+          fence_async_smem();
         }
-        s[j][e] = v;
-        mx[h] = fmaxf(mx[h], v);
+        fence_after();
+        for (int t = 0; t < ntile; ++t) {
+          const uint32_t qt = base + (uint32_t)(t * kQTile);
+#pragma unroll
+          for (int k = 0; k < kAD / 16; ++k) {
+            const uint32_t off = (uint32_t)((k >> 2) * kQHalf + (k & 3) * 32);
+            const uint32_t koff = (uint32_t)((k >> 2) * kKVHalf + (k & 3) * 32);
+            mma_f16(tmem + (uint32_t)(64 * t), desc_kmajor(qt + off), desc_kmajor(kst + koff),
+                    kIdescS, k > 0 ? 1u : 0u);
+          }
+          mma_commit(&sm.sfull[t]);
+        }
+        for (int t = 0; t < ntile; ++t) {
+          await(sm, &sm.pfull[t], ph);
+          fence_after();
+          const uint32_t pt = base + kOffP + (uint32_t)(t * kPTile);
+#pragma unroll
+          for (int k = 0; k < kKB / 16; ++k)
+            mma_f16(tmem + 128u + (uint32_t)(128 * t), desc_kmajor(pt + (uint32_t)(k * 32)),
+                    desc_mnmajor(vst + (uint32_t)(k * 2048)), kIdescPV,
+                    (j > 0 || k > 0) ? 1u : 0u);
+          mma_commit(&sm.pdone[t]);
+        }
+        mma_commit(&sm.kvempty[s]);
+      }
+      mma_commit(&sm.drain);
+      mbar_wait_bounded(&sm.drain, 0);
+    }
+  } else {
+    // ------------------------------------------------------------- softmax
+    const int t = (warp - 2) >> 2;   // tile
+    const int qd = warp & 3;         // TMEM lane quadrant of this warp
+    const int r = qd * 32 + lane;    // row within the tile
+    const int gr = row0 + t * kMT + r;
+    const bool valid = t < ntile && gr < R;
+    const int node = valid ? gr / G : 0;
+    const int hq = kvh * G + (valid ? gr % G : 0);
+    const uint64_t mb = valid ? mask_bits[(int64_t)b * N + node] : 0ull;
+    const int64_t qoff = (((int64_t)b * N + node) * Hq + hq) * kAD;
+    {  // stage this row of Q (zeros for padding rows)
+      const uint4* src = reinterpret_cast<const uint4*>(q + qoff);
+      unsigned char* qt = bp + t * kQTile;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const uint4 v = valid ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(qt + (c >> 3) * kQHalf + swz(r, c & 7)) = v;
+      }
+      fence_async_smem();
+      mbar_arrive(&sm.qready);
+    }
+    if (t < ntile) {
+      const uint32_t lanes = (uint32_t)(qd * 32) << 16;
+      const uint32_t tS = tmem + lanes + (uint32_t)(64 * t);
+      const uint32_t tO = tmem + lanes + 128u + (uint32_t)(128 * t);
+      unsigned char* pt = bp + kOffP + t * kPTile;
+      float mref = neg_inf(), l = 0.f;
+      for (int j = 0; j < nblk; ++j) {
+        await(sm, &sm.sfull[t], (uint32_t)(j & 1));
+        fence_after();
+        uint32_t ra[32], rb[32];
+        tld32(tS, ra);
+        tld32(tS + 32u, rb);
+        tld_wait();
+        float s[64];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          s[i] = __uint_as_float(ra[i]) * scale_log2;
+          s[32 + i] = __uint_as_float(rb[i]) * scale_log2;
+        }
+        const int key0 = j * kKB;
+        if (!valid) {
+#pragma unroll
+          for (int i = 0; i < 64; ++i) s[i] = neg_inf();
+        } else if (key0 + kKB > P) {  // the block reaches the drafted positions
+#pragma unroll
+          for (int i = 0; i < 64; ++i) {
+            const int tj = key0 + i - P;
+            const bool vis = tj < 0 || (tj < N && ((mb >> tj) & 1ull));
+            if (!vis) s[i] = neg_inf();
+          }
+        }
+        float bm = neg_inf();
+#pragma unroll
+        for (int i = 0; i < 64; ++i) bm = fmaxf(bm, s[i]);
+        // the previous block's P V is done before P_t and O_t are touched
+        if (j > 0) await(sm, &sm.pdone[t], (uint32_t)((j - 1) & 1));
+        fence_after();
+        const bool move = bm > mref + 8.f;  // also the first visible key
+        if (__any_sync(0xffffffffu, move)) {
+          const float mnew = move ? bm : mref;
+          const float corr = (move && mref != neg_inf()) ? ex2(mref - mnew) : 1.f;
+          l *= corr;
+          if (j > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
+#pragma unroll 1
+            for (int c = 0; c < kAD / 32; ++c) {
+              uint32_t o[32];
+              tld32(tO + (uint32_t)(32 * c), o);
+              tld_wait();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
+              tst32(tO + (uint32_t)(32 * c), o);
+            }
+            tst_wait();
+          }
+          mref = mnew;
+        }
+        const float mu = mref == neg_inf() ? 0.f : mref;
+        uint32_t pk[32];
+        float ls = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float p0 = ex2(s[2 * i] - mu), p1 = ex2(s[2 * i + 1] - mu);
+          ls += p0 + p1;
+          pk[i] = pack_bf16(p0, p1);
+        }
+        l += ls;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(pt + swz(r, c)) =
+              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        fence_async_smem();
+        fence_before();
+        mbar_arrive(&sm.pfull[t]);
+      }
+      // O_t / l after the last P V
+      await(sm, &sm.pdone[t], (uint32_t)((nblk - 1) & 1));
+      fence_after();
+      const float inv = 1.f / l;
+      uint4* dst = reinterpret_cast<uint4*>(out + qoff);
+#pragma unroll 1
+      for (int c = 0; c < kAD / 32; ++c) {
+        uint32_t o[32];
+        tld32(tO + (uint32_t)(32 * c), o);
+        tld_wait();
+        if (valid) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const int i = 8 * v;
+            dst[4 * c + v] = make_uint4(
+                pack_bf16(__uint_as_float(o[i]) * inv, __uint_as_float(o[i + 1]) * inv),
+                pack_bf16(__uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv),
+                pack_bf16(__uint_as_float(o[i + 4]) * inv, __uint_as_float(o[i + 5]) * inv),
+                pack_bf16(__uint_as_float(o[i + 6]) * inv, __uint_as_float(o[i + 7]) * inv));
+          }
+        }
       }
     }
-    float corr[2], mu[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
-      mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
-      const float mn = fmaxf(m[h], mx[h]);
-      mu[h] = mn == neg_inf() ? 0.f : mn;  // no visible key yet: nothing to scale
-      corr[h] = ex2(m[h] - mu[h]);
-      m[h] = mn;
-      l[h] *= corr[h];
-    }
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      o[j][0] *= corr[0];
-      o[j][1] *= corr[0];
-      o[j][2] *= corr[1];
-      o[j][3] *= corr[1];
-    }
-    // P = 2^(s - m) as bf16 A fragments, 4 steps of 16 keys
-    uint32_t pf[4][4];
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      float p[2][4];
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int j = 2 * kk + hh;
-        p[hh][0] = ex2(s[j][0] - mu[0]);
-        p[hh][1] = ex2(s[j][1] - mu[0]);
-        p[hh][2] = ex2(s[j][2] - mu[1]);
-        p[hh][3] = ex2(s[j][3] - mu[1]);
-        l[0] += p[hh][0] + p[hh][1];
-        l[1] += p[hh][2] + p[hh][3];
-      }
-      pf[kk][0] = pack_bf16(p[0][0], p[0][1]);
-      pf[kk][1] = pack_bf16(p[0][2], p[0][3]);
-      pf[kk][2] = pack_bf16(p[1][0], p[1][1]);
-      pf[kk][3] = pack_bf16(p[1][2], p[1][3]);
-    }
-    // O += P V: 16 head-dim groups of 8 (n) x 4 key steps of 16 (k)
-#pragma unroll
-    for (int jd = 0; jd < 16; jd += 2) {
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        // matrices: (keys 16 kk + 8 (mi & 1), dims 8 jd + 8 (mi >> 1)), mi = lane / 8
-        const int mi = lane >> 3;
-        const uint32_t addr = vb + (uint32_t)(((kk * 16 + (mi & 1) * 8 + (lane & 7)) * kAPitch +
-                                               jd * 8 + (mi >> 1) * 8) * 2);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(addr, b0, b1, b2, b3);
-        mma_bf16(o[jd], pf[kk], b0, b1);
-        mma_bf16(o[jd + 1], pf[kk], b2, b3);
-      }
-    }
-    __syncthreads();  // the buffer is refilled by the next iteration's load
   }
+  fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kATmemCols)
+                 : "memory");
+  }
+}
 
-  // normalise and store: rows g (c0, c1) and g + 8 (c2, c3)
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    l[h] += __shfl_xor_sync(0xffffffffu, l[h], 1);
-    l[h] += __shfl_xor_sync(0xffffffffu, l[h], 2);
-  }
-  const float inv0 = 1.f / l[0], inv1 = 1.f / l[1];
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    if (!valid[h]) continue;
-    uint32_t* dst =
-        reinterpret_cast<uint32_t*>(out + (((int64_t)b * N + node[h]) * Hq + hq[h]) * kAD);
-    const float inv = h ? inv1 : inv0;
-#pragma unroll
-    for (int jd = 0; jd < 16; ++jd)
-      dst[jd * 4 + t4] = pack_bf16(o[jd][2 * h] * inv, o[jd][2 * h + 1] * inv);
-  }
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &qr) == cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// A cache [rows, 128] bf16 as 64-dim x 64-key boxes, 128-byte swizzle.
+bool cache_map(CUtensorMap* map, const void* base, int64_t rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)kAD, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)kAD * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)kKB};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -290,17 +483,22 @@ extern "C" int spec_tree_attention(const void* q, const void* k_cache, const voi
       ((uintptr_t)q | (uintptr_t)out | (uintptr_t)prefix_len) % 4 != 0 ||
       (uintptr_t)mask_bits % 8 != 0)
     return SPEC_ERR_ARG;
+  // rows of q / out are read and written as 16-byte words
+  if (((uintptr_t)q | (uintptr_t)out) % 16 != 0) return SPEC_ERR_UNSUPPORTED;
+  const int64_t rows = (int64_t)B * Hkv * S;
+  if (rows > ((int64_t)1 << 31) - kKB) return SPEC_ERR_SHAPE;
+  CUtensorMap mk, mv;
+  if (!cache_map(&mk, k_cache, rows) || !cache_map(&mv, v_cache, rows)) return SPEC_ERR_CUDA;
   const int R = N * (Hq / Hkv);
-  const dim3 grid((unsigned)((R + kARows - 1) / kARows), (unsigned)Hkv, (unsigned)B);
-  const size_t smem = (size_t)4 * kATile * sizeof(uint16_t);
-  if (cudaFuncSetAttribute(tree_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem) != cudaSuccess)
+  const dim3 grid((unsigned)((R + kTiles * kMT - 1) / (kTiles * kMT)), (unsigned)Hkv, (unsigned)B);
+  if (cudaFuncSetAttribute(tree_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kASmemBytes) != cudaSuccess)
     return SPEC_ERR_CUDA;
   cudaStream_t st = (cudaStream_t)stream;
   prof_begin(SPEC_PROF_ATTN, st);
-  tree_attn_kernel<<<grid, kAThreads, smem, st>>>(
-      (const uint16_t*)q, (const uint16_t*)k_cache, (const uint16_t*)v_cache, prefix_len,
-      mask_bits, N, Hq, Hkv, S, scale * kLog2e, (uint16_t*)out);
+  tree_attn_tc<<<grid, kAThreads, kASmemBytes, st>>>(
+      mk, mv, (const uint16_t*)q, prefix_len, mask_bits, N, Hq, Hkv, S, scale * kLog2e,
+      (uint16_t*)out);
   prof_end(SPEC_PROF_ATTN, st);
   return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
