@@ -91,6 +91,14 @@ extern "C" {
 #define SPEC_OP_LMHEAD 4       /* spec_lm_head: B = rows M, n = 0           */
 #define SPEC_OP_TREE_LMHEAD 5  /* spec_verify_tree_lmhead: n = N            */
 
+/* Test-only flag of spec_verify_tree_lmhead (SPEC_ERR_ARG elsewhere): the
+   LM-head kernel's copy producer withholds the first shared-memory stage, so
+   that the tensor-core issuer's bounded wait on it gives up (after about a
+   second), SPEC_STATUS_TIMEOUT is set and the call still completes.  It
+   exercises the failure path of the device waits without faulting anything;
+   the outputs of such a call are meaningless. */
+#define SPEC_FLAG_TEST_STALL 0x80000000u
+
 /* Sampling parameters (plain data, 40 bytes). */
 typedef struct spec_params {
   float temperature;      /* > 0: sampling rule; == 0: greedy argmax rule  */
@@ -101,7 +109,7 @@ typedef struct spec_params {
   int32_t draft_kind;     /* SPEC_DRAFT_LOGITS or SPEC_DRAFT_PROBS         */
   uint64_t seed;          /* Philox key                                    */
   uint32_t philox_offset; /* fourth Philox counter word                    */
-  uint32_t flags;         /* reserved, must be 0                           */
+  uint32_t flags;         /* 0, or SPEC_FLAG_TEST_STALL (tests only)       */
   /* Optional device array [B, R] float32 (NULL = unused): the log2
      normaliser log2 sum_v 2^(z_v log2(e) / temperature) of each draft row.
      spec_eagle2_expand_rerank writes it (the expand already sums every

@@ -42,6 +42,7 @@ SPEC_STATUS_CDF_FALLBACK = 16
 SPEC_STATUS_BAD_TREE = 32
 SPEC_STATUS_TOKEN_RANGE = 64
 SPEC_STATUS_TIMEOUT = 128
+SPEC_FLAG_TEST_STALL = 0x80000000
 
 SPEC_OP_CHAIN = 1
 SPEC_OP_TREE = 2

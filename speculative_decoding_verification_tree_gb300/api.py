@@ -75,13 +75,13 @@ def _on(dev):
 
 
 def params(temperature=1.0, top_k=0, top_p=1.0, draft_kind="logits", seed=0,
-           offset=0, draft_lse=None) -> SpecParams:
+           offset=0, draft_lse=None, flags=0) -> SpecParams:
     if draft_lse is not None:
         if draft_lse.dtype != torch.float32 or not draft_lse.is_contiguous():
             raise ValueError("draft_lse must be a contiguous float32 tensor")
     return SpecParams(float(temperature), int(top_k), float(top_p),
                       _KIND[draft_kind], int(seed) & (2**64 - 1),
-                      int(offset) & 0xFFFFFFFF, 0,
+                      int(offset) & 0xFFFFFFFF, int(flags) & 0xFFFFFFFF,
                       None if draft_lse is None else draft_lse.data_ptr())
 
 
@@ -196,7 +196,7 @@ def spec_verify_tree_lmhead(hidden, w_vocab, draft, q_row, node_tokens,
                             parent, *, temperature=1.0, top_k=0, top_p=1.0,
                             draft_kind="logits", seed=0, offset=0,
                             logits=None, out=None, ws=None, stream=None,
-                            draft_lse=None):
+                            draft_lse=None, flags=0):
     """Tree verification whose target logits are hidden [B, N+1, H] x
     w_vocab^T (bf16; see spec_verify_tree for the rest).  logits: an
     optional [B, N+1, V] bf16 tensor that receives the computed logits.
@@ -224,7 +224,7 @@ def spec_verify_tree_lmhead(hidden, w_vocab, draft, q_row, node_tokens,
     _device(hidden, w_vocab, draft, q_row, node_tokens, parent, logits,
             draft_lse, *out, ws, stream=stream)
     prm = params(temperature, top_k, top_p, draft_kind, seed, offset,
-                 draft_lse)
+                 draft_lse, flags)
     with _on(dev):
         _lib.call("spec_verify_tree_lmhead", _ptr(hidden), _ptr(w_vocab), H,
                   _ptr(draft), _ptr(q_row), _ptr(node_tokens), _ptr(parent),

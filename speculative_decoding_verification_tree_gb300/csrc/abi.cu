@@ -47,10 +47,10 @@ Eagle2Ws eagle2_ws(int B, int R) {
 
 bool dtype_ok(int d) { return d == SPEC_F32 || d == SPEC_BF16; }
 
-int check_params(const spec_params_t* prm, int V) {
+int check_params(const spec_params_t* prm, int V, uint32_t allowed_flags = 0) {
   if (!prm) return SPEC_ERR_ARG;
   if (!(prm->temperature >= 0.f) || !std::isfinite(prm->temperature)) return SPEC_ERR_ARG;
-  if (prm->flags != 0) return SPEC_ERR_ARG;
+  if ((prm->flags & ~allowed_flags) != 0) return SPEC_ERR_ARG;
   if (prm->draft_kind != SPEC_DRAFT_LOGITS && prm->draft_kind != SPEC_DRAFT_PROBS) return SPEC_ERR_DTYPE;
   if (prm->top_k < 0) return SPEC_ERR_ARG;
   if (!(prm->top_p > 0.f && prm->top_p <= 1.f)) return SPEC_ERR_ARG;
@@ -238,7 +238,7 @@ int spec_verify_tree_lmhead(const void* hidden, const void* w_vocab, int H, cons
                             void* workspace, size_t ws_bytes, void* stream) {
   if (B < 0 || N < 0 || V < 1 || R < 0 || H < 1) return SPEC_ERR_SHAPE;
   if (V > SPEC_MAX_VOCAB || N > SPEC_MAX_TREE_NODES) return SPEC_ERR_SHAPE;
-  int rc = check_params(prm, V);
+  int rc = check_params(prm, V, SPEC_FLAG_TEST_STALL);
   if (rc != SPEC_OK) return rc;
   if (prm->draft_lse && prm->temperature > 0.f &&
       (prm->draft_kind != SPEC_DRAFT_LOGITS || truncation_k(prm, V) > 0))
@@ -283,7 +283,8 @@ int spec_verify_tree_lmhead(const void* hidden, const void* w_vocab, int H, cons
   const int M = B * (N + 1);
   rc = cuda_rc(launch_lmhead(hidden, w_vocab, M, H, V, prm->temperature, lg, V,
                              stats ? (float2*)(base + lw.off_stats) : nullptr,
-                             stats ? (float*)(base + lw.off_lse) : nullptr, a.status, st));
+                             stats ? (float*)(base + lw.off_lse) : nullptr, a.status, st,
+                             (prm->flags & SPEC_FLAG_TEST_STALL) != 0));
   if (rc != SPEC_OK) return rc;
   return launch_verify(s, a, st);
 }

@@ -146,9 +146,10 @@ cudaError_t launch_philox(uint64_t seed, uint32_t offset, const int32_t* b, cons
 // log normalisers at that temperature into `lse` [M] (stats: [M, V/256]).
 int lmhead_tiles_n(int V);
 bool lmhead_supported(const void* hidden, const void* w, int H);
+// test_stall: the producer withholds its first stage (bounded-wait test).
 cudaError_t launch_lmhead(const void* hidden, const void* w, int M, int H, int V, float temperature,
                           uint16_t* logits, int64_t ldo, float2* stats, float* lse,
-                          uint32_t* status, cudaStream_t st);
+                          uint32_t* status, cudaStream_t st, bool test_stall = false);
 
 // EAGLE-2 expand + rerank
 struct Eagle2Cand {

@@ -66,6 +66,7 @@ struct GemmParams {
   float2* stats;     // [M, nn] (max, sum) in base 2 at kt, or null
   float kt;
   uint32_t* status;
+  int test_stall;  // withhold the first stage's copies (bounded-wait test)
 };
 
 // Bounded wait on a CTA barrier that gives up at once when the CTA is dead.
@@ -189,16 +190,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol_b));
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t issued = 0;  // stages ever filled (for the drain below)
+      uint32_t fills[kStages] = {};  // copies issued into each stage
+      bool stall_pending = blockIdx.x == 0;  // the test stall: CTA 0 only
       for (int t = blockIdx.x; t < P.ntiles; t += gridDim.x) {
         const int mb = t % P.nm, nb = t / P.nm;
         for (int kb = 0; kb < P.nkb; ++kb) {
           gwait(sm, &sm.empty[stage], phase ^ 1u, P.status);
-          mbar_expect_tx(&sm.full[stage], (uint32_t)kStageBytes);
           const uint32_t sa = ring + (uint32_t)(stage * kStageBytes);
-          tma_load_2d(sa, &map_a, kb * BK, mb * BM, &sm.full[stage], pol_a);
-          tma_load_2d(sa + kABytes, &map_b, kb * BK, nb * BN, &sm.full[stage], pol_b);
-          ++issued;
+          if (P.test_stall && stall_pending) {
+            // test only: this stage is never filled; the MMA issuer's wait on
+            // it gives up and the CTA finishes without waiting any further
+            stall_pending = false;
+          } else {
+            mbar_expect_tx(&sm.full[stage], (uint32_t)kStageBytes);
+            tma_load_2d(sa, &map_a, kb * BK, mb * BM, &sm.full[stage], pol_a);
+            tma_load_2d(sa + kABytes, &map_b, kb * BK, nb * BN, &sm.full[stage], pol_b);
+            ++fills[stage];
+          }
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
@@ -207,11 +215,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // wait for this CTA's last copy into each stage (normally consumed
       // already; after a timeout they may still be in flight)
-      for (int s = 0; s < kStages && (uint32_t)s < issued; ++s) {
-        const uint32_t fills = (issued - (uint32_t)s + kStages - 1) / kStages;
-        const uint32_t par = (fills - 1) & 1u;
-        mbar_wait_bounded(&sm.full[s], par);
-      }
+      for (int s = 0; s < kStages; ++s)
+        if (fills[s] > 0) mbar_wait_bounded(&sm.full[s], (fills[s] - 1) & 1u);
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
@@ -384,7 +389,7 @@ bool lmhead_supported(const void* hidden, const void* w, int H) {
 
 cudaError_t launch_lmhead(const void* hidden, const void* w, int M, int H, int V, float temperature,
                           uint16_t* logits, int64_t ldo, float2* stats, float* lse,
-                          uint32_t* status, cudaStream_t st) {
+                          uint32_t* status, cudaStream_t st, bool test_stall) {
   if (M == 0) return cudaSuccess;
   if (!lmhead_supported(hidden, w, H)) return cudaErrorInvalidValue;
   CUtensorMap ma, mb;
@@ -403,6 +408,7 @@ cudaError_t launch_lmhead(const void* hidden, const void* w, int M, int H, int V
   P.stats = (stats && temperature > 0.f) ? stats : nullptr;
   P.kt = temperature > 0.f ? kLog2e / temperature : 0.f;
   P.status = status;
+  P.test_stall = test_stall ? 1 : 0;
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;

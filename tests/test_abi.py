@@ -260,6 +260,13 @@ def test_lm_head_argument_errors(lib):
     assert tree(hidden=None) == lib.SPEC_ERR_ARG
     assert tree(nbytes=t - 256) == lib.SPEC_ERR_WORKSPACE
     assert tree(p=_prm(lib, flags=1)) == lib.SPEC_ERR_ARG
+    # the test-only stall flag passes the parameter check here (the call
+    # then stops at the short workspace) and nowhere else
+    stall = _prm(lib, flags=lib.SPEC_FLAG_TEST_STALL)
+    assert tree(p=stall, nbytes=t - 256) == lib.SPEC_ERR_WORKSPACE
+    assert f("spec_verify_tree", FAKE, FAKE, FAKE, FAKE, FAKE, 2, 5, 6, 1000,
+             1, 0, ctypes.byref(stall), FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 30,
+             None) == lib.SPEC_ERR_ARG
     assert tree(p=_prm(lib, top_k=500)) == lib.SPEC_ERR_UNSUPPORTED
 
 

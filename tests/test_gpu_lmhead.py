@@ -146,3 +146,29 @@ def test_tree_lmhead_full_size_sampled():
     assert p.exact >= len(seqs) - 3, p
     plen = gpu[0].cpu().numpy()
     assert plen.mean() > 0.5  # the draft tracks the target's logits
+
+
+def test_bounded_wait_gives_up_and_the_next_call_is_clean():
+    # the test-only flag withholds one shared-memory stage of the LM-head
+    # kernel: the tensor-core issuer's bounded wait gives up (about a
+    # second), the call completes with SPEC_STATUS_TIMEOUT, and the context
+    # stays usable: the next call reports nothing and matches a clean call
+    from speculative_decoding_verification_tree_gb300 import _lib
+    w = synth.workload("lmhead_tree", B=2, V=2048, H=128, seed=17)
+    hidden, wv, draft, q_row, toks, par = synth.lmhead_tree_inputs(w, "cuda")
+    ws = api().workspace(_lib.SPEC_OP_TREE_LMHEAD, w.B, toks.shape[1], w.V)
+    kw = dict(temperature=w.temperature, draft_kind=w.draft_kind,
+              seed=w.decision_seed, ws=ws)
+    clean = [x.clone() for x in api().spec_verify_tree_lmhead(
+        hidden, wv, draft, q_row, toks, par, **kw)]
+    assert api().spec_get_status(ws) == 0
+    api().spec_verify_tree_lmhead(hidden, wv, draft, q_row, toks, par,
+                                  flags=_lib.SPEC_FLAG_TEST_STALL, **kw)
+    torch.cuda.synchronize()
+    assert api().spec_get_status(ws) & _lib.SPEC_STATUS_TIMEOUT
+    again = api().spec_verify_tree_lmhead(hidden, wv, draft, q_row, toks,
+                                          par, **kw)
+    torch.cuda.synchronize()
+    assert api().spec_get_status(ws) == 0
+    for a, b in zip(clean, again):
+        assert torch.equal(a, b)
