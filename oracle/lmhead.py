@@ -19,18 +19,22 @@ workload's target logits are bf16).  The oracle computes z exactly (float64
 products of bf16 values are exact; the sum of H of them is within float64
 rounding) and rounds it to bf16 from the format's definition.
 
-Because the device accumulates in float32, a logit whose exact value lies
-within ``delta`` of a bf16 rounding midpoint may round to either neighbour.
+Because the device accumulates in float32, its float32 logit lies within
+``delta`` of the exact one, and its bf16 logit is the rounding of that value:
+any bf16 value from ``lo`` = RN(z - delta) to ``hi`` = RN(z + delta).
 ``delta`` bounds the float32 accumulation error of H products summed in
 groups of 16 with round-to-nearest:
 
     delta[v] = (H / 16 + 16) * 2^-24 * sum_h |h[h] W[v, h]|.
 
-Such logits are "ambiguous": ``alt`` holds the other neighbour there.  The
-verification is run on both roundings; a sequence whose decisions (path and
-emitted tokens before the final draw) differ between the two is a rounding
-near tie and is excluded from exact comparison, like an accept test within
-1e-5 of its threshold.
+Away from zero that range is the exact value's two bf16 neighbours at most;
+near zero (a sum that cancels) a bf16 unit is far below delta and the range
+spans many bf16 values.  Logits with lo != hi are "ambiguous".  The
+verification is run on the nearest rounding and on the two ends of the range
+(every ambiguous logit at lo, then at hi); a sequence whose decisions (path
+and emitted tokens before the final draw) differ between the runs is a
+rounding near tie and is excluded from exact comparison, like an accept test
+within 1e-5 of its threshold.
 """
 
 from __future__ import annotations
@@ -69,8 +73,9 @@ def bf16_round(x):
 class LMHead:
     exact: np.ndarray      # [..., V] float64: sum_h h W (exact up to f64)
     rn: np.ndarray         # [..., V] float64: exact rounded to bf16
-    alt: np.ndarray        # [..., V]: the other bf16 neighbour where ambiguous
-    ambiguous: np.ndarray  # [..., V] bool
+    lo: np.ndarray         # [..., V]: RN(exact - delta), the lowest bf16 result
+    hi: np.ndarray         # [..., V]: RN(exact + delta), the highest
+    ambiguous: np.ndarray  # [..., V] bool: lo != hi
     delta: np.ndarray      # [..., V] the accumulation-error bound used
 
 
@@ -83,11 +88,9 @@ def lm_head_logits(hidden, w):
     exact = h @ w.T
     delta = (H / 16.0 + 16.0) * 2.0 ** -24 * (np.abs(h) @ np.abs(w).T)
     rn = bf16_round(exact)
-    lo, hi = bf16_neighbours(exact)
-    mid = 0.5 * (lo + hi)
-    ambiguous = (lo != hi) & (np.abs(exact - mid) < delta)
-    alt = np.where(ambiguous, np.where(rn == lo, hi, lo), rn)
-    return LMHead(exact, rn, alt, ambiguous, delta)
+    lo = bf16_round(exact - delta)
+    hi = bf16_round(exact + delta)
+    return LMHead(exact, rn, lo, hi, lo != hi, delta)
 
 
 @dataclass
@@ -103,14 +106,18 @@ def verify_tree_lmhead(hidden, w, draft, q_row, node_tokens, parent, **kw):
     result's ``ref.near_tie`` includes the rounding near ties."""
     lg = lm_head_logits(hidden, w)
     ref = verify_tree(lg.rn, draft, q_row, node_tokens, parent, **kw)
-    alt = verify_tree(lg.alt, draft, q_row, node_tokens, parent, **kw)
     B = ref.path_len.shape[0]
     tie = np.zeros(B, dtype=bool)
-    for b in range(B):
-        n = int(ref.path_len[b])
-        same = (n == int(alt.path_len[b]) and
-                np.array_equal(ref.path_nodes[b], alt.path_nodes[b]) and
-                np.array_equal(ref.tokens[b][:n], alt.tokens[b][:n]))
-        tie[b] = not same
+    if lg.ambiguous.any():
+        for end in (lg.lo, lg.hi):
+            other = verify_tree(end, draft, q_row, node_tokens, parent, **kw)
+            for b in range(B):
+                n = int(ref.path_len[b])
+                same = (n == int(other.path_len[b]) and
+                        np.array_equal(ref.path_nodes[b],
+                                       other.path_nodes[b]) and
+                        np.array_equal(ref.tokens[b][:n],
+                                       other.tokens[b][:n]))
+                tie[b] |= not same
     ref.near_tie = ref.near_tie | tie
     return LMHeadTreeResult(ref, tie, lg)

@@ -1,9 +1,10 @@
 """GPU parity of the target LM head (spec_lm_head) and of tree verification
 through it (spec_verify_tree_lmhead) against the oracle (oracle/lmhead.py).
 
-Logits: every bf16 logit equals the oracle's rounding of the exact product,
-or, where the exact value lies within the float32 accumulation bound of a
-rounding midpoint (``ambiguous``), the other neighbour.  Row normalisers:
+Logits: every bf16 logit lies in the oracle's range [RN(z - delta),
+RN(z + delta)] of the exact product z, delta the float32 accumulation bound
+(a single value, the nearest rounding, except near rounding midpoints and
+near zero).  Row normalisers:
 within 2e-5 of the oracle's on its rounded logits (a handful of ambiguous
 logits may round the other way, each moving the normaliser by under 1e-6).
 Verification: the rules of the other tree tests, with rounding near ties
@@ -41,12 +42,11 @@ def _inputs(M, H, V, seed, std=2.0):
 
 
 def _check_logits(got, lg):
-    """got: GPU logits (float64 numpy) of the rows lg covers."""
-    exact_rn = got == lg.rn
-    other = lg.ambiguous & (got == lg.alt)
-    bad = ~(exact_rn | other)
+    """got: GPU logits (float64 numpy) of the rows lg covers.  Returns how
+    many differ from the nearest rounding (all of them ambiguous)."""
+    bad = ~((lg.lo <= got) & (got <= lg.hi))
     assert not bad.any(), (int(bad.sum()), np.argwhere(bad)[:5].tolist())
-    return int(other.sum())
+    return int((got != lg.rn).sum())
 
 
 @pytest.mark.parametrize("M,H,V", [(1, 64, 256), (128, 64, 256),

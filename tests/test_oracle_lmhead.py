@@ -9,8 +9,9 @@ oracle to check itself:
 * the exact logits equal brute-force dot products in exact rational
   arithmetic;
 * the accumulation-error bound holds for an explicit float32 summation in
-  groups of 16, and logits outside the ambiguous band keep their rounding
-  under any perturbation within the bound;
+  groups of 16, whose bf16 rounding lies in the oracle's [lo, hi] range,
+  including sums that cancel to near zero (where the range spans many bf16
+  values);
 * with logits that are bf16 values already, verification through the LM
   head equals tree verification of those logits, with no rounding ties; an
   accept test whose ratio straddles the uniform under the two roundings is a
@@ -97,21 +98,43 @@ def test_error_bound_covers_float32_accumulation_in_groups():
         acc = acc + part
     err = np.abs(acc.astype(np.float64) - lg.exact)
     assert (err <= lg.delta).all(), float((err / lg.delta).max())
-    # logits outside the band keep their rounding anywhere within delta
+    # the float32 sum's bf16 rounding lies in the oracle's range, which
+    # holds the nearest rounding and is a single value where not ambiguous
+    got = bf16_round(acc.astype(np.float64))
+    assert ((lg.lo <= got) & (got <= lg.hi)).all()
+    assert ((lg.lo <= lg.rn) & (lg.rn <= lg.hi)).all()
     ok = ~lg.ambiguous
-    for s in (-0.999, 0.999):
-        moved = bf16_round(lg.exact + s * lg.delta)
-        assert np.array_equal(moved[ok], lg.rn[ok])
-    # inside the band the other neighbour is reachable: the value mirrored
-    # across the midpoint (as far from it, within delta) rounds to alt
-    amb = lg.ambiguous
-    assert amb.any()
-    lo, hi = bf16_neighbours(lg.exact[amb])
-    mid = 0.5 * (lo + hi)
-    mirrored = 2 * mid - lg.exact[amb]
-    off = mirrored != mid
-    assert np.array_equal(bf16_round(mirrored)[off], lg.alt[amb][off])
-    assert (lg.alt[amb] != lg.rn[amb]).all()
+    assert np.array_equal(lg.lo[ok], lg.rn[ok])
+    assert np.array_equal(lg.hi[ok], lg.rn[ok])
+    assert lg.ambiguous.any() and ok.any()
+    # away from zero the range is at most the two bf16 neighbours
+    big = np.abs(lg.exact) > 1.0
+    nlo, nhi = bf16_neighbours(lg.exact[big])
+    assert (lg.lo[big] >= nlo).all() and (lg.hi[big] <= nhi).all()
+
+
+def test_cancelling_sums_span_many_bf16_values():
+    # h . w that cancels to about 1e-6: a bf16 unit there is ~1e-14, far
+    # below the float32 accumulation error, so the range holds many values
+    # and still contains the float32 summation's rounding
+    H = 512
+    rng = np.random.default_rng(8)
+    h = _bf16(rng.standard_normal((1, H)))
+    w = _bf16(rng.standard_normal((1, H)) * 0.1)
+    w2 = w.copy()
+    w2[0, -1] = 0.0  # choose the last product so the sum nearly cancels
+    part = float((h @ w2.T)[0, 0])
+    w2[0, -1] = _bf16(np.array([-part / h[0, -1]]))[0]
+    lg = lm_head_logits(h, w2)
+    assert abs(lg.exact[0, 0]) < 1e-2 and lg.ambiguous[0, 0]
+    unit = np.ldexp(1.0, np.frexp(abs(lg.rn[0, 0]))[1] - 8)
+    assert lg.hi[0, 0] - lg.lo[0, 0] > 4 * unit
+    prod = (h * w2).astype(np.float32)[0]
+    acc = np.float32(0)
+    for g in range(0, H, 16):
+        acc = np.float32(acc + prod[g:g + 16].sum(dtype=np.float32))
+    got = bf16_round(float(acc))
+    assert lg.lo[0, 0] <= got <= lg.hi[0, 0]
 
 
 def _tree(B=2, V=40, H=8, seed=4):
