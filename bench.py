@@ -1568,13 +1568,14 @@ def attn_main(args, world, rank, local):
             tpk = 1900.0
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                 "unit": "GB/s", "frac": round(achieved / peak, 4),
-                "traffic": None, "kernel": "tree_attn_kernel",
+                "traffic": None, "kernel": "tree_attn_tc",
                 "bytes_per_launch": int(nbytes),
                 "avg_launch_ms": round(kern_ms, 5), "peak_source": peak_kind,
                 "tensor": {"achieved_tflops": round(tf, 1),
                            "peak_tflops": tpk, "frac": round(tf / tpk, 4),
                            "flops_per_launch": int(flops),
-                           "path": "mma.sync m16n8k16 bf16"},
+                           "path": "tcgen05.mma kind::f16, TMEM "
+                                   "accumulators, K/V by TMA"},
                 "profile_rc": rc}
     e2e = None
     if not args.no_e2e:

@@ -19,9 +19,11 @@
 //   warp 0     TMA producer: 64-key blocks of K and V (128-byte swizzle) into
 //              a 3-stage shared-memory ring;
 //   warp 1     allocates TMEM and issues, per key block and tile t,
-//              S_t = Q_t K^T (tcgen05.mma M 128, N 64, K 128) and, once the
-//              softmax has written P_t, O_t += P_t V (M 128, N 128, K 64; V is
-//              the MN-major operand, read as stored);
+//              S_t = Q_t K^T (tcgen05.mma M 128, N 64, K 128) into one of two
+//              S buffers -- the next block's S is computed while the softmax
+//              works on this one -- and, once the softmax has written P_t,
+//              O_t += P_t V (M 128, N 128, K 64; V is the MN-major operand,
+//              read as stored);
 //   warps 2-9  softmax, one thread per query row (warp w reads TMEM lanes of
 //              quadrant w % 4): they stage Q once, then per block read S with
 //              tcgen05.ld, apply the scale and the tree mask, run the online
@@ -29,7 +31,7 @@
 //              a row's maximum grows by more than 2^8 (then O_t is rescaled in
 //              TMEM), and write P as bf16 into 128-byte-swizzled shared memory
 //              for the next MMA; at the end O_t / l is rounded to bf16.
-// TMEM: S_t at columns 64 t, O_t at 128 + 128 t (384 of 512).  Every mbarrier
+// TMEM: S_t of buffer u at columns 64 (2 t + u), O_t at 256 + 128 t.  Every mbarrier
 // wait is bounded (SPEC_STATUS_TIMEOUT is not reported by this entry point,
 // which has no status word; a CTA that gives up stops waiting and still frees
 // its TMEM after waiting, bounded, for its own MMAs and copies).
@@ -64,7 +66,7 @@ constexpr uint32_t kATmemCols = 512;
 
 struct __align__(8) AttnSmem {
   uint64_t kvfull[kAStages], kvempty[kAStages];
-  uint64_t sfull[kTiles], pfull[kTiles], pdone[kTiles];
+  uint64_t sfull[kTiles][2], pfull[kTiles], pdone[kTiles];
   uint64_t qready, drain;
   uint32_t tmem_base;
   uint32_t dead;
@@ -212,7 +214,8 @@ __global__ void __launch_bounds__(kAThreads, 1)
       mbar_init(&sm.kvempty[s], 1);
     }
     for (int t = 0; t < kTiles; ++t) {
-      mbar_init(&sm.sfull[t], 1);
+      mbar_init(&sm.sfull[t][0], 1);
+      mbar_init(&sm.sfull[t][1], 1);
       mbar_init(&sm.pfull[t], kMT);
       mbar_init(&sm.pdone[t], 1);
     }
@@ -258,12 +261,12 @@ __global__ void __launch_bounds__(kAThreads, 1)
     if (lane == 0) {
       await(sm, &sm.qready, 0);
       fence_after();
-      for (int j = 0; j < nblk; ++j) {
+      // S_t of block j into buffer j & 1 (its previous contents, block j - 2,
+      // were read before the softmax released P of block j - 2)
+      auto issue_s = [&](int j) {
         const int s = j % kAStages;
-        const uint32_t ph = (uint32_t)(j & 1);
         await(sm, &sm.kvfull[s], (uint32_t)(j / kAStages) & 1u);
         const uint32_t kst = base + kOffKV + (uint32_t)(s * kAStage);
-        const uint32_t vst = kst + kKVTile;
         const int tail = L - j * kKB;  // keys of this block that exist
         if (tail < kKB) {
           // cache rows past the sequence's keys hold anything (NaN included);
@@ -280,22 +283,29 @@ __global__ void __launch_bounds__(kAThreads, 1)
         fence_after();
         for (int t = 0; t < ntile; ++t) {
           const uint32_t qt = base + (uint32_t)(t * kQTile);
+          const uint32_t ds = tmem + (uint32_t)(64 * (2 * t + (j & 1)));
 #pragma unroll
           for (int k = 0; k < kAD / 16; ++k) {
             const uint32_t off = (uint32_t)((k >> 2) * kQHalf + (k & 3) * 32);
             const uint32_t koff = (uint32_t)((k >> 2) * kKVHalf + (k & 3) * 32);
-            mma_f16(tmem + (uint32_t)(64 * t), desc_kmajor(qt + off), desc_kmajor(kst + koff),
-                    kIdescS, k > 0 ? 1u : 0u);
+            mma_f16(ds, desc_kmajor(qt + off), desc_kmajor(kst + koff), kIdescS,
+                    k > 0 ? 1u : 0u);
           }
-          mma_commit(&sm.sfull[t]);
+          mma_commit(&sm.sfull[t][j & 1]);
         }
+      };
+      if (nblk > 0) issue_s(0);
+      for (int j = 0; j < nblk; ++j) {
+        const int s = j % kAStages;
+        if (j + 1 < nblk) issue_s(j + 1);
+        const uint32_t vst = base + kOffKV + (uint32_t)(s * kAStage) + kKVTile;
         for (int t = 0; t < ntile; ++t) {
-          await(sm, &sm.pfull[t], ph);
+          await(sm, &sm.pfull[t], (uint32_t)(j & 1));
           fence_after();
           const uint32_t pt = base + kOffP + (uint32_t)(t * kPTile);
 #pragma unroll
           for (int k = 0; k < kKB / 16; ++k)
-            mma_f16(tmem + 128u + (uint32_t)(128 * t), desc_kmajor(pt + (uint32_t)(k * 32)),
+            mma_f16(tmem + 256u + (uint32_t)(128 * t), desc_kmajor(pt + (uint32_t)(k * 32)),
                     desc_mnmajor(vst + (uint32_t)(k * 2048)), kIdescPV,
                     (j > 0 || k > 0) ? 1u : 0u);
           mma_commit(&sm.pdone[t]);
@@ -329,16 +339,17 @@ __global__ void __launch_bounds__(kAThreads, 1)
     }
     if (t < ntile) {
       const uint32_t lanes = (uint32_t)(qd * 32) << 16;
-      const uint32_t tS = tmem + lanes + (uint32_t)(64 * t);
-      const uint32_t tO = tmem + lanes + 128u + (uint32_t)(128 * t);
+      const uint32_t tS = tmem + lanes + (uint32_t)(128 * t);  // + 64 * buffer
+      const uint32_t tO = tmem + lanes + 256u + (uint32_t)(128 * t);
       unsigned char* pt = bp + kOffP + t * kPTile;
       float mref = neg_inf(), l = 0.f;
       for (int j = 0; j < nblk; ++j) {
-        await(sm, &sm.sfull[t], (uint32_t)(j & 1));
+        await(sm, &sm.sfull[t][j & 1], (uint32_t)((j >> 1) & 1));
         fence_after();
         uint32_t ra[32], rb[32];
-        tld32(tS, ra);
-        tld32(tS + 32u, rb);
+        const uint32_t tSb = tS + (uint32_t)(64 * (j & 1));
+        tld32(tSb, ra);
+        tld32(tSb + 32u, rb);
         tld_wait();
         float s[64];
 #pragma unroll
@@ -361,28 +372,12 @@ __global__ void __launch_bounds__(kAThreads, 1)
         float bm = neg_inf();
 #pragma unroll
         for (int i = 0; i < 64; ++i) bm = fmaxf(bm, s[i]);
-        // the previous block's P V is done before P_t and O_t are touched
-        if (j > 0) await(sm, &sm.pdone[t], (uint32_t)((j - 1) & 1));
-        fence_after();
-        const bool move = bm > mref + 8.f;  // also the first visible key
-        if (__any_sync(0xffffffffu, move)) {
-          const float mnew = move ? bm : mref;
-          const float corr = (move && mref != neg_inf()) ? ex2(mref - mnew) : 1.f;
-          l *= corr;
-          if (j > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
-#pragma unroll 1
-            for (int c = 0; c < kAD / 32; ++c) {
-              uint32_t o[32];
-              tld32(tO + (uint32_t)(32 * c), o);
-              tld_wait();
-#pragma unroll
-              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
-              tst32(tO + (uint32_t)(32 * c), o);
-            }
-            tst_wait();
-          }
-          mref = mnew;
-        }
+        // the reference maximum moves only when the row's maximum grows by
+        // more than 2^8 (also at the first visible key): P stays below 2^8
+        const bool move = bm > mref + 8.f;
+        const float mnew = move ? bm : mref;
+        const float corr = (move && mref != neg_inf()) ? ex2(mref - mnew) : 1.f;
+        mref = mnew;
         const float mu = mref == neg_inf() ? 0.f : mref;
         uint32_t pk[32];
         float ls = 0.f;
@@ -392,7 +387,22 @@ __global__ void __launch_bounds__(kAThreads, 1)
           ls += p0 + p1;
           pk[i] = pack_bf16(p0, p1);
         }
-        l += ls;
+        l = l * corr + ls;
+        // the previous block's P V is done before P_t and O_t are touched
+        if (j > 0) await(sm, &sm.pdone[t], (uint32_t)((j - 1) & 1));
+        fence_after();
+        if (j > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
+#pragma unroll 1
+          for (int c = 0; c < kAD / 32; ++c) {
+            uint32_t o[32];
+            tld32(tO + (uint32_t)(32 * c), o);
+            tld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
+            tst32(tO + (uint32_t)(32 * c), o);
+          }
+          tst_wait();
+        }
 #pragma unroll
         for (int c = 0; c < 8; ++c)
           *reinterpret_cast<uint4*>(pt + swz(r, c)) =
