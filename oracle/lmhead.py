@@ -98,6 +98,24 @@ class LMHeadTreeResult:
     ref: TreeResult            # verification on the rounded logits
     rounding_tie: np.ndarray   # [B] bool: the other rounding decides otherwise
     logits: LMHead
+    mass_slack: np.ndarray = None  # [B, N+1]: bound on the acceptance-mass
+                                   # change any rounding in range can cause
+
+
+def mass_slack(lg, temperature):
+    """Per row, a bound on how far alpha = sum min(p, q) can move when the
+    logits take any values in [lo, hi] instead of rn (full-vocabulary
+    transform at temperature T > 0).  A logit moved by at most d = hi - lo
+    scales its unnormalised weight by at most e^(d / T); so p changes by at
+    most p (e^(d/T) - 1) at the moved tokens plus the normaliser's relative
+    change, which is bounded by the same sum: |d alpha| <= 2 sum_amb p_v
+    (e^(d_v / T) - 1)."""
+    z = lg.rn / temperature
+    z = z - z.max(axis=-1, keepdims=True)
+    p = np.exp(z)
+    p /= p.sum(axis=-1, keepdims=True)
+    d = np.where(lg.ambiguous, lg.hi - lg.lo, 0.0) / temperature
+    return 2.0 * (p * np.expm1(d)).sum(axis=-1)
 
 
 def verify_tree_lmhead(hidden, w, draft, q_row, node_tokens, parent, **kw):
@@ -120,4 +138,6 @@ def verify_tree_lmhead(hidden, w, draft, q_row, node_tokens, parent, **kw):
                                        other.tokens[b][:n]))
                 tie[b] |= not same
     ref.near_tie = ref.near_tie | tie
-    return LMHeadTreeResult(ref, tie, lg)
+    T = kw.get("temperature", 0.0)
+    slack = mass_slack(lg, T) if T > 0 else None
+    return LMHeadTreeResult(ref, tie, lg, slack)

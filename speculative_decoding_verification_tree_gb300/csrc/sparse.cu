@@ -16,7 +16,8 @@
 //     vocabulary order (a leaf: the bonus token from p).
 // Kernels: topk_rows (one CTA per target row and per draft row, one HBM
 // pass), row_meta (children and uniforms, shared with the streaming path),
-// sparse_units (one CTA per row, all math on the candidate lists),
+// sparse_warp (one warp per row, all math on the candidate lists as warp-wide
+// sums and scans),
 // sparse_walk.
 #include "sample_stream.cuh"
 #include "topk.cuh"
@@ -63,135 +64,186 @@ __global__ void __launch_bounds__(topk::kThreads) topk_rows(VerifyShape s, Verif
                             nullptr);
 }
 
-// Probabilities of a candidate list (raw values, best first) after the
-// temperature, softmax and top-p steps; entries past the cut get 0.
-// Thread 0 only; deterministic order.
-__device__ int transform_list(const float* val, int cnt, bool probs, float kt, float invT,
-                              float top_p, float* prob) {
-  if (cnt <= 0) return 0;
-  float s0;
-  for (int i = 0; i < cnt; ++i) {
-    const float sv = probs ? __fmul_rn(lg2(val[i]), invT) : __fmul_rn(val[i], kt);
-    if (i == 0) s0 = sv;
-    prob[i] = (s0 == neg_inf()) ? 0.f : ex2(sv - s0);
+constexpr int kSW = 4;  // rows (warps) per CTA of sparse_warp
+constexpr unsigned kFull = 0xffffffffu;
+
+// Sum over the warp, the same value in every lane (taken from lane 0).
+__device__ __forceinline__ float wsum(float v) {
+  return __shfl_sync(kFull, warp_sum(v), 0);
+}
+// Inclusive prefix sum of one value per lane.
+__device__ __forceinline__ float wscan(float v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_up_sync(kFull, v, o);
+    if (lane >= o) v += y;
   }
-  float Z = 0.f;
-  for (int i = 0; i < cnt; ++i) Z += prob[i];
+  return v;
+}
+
+// Probabilities of a candidate list (raw values, best first; lane l holds
+// positions l + 32 i) after the temperature, softmax and top-p steps, written
+// to prob[pos] (0 past the cut).  Returns the kept count.
+__device__ int warp_transform(const float (&val)[4], int cnt, bool probs, float kt, float invT,
+                              float top_p, float* prob, int lane) {
+  if (cnt <= 0) return 0;
+  float e[4], loc = 0.f;
+  float sv[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int pos = lane + 32 * i;
+    sv[i] = pos < cnt ? (probs ? __fmul_rn(lg2(val[i]), invT) : __fmul_rn(val[i], kt)) : neg_inf();
+  }
+  const float s0 = __shfl_sync(kFull, sv[0], 0);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int pos = lane + 32 * i;
+    e[i] = (pos < cnt && s0 != neg_inf()) ? ex2(sv[i] - s0) : 0.f;
+    loc += e[i];
+  }
+  const float Z = wsum(loc);
   if (!(Z > 0.f)) {  // no finite logit among the candidates
-    for (int i = 0; i < cnt; ++i) prob[i] = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (lane + 32 * i < cnt) prob[lane + 32 * i] = 0.f;
     return 0;
   }
-  for (int i = 0; i < cnt; ++i) prob[i] = prob[i] / Z;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) e[i] = e[i] / Z;
   int keep = cnt;
   if (top_p < 1.f) {
-    float c = 0.f;
-    keep = cnt;
-    for (int i = 0; i < cnt; ++i) {
-      c += prob[i];
-      if (c >= top_p) {
-        keep = i + 1;
-        break;
+    // shortest prefix (list order) whose mass reaches top_p, at least one
+    float carry = 0.f;
+    bool found = false;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int pos = lane + 32 * i;
+      const float c = carry + wscan(e[i], lane);
+      const unsigned hit = __ballot_sync(kFull, pos < cnt && c >= top_p);
+      if (!found && hit) {
+        keep = 32 * i + __ffs(hit);
+        found = true;
       }
+      carry = __shfl_sync(kFull, c, 31);
     }
     float z2 = 0.f;
-    for (int i = 0; i < keep; ++i) z2 += prob[i];
-    for (int i = 0; i < cnt; ++i) prob[i] = (i < keep) ? prob[i] / z2 : 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) z2 += (lane + 32 * i < keep) ? e[i] : 0.f;
+    z2 = wsum(z2);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) e[i] = (lane + 32 * i < keep) ? e[i] / z2 : 0.f;
   }
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    if (lane + 32 * i < cnt) prob[lane + 32 * i] = e[i];
   return keep;
 }
 
+// One warp per tree row: the transform of both candidate lists, the
+// acceptance mass, the children's tests and the draw, all as warp-wide sums
+// and scans over the at most kK candidates (no block barrier).
 template <typename TT, typename TD>
-__global__ void __launch_bounds__(kK) sparse_units(VerifyShape s, VerifyArgs a, TopkOut o,
-                                                   float kt, float invT, int rec_bytes,
-                                                   int kidcap) {
-  __shared__ float pk[kK], qk[kK];          // probabilities, list order
-  __shared__ int ptok_v[kK];                // support of p in vocabulary order
-  __shared__ float pv_v[kK], qv_v[kK];      // p and q at those tokens
-  __shared__ float tvs[kK], dvs[kK];        // candidate values (target, draft)
-  __shared__ int32_t tis[kK], dis[kK];      // candidate tokens
-  __shared__ int s_np, s_nq;
-  const int64_t u = blockIdx.x;
+__global__ void __launch_bounds__(32 * kSW) sparse_warp(VerifyShape s, VerifyArgs a, TopkOut o,
+                                                        float kt, float invT, int rec_bytes,
+                                                        int kidcap) {
+  struct WarpMem {
+    float pk[kK], qk[kK];        // probabilities, list order
+    int32_t tis[kK], dis[kK];    // candidate tokens, list order
+    int32_t ptok_v[kK];          // support of p in vocabulary order
+    float pv_v[kK], qv_v[kK];    // p and q at those tokens
+  };
+  __shared__ WarpMem wmem[kSW];
+  const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5;
   const int64_t rows = s.rows();
-  const int tid = threadIdx.x;
+  const int64_t u = (int64_t)blockIdx.x * kSW + wi;
+  if (u >= rows) return;  // the whole warp
+  WarpMem& m = wmem[wi];
   const int V = s.V;
   const stream::Meta* M = reinterpret_cast<const stream::Meta*>(a.meta + u * (int64_t)rec_bytes);
   const float* ukid = reinterpret_cast<const float*>(a.meta + u * (int64_t)rec_bytes + 16 +
                                                      16 * kidcap);
   const bool probs = a.prm.draft_kind == SPEC_DRAFT_PROBS;
   const int ct = o.cnt[u], cq = o.cnt[rows + u];
-  const float* tv = o.val + u * kK;
-  const int32_t* ti = o.idx + u * kK;
-  const float* dv = o.val + (rows + u) * kK;
-  const int32_t* di = o.idx + (rows + u) * kK;
   const bool has_q = M->qr >= 0 && cq > 0;
-  // the candidate lists into shared memory (one element per thread: at most
-  // kK each), so that the serial steps below read no global memory
-  if (tid < ct) {
-    tvs[tid] = tv[tid];
-    tis[tid] = ti[tid];
+  float tval[4], dval[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int pos = lane + 32 * i;
+    tval[i] = pos < ct ? o.val[u * kK + pos] : neg_inf();
+    m.tis[pos] = pos < ct ? o.idx[u * kK + pos] : INT_MAX;
+    dval[i] = pos < cq ? o.val[(rows + u) * kK + pos] : neg_inf();
+    m.dis[pos] = pos < cq ? o.idx[(rows + u) * kK + pos] : -1;
   }
-  if (tid < cq) {
-    dvs[tid] = dv[tid];
-    dis[tid] = di[tid];
-  }
-  __syncthreads();
-  if (tid == 0) {
+  __syncwarp();
+  const int np = warp_transform(tval, ct, false, kt, invT, a.prm.top_p, m.pk, lane);
+  const int nq = has_q ? warp_transform(dval, cq, probs, kt, invT, a.prm.top_p, m.qk, lane) : 0;
+  if (lane == 0) {
     uint32_t bad = M->bad;
     if (ct <= 0) bad |= SPEC_STATUS_NAN;
-    s_np = transform_list(tvs, ct, false, kt, invT, a.prm.top_p, pk);
-    s_nq = has_q ? transform_list(dvs, cq, probs, kt, invT, a.prm.top_p, qk) : 0;
     if (bad) flag_status(a.status, bad);
   }
-  __syncthreads();
-  const int np = s_np, nq = s_nq;
+  __syncwarp();
   // support of p in vocabulary order (tokens are distinct: rank by counting)
-  if (tid < np) {
-    const int t = tis[tid];
-    int rk = 0;
-    for (int j = 0; j < np; ++j) rk += (tis[j] < t) ? 1 : 0;
-    float qa = 0.f;
-    for (int j = 0; j < nq; ++j)
-      if (dis[j] == t) qa = qk[j];
-    ptok_v[rk] = t;
-    pv_v[rk] = pk[tid];
-    qv_v[rk] = qa;
-  }
-  __syncthreads();
-  if (tid != 0) return;
-
-  auto p_at = [&](int x) -> float {
-    int lo = 0, hi = np - 1;
-    while (lo <= hi) {
-      const int mid = (lo + hi) >> 1;
-      if (ptok_v[mid] == x) return pv_v[mid];
-      if (ptok_v[mid] < x) lo = mid + 1;
-      else hi = mid - 1;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int pos = lane + 32 * i;
+    if (pos < np) {
+      const int t = m.tis[pos];
+      int rk = 0;
+      for (int j = 0; j < np; ++j) rk += (m.tis[j] < t) ? 1 : 0;
+      float qa = 0.f;
+      for (int j = 0; j < nq; ++j)
+        if (m.dis[j] == t) qa = m.qk[j];
+      m.ptok_v[rk] = t;
+      m.pv_v[rk] = m.pk[pos];
+      m.qv_v[rk] = qa;
     }
-    return 0.f;
+  }
+  __syncwarp();
+  auto p_at = [&](int x) -> float {  // at most one match: the sum is exact
+    float r = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int pos = lane + 32 * i;
+      if (pos < np && m.ptok_v[pos] == x) r = m.pv_v[pos];
+    }
+    return wsum(r);
   };
   auto q_at = [&](int x) -> float {
-    for (int j = 0; j < nq; ++j)
-      if (dis[j] == x) return qk[j];
-    return 0.f;
+    float r = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int pos = lane + 32 * i;
+      if (pos < nq && m.dis[pos] == x) r = m.qk[pos];
+    }
+    return wsum(r);
   };
   // acceptance mass over the common support
-  float alpha = 0.f;
-  for (int i = 0; i < np; ++i) alpha += fminf(pv_v[i], qv_v[i]);
-  if (M->qr >= 0) a.alpha_part[u * kAlphaSlots] = alpha;
+  float al = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int pos = lane + 32 * i;
+    if (pos < np) al += fminf(m.pv_v[pos], m.qv_v[pos]);
+  }
+  const float alpha = wsum(al);
+  if (lane == 0 && M->qr >= 0) a.alpha_part[u * kAlphaSlots] = alpha;
 
   uint32_t st_bits = 0;
   float Cc = 0.f, W = 1.f, D = 1.f;
   int accepted = -1;
   const int nk = has_q ? M->nk : 0;
   if (M->nk > 0 && !has_q) st_bits |= SPEC_STATUS_BAD_TREE;
-  for (int k = 0; k < nk; ++k) {
+  for (int k = 0; k < nk; ++k) {  // every lane takes the same branches
     const int x = M->kid[k].tok;
     bool removed = false;
     for (int i = 0; i < k; ++i) removed |= (M->kid[i].tok == x);
-    if (x < 0 || x >= V) {
+    const bool valid = x >= 0 && x < V;
+    float qx = 0.f;
+    if (!valid) {
       st_bits |= SPEC_STATUS_TOKEN_RANGE;
     } else {
-      const float px = p_at(x), qx = q_at(x);
+      const float px = p_at(x);
+      qx = q_at(x);
       const float ax = Cc == 0.f ? px : fmaxf(0.f, fmaf(-Cc, qx, px));
       const float qj = removed ? 0.f : qx / D;
       if (qj == 0.f) {
@@ -206,43 +258,59 @@ __global__ void __launch_bounds__(kK) sparse_units(VerifyShape s, VerifyArgs a, 
     }
     // rejected: residual max(0, p - Cn q) over the support of p
     const float Cn = Cc + W / D;
-    float Wn = 0.f;
-    for (int i = 0; i < np; ++i) Wn += fmaxf(0.f, fmaf(-Cn, qv_v[i], pv_v[i]));
+    float wl = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int pos = lane + 32 * i;
+      if (pos < np) wl += fmaxf(0.f, fmaf(-Cn, m.qv_v[pos], m.pv_v[pos]));
+    }
+    const float Wn = wsum(wl);
     if (Wn > 0.f) {
       Cc = Cn;
       W = Wn;
     } else {
       st_bits |= SPEC_STATUS_RESIDUAL_ZERO;
     }
-    if (x >= 0 && x < V && !removed) D -= q_at(x);
+    if (valid && !removed) D -= qx;
     if (D <= 0.f) {
       st_bits |= SPEC_STATUS_DRAFT_EXHAUSTED;
       break;
     }
   }
   if (accepted < 0) {
-    float tot = 0.f;
-    for (int i = 0; i < np; ++i) tot += (Cc == 0.f) ? pv_v[i] : fmaxf(0.f, fmaf(-Cc, qv_v[i], pv_v[i]));
-    const float t = M->u_draw * tot;
-    float c = 0.f;
-    int tok = -1, last = -1;
-    for (int i = 0; i < np; ++i) {
-      const float w = (Cc == 0.f) ? pv_v[i] : fmaxf(0.f, fmaf(-Cc, qv_v[i], pv_v[i]));
-      if (w > 0.f) last = ptok_v[i];
-      c += w;
-      if (w > 0.f && c > t) {
-        tok = ptok_v[i];
-        break;
-      }
+    // inverse CDF of the final weights in vocabulary order
+    float w[4], tl = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int pos = lane + 32 * i;
+      w[i] = pos < np ? ((Cc == 0.f) ? m.pv_v[pos]
+                                     : fmaxf(0.f, fmaf(-Cc, m.qv_v[pos], m.pv_v[pos])))
+                      : 0.f;
+      tl += w[i];
+    }
+    const float t = M->u_draw * wsum(tl);
+    float carry = 0.f;
+    int tok = -1, lastpos = -1;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int pos = lane + 32 * i;
+      const float c = carry + wscan(w[i], lane);
+      const unsigned pos_mask = __ballot_sync(kFull, w[i] > 0.f);
+      if (pos_mask) lastpos = 32 * i + 31 - __clz(pos_mask);
+      const unsigned hit = __ballot_sync(kFull, w[i] > 0.f && c > t);
+      if (tok < 0 && hit) tok = m.ptok_v[32 * i + __ffs(hit) - 1];
+      carry = __shfl_sync(kFull, c, 31);
     }
     if (tok < 0) {
-      tok = last < 0 ? 0 : last;
+      tok = lastpos < 0 ? 0 : m.ptok_v[lastpos];
       st_bits |= SPEC_STATUS_CDF_FALLBACK;
     }
-    a.row_token[u] = tok;
+    if (lane == 0) a.row_token[u] = tok;
   }
-  a.row_child[u] = accepted;
-  if (st_bits) flag_status(a.status, st_bits);
+  if (lane == 0) {
+    a.row_child[u] = accepted;
+    if (st_bits) flag_status(a.status, st_bits);
+  }
 }
 
 // Per row: acceptance mass; per sequence (row 0's thread): the walk along
@@ -312,7 +380,8 @@ cudaError_t launch_sparse_t(const VerifyShape& s, const VerifyArgs& a, int k, cu
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const float T = a.prm.temperature;
-  sparse_units<TT, TD><<<(unsigned)rows, kK, 0, st>>>(s, a, o, kLog2e / T, 1.f / T, rec, kidcap);
+  sparse_warp<TT, TD><<<(unsigned)((rows + kSW - 1) / kSW), 32 * kSW, 0, st>>>(
+      s, a, o, kLog2e / T, 1.f / T, rec, kidcap);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   sparse_walk<<<(unsigned)((rows + 127) / 128), 128, 0, st>>>(s, a);

@@ -25,7 +25,8 @@ import pytest
 import torch
 
 from oracle.lmhead import (bf16_neighbours, bf16_round, lm_head_logits,
-                           verify_tree_lmhead)
+                           mass_slack, verify_tree_lmhead)
+from oracle.sampling import acceptance_mass, transform
 from oracle.tree import verify_tree
 
 
@@ -202,3 +203,25 @@ def test_rounding_tie_when_the_two_roundings_decide_differently():
     assert run(u_between).ref.near_tie[0]
     assert not run(0.05).rounding_tie[0]    # accepted either way
     assert not run(0.999).rounding_tie[0]   # rejected either way
+
+
+def test_mass_slack_bounds_any_rounding_in_range():
+    # logits taking arbitrary values in [lo, hi] (each ambiguous logit at a
+    # random end) move alpha = sum min(p, q) by no more than the slack
+    rng = np.random.default_rng(9)
+    H, V, T = 512, 3000, 0.8
+    h = _bf16(rng.standard_normal((4, H)))
+    w = _bf16(rng.standard_normal((V, H)) * (3.0 / np.sqrt(H)))
+    lg = lm_head_logits(h, w)
+    slack = mass_slack(lg, T)
+    assert lg.ambiguous.any() and (slack > 0).all()
+    q = rng.dirichlet(np.ones(V) * 0.3, size=4)
+    for trial in range(5):
+        pick = rng.random(lg.rn.shape) < 0.5
+        moved = np.where(lg.ambiguous, np.where(pick, lg.lo, lg.hi), lg.rn)
+        for r in range(4):
+            p0, _ = transform(lg.rn[r], "logits", T)
+            p1, _ = transform(moved[r], "logits", T)
+            a0 = acceptance_mass(p0, q[r])
+            a1 = acceptance_mass(p1, q[r])
+            assert abs(a1 - a0) <= slack[r], (trial, r, a1 - a0, slack[r])
