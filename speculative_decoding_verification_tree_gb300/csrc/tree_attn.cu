@@ -351,11 +351,13 @@ __global__ void __launch_bounds__(kAThreads, 1)
         tld32(tSb, ra);
         tld32(tSb + 32u, rb);
         tld_wait();
+        // raw scores q.k (the scale is applied inside the exponent below;
+        // it is positive, so the maximum is taken on the raw scores)
         float s[64];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          s[i] = __uint_as_float(ra[i]) * scale_log2;
-          s[32 + i] = __uint_as_float(rb[i]) * scale_log2;
+          s[i] = __uint_as_float(ra[i]);
+          s[32 + i] = __uint_as_float(rb[i]);
         }
         const int key0 = j * kKB;
         if (!valid) {
@@ -369,24 +371,33 @@ __global__ void __launch_bounds__(kAThreads, 1)
             if (!vis) s[i] = neg_inf();
           }
         }
-        float bm = neg_inf();
+        // eight independent chains, then their combination
+        float bm8[8];
 #pragma unroll
-        for (int i = 0; i < 64; ++i) bm = fmaxf(bm, s[i]);
+        for (int c = 0; c < 8; ++c) bm8[c] = s[c];
+#pragma unroll
+        for (int i = 8; i < 64; ++i) bm8[i & 7] = fmaxf(bm8[i & 7], s[i]);
+        const float bm = fmaxf(fmaxf(fmaxf(bm8[0], bm8[1]), fmaxf(bm8[2], bm8[3])),
+                               fmaxf(fmaxf(bm8[4], bm8[5]), fmaxf(bm8[6], bm8[7]))) *
+                         scale_log2;
         // the reference maximum moves only when the row's maximum grows by
         // more than 2^8 (also at the first visible key): P stays below 2^8
         const bool move = bm > mref + 8.f;
         const float mnew = move ? bm : mref;
         const float corr = (move && mref != neg_inf()) ? ex2(mref - mnew) : 1.f;
         mref = mnew;
-        const float mu = mref == neg_inf() ? 0.f : mref;
+        const float nmu = mref == neg_inf() ? 0.f : -mref;
         uint32_t pk[32];
-        float ls = 0.f;
+        float ls8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const float p0 = ex2(s[2 * i] - mu), p1 = ex2(s[2 * i + 1] - mu);
-          ls += p0 + p1;
+          const float p0 = ex2(fmaf(s[2 * i], scale_log2, nmu));
+          const float p1 = ex2(fmaf(s[2 * i + 1], scale_log2, nmu));
+          ls8[i & 7] += p0 + p1;
           pk[i] = pack_bf16(p0, p1);
         }
+        const float ls = ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) +
+                         ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
         l = l * corr + ls;
         // the previous block's P V is done before P_t and O_t are touched
         if (j > 0) await(sm, &sm.pdone[t], (uint32_t)((j - 1) & 1));
