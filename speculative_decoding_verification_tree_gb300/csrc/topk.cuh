@@ -334,11 +334,10 @@ __device__ void row_topk(const T* __restrict__ rp, int V, int k, float kt, Cand*
 
 // Streaming top-k, bound-and-rescan form (aligned rows).  One pass in which
 // every thread keeps its running maximum (and, if lse is wanted, the row's
-// log-sum-exp); the smallest over the warps of each warp's ceil(k / warps)-th
-// largest thread maximum is a lower bound on the k-th largest logit, so only
-// the threads whose maximum reaches it have logits at or above it: the CTA
-// rescans just those threads' logits (recently read, from L2) and ranks the
-// candidates exactly by (logit desc, index asc).
+// log-sum-exp); the k-th largest thread maximum is a lower bound on the k-th
+// largest logit, so only the threads whose maximum reaches it have logits at
+// or above it: the CTA rescans just those threads' logits (recently read,
+// from L2) and ranks the candidates exactly by (logit desc, index asc).
 // Rows where that leaves fewer than k or more than kCandCap candidates (many
 // ties at the bound, NaN, -inf) take row_topk.  Same outputs as row_topk.
 constexpr int kCandCap = 1024;
@@ -412,39 +411,24 @@ __device__ void row_topk_fast(const T* __restrict__ rp, int V, int k, float kt, 
         red_z[warp] = ms.z;
       }
     }
-    // bound: each warp's m-th largest thread maximum, m = ceil(k / warps)
-    // (a bitonic sort of the warp's 32 order keys by shuffles); the smallest
-    // of them is reached by the maxima of at least m threads in every warp,
-    // so at least k logits are at or above it: a lower bound on the k-th
-    // largest logit
+    // bound: k-th largest thread maximum (order keys; radix select by warp 0)
     const uint32_t mykey = fkey(mx);
-    uint32_t sk = mykey;
-#pragma unroll
-    for (int size = 2; size <= 32; size <<= 1) {
-#pragma unroll
-      for (int stride = size >> 1; stride > 0; stride >>= 1) {
-        const uint32_t other = __shfl_xor_sync(0xffffffffu, sk, stride);
-        const bool desc = (lane & size) == 0;  // every lane at size 32
-        const bool lower = (lane & stride) == 0;
-        sk = (lower == desc) ? max(sk, other) : min(sk, other);
-      }
-    }
-    const int mth = (k + kWarps - 1) / kWarps;  // <= 16 for k <= kMaxK
-    const uint32_t tw = __shfl_sync(0xffffffffu, sk, (mth - 1) & 31);
-    if (lane == 0) hist[warp] = tw;
+    smem[tid] = Cand{mykey, tid};
     if (tid == 0) {
       s_nc = 0;
       s_nf = 0;
     }
     __syncthreads();
-    if (tid == 0) {
-      uint32_t t = hist[0];
-      for (int w = 1; w < kWarps; ++w) t = min(t, hist[w]);
-      s_tau = t;
-      if (lse) {
-        MaxSum A{red_m[0], red_z[0]};
-        for (int w = 1; w < kWarps; ++w) A = ms_combine(A, MaxSum{red_m[w], red_z[w]});
-        *lse = A.m + log2f(A.z);
+    if (warp == 0) {
+      uint32_t kth = 0u;
+      warp_select(smem, kNT, k, lane, hist, &kth);
+      if (lane == 0) {
+        s_tau = kth;
+        if (lse) {
+          MaxSum A{red_m[0], red_z[0]};
+          for (int w = 1; w < kWarps; ++w) A = ms_combine(A, MaxSum{red_m[w], red_z[w]});
+          *lse = A.m + log2f(A.z);
+        }
       }
     }
     __syncthreads();

@@ -18,13 +18,16 @@
 // one stream of its keys and values -- as two 128-row tiles:
 //   warp 0     TMA producer: 64-key blocks of K and V (128-byte swizzle) into
 //              a 3-stage shared-memory ring;
+//              (and prefetches blocks further ahead into L2);
 //   warp 1     allocates TMEM and issues, per key block and tile t,
 //              S_t = Q_t K^T (tcgen05.mma M 128, N 64, K 128) into one of two
-//              S buffers -- the next block's S is computed while the softmax
-//              works on this one -- and, once the softmax has written P_t,
-//              O_t += P_t V (M 128, N 128, K 64; V is the MN-major operand,
-//              read as stored);
-//   warps 2-9  softmax, one thread per query row (warp w reads TMEM lanes of
+//              S buffers, as soon as the block's keys have landed and the
+//              softmax has released that buffer;
+//   warp 2     issues O_t += P_t V (M 128, N 128, K 64; V is the MN-major
+//              operand, read as stored) as soon as the softmax has written
+//              P_t -- two issuing threads, so that waiting for the next
+//              block's keys never holds back this block's P V;
+//   warps 3-10 softmax, one thread per query row (warp w reads TMEM lanes of
 //              quadrant w % 4): they stage Q once, then per block read S with
 //              tcgen05.ld, apply the scale and the tree mask, run the online
 //              base-2 softmax against a reference maximum that moves only when
@@ -60,14 +63,15 @@ constexpr int kPTile = kMT * kKB * 2;    // 16 KB: 128 rows x 64 keys
 constexpr int kOffKV = kTiles * kQTile;                  // 64 KB
 constexpr int kOffP = kOffKV + kAStages * kAStage;       // 160 KB
 constexpr int kOffBar = kOffP + kTiles * kPTile;         // 192 KB
-constexpr int kAThreads = 320;
+constexpr int kAThreads = 352;
+constexpr int kPrefetch = 6;  // key blocks prefetched into L2 ahead of the ring
 constexpr int kSoftThreads = 256;
 constexpr uint32_t kATmemCols = 512;
 
 struct __align__(8) AttnSmem {
   uint64_t kvfull[kAStages], kvempty[kAStages];
-  uint64_t sfull[kTiles][2], pfull[kTiles], pdone[kTiles];
-  uint64_t qready, drain;
+  uint64_t sfull[kTiles][2], sfree[kTiles][2], pfull[kTiles], pdone[kTiles];
+  uint64_t qready, drain, drain2;
   uint32_t tmem_base;
   uint32_t dead;
 };
@@ -114,6 +118,12 @@ __device__ __forceinline__ void tma2d(uint32_t dst, const CUtensorMap* map, int 
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
       : "memory");
+}
+__device__ __forceinline__ void tma2d_prefetch(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
 }
 __device__ __forceinline__ void mma_f16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
                                         uint32_t acc) {
@@ -216,11 +226,14 @@ __global__ void __launch_bounds__(kAThreads, 1)
     for (int t = 0; t < kTiles; ++t) {
       mbar_init(&sm.sfull[t][0], 1);
       mbar_init(&sm.sfull[t][1], 1);
+      mbar_init(&sm.sfree[t][0], kMT);
+      mbar_init(&sm.sfree[t][1], kMT);
       mbar_init(&sm.pfull[t], kMT);
       mbar_init(&sm.pdone[t], 1);
     }
     mbar_init(&sm.qready, kSoftThreads);
     mbar_init(&sm.drain, 1);
+    mbar_init(&sm.drain2, 1);
     sm.dead = 0;
     fence_mbar_init();
   }
@@ -239,8 +252,17 @@ __global__ void __launch_bounds__(kAThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      auto prefetch = [&](int j) {
+        const int y = kvrow0 + j * kKB;
+        tma2d_prefetch(&map_k, 0, y);
+        tma2d_prefetch(&map_k, 64, y);
+        tma2d_prefetch(&map_v, 0, y);
+        tma2d_prefetch(&map_v, 64, y);
+      };
+      for (int j = kAStages; j < kAStages + kPrefetch && j < nblk; ++j) prefetch(j);
       for (int j = 0; j < nblk; ++j) {
         const int s = j % kAStages;
+        if (j + kAStages + kPrefetch < nblk) prefetch(j + kAStages + kPrefetch);
         await(sm, &sm.kvempty[s], ((uint32_t)(j / kAStages) & 1u) ^ 1u);
         mbar_expect_tx(&sm.kvfull[s], (uint32_t)kAStage);
         const uint32_t st = base + kOffKV + (uint32_t)(s * kAStage);
@@ -257,31 +279,18 @@ __global__ void __launch_bounds__(kAThreads, 1)
       }
     }
   } else if (warp == 1) {
-    // ----------------------------------------------------------------- MMA
+    // ------------------------------------------------------------ S = Q K^T
     if (lane == 0) {
       await(sm, &sm.qready, 0);
       fence_after();
-      // S_t of block j into buffer j & 1 (its previous contents, block j - 2,
-      // were read before the softmax released P of block j - 2)
-      auto issue_s = [&](int j) {
+      for (int j = 0; j < nblk; ++j) {
         const int s = j % kAStages;
         await(sm, &sm.kvfull[s], (uint32_t)(j / kAStages) & 1u);
         const uint32_t kst = base + kOffKV + (uint32_t)(s * kAStage);
-        const int tail = L - j * kKB;  // keys of this block that exist
-        if (tail < kKB) {
-          // cache rows past the sequence's keys hold anything (NaN included);
-          // their P is 0, but 0 * NaN is not, so their V rows become zeros
-          unsigned char* vz = bp + kOffKV + s * kAStage + kKVTile;
-          for (int rr = tail; rr < kKB; ++rr)
-            for (int hb = 0; hb < 2; ++hb) {
-              uint4* z = reinterpret_cast<uint4*>(vz + hb * kKVHalf + rr * 128);
-#pragma unroll
-              for (int c = 0; c < 8; ++c) z[c] = make_uint4(0u, 0u, 0u, 0u);
-            }
-          fence_async_smem();
-        }
-        fence_after();
         for (int t = 0; t < ntile; ++t) {
+          // S buffer j & 1 was last read by the softmax at block j - 2
+          if (j >= 2) await(sm, &sm.sfree[t][j & 1], (uint32_t)(((j >> 1) - 1) & 1));
+          fence_after();
           const uint32_t qt = base + (uint32_t)(t * kQTile);
           const uint32_t ds = tmem + (uint32_t)(64 * (2 * t + (j & 1)));
 #pragma unroll
@@ -293,12 +302,32 @@ __global__ void __launch_bounds__(kAThreads, 1)
           }
           mma_commit(&sm.sfull[t][j & 1]);
         }
-      };
-      if (nblk > 0) issue_s(0);
+      }
+      mma_commit(&sm.drain);
+      mbar_wait_bounded(&sm.drain, 0);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------- O += P V
+    if (lane == 0) {
       for (int j = 0; j < nblk; ++j) {
         const int s = j % kAStages;
-        if (j + 1 < nblk) issue_s(j + 1);
+        // the block's V landed (the S issuer waited for it too)
+        await(sm, &sm.kvfull[s], (uint32_t)(j / kAStages) & 1u);
         const uint32_t vst = base + kOffKV + (uint32_t)(s * kAStage) + kKVTile;
+        const int tail = L - j * kKB;  // keys of this block that exist
+        if (tail < kKB) {
+          // cache rows past the sequence's keys hold anything (NaN included);
+          // their P is 0, but 0 * NaN is not, so their V rows become zeros
+          // (written by this thread, made visible to its own MMAs below)
+          unsigned char* vz = bp + kOffKV + s * kAStage + kKVTile;
+          for (int rr = tail; rr < kKB; ++rr)
+            for (int hb = 0; hb < 2; ++hb) {
+              uint4* z = reinterpret_cast<uint4*>(vz + hb * kKVHalf + rr * 128);
+#pragma unroll
+              for (int c = 0; c < 8; ++c) z[c] = make_uint4(0u, 0u, 0u, 0u);
+            }
+          fence_async_smem();
+        }
         for (int t = 0; t < ntile; ++t) {
           await(sm, &sm.pfull[t], (uint32_t)(j & 1));
           fence_after();
@@ -310,14 +339,16 @@ __global__ void __launch_bounds__(kAThreads, 1)
                     (j > 0 || k > 0) ? 1u : 0u);
           mma_commit(&sm.pdone[t]);
         }
+        // K and V of the block are free: the softmax read S (so the S MMAs
+        // are done) before releasing P, and these P V MMAs are committed
         mma_commit(&sm.kvempty[s]);
       }
-      mma_commit(&sm.drain);
-      mbar_wait_bounded(&sm.drain, 0);
+      mma_commit(&sm.drain2);
+      mbar_wait_bounded(&sm.drain2, 0);
     }
   } else {
     // ------------------------------------------------------------- softmax
-    const int t = (warp - 2) >> 2;   // tile
+    const int t = (warp - 3) >> 2;   // tile
     const int qd = warp & 3;         // TMEM lane quadrant of this warp
     const int r = qd * 32 + lane;    // row within the tile
     const int gr = row0 + t * kMT + r;
@@ -351,6 +382,8 @@ __global__ void __launch_bounds__(kAThreads, 1)
         tld32(tSb, ra);
         tld32(tSb + 32u, rb);
         tld_wait();
+        fence_before();
+        mbar_arrive(&sm.sfree[t][j & 1]);  // the S issuer may refill the buffer
         // raw scores q.k (the scale is applied inside the exponent below;
         // it is positive, so the maximum is taken on the raw scores)
         float s[64];
