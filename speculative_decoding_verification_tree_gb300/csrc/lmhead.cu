@@ -24,7 +24,12 @@
 //              row per thread), bf16 rounding, stores, tile statistics.
 // Tiles are taken in vocabulary-block-major order so that the CTAs working at
 // one time share a few 256-row slices of W through L2 while the hidden states
-// (a few MB) stay resident.  Every mbarrier wait is bounded: a wait that gives
+// (a few MB) stay resident.  CTAs run in clusters of two that take the two
+// 128-row halves of a 256-row block of the same W tile: each loads its own
+// hidden tile and one 128-row half of the W tile, multicast into both CTAs'
+// shared memory, so a CTA pulls 32 KB instead of 48 KB from L2 per K step; a
+// ring stage is refilled only when both CTAs' MMAs have released it (each
+// MMA commit arrives on both CTAs' "empty" barriers).  Every mbarrier wait is bounded: a wait that gives
 // up sets SPEC_STATUS_TIMEOUT and a CTA-wide flag after which no wait blocks,
 // and before TMEM is freed the CTA waits (again bounded) for its own MMAs and
 // copies in flight.
@@ -60,7 +65,7 @@ constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + 1024 + sizeof(Gemm
 
 struct GemmParams {
   int M, N, K;
-  int nm, nn, ntiles, nkb;
+  int nm, nn, ntiles, nkb;  // ntiles: work units (tiles, or tile pairs)
   uint16_t* logits;  // [M, ldo] bf16 bits
   int64_t ldo;
   float2* stats;     // [M, nn] (max, sum) in base 2 at kt, or null
@@ -108,6 +113,18 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// The same box into this CTA and its cluster peer (same shared-memory
+// offsets), completing its bytes on each CTA's barrier at `bar`'s offset.
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                               uint64_t* bar, uint16_t mask, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".multicast::cluster.L2::cache_hint [%0], [%1, {%4, %5}], [%2], %3, %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "h"(mask), "r"(x), "r"(y),
+      "l"(policy)
+      : "memory");
+}
+
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                           uint32_t accumulate) {
   asm volatile(
@@ -120,6 +137,15 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           smem_u32(bar))
+      : "memory");
+}
+
+// Commit arriving on the barrier at the same offset in every CTA of `mask`.
+__device__ __forceinline__ void umma_commit_mc(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_u32(bar)),
+      "h"(mask)
       : "memory");
 }
 
@@ -146,9 +172,19 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+template <int CL>  // CTAs per cluster: 1, or 2 sharing each W tile
 __global__ void __launch_bounds__(kThreads, 1)
     lmhead_gemm(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                 GemmParams P) {
+  const int rank = CL == 2 ? (int)cluster_ctarank() : 0;
+  const int unit0 = CL == 2 ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int units = CL == 2 ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  const int nmu = CL == 2 ? (P.nm + 1) >> 1 : P.nm;  // M units per W tile
+  // work unit -> (m tile, n tile) of this CTA
+  auto tile_of = [&](int t, int& mb, int& nb) {
+    nb = t / nmu;
+    mb = CL == 2 ? 2 * (t - nb * nmu) + rank : t - nb * nmu;
+  };
   extern __shared__ __align__(1024) unsigned char dyn_raw[];
   // the ring starts on a 1024-byte boundary (128-byte swizzle atoms)
   const uint32_t raw = smem_u32(dyn_raw);
@@ -160,7 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.full[s], 1);
-      mbar_init(&sm.empty[s], 1);
+      mbar_init(&sm.empty[s], CL);  // released by the MMAs of every CTA
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&sm.tfull[a], 1);
@@ -179,6 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (CL == 2) cluster_sync();  // the peer's barriers exist before any multicast
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
 
@@ -192,8 +229,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       uint32_t fills[kStages] = {};  // copies issued into each stage
       bool stall_pending = blockIdx.x == 0;  // the test stall: CTA 0 only
-      for (int t = blockIdx.x; t < P.ntiles; t += gridDim.x) {
-        const int mb = t % P.nm, nb = t / P.nm;
+      for (int t = unit0; t < P.ntiles; t += units) {
+        int mb, nb;
+        tile_of(t, mb, nb);
         for (int kb = 0; kb < P.nkb; ++kb) {
           gwait(sm, &sm.empty[stage], phase ^ 1u, P.status);
           const uint32_t sa = ring + (uint32_t)(stage * kStageBytes);
@@ -204,7 +242,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             mbar_expect_tx(&sm.full[stage], (uint32_t)kStageBytes);
             tma_load_2d(sa, &map_a, kb * BK, mb * BM, &sm.full[stage], pol_a);
-            tma_load_2d(sa + kABytes, &map_b, kb * BK, nb * BN, &sm.full[stage], pol_b);
+            if constexpr (CL == 2) {
+              // this CTA's half of the W tile, into both CTAs
+              const uint32_t half = (uint32_t)(kBBytes / 2);
+              tma_load_2d_mc(sa + kABytes + (uint32_t)rank * half, &map_b, kb * BK,
+                             nb * BN + rank * (BN / 2), &sm.full[stage], (uint16_t)3, pol_b);
+            } else {
+              tma_load_2d(sa + kABytes, &map_b, kb * BK, nb * BN, &sm.full[stage], pol_b);
+            }
             ++fills[stage];
           }
           if (++stage == kStages) {
@@ -223,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
-      for (int t = blockIdx.x; t < P.ntiles; t += gridDim.x) {
+      for (int t = unit0; t < P.ntiles; t += units) {
         gwait(sm, &sm.tempty[acc], acc_phase ^ 1u, P.status);
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(acc * BN);
@@ -235,7 +280,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)  // +32 bytes of K per step
             umma_bf16(d, da + 2u * k, db + 2u * k, (kb | k) != 0 ? 1u : 0u);
-          umma_commit(&sm.empty[stage]);
+          if constexpr (CL == 2) umma_commit_mc(&sm.empty[stage], (uint16_t)3);
+          else umma_commit(&sm.empty[stage]);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
@@ -258,12 +304,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     const bool vec = (P.ldo % 8) == 0 && ((uintptr_t)P.logits % 16) == 0;
-    for (int t = blockIdx.x; t < P.ntiles; t += gridDim.x) {
-      const int mb = t % P.nm, nb = t / P.nm;
+    for (int t = unit0; t < P.ntiles; t += units) {
+      int mb, nb;
+      tile_of(t, mb, nb);
       gwait(sm, &sm.tfull[acc], acc_phase, P.status);
       tc_fence_after();
       const int row = mb * BM + r_in;
-      const bool live = row < P.M;
+      const bool live = row < P.M;  // (the odd last M tile's partner: none)
       uint16_t* out = P.logits + (int64_t)(live ? row : 0) * P.ldo;
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
       float m = neg_inf(), s = 0.f;
@@ -328,6 +375,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  // no CTA leaves while its peer may still multicast into it or arrive on
+  // its barriers
+  if (CL == 2) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
@@ -392,16 +442,19 @@ cudaError_t launch_lmhead(const void* hidden, const void* w, int M, int H, int V
                           uint32_t* status, cudaStream_t st, bool test_stall) {
   if (M == 0) return cudaSuccess;
   if (!lmhead_supported(hidden, w, H)) return cudaErrorInvalidValue;
+  // clusters of two CTAs share each W tile when there are two M tiles to pair
+  const int nm = (M + BM - 1) / BM;
+  const int CL = nm >= 2 ? 2 : 1;
   CUtensorMap ma, mb;
-  if (!make_map(&ma, hidden, M, H, BM) || !make_map(&mb, w, V, H, BN))
+  if (!make_map(&ma, hidden, M, H, BM) || !make_map(&mb, w, V, H, BN / CL))
     return cudaErrorInvalidValue;
   GemmParams P{};
   P.M = M;
   P.N = V;
   P.K = H;
-  P.nm = (M + BM - 1) / BM;
+  P.nm = nm;
   P.nn = (V + BN - 1) / BN;
-  P.ntiles = P.nm * P.nn;
+  P.ntiles = ((P.nm + CL - 1) / CL) * P.nn;  // work units
   P.nkb = (H + BK - 1) / BK;
   P.logits = logits;
   P.ldo = ldo;
@@ -414,13 +467,27 @@ cudaError_t launch_lmhead(const void* hidden, const void* w, int M, int H, int V
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(lmhead_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)kSmemBytes);
+  auto kern = CL == 2 ? lmhead_gemm<2> : lmhead_gemm<1>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
-  const int grid = P.ntiles < sms ? P.ntiles : sms;
+  const int slots = sms / CL;  // clusters (or CTAs) resident at once
+  const int units = P.ntiles < slots ? P.ntiles : slots;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(units * CL));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   prof_begin(SPEC_PROF_LMHEAD, st);
-  lmhead_gemm<<<grid, kThreads, kSmemBytes, st>>>(ma, mb, P);
+  e = cudaLaunchKernelEx(&cfg, kern, ma, mb, P);
   prof_end(SPEC_PROF_LMHEAD, st);
+  if (e != cudaSuccess) return e;
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (P.stats && lse) {
