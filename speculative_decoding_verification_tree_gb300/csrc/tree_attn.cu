@@ -19,14 +19,14 @@
 //   warp 0     TMA producer: 64-key blocks of K and V (128-byte swizzle) into
 //              a 3-stage shared-memory ring;
 //              (and prefetches blocks further ahead into L2);
-//   warp 1     allocates TMEM and issues, per key block and tile t,
-//              S_t = Q_t K^T (tcgen05.mma M 128, N 64, K 128) into one of two
-//              S buffers, as soon as the block's keys have landed and the
-//              softmax has released that buffer;
-//   warp 2     issues O_t += P_t V (M 128, N 128, K 64; V is the MN-major
-//              operand, read as stored) as soon as the softmax has written
-//              P_t -- two issuing threads, so that waiting for the next
-//              block's keys never holds back this block's P V;
+//   warps 1-2  one tensor-core issuer per tile t (warp 1 also allocates
+//              TMEM): S_t = Q_t K^T of the next key block (tcgen05.mma M 128,
+//              N 64, K 128) into one of two S buffers once the block's keys
+//              have landed and the softmax has released that buffer, then
+//              O_t += P_t V of this block (M 128, N 128, K 64; V is the
+//              MN-major operand, read as stored) once the softmax has written
+//              P_t -- one thread per tile, so the tiles never wait on each
+//              other;
 //   warps 3-10 softmax, one thread per query row (warp w reads TMEM lanes of
 //              quadrant w % 4): they stage Q once, then per block read S with
 //              tcgen05.ld, apply the scale and the tree mask, run the online
@@ -71,7 +71,7 @@ constexpr uint32_t kATmemCols = 512;
 struct __align__(8) AttnSmem {
   uint64_t kvfull[kAStages], kvempty[kAStages];
   uint64_t sfull[kTiles][2], sfree[kTiles][2], pfull[kTiles], pdone[kTiles];
-  uint64_t qready, drain, drain2;
+  uint64_t qready, drain[kTiles];
   uint32_t tmem_base;
   uint32_t dead;
 };
@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(kAThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kAStages; ++s) {
       mbar_init(&sm.kvfull[s], 1);
-      mbar_init(&sm.kvempty[s], 1);
+      mbar_init(&sm.kvempty[s], ntile);  // released by every tile's issuer
     }
     for (int t = 0; t < kTiles; ++t) {
       mbar_init(&sm.sfull[t][0], 1);
@@ -232,8 +232,8 @@ __global__ void __launch_bounds__(kAThreads, 1)
       mbar_init(&sm.pdone[t], 1);
     }
     mbar_init(&sm.qready, kSoftThreads);
-    mbar_init(&sm.drain, 1);
-    mbar_init(&sm.drain2, 1);
+    mbar_init(&sm.drain[0], 1);
+    mbar_init(&sm.drain[1], 1);
     sm.dead = 0;
     fence_mbar_init();
   }
@@ -278,47 +278,42 @@ __global__ void __launch_bounds__(kAThreads, 1)
         mbar_wait_bounded(&sm.kvfull[s], (uint32_t)(fills - 1) & 1u);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ S = Q K^T
-    if (lane == 0) {
+  } else if (warp <= 2) {
+    // ------------------------------------------- tile t's tensor-core issuer
+    // Warp 1 + t issues tile t's S = Q K^T of the next block, then its
+    // O += P V of this block as soon as the softmax has written P: the two
+    // tiles never wait on each other.
+    const int t = warp - 1;
+    if (lane == 0 && t < ntile) {
       await(sm, &sm.qready, 0);
       fence_after();
-      for (int j = 0; j < nblk; ++j) {
+      const uint32_t qt = base + (uint32_t)(t * kQTile);
+      auto issue_s = [&](int j) {
         const int s = j % kAStages;
         await(sm, &sm.kvfull[s], (uint32_t)(j / kAStages) & 1u);
+        // S buffer j & 1 was last read by the softmax at block j - 2
+        if (j >= 2) await(sm, &sm.sfree[t][j & 1], (uint32_t)(((j >> 1) - 1) & 1));
+        fence_after();
         const uint32_t kst = base + kOffKV + (uint32_t)(s * kAStage);
-        for (int t = 0; t < ntile; ++t) {
-          // S buffer j & 1 was last read by the softmax at block j - 2
-          if (j >= 2) await(sm, &sm.sfree[t][j & 1], (uint32_t)(((j >> 1) - 1) & 1));
-          fence_after();
-          const uint32_t qt = base + (uint32_t)(t * kQTile);
-          const uint32_t ds = tmem + (uint32_t)(64 * (2 * t + (j & 1)));
+        const uint32_t ds = tmem + (uint32_t)(64 * (2 * t + (j & 1)));
 #pragma unroll
-          for (int k = 0; k < kAD / 16; ++k) {
-            const uint32_t off = (uint32_t)((k >> 2) * kQHalf + (k & 3) * 32);
-            const uint32_t koff = (uint32_t)((k >> 2) * kKVHalf + (k & 3) * 32);
-            mma_f16(ds, desc_kmajor(qt + off), desc_kmajor(kst + koff), kIdescS,
-                    k > 0 ? 1u : 0u);
-          }
-          mma_commit(&sm.sfull[t][j & 1]);
+        for (int k = 0; k < kAD / 16; ++k) {
+          const uint32_t off = (uint32_t)((k >> 2) * kQHalf + (k & 3) * 32);
+          const uint32_t koff = (uint32_t)((k >> 2) * kKVHalf + (k & 3) * 32);
+          mma_f16(ds, desc_kmajor(qt + off), desc_kmajor(kst + koff), kIdescS, k > 0 ? 1u : 0u);
         }
-      }
-      mma_commit(&sm.drain);
-      mbar_wait_bounded(&sm.drain, 0);
-    }
-  } else if (warp == 2) {
-    // ------------------------------------------------------------- O += P V
-    if (lane == 0) {
+        mma_commit(&sm.sfull[t][j & 1]);
+      };
+      if (nblk > 0) issue_s(0);
       for (int j = 0; j < nblk; ++j) {
+        if (j + 1 < nblk) issue_s(j + 1);
         const int s = j % kAStages;
-        // the block's V landed (the S issuer waited for it too)
-        await(sm, &sm.kvfull[s], (uint32_t)(j / kAStages) & 1u);
         const uint32_t vst = base + kOffKV + (uint32_t)(s * kAStage) + kKVTile;
         const int tail = L - j * kKB;  // keys of this block that exist
         if (tail < kKB) {
           // cache rows past the sequence's keys hold anything (NaN included);
           // their P is 0, but 0 * NaN is not, so their V rows become zeros
-          // (written by this thread, made visible to its own MMAs below)
+          // (each tile's issuer writes the same zeros before its own MMAs)
           unsigned char* vz = bp + kOffKV + s * kAStage + kKVTile;
           for (int rr = tail; rr < kKB; ++rr)
             for (int hb = 0; hb < 2; ++hb) {
@@ -328,23 +323,20 @@ __global__ void __launch_bounds__(kAThreads, 1)
             }
           fence_async_smem();
         }
-        for (int t = 0; t < ntile; ++t) {
-          await(sm, &sm.pfull[t], (uint32_t)(j & 1));
-          fence_after();
-          const uint32_t pt = base + kOffP + (uint32_t)(t * kPTile);
+        await(sm, &sm.pfull[t], (uint32_t)(j & 1));
+        fence_after();
+        const uint32_t pt = base + kOffP + (uint32_t)(t * kPTile);
 #pragma unroll
-          for (int k = 0; k < kKB / 16; ++k)
-            mma_f16(tmem + 256u + (uint32_t)(128 * t), desc_kmajor(pt + (uint32_t)(k * 32)),
-                    desc_mnmajor(vst + (uint32_t)(k * 2048)), kIdescPV,
-                    (j > 0 || k > 0) ? 1u : 0u);
-          mma_commit(&sm.pdone[t]);
-        }
-        // K and V of the block are free: the softmax read S (so the S MMAs
-        // are done) before releasing P, and these P V MMAs are committed
+        for (int k = 0; k < kKB / 16; ++k)
+          mma_f16(tmem + 256u + (uint32_t)(128 * t), desc_kmajor(pt + (uint32_t)(k * 32)),
+                  desc_mnmajor(vst + (uint32_t)(k * 2048)), kIdescPV, (j > 0 || k > 0) ? 1u : 0u);
+        mma_commit(&sm.pdone[t]);
+        // this tile is done with the block's K and V (the softmax read S
+        // before releasing P, so the S MMAs are complete too)
         mma_commit(&sm.kvempty[s]);
       }
-      mma_commit(&sm.drain2);
-      mbar_wait_bounded(&sm.drain2, 0);
+      mma_commit(&sm.drain[t]);
+      mbar_wait_bounded(&sm.drain[t], 0);
     }
   } else {
     // ------------------------------------------------------------- softmax
