@@ -418,7 +418,7 @@ int spec_accept_stats(const int32_t* count, const int32_t* parent,
  * prefix_len not 4-byte aligned, or mask_bits not 8-byte aligned;
  * SPEC_ERR_SHAPE when B * Hkv * S reaches 2^31 cache rows; SPEC_ERR_CUDA if
  * the caches cannot be described to the copy engine.  B == 0 does nothing.
- * Runs on the tensor cores (tcgen05): one CTA per 128 query rows of one
+ * Runs on the tensor cores (tcgen05): one CTA per 256 query rows of one
  * (sequence, key/value head).
  */
 int spec_tree_attention(const void* q, const void* k_cache,

@@ -12,27 +12,31 @@
 // with grouped-query heads (query head h reads key/value head h / (Hq/Hkv)).
 //
 // Organisation (head dim 128, bf16 inputs, float32 accumulation) on the
-// fifth-generation tensor cores.  A CTA takes 128 query rows of one
+// fifth-generation tensor cores.  A CTA takes up to 256 query rows of one
 // (sequence, key/value head) -- the rows are (node, head in the group) pairs,
 // node-major, so the G query heads that share a key/value head are served by
-// one stream of its keys and values; the CTAs of the other rows of the same
-// head are adjacent in launch order and meet the same keys in L2:
-//   warp 0     TMA producer: 128-key blocks of K and V (128-byte swizzle) into
-//              a 2-stage shared-memory ring, and L2 prefetches further ahead;
-//   warp 1     allocates TMEM and issues the next block's S = Q K^T
-//              (tcgen05.mma M 128, N 128, K 128) into one of two S buffers
-//              once its keys have landed and the softmax has released that
-//              buffer, then this block's O += P V (M 128, N 128, K 128; V is
-//              the MN-major operand, read as stored) once the softmax has
-//              written P;
-//   warps 2-5  softmax, one thread per query row (warp w reads TMEM lanes of
+// one stream of its keys and values -- as two 128-row tiles:
+//   warp 0     TMA producers: 64-key blocks of K (lane 0) and of V (lane 1)
+//              (128-byte swizzle) into a 3-stage shared-memory ring whose K
+//              and V halves are released separately -- K once both tiles' S
+//              MMAs have read it, V after their P V -- and prefetches of
+//              blocks further ahead into L2;
+//   warps 1-2  one tensor-core issuer per tile t (warp 1 also allocates
+//              TMEM): S_t = Q_t K^T of the next key block (tcgen05.mma M 128,
+//              N 64, K 128) into one of two S buffers once the block's keys
+//              have landed and the softmax has released that buffer, then
+//              O_t += P_t V of this block (M 128, N 128, K 64; V is the
+//              MN-major operand, read as stored) once the softmax has written
+//              P_t -- one thread per tile, so the tiles never wait on each
+//              other;
+//   warps 3-10 softmax, one thread per query row (warp w reads TMEM lanes of
 //              quadrant w % 4): they stage Q once, then per block read S with
 //              tcgen05.ld, apply the scale and the tree mask, run the online
 //              base-2 softmax against a reference maximum that moves only when
-//              a row's maximum grows by more than 2^8 (then O is rescaled in
+//              a row's maximum grows by more than 2^8 (then O_t is rescaled in
 //              TMEM), and write P as bf16 into 128-byte-swizzled shared memory
-//              for the P V MMA; at the end O / l is rounded to bf16.
-// TMEM: S buffer u at columns 128 u, O at 256 (384 of 512).  Every mbarrier
+//              for the next MMA; at the end O_t / l is rounded to bf16.
+// TMEM: S_t of buffer u at columns 64 (2 t + u), O_t at 256 + 128 t.  Every mbarrier
 // wait is bounded (SPEC_STATUS_TIMEOUT is not reported by this entry point,
 // which has no status word; a CTA that gives up stops waiting and still frees
 // its TMEM after waiting, bounded, for its own MMAs and copies).
@@ -47,35 +51,35 @@
 namespace sv {
 namespace {
 
-constexpr int kAD = 128;    // head dim
-constexpr int kKB = 128;    // keys per block
-constexpr int kMT = 128;    // query rows per CTA
-constexpr int kAStages = 2;
+constexpr int kAD = 128;   // head dim
+constexpr int kKB = 64;    // keys per block
+constexpr int kMT = 128;   // query rows per tile
+constexpr int kTiles = 2;  // tiles per CTA
+constexpr int kAStages = 3;
 constexpr int kQHalf = kMT * 64 * 2;     // 16 KB: 128 rows x 64 dims
 constexpr int kQTile = 2 * kQHalf;       // 32 KB
-constexpr int kKVHalf = kKB * 64 * 2;    // 16 KB: 128 keys x 64 dims
-constexpr int kKVTile = 2 * kKVHalf;     // 32 KB
-constexpr int kAStage = 2 * kKVTile;     // K then V: 64 KB
-constexpr int kPHalf = kMT * 64 * 2;     // 16 KB: 128 rows x 64 keys
-constexpr int kPTile = 2 * kPHalf;       // 32 KB
-constexpr int kOffKV = kQTile;                        // 32 KB
-constexpr int kOffP = kOffKV + kAStages * kAStage;    // 160 KB
-constexpr int kOffBar = kOffP + kPTile;               // 192 KB
-constexpr int kAThreads = 192;
-constexpr int kPrefetch = 3;  // key blocks prefetched into L2 ahead of the ring
-constexpr int kSoftThreads = 128;
+constexpr int kKVHalf = kKB * 64 * 2;    // 8 KB: 64 keys x 64 dims
+constexpr int kKVTile = 2 * kKVHalf;     // 16 KB
+constexpr int kAStage = 2 * kKVTile;     // K then V: 32 KB
+constexpr int kPTile = kMT * kKB * 2;    // 16 KB: 128 rows x 64 keys
+constexpr int kOffKV = kTiles * kQTile;                  // 64 KB
+constexpr int kOffP = kOffKV + kAStages * kAStage;       // 160 KB
+constexpr int kOffBar = kOffP + kTiles * kPTile;         // 192 KB
+constexpr int kAThreads = 352;
+constexpr int kPrefetch = 6;  // key blocks prefetched into L2 ahead of the ring
+constexpr int kSoftThreads = 256;
 constexpr uint32_t kATmemCols = 512;
 
 struct __align__(8) AttnSmem {
-  uint64_t kvfull[kAStages], kvempty[kAStages];
-  uint64_t sfull[2], sfree[2], pfull, pdone;
-  uint64_t qready, drain;
+  uint64_t kfull[kAStages], kempty[kAStages], vfull[kAStages], vempty[kAStages];
+  uint64_t sfull[kTiles][2], sfree[kTiles][2], pfull[kTiles], pdone[kTiles];
+  uint64_t qready, drain[kTiles];
   uint32_t tmem_base;
   uint32_t dead;
 };
 constexpr size_t kASmemBytes = (size_t)kOffBar + sizeof(AttnSmem) + 1024;
 
-// S = Q K^T: M 128, N 128, bf16 K-major A and B, float32 D.
+// S = Q K^T: M 128, N 64, bf16 K-major A and B, float32 D.
 constexpr uint32_t kIdescS = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kKB >> 3) << 17) |
                              ((uint32_t)(kMT >> 4) << 24);
 // O += P V: M 128, N 128, A K-major, B MN-major (bit 16).
@@ -208,7 +212,8 @@ __global__ void __launch_bounds__(kAThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.z, kvh = blockIdx.y;
   const int G = Hq / Hkv, R = N * G;
-  const int row0 = blockIdx.x * kMT;
+  const int row0 = blockIdx.x * (kTiles * kMT);
+  const int ntile = min(kTiles, (R - row0 + kMT - 1) / kMT);
   int P = prefix_len[b];
   P = P < 0 ? 0 : (P > S - N ? S - N : P);
   const int L = P + N;
@@ -217,17 +222,22 @@ __global__ void __launch_bounds__(kAThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kAStages; ++s) {
-      mbar_init(&sm.kvfull[s], 1);
-      mbar_init(&sm.kvempty[s], 1);
+      mbar_init(&sm.kfull[s], 1);
+      mbar_init(&sm.kempty[s], ntile);  // released by every tile's issuer
+      mbar_init(&sm.vfull[s], 1);
+      mbar_init(&sm.vempty[s], ntile);
     }
-    for (int u = 0; u < 2; ++u) {
-      mbar_init(&sm.sfull[u], 1);
-      mbar_init(&sm.sfree[u], kMT);
+    for (int t = 0; t < kTiles; ++t) {
+      mbar_init(&sm.sfull[t][0], 1);
+      mbar_init(&sm.sfull[t][1], 1);
+      mbar_init(&sm.sfree[t][0], kMT);
+      mbar_init(&sm.sfree[t][1], kMT);
+      mbar_init(&sm.pfull[t], kMT);
+      mbar_init(&sm.pdone[t], 1);
     }
-    mbar_init(&sm.pfull, kMT);
-    mbar_init(&sm.pdone, 1);
     mbar_init(&sm.qready, kSoftThreads);
-    mbar_init(&sm.drain, 1);
+    mbar_init(&sm.drain[0], 1);
+    mbar_init(&sm.drain[1], 1);
     sm.dead = 0;
     fence_mbar_init();
   }
@@ -245,7 +255,15 @@ __global__ void __launch_bounds__(kAThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    // lane 0 fills the K halves of the ring, lane 1 the V halves: K of a
+    // block is released once both tiles' S MMAs have read it, V only after
+    // their P V, so the next blocks' keys never wait for this block's P V
+    if (lane < 2) {
+      const bool isk = lane == 0;
+      const CUtensorMap* map = isk ? &map_k : &map_v;
+      uint64_t* full = isk ? sm.kfull : sm.vfull;
+      uint64_t* empty = isk ? sm.kempty : sm.vempty;
+      const uint32_t half = isk ? 0u : (uint32_t)kKVTile;
       auto prefetch = [&](int j) {
         const int y = kvrow0 + j * kKB;
         tma2d_prefetch(&map_k, 0, y);
@@ -253,55 +271,62 @@ __global__ void __launch_bounds__(kAThreads, 1)
         tma2d_prefetch(&map_v, 0, y);
         tma2d_prefetch(&map_v, 64, y);
       };
-      for (int j = kAStages; j < kAStages + kPrefetch && j < nblk; ++j) prefetch(j);
+      if (isk)
+        for (int j = kAStages; j < kAStages + kPrefetch && j < nblk; ++j) prefetch(j);
       for (int j = 0; j < nblk; ++j) {
         const int s = j % kAStages;
-        if (j + kAStages + kPrefetch < nblk) prefetch(j + kAStages + kPrefetch);
-        await(sm, &sm.kvempty[s], ((uint32_t)(j / kAStages) & 1u) ^ 1u);
-        mbar_expect_tx(&sm.kvfull[s], (uint32_t)kAStage);
-        const uint32_t st = base + kOffKV + (uint32_t)(s * kAStage);
+        if (isk && j + kAStages + kPrefetch < nblk) prefetch(j + kAStages + kPrefetch);
+        await(sm, &empty[s], ((uint32_t)(j / kAStages) & 1u) ^ 1u);
+        mbar_expect_tx(&full[s], (uint32_t)kKVTile);
+        const uint32_t st = base + kOffKV + (uint32_t)(s * kAStage) + half;
         const int y = kvrow0 + j * kKB;
-        tma2d(st, &map_k, 0, y, &sm.kvfull[s]);
-        tma2d(st + kKVHalf, &map_k, 64, y, &sm.kvfull[s]);
-        tma2d(st + kKVTile, &map_v, 0, y, &sm.kvfull[s]);
-        tma2d(st + kKVTile + kKVHalf, &map_v, 64, y, &sm.kvfull[s]);
+        tma2d(st, map, 0, y, &full[s]);
+        tma2d(st + kKVHalf, map, 64, y, &full[s]);
       }
       // this CTA's last copy into each stage has landed before it exits
       for (int s = 0; s < kAStages && s < nblk; ++s) {
         const int fills = (nblk - s + kAStages - 1) / kAStages;
-        mbar_wait_bounded(&sm.kvfull[s], (uint32_t)(fills - 1) & 1u);
+        mbar_wait_bounded(&full[s], (uint32_t)(fills - 1) & 1u);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------ tensor-core issuer
-    if (lane == 0) {
+  } else if (warp <= 2) {
+    // ------------------------------------------- tile t's tensor-core issuer
+    // Warp 1 + t issues tile t's S = Q K^T of the next block, then its
+    // O += P V of this block as soon as the softmax has written P: the two
+    // tiles never wait on each other.
+    const int t = warp - 1;
+    if (lane == 0 && t < ntile) {
       await(sm, &sm.qready, 0);
       fence_after();
+      const uint32_t qt = base + (uint32_t)(t * kQTile);
       auto issue_s = [&](int j) {
         const int s = j % kAStages;
-        await(sm, &sm.kvfull[s], (uint32_t)(j / kAStages) & 1u);
+        await(sm, &sm.kfull[s], (uint32_t)(j / kAStages) & 1u);
         // S buffer j & 1 was last read by the softmax at block j - 2
-        if (j >= 2) await(sm, &sm.sfree[j & 1], (uint32_t)(((j >> 1) - 1) & 1));
+        if (j >= 2) await(sm, &sm.sfree[t][j & 1], (uint32_t)(((j >> 1) - 1) & 1));
         fence_after();
         const uint32_t kst = base + kOffKV + (uint32_t)(s * kAStage);
-        const uint32_t ds = tmem + (uint32_t)(128 * (j & 1));
+        const uint32_t ds = tmem + (uint32_t)(64 * (2 * t + (j & 1)));
 #pragma unroll
         for (int k = 0; k < kAD / 16; ++k) {
           const uint32_t off = (uint32_t)((k >> 2) * kQHalf + (k & 3) * 32);
           const uint32_t koff = (uint32_t)((k >> 2) * kKVHalf + (k & 3) * 32);
-          mma_f16(ds, desc_kmajor(base + off), desc_kmajor(kst + koff), kIdescS, k > 0 ? 1u : 0u);
+          mma_f16(ds, desc_kmajor(qt + off), desc_kmajor(kst + koff), kIdescS, k > 0 ? 1u : 0u);
         }
-        mma_commit(&sm.sfull[j & 1]);
+        mma_commit(&sm.sfull[t][j & 1]);
+        mma_commit(&sm.kempty[s]);  // this tile is done with the block's K
       };
       if (nblk > 0) issue_s(0);
       for (int j = 0; j < nblk; ++j) {
         if (j + 1 < nblk) issue_s(j + 1);
         const int s = j % kAStages;
+        await(sm, &sm.vfull[s], (uint32_t)(j / kAStages) & 1u);
         const uint32_t vst = base + kOffKV + (uint32_t)(s * kAStage) + kKVTile;
         const int tail = L - j * kKB;  // keys of this block that exist
         if (tail < kKB) {
           // cache rows past the sequence's keys hold anything (NaN included);
           // their P is 0, but 0 * NaN is not, so their V rows become zeros
+          // (each tile's issuer writes the same zeros before its own MMAs)
           unsigned char* vz = bp + kOffKV + s * kAStage + kKVTile;
           for (int rr = tail; rr < kKB; ++rr)
             for (int hb = 0; hb < 2; ++hb) {
@@ -311,157 +336,151 @@ __global__ void __launch_bounds__(kAThreads, 1)
             }
           fence_async_smem();
         }
-        await(sm, &sm.pfull, (uint32_t)(j & 1));
+        await(sm, &sm.pfull[t], (uint32_t)(j & 1));
         fence_after();
-        const uint32_t pt = base + kOffP;
+        const uint32_t pt = base + kOffP + (uint32_t)(t * kPTile);
 #pragma unroll
         for (int k = 0; k < kKB / 16; ++k)
-          mma_f16(tmem + 256u, desc_kmajor(pt + (uint32_t)((k >> 2) * kPHalf + (k & 3) * 32)),
+          mma_f16(tmem + 256u + (uint32_t)(128 * t), desc_kmajor(pt + (uint32_t)(k * 32)),
                   desc_mnmajor(vst + (uint32_t)(k * 2048)), kIdescPV, (j > 0 || k > 0) ? 1u : 0u);
-        mma_commit(&sm.pdone);
-        // K and V of the block are free: the softmax read S before releasing
-        // P (the S MMAs are complete) and these P V MMAs are committed
-        mma_commit(&sm.kvempty[s]);
+        mma_commit(&sm.pdone[t]);
+        mma_commit(&sm.vempty[s]);  // this tile is done with the block's V
       }
-      mma_commit(&sm.drain);
-      mbar_wait_bounded(&sm.drain, 0);
+      mma_commit(&sm.drain[t]);
+      mbar_wait_bounded(&sm.drain[t], 0);
     }
   } else {
     // ------------------------------------------------------------- softmax
+    const int t = (warp - 3) >> 2;   // tile
     const int qd = warp & 3;         // TMEM lane quadrant of this warp
     const int r = qd * 32 + lane;    // row within the tile
-    const int gr = row0 + r;
-    const bool valid = gr < R;
+    const int gr = row0 + t * kMT + r;
+    const bool valid = t < ntile && gr < R;
     const int node = valid ? gr / G : 0;
     const int hq = kvh * G + (valid ? gr % G : 0);
     const uint64_t mb = valid ? mask_bits[(int64_t)b * N + node] : 0ull;
     const int64_t qoff = (((int64_t)b * N + node) * Hq + hq) * kAD;
     {  // stage this row of Q (zeros for padding rows)
       const uint4* src = reinterpret_cast<const uint4*>(q + qoff);
+      unsigned char* qt = bp + t * kQTile;
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
         const uint4 v = valid ? src[c] : make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4*>(bp + (c >> 3) * kQHalf + swz(r, c & 7)) = v;
+        *reinterpret_cast<uint4*>(qt + (c >> 3) * kQHalf + swz(r, c & 7)) = v;
       }
       fence_async_smem();
       mbar_arrive(&sm.qready);
     }
-    const uint32_t lanes = (uint32_t)(qd * 32) << 16;
-    const uint32_t tS = tmem + lanes;          // + 128 * buffer
-    const uint32_t tO = tmem + lanes + 256u;
-    unsigned char* pt = bp + kOffP;
-    float mref = neg_inf(), l = 0.f;
-    for (int j = 0; j < nblk; ++j) {
-      await(sm, &sm.sfull[j & 1], (uint32_t)((j >> 1) & 1));
-      fence_after();
-      // raw scores q.k (the scale is applied inside the exponent below; it is
-      // positive, so the maximum is taken on the raw scores), later
-      // overwritten in place by P: 128 registers for the whole row
-      uint32_t sr[kKB];
-      {
-        const uint32_t tSb = tS + (uint32_t)(128 * (j & 1));
-#pragma unroll
-        for (int c = 0; c < kKB / 32; ++c)
-          tld32(tSb + (uint32_t)(32 * c), *reinterpret_cast<uint32_t(*)[32]>(sr + 32 * c));
+    if (t < ntile) {
+      const uint32_t lanes = (uint32_t)(qd * 32) << 16;
+      const uint32_t tS = tmem + lanes + (uint32_t)(128 * t);  // + 64 * buffer
+      const uint32_t tO = tmem + lanes + 256u + (uint32_t)(128 * t);
+      unsigned char* pt = bp + kOffP + t * kPTile;
+      float mref = neg_inf(), l = 0.f;
+      for (int j = 0; j < nblk; ++j) {
+        await(sm, &sm.sfull[t][j & 1], (uint32_t)((j >> 1) & 1));
+        fence_after();
+        uint32_t ra[32], rb[32];
+        const uint32_t tSb = tS + (uint32_t)(64 * (j & 1));
+        tld32(tSb, ra);
+        tld32(tSb + 32u, rb);
         tld_wait();
-      }
-      fence_before();
-      mbar_arrive(&sm.sfree[j & 1]);  // the issuer may refill this S buffer
-      const int key0 = j * kKB;
-      if (!valid || key0 + kKB > P) {
-        // visibility of the block's keys as two 64-bit words: the prefix
-        // (keys < P) and the drafted keys P + i whose bit i is set in the
-        // node's mask row (its ancestors and itself; bits only below N)
-        uint64_t vis[2];
+        fence_before();
+        mbar_arrive(&sm.sfree[t][j & 1]);  // the S issuer may refill the buffer
+        // raw scores q.k (the scale is applied inside the exponent below;
+        // it is positive, so the maximum is taken on the raw scores)
+        float s[64];
 #pragma unroll
-        for (int w = 0; w < 2; ++w) {
-          const int start = key0 + 64 * w;
-          const int npre = min(max(P - start, 0), 64);
+        for (int i = 0; i < 32; ++i) {
+          s[i] = __uint_as_float(ra[i]);
+          s[32 + i] = __uint_as_float(rb[i]);
+        }
+        const int key0 = j * kKB;
+        if (!valid || key0 + kKB > P) {
+          // visibility of the block's 64 keys as one word: the prefix (keys
+          // < P) and the drafted keys P + i whose bit i is set in the node's
+          // mask row (its ancestors and itself; bits only below N)
+          const int npre = min(max(P - key0, 0), 64);
           const uint64_t pre = npre >= 64 ? ~0ull : ((1ull << npre) - 1ull);
-          const int off = start - P;
+          const int off = key0 - P;
           const uint64_t dr = off >= 0 ? (off < 64 ? (mb >> off) : 0ull)
                                        : (off > -64 ? (mb << (-off)) : 0ull);
-          vis[w] = valid ? (pre | dr) : 0ull;
+          const uint64_t vis = valid ? (pre | dr) : 0ull;
+#pragma unroll
+          for (int i = 0; i < 64; ++i)
+            if (!((vis >> i) & 1ull)) s[i] = neg_inf();
+        }
+        // eight independent chains, then their combination
+        float bm8[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) bm8[c] = s[c];
+#pragma unroll
+        for (int i = 8; i < 64; ++i) bm8[i & 7] = fmaxf(bm8[i & 7], s[i]);
+        const float bm = fmaxf(fmaxf(fmaxf(bm8[0], bm8[1]), fmaxf(bm8[2], bm8[3])),
+                               fmaxf(fmaxf(bm8[4], bm8[5]), fmaxf(bm8[6], bm8[7]))) *
+                         scale_log2;
+        // the reference maximum moves only when the row's maximum grows by
+        // more than 2^8 (also at the first visible key): P stays below 2^8
+        const bool move = bm > mref + 8.f;
+        const float mnew = move ? bm : mref;
+        const float corr = (move && mref != neg_inf()) ? ex2(mref - mnew) : 1.f;
+        mref = mnew;
+        const float nmu = mref == neg_inf() ? 0.f : -mref;
+        uint32_t pk[32];
+        float ls8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float p0 = ex2(fmaf(s[2 * i], scale_log2, nmu));
+          const float p1 = ex2(fmaf(s[2 * i + 1], scale_log2, nmu));
+          ls8[i & 7] += p0 + p1;
+          pk[i] = pack_bf16(p0, p1);
+        }
+        const float ls = ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) +
+                         ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
+        l = l * corr + ls;
+        // the previous block's P V is done before P_t and O_t are touched
+        if (j > 0) await(sm, &sm.pdone[t], (uint32_t)((j - 1) & 1));
+        fence_after();
+        if (j > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
+#pragma unroll 1
+          for (int c = 0; c < kAD / 32; ++c) {
+            uint32_t o[32];
+            tld32(tO + (uint32_t)(32 * c), o);
+            tld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
+            tst32(tO + (uint32_t)(32 * c), o);
+          }
+          tst_wait();
         }
 #pragma unroll
-        for (int i = 0; i < kKB; ++i)
-          if (!((vis[i >> 6] >> (i & 63)) & 1ull)) sr[i] = 0xff800000u;  // -inf
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(pt + swz(r, c)) =
+              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        fence_async_smem();
+        fence_before();
+        mbar_arrive(&sm.pfull[t]);
       }
-      // eight independent chains, then their combination
-      float bm8[8];
-#pragma unroll
-      for (int c = 0; c < 8; ++c) bm8[c] = __uint_as_float(sr[c]);
-#pragma unroll
-      for (int i = 8; i < kKB; ++i) bm8[i & 7] = fmaxf(bm8[i & 7], __uint_as_float(sr[i]));
-      const float bm = fmaxf(fmaxf(fmaxf(bm8[0], bm8[1]), fmaxf(bm8[2], bm8[3])),
-                             fmaxf(fmaxf(bm8[4], bm8[5]), fmaxf(bm8[6], bm8[7]))) *
-                       scale_log2;
-      // the reference maximum moves only when the row's maximum grows by
-      // more than 2^8 (also at the first visible key): P stays below 2^8
-      const bool move = bm > mref + 8.f;
-      const float mnew = move ? bm : mref;
-      const float corr = (move && mref != neg_inf()) ? ex2(mref - mnew) : 1.f;
-      mref = mnew;
-      const float nmu = mref == neg_inf() ? 0.f : -mref;
-      float ls8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int i = 0; i < kKB; ++i) {
-        const float p = ex2(fmaf(__uint_as_float(sr[i]), scale_log2, nmu));
-        ls8[i & 7] += p;
-        sr[i] = __float_as_uint(p);
-      }
-      const float ls = ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) +
-                       ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
-      l = l * corr + ls;
-      // the previous block's P V is done before P and O are touched
-      if (j > 0) await(sm, &sm.pdone, (uint32_t)((j - 1) & 1));
+      // O_t / l after the last P V
+      await(sm, &sm.pdone[t], (uint32_t)((nblk - 1) & 1));
       fence_after();
-      if (j > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
+      const float inv = 1.f / l;
+      uint4* dst = reinterpret_cast<uint4*>(out + qoff);
 #pragma unroll 1
-        for (int c = 0; c < kAD / 32; ++c) {
-          uint32_t o[32];
-          tld32(tO + (uint32_t)(32 * c), o);
-          tld_wait();
+      for (int c = 0; c < kAD / 32; ++c) {
+        uint32_t o[32];
+        tld32(tO + (uint32_t)(32 * c), o);
+        tld_wait();
+        if (valid) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
-          tst32(tO + (uint32_t)(32 * c), o);
-        }
-        tst_wait();
-      }
-      // P row as bf16: keys 0-63 in the first 64-key block, 64-127 in the
-      // second
-#pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const int i = 8 * c;
-        *reinterpret_cast<uint4*>(pt + (c >> 3) * kPHalf + swz(r, c & 7)) = make_uint4(
-            pack_bf16(__uint_as_float(sr[i]), __uint_as_float(sr[i + 1])),
-            pack_bf16(__uint_as_float(sr[i + 2]), __uint_as_float(sr[i + 3])),
-            pack_bf16(__uint_as_float(sr[i + 4]), __uint_as_float(sr[i + 5])),
-            pack_bf16(__uint_as_float(sr[i + 6]), __uint_as_float(sr[i + 7])));
-      }
-      fence_async_smem();
-      fence_before();
-      mbar_arrive(&sm.pfull);
-    }
-    // O / l after the last P V
-    await(sm, &sm.pdone, (uint32_t)((nblk - 1) & 1));
-    fence_after();
-    const float inv = 1.f / l;
-    uint4* dst = reinterpret_cast<uint4*>(out + qoff);
-#pragma unroll 1
-    for (int c = 0; c < kAD / 32; ++c) {
-      uint32_t o[32];
-      tld32(tO + (uint32_t)(32 * c), o);
-      tld_wait();
-      if (valid) {
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          const int i = 8 * v;
-          dst[4 * c + v] = make_uint4(
-              pack_bf16(__uint_as_float(o[i]) * inv, __uint_as_float(o[i + 1]) * inv),
-              pack_bf16(__uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv),
-              pack_bf16(__uint_as_float(o[i + 4]) * inv, __uint_as_float(o[i + 5]) * inv),
-              pack_bf16(__uint_as_float(o[i + 6]) * inv, __uint_as_float(o[i + 7]) * inv));
+          for (int v = 0; v < 4; ++v) {
+            const int i = 8 * v;
+            dst[4 * c + v] = make_uint4(
+                pack_bf16(__uint_as_float(o[i]) * inv, __uint_as_float(o[i + 1]) * inv),
+                pack_bf16(__uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv),
+                pack_bf16(__uint_as_float(o[i + 4]) * inv, __uint_as_float(o[i + 5]) * inv),
+                pack_bf16(__uint_as_float(o[i + 6]) * inv, __uint_as_float(o[i + 7]) * inv));
+          }
         }
       }
     }
@@ -531,7 +550,7 @@ extern "C" int spec_tree_attention(const void* q, const void* k_cache, const voi
   CUtensorMap mk, mv;
   if (!cache_map(&mk, k_cache, rows) || !cache_map(&mv, v_cache, rows)) return SPEC_ERR_CUDA;
   const int R = N * (Hq / Hkv);
-  const dim3 grid((unsigned)((R + kMT - 1) / kMT), (unsigned)Hkv, (unsigned)B);
+  const dim3 grid((unsigned)((R + kTiles * kMT - 1) / (kTiles * kMT)), (unsigned)Hkv, (unsigned)B);
   if (cudaFuncSetAttribute(tree_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kASmemBytes) != cudaSuccess)
     return SPEC_ERR_CUDA;
