@@ -16,11 +16,9 @@
 // (sequence, key/value head) -- the rows are (node, head in the group) pairs,
 // node-major, so the G query heads that share a key/value head are served by
 // one stream of its keys and values -- as two 128-row tiles:
-//   warp 0     TMA producers: 64-key blocks of K (lane 0) and of V (lane 1)
-//              (128-byte swizzle) into a 3-stage shared-memory ring whose K
-//              and V halves are released separately -- K once both tiles' S
-//              MMAs have read it, V after their P V -- and prefetches of
-//              blocks further ahead into L2;
+//   warp 0     TMA producer: 64-key blocks of K and V (128-byte swizzle) into
+//              a 3-stage shared-memory ring;
+//              (and prefetches blocks further ahead into L2);
 //   warps 1-2  one tensor-core issuer per tile t (warp 1 also allocates
 //              TMEM): S_t = Q_t K^T of the next key block (tcgen05.mma M 128,
 //              N 64, K 128) into one of two S buffers once the block's keys
@@ -71,7 +69,7 @@ constexpr int kSoftThreads = 256;
 constexpr uint32_t kATmemCols = 512;
 
 struct __align__(8) AttnSmem {
-  uint64_t kfull[kAStages], kempty[kAStages], vfull[kAStages], vempty[kAStages];
+  uint64_t kvfull[kAStages], kvempty[kAStages];
   uint64_t sfull[kTiles][2], sfree[kTiles][2], pfull[kTiles], pdone[kTiles];
   uint64_t qready, drain[kTiles];
   uint32_t tmem_base;
@@ -222,10 +220,8 @@ __global__ void __launch_bounds__(kAThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kAStages; ++s) {
-      mbar_init(&sm.kfull[s], 1);
-      mbar_init(&sm.kempty[s], ntile);  // released by every tile's issuer
-      mbar_init(&sm.vfull[s], 1);
-      mbar_init(&sm.vempty[s], ntile);
+      mbar_init(&sm.kvfull[s], 1);
+      mbar_init(&sm.kvempty[s], ntile);  // released by every tile's issuer
     }
     for (int t = 0; t < kTiles; ++t) {
       mbar_init(&sm.sfull[t][0], 1);
@@ -255,15 +251,7 @@ __global__ void __launch_bounds__(kAThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // lane 0 fills the K halves of the ring, lane 1 the V halves: K of a
-    // block is released once both tiles' S MMAs have read it, V only after
-    // their P V, so the next blocks' keys never wait for this block's P V
-    if (lane < 2) {
-      const bool isk = lane == 0;
-      const CUtensorMap* map = isk ? &map_k : &map_v;
-      uint64_t* full = isk ? sm.kfull : sm.vfull;
-      uint64_t* empty = isk ? sm.kempty : sm.vempty;
-      const uint32_t half = isk ? 0u : (uint32_t)kKVTile;
+    if (lane == 0) {
       auto prefetch = [&](int j) {
         const int y = kvrow0 + j * kKB;
         tma2d_prefetch(&map_k, 0, y);
@@ -271,22 +259,23 @@ __global__ void __launch_bounds__(kAThreads, 1)
         tma2d_prefetch(&map_v, 0, y);
         tma2d_prefetch(&map_v, 64, y);
       };
-      if (isk)
-        for (int j = kAStages; j < kAStages + kPrefetch && j < nblk; ++j) prefetch(j);
+      for (int j = kAStages; j < kAStages + kPrefetch && j < nblk; ++j) prefetch(j);
       for (int j = 0; j < nblk; ++j) {
         const int s = j % kAStages;
-        if (isk && j + kAStages + kPrefetch < nblk) prefetch(j + kAStages + kPrefetch);
-        await(sm, &empty[s], ((uint32_t)(j / kAStages) & 1u) ^ 1u);
-        mbar_expect_tx(&full[s], (uint32_t)kKVTile);
-        const uint32_t st = base + kOffKV + (uint32_t)(s * kAStage) + half;
+        if (j + kAStages + kPrefetch < nblk) prefetch(j + kAStages + kPrefetch);
+        await(sm, &sm.kvempty[s], ((uint32_t)(j / kAStages) & 1u) ^ 1u);
+        mbar_expect_tx(&sm.kvfull[s], (uint32_t)kAStage);
+        const uint32_t st = base + kOffKV + (uint32_t)(s * kAStage);
         const int y = kvrow0 + j * kKB;
-        tma2d(st, map, 0, y, &full[s]);
-        tma2d(st + kKVHalf, map, 64, y, &full[s]);
+        tma2d(st, &map_k, 0, y, &sm.kvfull[s]);
+        tma2d(st + kKVHalf, &map_k, 64, y, &sm.kvfull[s]);
+        tma2d(st + kKVTile, &map_v, 0, y, &sm.kvfull[s]);
+        tma2d(st + kKVTile + kKVHalf, &map_v, 64, y, &sm.kvfull[s]);
       }
       // this CTA's last copy into each stage has landed before it exits
       for (int s = 0; s < kAStages && s < nblk; ++s) {
         const int fills = (nblk - s + kAStages - 1) / kAStages;
-        mbar_wait_bounded(&full[s], (uint32_t)(fills - 1) & 1u);
+        mbar_wait_bounded(&sm.kvfull[s], (uint32_t)(fills - 1) & 1u);
       }
     }
   } else if (warp <= 2) {
@@ -301,7 +290,7 @@ __global__ void __launch_bounds__(kAThreads, 1)
       const uint32_t qt = base + (uint32_t)(t * kQTile);
       auto issue_s = [&](int j) {
         const int s = j % kAStages;
-        await(sm, &sm.kfull[s], (uint32_t)(j / kAStages) & 1u);
+        await(sm, &sm.kvfull[s], (uint32_t)(j / kAStages) & 1u);
         // S buffer j & 1 was last read by the softmax at block j - 2
         if (j >= 2) await(sm, &sm.sfree[t][j & 1], (uint32_t)(((j >> 1) - 1) & 1));
         fence_after();
@@ -314,13 +303,11 @@ __global__ void __launch_bounds__(kAThreads, 1)
           mma_f16(ds, desc_kmajor(qt + off), desc_kmajor(kst + koff), kIdescS, k > 0 ? 1u : 0u);
         }
         mma_commit(&sm.sfull[t][j & 1]);
-        mma_commit(&sm.kempty[s]);  // this tile is done with the block's K
       };
       if (nblk > 0) issue_s(0);
       for (int j = 0; j < nblk; ++j) {
         if (j + 1 < nblk) issue_s(j + 1);
         const int s = j % kAStages;
-        await(sm, &sm.vfull[s], (uint32_t)(j / kAStages) & 1u);
         const uint32_t vst = base + kOffKV + (uint32_t)(s * kAStage) + kKVTile;
         const int tail = L - j * kKB;  // keys of this block that exist
         if (tail < kKB) {
@@ -344,7 +331,9 @@ __global__ void __launch_bounds__(kAThreads, 1)
           mma_f16(tmem + 256u + (uint32_t)(128 * t), desc_kmajor(pt + (uint32_t)(k * 32)),
                   desc_mnmajor(vst + (uint32_t)(k * 2048)), kIdescPV, (j > 0 || k > 0) ? 1u : 0u);
         mma_commit(&sm.pdone[t]);
-        mma_commit(&sm.vempty[s]);  // this tile is done with the block's V
+        // this tile is done with the block's K and V (the softmax read S
+        // before releasing P, so the S MMAs are complete too)
+        mma_commit(&sm.kvempty[s]);
       }
       mma_commit(&sm.drain[t]);
       mbar_wait_bounded(&sm.drain[t], 0);
@@ -358,7 +347,9 @@ __global__ void __launch_bounds__(kAThreads, 1)
     const bool valid = t < ntile && gr < R;
     const int node = valid ? gr / G : 0;
     const int hq = kvh * G + (valid ? gr % G : 0);
-    const uint64_t mb = valid ? mask_bits[(int64_t)b * N + node] : 0ull;
+    const uint64_t mb = valid ? (mask_bits[(int64_t)b * N + node] &
+                                 (N >= 64 ? ~0ull : ((1ull << N) - 1ull)))
+                              : 0ull;
     const int64_t qoff = (((int64_t)b * N + node) * Hq + hq) * kAD;
     {  // stage this row of Q (zeros for padding rows)
       const uint4* src = reinterpret_cast<const uint4*>(q + qoff);
