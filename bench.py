@@ -197,6 +197,20 @@ def _peaks():
         return 6800.0, "fallback"
 
 
+def _chain_single_launch(B, K, V, tsz, dsz, device):
+    """Whether the library verifies this sampled chain (no truncation) in
+    its single-launch form: 1 <= K <= 16, V a multiple of 8, one 8-CTA
+    cluster per sequence within one wave of the GPU's SMs, and each CTA's
+    eighth of the K + 1 target and K draft rows within 200 KB of shared
+    memory."""
+    import torch
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    if not (1 <= K <= 16) or V % 8 or B * 8 > sms:
+        return False
+    sl = ((V + 7) // 8 + 7) // 8 * 8
+    return (K + 1) * sl * tsz + K * sl * dsz <= 200 * 1024
+
+
 # ------------------------------------------------------------- workloads
 class Work:
     """Device inputs, outputs and one step of a workload (GPU arm)."""
@@ -238,6 +252,13 @@ class Work:
             self.launches_per_step = (2 if w.temperature == 0 else
                                       4 if (w.top_k > 0 or w.top_p < 1)
                                       else 3)
+            if w.temperature > 0 and w.top_k == 0 and w.top_p >= 1 and \
+                    _chain_single_launch(B, K, V, tb,
+                                         self.draft.element_size(), device):
+                # one cluster of 8 CTAs per sequence, every row resident in
+                # shared memory: a single launch
+                self.kernel_name = "chain_small"
+                self.launches_per_step = 1
         elif name == "tree_static":
             self.kind = "tree"
             (self.target, self.draft, self.q_row, self.toks,

@@ -115,8 +115,10 @@ int run_verify(const VerifyShape& s, VerifyArgs& a, void* ws, size_t ws_bytes, c
   int rc = bind_verify_ws(s, a, ws, ws_bytes);
   if (rc != SPEC_OK) return rc;
   if (a.prm.temperature != 0.f && !sampled_supported(s, a)) return SPEC_ERR_UNSUPPORTED;
-  cudaError_t e = cudaMemsetAsync(a.status, 0, 2 * sizeof(uint32_t), st);
-  if (e != cudaSuccess) return SPEC_ERR_CUDA;
+  if (!(a.prm.temperature != 0.f && chain_small_writes_status(s, a))) {
+    cudaError_t e = cudaMemsetAsync(a.status, 0, 2 * sizeof(uint32_t), st);
+    if (e != cudaSuccess) return SPEC_ERR_CUDA;
+  }
   return launch_verify(s, a, st);
 }
 

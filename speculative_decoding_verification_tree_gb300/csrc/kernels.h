@@ -135,6 +135,16 @@ void prof_end(int kind, cudaStream_t st);
 
 cudaError_t launch_greedy(const VerifyShape& s, const VerifyArgs& a, cudaStream_t st);
 cudaError_t launch_sampled(const VerifyShape& s, const VerifyArgs& a, cudaStream_t st);
+// Single-launch chain verification for a few sequences (one cluster of 8
+// CTAs per sequence, rows resident in shared memory): whether it applies,
+// and its launch.
+bool chain_small_fits(const VerifyShape& s, const VerifyArgs& a, int sms, int* slice,
+                      size_t* smem);
+cudaError_t launch_chain_small(const VerifyShape& s, const VerifyArgs& a, int slice, size_t smem,
+                               cudaStream_t st);
+// True when the call will be one single-cluster launch of that kernel, which
+// then writes the status word itself (the caller skips clearing it).
+bool chain_small_writes_status(const VerifyShape& s, const VerifyArgs& a);
 bool sampled_supported(const VerifyShape& s, const VerifyArgs& a);
 cudaError_t launch_tree_mask(const int32_t* parent, int B, int N, uint8_t* mask,
                              uint64_t* bits, cudaStream_t st);

@@ -135,9 +135,12 @@ extern "C" int spec_verify_chain_noalloc(const void* target_logits, const void* 
                        kOutBytes);
   a.qcount = (int32_t*)(p + 4);  // beside the status word, zeroed with it
   if (meta_rec_bytes(true) != 48) return SPEC_ERR_CUDA;  // chain row record size
-  // the status word must start at zero; everything else is written before it
-  // is read within the call
-  if (cudaMemsetAsync(a.status, 0, 2 * sizeof(uint32_t), st) != cudaSuccess) return SPEC_ERR_CUDA;
+  // the status word must start at zero (a single-cluster chain launch writes
+  // the whole word itself); everything else is written before it is read
+  // within the call
+  if (!(!greedy && chain_small_writes_status(s, a)) &&
+      cudaMemsetAsync(a.status, 0, 2 * sizeof(uint32_t), st) != cudaSuccess)
+    return SPEC_ERR_CUDA;
   if (B == 0) return SPEC_OK;
   const cudaError_t e = greedy ? launch_greedy(s, a, st) : launch_sampled(s, a, st);
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;

@@ -726,6 +726,11 @@ cudaError_t launch_sampled(const VerifyShape& s, const VerifyArgs& a, cudaStream
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return cudaErrorInvalidDevice;
+  // a few sampled chains: one launch, every row resident in shared memory
+  int cs_slice = 0;
+  size_t cs_smem = 0;
+  if (!a.tlse && chain_small_fits(s, a, sms, &cs_slice, &cs_smem))
+    return launch_chain_small(s, a, cs_slice, cs_smem, st);
   // pass A reads the target row unless its normaliser is given (LM head
   // epilogue), and the draft row unless its normaliser is given
   const int passA = (a.tlse ? 0 : tsz) + ((qk == Q_LOGITS && a.prm.draft_lse) ? 0 : dsz);

@@ -131,3 +131,94 @@ def test_chain_batched_full_vocab_llama_size():
     gpu, ref = run(w, seqs=seqs, target=target, draft=draft, toks=toks)
     p = compare_chain(gpu, ref, seqs=seqs, max_excluded=2)
     assert p.exact >= w.B - 4, p
+
+
+# ---- the single-launch form: a few sampled chains with every row resident
+# in shared memory (one cluster of 8 CTAs per sequence)
+
+@pytest.mark.parametrize("V", [8, 16, 24, 64, 4096, 32000])
+def test_chain_small_vocab_slices(V):
+    # V = 8..24: some of the 8 CTAs own no part of the vocabulary
+    w = synth.workload("chain_sample", B=5, K=3, V=V, seed=500 + V)
+    gpu, ref = run(w)
+    compare_chain(gpu, ref, max_excluded=1)
+
+
+@pytest.mark.parametrize("B", [19, 20])
+def test_chain_small_longest_chain_and_wave_edge(B):
+    # K = 16 drafts (the most the single launch takes); B = 19 fills one wave
+    # of 8-CTA clusters on 152 SMs, B = 20 goes to the streaming kernel
+    w = synth.workload("chain_sample", B=B, K=16, V=4096,
+                       target_dtype=torch.bfloat16,
+                       draft_dtype=torch.bfloat16, draft_noise=0.3, seed=B)
+    gpu, ref = run(w)
+    compare_chain(gpu, ref, max_excluded=1)
+    assert (ref.accepted > 4).any()
+
+
+@pytest.mark.parametrize("T", [1.0, 0.6])
+@pytest.mark.parametrize("ddt", [torch.float32, torch.bfloat16])
+def test_chain_small_probs_draft(T, ddt):
+    w = synth.workload("chain_sample", B=4, K=5, V=12000, draft_kind="probs",
+                       draft_dtype=ddt, temperature=T, seed=int(T * 10))
+    gpu, ref = run(w)
+    compare_chain(gpu, ref, max_excluded=1)
+
+
+def test_chain_small_zero_q_and_out_of_range_tokens():
+    from speculative_decoding_verification_tree_gb300 import _lib
+    V = 704
+    w = synth.workload("chain_sample", B=3, K=2, V=V, seed=4)
+    target, draft, toks = synth.chain_inputs(w, "cuda")
+    draft[0, 0, 11] = float("-inf")
+    toks[0, 0] = 11             # q(x) = 0: accepted
+    toks[1, 1] = V + 5          # out of range: rejected
+    toks[2, 0] = -1
+    a = api()
+    ws = a.workspace(_lib.SPEC_OP_CHAIN, 3, 2, V)
+    gpu = a.spec_verify_chain(target, draft, toks, temperature=1.0,
+                              seed=w.decision_seed, ws=ws)
+    st = a.spec_get_status(ws)
+    ref = verify_chain(np64(target), np64(draft), toks.cpu().numpy(),
+                       temperature=1.0, seed=w.decision_seed)
+    compare_chain(gpu, ref)
+    assert st & _lib.SPEC_STATUS_QZERO_ACCEPT
+    assert st & _lib.SPEC_STATUS_TOKEN_RANGE
+    assert st == ref.status
+
+
+def test_chain_small_bonus_from_p_when_all_accepted():
+    # draft == target: every token accepted, the bonus drawn from p_K
+    w = synth.workload("chain_sample", B=6, K=4, V=2048, seed=6)
+    target, draft, toks = synth.chain_inputs(w, "cuda")
+    draft = target[:, :4].contiguous()
+    gpu, ref = run(w, target=target, draft=draft, toks=toks)
+    compare_chain(gpu, ref)
+    assert (gpu[0].cpu() == 4).all()
+    np.testing.assert_allclose(gpu[2].cpu().numpy(), 1.0, rtol=1e-5)
+
+
+def test_chain_small_single_sequence_rewrites_status():
+    # one sequence: the single cluster writes the whole status word, so a
+    # flag of the previous call on the same workspace must not survive
+    from speculative_decoding_verification_tree_gb300 import _lib
+    V = 704
+    w = synth.workload("chain_sample", B=1, K=2, V=V, seed=8)
+    target, draft, toks = synth.chain_inputs(w, "cuda")
+    a = api()
+    ws = a.workspace(_lib.SPEC_OP_CHAIN, 1, 2, V)
+    bad = toks.clone()
+    bad[0, 0] = V + 1            # out of range: rejected, flagged
+    gpu = a.spec_verify_chain(target, draft, bad, temperature=1.0,
+                              seed=w.decision_seed, ws=ws)
+    assert a.spec_get_status(ws) & _lib.SPEC_STATUS_TOKEN_RANGE
+    ref = verify_chain(np64(target), np64(draft), bad.cpu().numpy(),
+                       temperature=1.0, seed=w.decision_seed)
+    compare_chain(gpu, ref)
+    gpu = a.spec_verify_chain(target, draft, toks, temperature=1.0,
+                              seed=w.decision_seed, ws=ws)
+    st = a.spec_get_status(ws)
+    ref = verify_chain(np64(target), np64(draft), toks.cpu().numpy(),
+                       temperature=1.0, seed=w.decision_seed)
+    compare_chain(gpu, ref)
+    assert st == ref.status == 0
