@@ -67,6 +67,7 @@ constexpr int kAThreads = 352;
 constexpr int kPrefetch = 6;  // key blocks prefetched into L2 ahead of the ring
 constexpr int kSoftThreads = 256;
 constexpr uint32_t kATmemCols = 512;
+constexpr int kOrderMax = 256;  // sequences ordered longest first up to this batch
 
 struct __align__(8) AttnSmem {
   uint64_t kvfull[kAStages], kvempty[kAStages];
@@ -74,6 +75,7 @@ struct __align__(8) AttnSmem {
   uint64_t qready, drain[kTiles];
   uint32_t tmem_base;
   uint32_t dead;
+  int seq;
 };
 constexpr size_t kASmemBytes = (size_t)kOffBar + sizeof(AttnSmem) + 1024;
 
@@ -208,9 +210,36 @@ __global__ void __launch_bounds__(kAThreads, 1)
   unsigned char* bp = araw + (base - raw);
   AttnSmem& sm = *reinterpret_cast<AttnSmem*>(bp + kOffBar);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = blockIdx.z, kvh = blockIdx.y;
   const int G = Hq / Hkv, R = N * G;
-  const int row0 = blockIdx.x * (kTiles * kMT);
+  int b = blockIdx.z, kvh = blockIdx.y, tile = blockIdx.x;
+  if (gridDim.z <= (unsigned)kOrderMax) {
+    // longest sequences first: the CTAs launched first (lowest linear index)
+    // take the sequences with the most keys, so the last CTAs to start are
+    // the shortest ones and the tail of the grid is short
+    const int nb = (int)gridDim.z, gx = (int)gridDim.x;
+    const int lin = blockIdx.x + gx * (blockIdx.y + Hkv * blockIdx.z);
+    const int want = lin / (gx * Hkv), rem = lin % (gx * Hkv);
+    int* len_s = reinterpret_cast<int*>(bp + kOffP);  // P tiles are written later
+    for (int i = threadIdx.x; i < nb; i += kAThreads) {
+      const int p = prefix_len[i];
+      len_s[i] = p < 0 ? 0 : (p > S - N ? S - N : p);
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < nb; i += kAThreads) {
+      const int li = len_s[i];
+      int rank = 0;
+      for (int j = 0; j < nb; ++j) {
+        const int lj = len_s[j];
+        rank += (lj > li || (lj == li && j < i)) ? 1 : 0;
+      }
+      if (rank == want) sm.seq = i;
+    }
+    __syncthreads();
+    b = sm.seq;
+    kvh = rem / gx;
+    tile = rem % gx;
+  }
+  const int row0 = tile * (kTiles * kMT);
   const int ntile = min(kTiles, (R - row0 + kMT - 1) / kMT);
   int P = prefix_len[b];
   P = P < 0 ? 0 : (P > S - N ? S - N : P);

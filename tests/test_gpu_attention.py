@@ -83,6 +83,20 @@ def test_tree_attention_matches_oracle(N, Hq, Hkv, prefix):
     _check(out, ref)
 
 
+def test_many_sequences_longest_first_with_ties():
+    # the CTAs take sequences longest first (ties by index): every sequence,
+    # equal prefixes included, must still land in its own output rows
+    prefix = [5, 300, 300, 0, 129, 64, 300, 1, 257, 5, 77, 200]
+    B, N, Hq, Hkv = len(prefix), 7, 8, 2
+    S = max(prefix) + N + 3
+    q, k, v, pre, parent = _case(31, B, N, Hq, Hkv, prefix, S)
+    out = api().spec_tree_attention(q, k, v, pre, _bits(parent), scale=0.09)
+    torch.cuda.synchronize()
+    ref = tree_attention(q.float().cpu().numpy(), k.float().cpu().numpy(),
+                         v.float().cpu().numpy(), prefix, parent, 0.09)
+    _check(out, ref)
+
+
 def test_chain_and_static_tree_masks():
     w = synth.workload("tree_static")
     static = synth.static_tree(w).numpy()
