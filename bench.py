@@ -247,10 +247,11 @@ class Work:
             self.kernel_bytes = B * (K + 1) * V * tb
             if w.temperature > 0:
                 self.kernel_bytes += B * K * V * self.draft.element_size()
-            # argmax + finalize; top-k rows, records, units, walk; or
-            # records, streaming verification, walk
+            # argmax + finalize; top-k rows (with the row records) and the
+            # candidate-list verification (with the walk); or records,
+            # streaming verification, walk
             self.launches_per_step = (2 if w.temperature == 0 else
-                                      4 if (w.top_k > 0 or w.top_p < 1)
+                                      2 if (w.top_k > 0 or w.top_p < 1)
                                       else 3)
             if w.temperature > 0 and w.top_k == 0 and w.top_p >= 1 and \
                     _chain_single_launch(B, K, V, tb,
@@ -282,8 +283,9 @@ class Work:
             self.kernel_bytes = B * (N + 1) * V * (
                 self.target.element_size() + self.draft.element_size())
             # mask, row records, row verification, walk (top-k / top-p:
-            # mask, top-k rows, records, units, walk)
-            self.launches_per_step = (5 if (w.top_k > 0 or w.top_p < 1)
+            # mask, top-k rows with the records, candidate-list verification
+            # with the walk)
+            self.launches_per_step = (3 if (w.top_k > 0 or w.top_p < 1)
                                       else 4)
         elif name == "eagle2":
             self.kind = "eagle2"

@@ -47,7 +47,8 @@ __global__ void __launch_bounds__(topk::kThreads) eagle2_rows(const T* __restric
   __shared__ float lse;
   const int64_t row = blockIdx.x;
   topk::row_topk_fast<T, kVec>(x + row * (int64_t)V, V, k, kt,
-                               reinterpret_cast<topk::Cand*>(smraw), idx, val, &cnt, &lse);
+                               reinterpret_cast<topk::Cand*>(smraw), idx, val, &cnt, &lse,
+                               0);  // long rows: the flagged threads' rescan
   const int i = threadIdx.x;
   if (i < k) {
     Eagle2Cand* o = out + row * SPEC_EAGLE2_MAX_TOPK;

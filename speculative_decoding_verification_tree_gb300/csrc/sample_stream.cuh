@@ -81,13 +81,12 @@ static_assert(sizeof(Meta) == 16 + 20 * kMaxKids, "record layout");
 // One warp per row: the row's draft row, its children in index order with
 // their tokens and the two logits at each token, and its Philox uniforms
 // (slot 0 of each child, slot 1 of the row), so that the streaming kernel
-// issues no dependent loads and no Philox rounds.
+// issues no dependent loads and no Philox rounds.  With a.qlist set the row
+// also goes on the streaming kernel's work list (or, without a draft row,
+// gets its final row outcome).
 template <typename TT, typename TD>
-__global__ void __launch_bounds__(256) row_meta(VerifyShape s, VerifyArgs a, int kidcap,
-                                                int rec_bytes) {
-  const int lane = threadIdx.x & 31;
-  const int64_t unit = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (unit >= s.rows()) return;
+__device__ void row_meta_warp(const VerifyShape& s, const VerifyArgs& a, int64_t unit, int lane,
+                              int kidcap, int rec_bytes) {
   const int n = s.n, V = s.V;
   const int b = (int)(unit / (n + 1));
   const int r = (int)(unit - (int64_t)b * (n + 1));
@@ -169,6 +168,13 @@ __global__ void __launch_bounds__(256) row_meta(VerifyShape s, VerifyArgs a, int
       }
     }
   }
+}
+template <typename TT, typename TD>
+__global__ void __launch_bounds__(256) row_meta(VerifyShape s, VerifyArgs a, int kidcap,
+                                                int rec_bytes) {
+  const int64_t unit = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (unit >= s.rows()) return;
+  row_meta_warp<TT, TD>(s, a, unit, threadIdx.x & 31, kidcap, rec_bytes);
 }
 
 // State of a row between its first decision and its last (two row-times).

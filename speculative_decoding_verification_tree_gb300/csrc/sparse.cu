@@ -15,10 +15,10 @@
 //   * no child accepted: inverse-CDF draw from the final weights in
 //     vocabulary order (a leaf: the bonus token from p).
 // Kernels: topk_rows (one CTA per target row and per draft row, one HBM
-// pass), row_meta (children and uniforms, shared with the streaming path),
-// sparse_warp (one warp per row, all math on the candidate lists as warp-wide
-// sums and scans),
-// sparse_walk.
+// pass; a target row's CTA also builds the row's record -- children and
+// uniforms, as for the streaming path) and sparse_warp (one warp per row,
+// all math on the candidate lists as warp-wide sums and scans; the warp that
+// finishes a sequence's last row walks the sequence).
 #include "sample_stream.cuh"
 #include "topk.cuh"
 
@@ -26,6 +26,10 @@ namespace sv {
 namespace {
 
 constexpr int kK = topk::kMaxK;
+// topk_rows' dynamic shared memory: the fallback's buffers, whose space also
+// holds the group keys of rows of up to gk_slots_for(kTopkSmem) groups per
+// thread
+constexpr size_t kTopkSmem = (size_t)topk::kWarps * topk::kBufCap * sizeof(topk::Cand);
 
 struct TopkOut {
   int32_t* idx;   // [2 * rows * kK]: target rows, then draft rows
@@ -35,18 +39,29 @@ struct TopkOut {
 
 // blockIdx.x < rows: target row; else the draft row of tree row
 // blockIdx.x - rows (none: count 0).
+// Five CTAs per SM (at most 48 registers, four 16-byte loads in flight per
+// thread): 760 rows resident at once, so a batch of that many rows streams
+// in one wave and the per-row tails (bound, rescan, ranking) overlap.
+// The target row's CTA also builds the row's record (its last warp, while
+// the others rank the candidates) and, for a sequence's first row, clears
+// the sequence's counter of finished rows.
 template <typename TT, typename TD, bool kVecT, bool kVecD>
-__global__ void __launch_bounds__(topk::kThreads) topk_rows(VerifyShape s, VerifyArgs a, int k,
-                                                            TopkOut o) {
+__global__ void __launch_bounds__(topk::kThreads, 5) topk_rows(VerifyShape s, VerifyArgs a, int k,
+                                                               TopkOut o, int kidcap,
+                                                               int rec_bytes, int32_t* seqcnt) {
   extern __shared__ __align__(16) unsigned char smraw[];
   topk::Cand* smem = reinterpret_cast<topk::Cand*>(smraw);
   const int64_t rows = s.rows();
   const int64_t i = blockIdx.x;
   const int n = s.n, V = s.V;
   if (i < rows) {
+    if (threadIdx.x == 0 && i % (n + 1) == 0) seqcnt[i / (n + 1)] = 0;
     const TT* rp = reinterpret_cast<const TT*>(a.target) + i * (int64_t)V;
-    topk::row_topk_fast<TT, kVecT>(rp, V, k, 1.f, smem, o.idx + i * kK, o.val + i * kK, o.cnt + i,
-                              nullptr);
+    auto record = [&](int lane) {
+      stream::row_meta_warp<TT, TD>(s, a, i, lane, kidcap, rec_bytes);
+    };
+    topk::row_topk_fast<TT, kVecT, 4>(rp, V, k, 1.f, smem, o.idx + i * kK, o.val + i * kK,
+                                      o.cnt + i, nullptr, topk::gk_slots_for(kTopkSmem), record);
     return;
   }
   const int64_t u = i - rows;
@@ -60,8 +75,8 @@ __global__ void __launch_bounds__(topk::kThreads) topk_rows(VerifyShape s, Verif
     return;
   }
   const TD* rp = reinterpret_cast<const TD*>(a.draft) + ((int64_t)b * s.R + q) * V;
-  topk::row_topk_fast<TD, kVecD>(rp, V, k, 1.f, smem, o.idx + i * kK, o.val + i * kK, o.cnt + i,
-                            nullptr);
+  topk::row_topk_fast<TD, kVecD, 4>(rp, V, k, 1.f, smem, o.idx + i * kK, o.val + i * kK,
+                                    o.cnt + i, nullptr, topk::gk_slots_for(kTopkSmem));
 }
 
 constexpr int kSW = 4;  // rows (warps) per CTA of sparse_warp
@@ -145,8 +160,10 @@ __device__ int warp_transform(const float (&val)[4], int cnt, bool probs, float 
 template <typename TT, typename TD>
 __global__ void __launch_bounds__(32 * kSW) sparse_warp(VerifyShape s, VerifyArgs a, TopkOut o,
                                                         float kt, float invT, int rec_bytes,
-                                                        int kidcap) {
+                                                        int kidcap, int32_t* seqcnt) {
+  constexpr int kRecMax = (16 + 20 * SPEC_MAX_CHILDREN + 15) / 16;  // 16-byte words
   struct WarpMem {
+    uint4 rec[kRecMax];          // the row's record
     float pk[kK], qk[kK];        // probabilities, list order
     int32_t tis[kK], dis[kK];    // candidate tokens, list order
     int32_t ptok_v[kK];          // support of p in vocabulary order
@@ -159,12 +176,15 @@ __global__ void __launch_bounds__(32 * kSW) sparse_warp(VerifyShape s, VerifyArg
   if (u >= rows) return;  // the whole warp
   WarpMem& m = wmem[wi];
   const int V = s.V;
-  const stream::Meta* M = reinterpret_cast<const stream::Meta*>(a.meta + u * (int64_t)rec_bytes);
-  const float* ukid = reinterpret_cast<const float*>(a.meta + u * (int64_t)rec_bytes + 16 +
-                                                     16 * kidcap);
+  {  // the record into shared memory, its loads beside the lists' below
+    const uint4* src = reinterpret_cast<const uint4*>(a.meta + u * (int64_t)rec_bytes);
+    for (int i = lane; i < rec_bytes / 16; i += 32) m.rec[i] = src[i];
+  }
+  const stream::Meta* M = reinterpret_cast<const stream::Meta*>(m.rec);
+  const float* ukid = reinterpret_cast<const float*>(
+      reinterpret_cast<const unsigned char*>(m.rec) + 16 + 16 * kidcap);
   const bool probs = a.prm.draft_kind == SPEC_DRAFT_PROBS;
   const int ct = o.cnt[u], cq = o.cnt[rows + u];
-  const bool has_q = M->qr >= 0 && cq > 0;
   float tval[4], dval[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -175,6 +195,7 @@ __global__ void __launch_bounds__(32 * kSW) sparse_warp(VerifyShape s, VerifyArg
     m.dis[pos] = pos < cq ? o.idx[(rows + u) * kK + pos] : -1;
   }
   __syncwarp();
+  const bool has_q = M->qr >= 0 && cq > 0;
   const int np = warp_transform(tval, ct, false, kt, invT, a.prm.top_p, m.pk, lane);
   const int nq = has_q ? warp_transform(dval, cq, probs, kt, invT, a.prm.top_p, m.qk, lane) : 0;
   if (lane == 0) {
@@ -190,8 +211,10 @@ __global__ void __launch_bounds__(32 * kSW) sparse_warp(VerifyShape s, VerifyArg
     if (pos < np) {
       const int t = m.tis[pos];
       int rk = 0;
+#pragma unroll 8
       for (int j = 0; j < np; ++j) rk += (m.tis[j] < t) ? 1 : 0;
       float qa = 0.f;
+#pragma unroll 8
       for (int j = 0; j < nq; ++j)
         if (m.dis[j] == t) qa = m.qk[j];
       m.ptok_v[rk] = t;
@@ -226,7 +249,6 @@ __global__ void __launch_bounds__(32 * kSW) sparse_warp(VerifyShape s, VerifyArg
     if (pos < np) al += fminf(m.pv_v[pos], m.qv_v[pos]);
   }
   const float alpha = wsum(al);
-  if (lane == 0 && M->qr >= 0) a.alpha_part[u * kAlphaSlots] = alpha;
 
   uint32_t st_bits = 0;
   float Cc = 0.f, W = 1.f, D = 1.f;
@@ -293,7 +315,6 @@ __global__ void __launch_bounds__(32 * kSW) sparse_warp(VerifyShape s, VerifyArg
     int tok = -1, lastpos = -1;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const int pos = lane + 32 * i;
       const float c = carry + wscan(w[i], lane);
       const unsigned pos_mask = __ballot_sync(kFull, w[i] > 0.f);
       if (pos_mask) lastpos = 32 * i + 31 - __clz(pos_mask);
@@ -307,64 +328,70 @@ __global__ void __launch_bounds__(32 * kSW) sparse_warp(VerifyShape s, VerifyArg
     }
     if (lane == 0) a.row_token[u] = tok;
   }
+  const int n = s.n;
+  const int64_t bq = u / (n + 1);
   if (lane == 0) {
     a.row_child[u] = accepted;
     if (st_bits) flag_status(a.status, st_bits);
+    // the row's acceptance mass (NaN for a row without a draft row)
+    const int r = (int)(u - bq * (n + 1));
+    const float mm = M->qr >= 0 ? alpha : __int_as_float(0x7fc00000);
+    if (s.chain) {
+      if (r < n) a.mass[bq * n + r] = mm;
+    } else {
+      a.mass[u] = mm;
+    }
   }
-}
-
-// Per row: acceptance mass; per sequence (row 0's thread): the walk along
-// accepted children and the token drawn at the row where it stops.
-__global__ void sparse_walk(VerifyShape s, VerifyArgs a) {
-  const int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (row >= s.rows()) return;
-  const int n = s.n;
-  const int b = (int)(row / (n + 1));
-  const int r = (int)(row - (int64_t)b * (n + 1));
-  bool has_q;
-  if (s.chain) {
-    has_q = r < n;
-  } else {
-    const int q = a.q_row ? a.q_row[row] : -1;
-    has_q = q >= 0 && q < s.R;
-  }
-  const float m = has_q ? a.alpha_part[row * kAlphaSlots] : __int_as_float(0x7fc00000);
-  if (s.chain) {
-    if (r < n) a.mass[(int64_t)b * n + r] = m;
-  } else {
-    a.mass[row] = m;
-  }
-  if (r != 0) return;
-  int32_t* out = a.out_tokens + row;
+  // the warp that finishes a sequence's last row walks the sequence: along
+  // the accepted children, then the token drawn where the walk stops
+  __threadfence();
+  int last = 0;
+  if (lane == 0) last = atomicAdd(&seqcnt[bq], 1) == n ? 1 : 0;
+  if (!__shfl_sync(kFull, last, 0)) return;
+  __threadfence();
+  if (lane != 0) return;
+  const int64_t row0 = bq * (n + 1);
+  int32_t* out = a.out_tokens + row0;
   int rr = 0, len = 0;
   while (true) {
-    const int j = a.row_child[row + rr];
+    const int j = __ldcg(a.row_child + row0 + rr);
     if (j < 0 || j >= n || len >= n) break;
-    if (!s.chain) a.path_nodes[(int64_t)b * n + len] = j;
-    out[len] = a.node_tokens[(int64_t)b * n + j];
+    if (!s.chain) a.path_nodes[bq * n + len] = j;
+    out[len] = a.node_tokens[bq * n + j];
     ++len;
     rr = j + 1;
   }
-  out[len] = a.row_token[row + rr];
+  out[len] = __ldcg(a.row_token + row0 + rr);
   for (int k = len + 1; k <= n; ++k) out[k] = -1;
   if (!s.chain)
-    for (int k = len; k < n; ++k) a.path_nodes[(int64_t)b * n + k] = -1;
-  a.count[b] = len;
+    for (int k = len; k < n; ++k) a.path_nodes[bq * n + k] = -1;
+  a.count[bq] = len;
 }
 
 template <typename TT, typename TD>
 cudaError_t launch_sparse_t(const VerifyShape& s, const VerifyArgs& a, int k, cudaStream_t st) {
   const int64_t rows = s.rows();
   TopkOut o{a.topk_idx, a.topk_val, a.topk_cnt};
+  // per-sequence counters of finished rows live in the streaming path's work
+  // list (unused here); the row records skip that list
+  int32_t* seqcnt = a.qlist;
+  if (!seqcnt) return cudaErrorInvalidValue;
+  VerifyArgs am = a;
+  am.qlist = nullptr;
+  const int kidcap = meta_kidcap(s.chain), rec = meta_rec_bytes(s.chain);
   const bool vt = ((uintptr_t)a.target % 16 == 0) && ((int64_t)s.V * sizeof(TT) % 16 == 0) &&
                   (s.V % 8 == 0);
   const bool vd = a.draft && ((uintptr_t)a.draft % 16 == 0) &&
                   ((int64_t)s.V * sizeof(TD) % 16 == 0) && (s.V % 8 == 0);
-  const size_t smem = (size_t)topk::kWarps * topk::kBufCap * sizeof(topk::Cand);
+  const size_t smem = kTopkSmem;
   auto launch = [&](auto kern) -> cudaError_t {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)(2 * rows), topk::kThreads, smem, st>>>(s, a, k, o);
+    // the largest shared-memory carveout, so that five CTAs fit on an SM
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    kern<<<(unsigned)(2 * rows), topk::kThreads, smem, st>>>(s, am, k, o, kidcap, rec, seqcnt);
     return cudaGetLastError();
   };
   cudaError_t e;
@@ -375,16 +402,9 @@ cudaError_t launch_sparse_t(const VerifyShape& s, const VerifyArgs& a, int k, cu
   else e = launch(topk_rows<TT, TD, false, false>);
   prof_end(SPEC_PROF_VERIFY, st);
   if (e != cudaSuccess) return e;
-  const int kidcap = meta_kidcap(s.chain), rec = meta_rec_bytes(s.chain);
-  stream::row_meta<TT, TD><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(s, a, kidcap, rec);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
   const float T = a.prm.temperature;
   sparse_warp<TT, TD><<<(unsigned)((rows + kSW - 1) / kSW), 32 * kSW, 0, st>>>(
-      s, a, o, kLog2e / T, 1.f / T, rec, kidcap);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  sparse_walk<<<(unsigned)((rows + 127) / 128), 128, 0, st>>>(s, a);
+      s, a, o, kLog2e / T, 1.f / T, rec, kidcap, seqcnt);
   return cudaGetLastError();
 }
 

@@ -332,6 +332,23 @@ __device__ void row_topk(const T* __restrict__ rp, int V, int k, float kt, Cand*
   __syncthreads();
 }
 
+// Bitonic sort of one 64-bit value per lane across the warp, descending:
+// lane j ends with the (j + 1)-th largest.
+__device__ __forceinline__ uint64_t warp_sort_desc(uint64_t v, int lane) {
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const uint64_t o = __shfl_xor_sync(0xffffffffu, v, stride);
+      // in blocks that end up descending the lower lane keeps the larger
+      const bool desc = (lane & size) == 0 || size == 32;
+      const bool lower = (lane & stride) == 0;
+      v = (lower == desc) ? (v > o ? v : o) : (v < o ? v : o);
+    }
+  }
+  return v;
+}
+
 // Streaming top-k, bound-and-rescan form (aligned rows).  One pass in which
 // every thread keeps its running maximum (and, if lse is wanted, the row's
 // log-sum-exp); the k-th largest thread maximum is a lower bound on the k-th
@@ -342,11 +359,28 @@ __device__ void row_topk(const T* __restrict__ rp, int V, int k, float kt, Cand*
 // ties at the bound, NaN, -inf) take row_topk.  Same outputs as row_topk.
 constexpr int kCandCap = 1024;
 constexpr int kRowBatch = 8;  // 16-byte groups in flight per thread
+// Shared memory of row_topk_fast: the bound's sorted lists (2 KB), the
+// flagged threads (1 KB), the candidates (kCandCap entries) and, from byte
+// kGkOff, one 16-bit order key (top half of the key of its maximum) per
+// 8-logit group, gk_slots groups per thread (0: rescan the flagged threads'
+// groups instead); the fallback reuses it all.  gk_slots_for gives the slots
+// an allocation holds.
+constexpr size_t kGkOff = 4096 + kCandCap * sizeof(Cand);
+constexpr int gk_slots_for(size_t smem_bytes) {
+  return smem_bytes > kGkOff ? (int)((smem_bytes - kGkOff) / (kThreads * 2)) : 0;
+}
 
-template <typename T, bool kVec>
+// Nothing extra for the last warp to do (see row_topk_fast's `extra`).
+struct NoExtra {
+  __device__ void operator()(int) const {}
+};
+
+// `extra(lane)` runs once on the last warp, at the end, where that warp is
+// usually idle (the ranking needs a thread per candidate).
+template <typename T, bool kVec, int kBatch = kRowBatch, typename F = NoExtra>
 __device__ void row_topk_fast(const T* __restrict__ rp, int V, int k, float kt, Cand* smem,
-                              int32_t* out_idx, float* out_val, int* out_n, float* lse) {
-  __shared__ uint32_t hist[256];
+                              int32_t* out_idx, float* out_val, int* out_n, float* lse,
+                              int gk_slots, F extra = F{}) {
   __shared__ uint32_t s_tau;
   __shared__ int s_nc, s_nf;
   __shared__ float red_m[kWarps], red_z[kWarps];
@@ -370,10 +404,17 @@ __device__ void row_topk_fast(const T* __restrict__ rp, int V, int k, float kt, 
         v[6] = __uint_as_float(r[kU - 1].z); v[7] = __uint_as_float(r[kU - 1].w);
       }
     };
-    for (int g0 = tid; g0 < G; g0 += kNT * kRowBatch) {
-      uint4 r[kRowBatch][kU];
+    // group maxima as 16-bit order keys, [slot][thread] (rows of at most
+    // gk_slots groups per thread); the rescan then reloads only the groups
+    // that can hold an entry at or above the bound
+    uint16_t* gk = G <= gk_slots * kNT
+                       ? reinterpret_cast<uint16_t*>(reinterpret_cast<unsigned char*>(smem) + kGkOff)
+                       : nullptr;
+    int slot0 = 0;
+    for (int g0 = tid; g0 < G; g0 += kNT * kBatch, slot0 += kBatch) {
+      uint4 r[kBatch][kU];
 #pragma unroll
-      for (int bI = 0; bI < kRowBatch; ++bI) {
+      for (int bI = 0; bI < kBatch; ++bI) {
         const int g = g0 + bI * kNT;
         if (g < G) {
 #pragma unroll
@@ -381,13 +422,14 @@ __device__ void row_topk_fast(const T* __restrict__ rp, int V, int k, float kt, 
         }
       }
 #pragma unroll
-      for (int bI = 0; bI < kRowBatch; ++bI) {
+      for (int bI = 0; bI < kBatch; ++bI) {
         if (g0 + bI * kNT < G) {
           float v[8];
           unpack(r[bI], v);
           const float gm = fmaxf(fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3])),
                                  fmaxf(fmaxf(v[4], v[5]), fmaxf(v[6], v[7])));
           mx = fmaxf(mx, gm);
+          if (gk) gk[(slot0 + bI) * kNT + tid] = (uint16_t)(fkey(gm) >> 16);
           if (lse) {
             const float mt = __fmul_rn(gm, kt);
             if (mt > ms.m) {
@@ -411,52 +453,146 @@ __device__ void row_topk_fast(const T* __restrict__ rp, int V, int k, float kt, 
         red_z[warp] = ms.z;
       }
     }
-    // bound: k-th largest thread maximum (order keys; radix select by warp 0)
+    // bound: the k-th largest thread maximum, exactly.  Each warp sorts its
+    // 32 (key, thread) pairs (unique, thread ascending among equal keys);
+    // every thread then counts the pairs above its own in the other warps'
+    // sorted lists by binary search, and the thread of rank k - 1 holds the
+    // bound.  No warp waits on another's serial selection.
     const uint32_t mykey = fkey(mx);
-    smem[tid] = Cand{mykey, tid};
-    if (tid == 0) {
-      s_nc = 0;
-      s_nf = 0;
-    }
-    __syncthreads();
-    if (warp == 0) {
-      uint32_t kth = 0u;
-      warp_select(smem, kNT, k, lane, hist, &kth);
-      if (lane == 0) {
-        s_tau = kth;
-        if (lse) {
-          MaxSum A{red_m[0], red_z[0]};
-          for (int w = 1; w < kWarps; ++w) A = ms_combine(A, MaxSum{red_m[w], red_z[w]});
-          *lse = A.m + log2f(A.z);
-        }
+    uint64_t* lists = reinterpret_cast<uint64_t*>(smem);  // kNT entries
+    {
+      const uint64_t c = warp_sort_desc(((uint64_t)mykey << 32) | (uint32_t)(kNT - 1 - tid), lane);
+      lists[warp * 32 + lane] = c;
+      if (tid == 0) {
+        s_nc = 0;
+        s_nf = 0;
+      }
+      __syncthreads();
+      int rank = lane;
+#pragma unroll
+      for (int w2 = 0; w2 < kWarps; ++w2) {
+        if (w2 == warp) continue;
+        const uint64_t* L = lists + w2 * 32;
+        int lo = 0;  // entries of L above c (L descending)
+#pragma unroll
+        for (int step = 16; step > 0; step >>= 1)
+          if (L[lo + step - 1] > c) lo += step;
+        rank += lo + ((lo == 31 && L[31] > c) ? 1 : 0);
+      }
+      if (rank == k - 1) s_tau = (uint32_t)(c >> 32);
+      if (tid == 0 && lse) {
+        MaxSum A{red_m[0], red_z[0]};
+        for (int w = 1; w < kWarps; ++w) A = ms_combine(A, MaxSum{red_m[w], red_z[w]});
+        *lse = A.m + log2f(A.z);
       }
     }
     __syncthreads();
     const uint32_t tau = s_tau;
     int* flagged = reinterpret_cast<int*>(smem + kNT);
     Cand* cand = smem + 2 * kNT;
-    if (mykey >= tau) flagged[atomicAdd(&s_nf, 1)] = tid;  // at most kNT entries
-    __syncthreads();
-    const int nf = s_nf;
-    // the flagged threads' groups, rescanned by the whole CTA
-    const int gpt = (G + kNT - 1) / kNT;
-#pragma unroll 2
-    for (int w = tid; w < nf * gpt; w += kNT) {
-      const int f = w / gpt;
-      const int g = flagged[f] + (w - f * gpt) * kNT;
-      if (g < G) {
-        uint4 r[kU];
+    auto append_all = [&](int g, const float (&v)[8]) {  // one atomic per entry
 #pragma unroll
-        for (int u = 0; u < kU; ++u) r[u] = ldg_stream16(base + (int64_t)g * kU + u);
-        float v[8];
-        unpack(r, v);
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t kj = fkey(v[j]);
+        if (kj >= tau) {
+          const int pos = atomicAdd(&s_nc, 1);
+          if (pos < kCandCap) cand[pos] = Cand{kj, g * 8 + j};
+        }
+      }
+    };
+    if (gk) {
+      // each thread reloads its own groups whose key reaches the bound (the
+      // group of its maximum, rarely more), two at most in registers with
+      // one shared atomic per warp; more go through the per-entry path
+      const uint32_t tau16 = tau >> 16;
+      int nq = 0, ga = -1, gb = -1;
+      if (mykey >= tau) {
+        for (int j = 0, g = tid; g < G; ++j, g += kNT)
+          if (gk[j * kNT + tid] >= tau16) {
+            if (nq == 0) ga = g;
+            else if (nq == 1) gb = g;
+            ++nq;
+          }
+      }
+      uint4 ra[kU], rb[kU];
+      if (nq >= 1 && nq <= 2) {
+#pragma unroll
+        for (int u = 0; u < kU; ++u) ra[u] = ldg_stream16(base + (int64_t)ga * kU + u);
+      }
+      if (nq == 2) {
+#pragma unroll
+        for (int u = 0; u < kU; ++u) rb[u] = ldg_stream16(base + (int64_t)gb * kU + u);
+      }
+      float va[8], vb[8];
+      int c = 0;
+      if (nq >= 1 && nq <= 2) {
+        unpack(ra, va);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) c += fkey(va[j]) >= tau ? 1 : 0;
+      }
+      if (nq == 2) {
+        unpack(rb, vb);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) c += fkey(vb[j]) >= tau ? 1 : 0;
+      }
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      int wbase = 0;
+      if (lane == 31 && incl > 0) wbase = atomicAdd(&s_nc, incl);
+      wbase = __shfl_sync(0xffffffffu, wbase, 31);
+      int pos = wbase + incl - c;
+      if (nq >= 1 && nq <= 2) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const uint32_t kj = fkey(v[j]);
+          const uint32_t kj = fkey(va[j]);
           if (kj >= tau) {
-            const int pos = atomicAdd(&s_nc, 1);
-            if (pos < kCandCap) cand[pos] = Cand{kj, g * 8 + j};
+            if (pos < kCandCap) cand[pos] = Cand{kj, ga * 8 + j};
+            ++pos;
           }
+        }
+      }
+      if (nq == 2) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t kj = fkey(vb[j]);
+          if (kj >= tau) {
+            if (pos < kCandCap) cand[pos] = Cand{kj, gb * 8 + j};
+            ++pos;
+          }
+        }
+      }
+      if (nq > 2) {
+        for (int j = 0, g = tid; g < G; ++j, g += kNT)
+          if (gk[j * kNT + tid] >= tau16) {
+            uint4 r[kU];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) r[u] = ldg_stream16(base + (int64_t)g * kU + u);
+            float v[8];
+            unpack(r, v);
+            append_all(g, v);
+          }
+      }
+    } else {
+      if (mykey >= tau) flagged[atomicAdd(&s_nf, 1)] = tid;  // at most kNT entries
+      __syncthreads();
+      const int nf = s_nf;
+      // the flagged threads' groups, rescanned by the whole CTA
+      const int gpt = (G + kNT - 1) / kNT;
+#pragma unroll 2
+      for (int w = tid; w < nf * gpt; w += kNT) {
+        const int f = w / gpt;
+        const int g = flagged[f] + (w - f * gpt) * kNT;
+        if (g < G) {
+          uint4 r[kU];
+#pragma unroll
+          for (int u = 0; u < kU; ++u) r[u] = ldg_stream16(base + (int64_t)g * kU + u);
+          float v[8];
+          unpack(r, v);
+          append_all(g, v);
         }
       }
     }
@@ -468,6 +604,7 @@ __device__ void row_topk_fast(const T* __restrict__ rp, int V, int k, float kt, 
       for (int i = tid; i < nc; i += kNT) {
         const Cand c = cand[i];
         int rk = 0;
+#pragma unroll 8
         for (int j2 = 0; j2 < nc; ++j2) {
           const Cand d = cand[j2];
           rk += before(d.key, d.idx, c.key, c.idx) ? 1 : 0;
@@ -479,9 +616,13 @@ __device__ void row_topk_fast(const T* __restrict__ rp, int V, int k, float kt, 
       }
       if (tid == 0) *out_n = k;
     }
+    if (warp == kWarps - 1) extra(lane);
     __syncthreads();
   }
   if (fallback) row_topk<T, kVec>(rp, V, k, kt, smem, out_idx, out_val, out_n, lse);
+  if constexpr (!kVec) {
+    if (warp == kWarps - 1) extra(lane);
+  }
 }
 
 }  // namespace
