@@ -85,14 +85,14 @@ def metric_of(w):
 _STREAM_SRC = ("sample_stream.cuh", "sample_stream_bf16.cu",
                "sample_stream_f32.cu", "common.cuh", "kernels.h")
 TRAFFIC = {
-    # unit_stream, tree_static at B=16 (clusters of 2): 760.44 MB read +
-    # 3.38 MB written, 976 rows
-    "tree_static": {"bytes_per_unit": 763.82e6 / 976, "src": _STREAM_SRC,
-                    "hash": "7ea3859da293773b"},
-    # unit_stream, eagle2 at B=32 (one CTA per row): 403.52 MB read + 3.28 MB
+    # unit_stream, tree_static at B=16 (clusters of 2): 761.56 MB read +
+    # 3.31 MB written, 976 rows
+    "tree_static": {"bytes_per_unit": 764.87e6 / 976, "src": _STREAM_SRC,
+                    "hash": "bb45002fbbca7d60"},
+    # unit_stream, eagle2 at B=32 (one CTA per row): 403.26 MB read + 3.22 MB
     # written, 782 rows with a draft row
-    "eagle2": {"bytes_per_unit": 406.80e6 / 782, "src": _STREAM_SRC,
-               "hash": "7ea3859da293773b"},
+    "eagle2": {"bytes_per_unit": 406.48e6 / 782, "src": _STREAM_SRC,
+               "hash": "bb45002fbbca7d60"},
     # accept_stats_warp at B=65536 rounds: 47.46 MB read + 9.7 KB written
     "accept_stats": {"bytes_per_unit": 47.47e6 / 65536,
                      "src": ("accept_stats.cu", "common.cuh", "kernels.h"),

@@ -184,9 +184,11 @@ __global__ void __launch_bounds__(kST, 1)
   const TD* dsm = reinterpret_cast<const TD*>(dyn + (size_t)(K + 1) * slice * sizeof(TT));
   uint32_t bits = 0;
 
-  if (tid < nrows) mbar_init(&sh.bar[tid], 1);
+  if (tid < nrows) {  // each initialising thread makes its barrier visible
+    mbar_init(&sh.bar[tid], 1);
+    fence_mbar_init();
+  }
   if (tid == 0) sh.cta_bits = 0;
-  fence_mbar_init();
   cluster_arrive_relaxed();
   __syncthreads();
   if (tid == 0 && len > 0) {
