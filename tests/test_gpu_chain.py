@@ -222,3 +222,14 @@ def test_chain_small_single_sequence_rewrites_status():
                        temperature=1.0, seed=w.decision_seed)
     compare_chain(gpu, ref)
     assert st == ref.status == 0
+
+
+@pytest.mark.parametrize("K", [2, 3])
+def test_chain_small_shared_memory_limit_llama_vocab(K):
+    # V = 128256 bf16: K = 2 keeps five 32 KB row slices per CTA (160 KB,
+    # the single launch); K = 3 needs seven (224 KB) and streams instead
+    w = synth.workload("chain_sample", B=2, K=K, V=128256,
+                       target_dtype=torch.bfloat16,
+                       draft_dtype=torch.bfloat16, seed=40 + K)
+    gpu, ref = run(w)
+    compare_chain(gpu, ref, max_excluded=1)

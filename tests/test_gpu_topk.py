@@ -109,3 +109,29 @@ def test_topk_tree():
                       temperature=w.temperature, top_k=w.top_k, top_p=w.top_p,
                       seed=w.decision_seed)
     compare_tree(gpu, ref, max_excluded=1)
+
+
+@pytest.mark.parametrize("V,dt", [(128256, torch.bfloat16),
+                                  (90000, torch.float32)])
+def test_topk_long_rows_rescan_flagged_threads(V, dt):
+    # rows of more groups per thread than the group-key table holds: the
+    # threads whose maximum reaches the bound rescan all their groups
+    w = synth.workload("chain_topk", B=4, K=3, V=V, target_dtype=dt,
+                       draft_dtype=dt, seed=V % 977)
+    gpu, ref = run_chain(w)
+    compare_chain(gpu, ref, max_excluded=1)
+
+
+def test_topk_constant_rows_overflow_the_candidates():
+    # every logit of a row ties at the bound: more candidates than the
+    # shared list holds, so the row takes the exact fallback selection (the
+    # k lowest indices of the tied value)
+    w = synth.workload("chain_topk", B=3, K=2, V=32000, top_k=50, top_p=1.0,
+                       seed=17)
+    target, draft, toks = synth.chain_inputs(w, "cuda")
+    target[0].zero_()
+    draft[1].fill_(1.5)
+    toks[0, 0] = 7        # inside the tied row's top-k
+    toks[1, 1] = 40000 % w.V
+    gpu, ref = run_chain(w, target=target, draft=draft, toks=toks)
+    compare_chain(gpu, ref, max_excluded=1)
