@@ -349,19 +349,44 @@ __global__ void __launch_bounds__(32 * kSW) sparse_warp(VerifyShape s, VerifyArg
   if (lane == 0) last = atomicAdd(&seqcnt[bq], 1) == n ? 1 : 0;
   if (!__shfl_sync(kFull, last, 0)) return;
   __threadfence();
-  if (lane != 0) return;
   const int64_t row0 = bq * (n + 1);
   int32_t* out = a.out_tokens + row0;
   int rr = 0, len = 0;
-  while (true) {
-    const int j = __ldcg(a.row_child + row0 + rr);
-    if (j < 0 || j >= n || len >= n) break;
-    if (!s.chain) a.path_nodes[bq * n + len] = j;
-    out[len] = a.node_tokens[bq * n + j];
-    ++len;
-    rr = j + 1;
+  if (n < kK) {
+    // every row's outcome and every node's token in one round of loads (the
+    // lanes in parallel), then the walk from shared memory
+    int32_t* rc = m.ptok_v;  // [n + 1] accepted child per row (free by now)
+    int32_t* rt = m.tis;     // [n + 1] token drawn per row
+    int32_t* nt = m.dis;     // [n] drafted token per node
+    __syncwarp();
+    for (int r = lane; r <= n; r += 32) {
+      rc[r] = __ldcg(a.row_child + row0 + r);
+      rt[r] = __ldcg(a.row_token + row0 + r);
+      if (r < n) nt[r] = a.node_tokens[bq * n + r];
+    }
+    __syncwarp();
+    if (lane != 0) return;
+    while (true) {
+      const int j = rc[rr];
+      if (j < 0 || j >= n || len >= n) break;
+      if (!s.chain) a.path_nodes[bq * n + len] = j;
+      out[len] = nt[j];
+      ++len;
+      rr = j + 1;
+    }
+    out[len] = rt[rr];
+  } else {  // long sequences: the walk's loads one after another
+    if (lane != 0) return;
+    while (true) {
+      const int j = __ldcg(a.row_child + row0 + rr);
+      if (j < 0 || j >= n || len >= n) break;
+      if (!s.chain) a.path_nodes[bq * n + len] = j;
+      out[len] = a.node_tokens[bq * n + j];
+      ++len;
+      rr = j + 1;
+    }
+    out[len] = __ldcg(a.row_token + row0 + rr);
   }
-  out[len] = __ldcg(a.row_token + row0 + rr);
   for (int k = len + 1; k <= n; ++k) out[k] = -1;
   if (!s.chain)
     for (int k = len; k < n; ++k) a.path_nodes[bq * n + k] = -1;
