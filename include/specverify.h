@@ -480,8 +480,10 @@ int spec_get_status_noalloc(uint32_t* status, void* stream);
 /*
  * Kernel timing for benchmarks.  spec_profile_enable(1) clears the record and
  * makes every later call bracket its dominant kernel with a pair of CUDA
- * events recorded on the caller's stream (at most 16384 pairs); 0 turns it
- * off.  spec_profile_read waits for the recorded events and returns the total
+ * events recorded on the caller's stream (at most 16384 pairs); n > 1
+ * brackets only every n-th launch of each kind (a sample, so that the
+ * events' own cost stays off most calls); 0 turns it off; a negative n is
+ * SPEC_ERR_ARG.  spec_profile_read waits for the recorded events and returns the total
  * milliseconds and number of launches of one kernel kind:
  *   SPEC_PROF_ARGMAX    greedy argmax streaming kernel,
  *   SPEC_PROF_VERIFY    sampled row-verification kernel,

@@ -1,7 +1,8 @@
 // Optional per-kernel timing: when enabled, every launch of a profiled kernel
-// kind is bracketed by a pair of CUDA events recorded on the launching stream.
-// Reading the totals waits for the recorded events.  Not thread-safe: meant
-// for a benchmark driving one stream.
+// kind (or every n-th, a sample that keeps the events' own cost off most
+// launches) is bracketed by a pair of CUDA events recorded on the launching
+// stream.  Reading the totals waits for the recorded events.  Not
+// thread-safe: meant for a benchmark driving one stream.
 #include <vector>
 
 #include "kernels.h"
@@ -11,8 +12,12 @@ namespace {
 
 constexpr int kMaxPairs = 1 << 14;
 
+constexpr int kKinds = 8;
+
 struct Prof {
   bool on = false;
+  int period = 1;                 // bracket every period-th launch of a kind
+  int seen[kKinds] = {};          // launches of each kind since enabled
   std::vector<cudaEvent_t> ev;    // 2 per pair
   std::vector<int> kind;          // kind of each recorded pair
   int used = 0;
@@ -26,6 +31,7 @@ Prof g_prof;
 void prof_begin(int kind, cudaStream_t st) {
   Prof& p = g_prof;
   if (!p.on) return;
+  if (kind >= 0 && kind < kKinds && p.seen[kind]++ % p.period != 0) return;
   if (p.used >= kMaxPairs) {
     ++p.dropped;
     return;
@@ -61,7 +67,10 @@ using namespace sv;
 extern "C" {
 
 int spec_profile_enable(int on) {
+  if (on < 0) return SPEC_ERR_ARG;
   g_prof.on = on != 0;
+  g_prof.period = on > 1 ? on : 1;
+  for (int k = 0; k < kKinds; ++k) g_prof.seen[k] = 0;
   g_prof.used = 0;
   g_prof.open = -1;
   g_prof.dropped = 0;
