@@ -17,24 +17,29 @@
 // node-major, so the G query heads that share a key/value head are served by
 // one stream of its keys and values -- as two 128-row tiles:
 //   warp 0     TMA producer: 64-key blocks of K and V (128-byte swizzle) into
-//              a 3-stage shared-memory ring;
-//              (and prefetches blocks further ahead into L2);
-//   warps 1-2  one tensor-core issuer per tile t (warp 1 also allocates
-//              TMEM): S_t = Q_t K^T of the next key block (tcgen05.mma M 128,
-//              N 64, K 128) into one of two S buffers once the block's keys
-//              have landed and the softmax has released that buffer, then
-//              O_t += P_t V of this block (M 128, N 128, K 64; V is the
-//              MN-major operand, read as stored) once the softmax has written
-//              P_t -- one thread per tile, so the tiles never wait on each
-//              other;
-//   warps 3-10 softmax, one thread per query row (warp w reads TMEM lanes of
-//              quadrant w % 4): they stage Q once, then per block read S with
-//              tcgen05.ld, apply the scale and the tree mask, run the online
-//              base-2 softmax against a reference maximum that moves only when
-//              a row's maximum grows by more than 2^8 (then O_t is rescaled in
-//              TMEM), and write P as bf16 into 128-byte-swizzled shared memory
-//              for the next MMA; at the end O_t / l is rounded to bf16.
-// TMEM: S_t of buffer u at columns 64 (2 t + u), O_t at 256 + 128 t.  Every mbarrier
+//              a 6-stage shared-memory ring (and a prefetch into L2 of the
+//              block that will next fill the stage it waits for);
+//   warps 1-2  tile t's S issuer (warp 1 also allocates TMEM): S_t = Q_t K^T
+//              of each key block (tcgen05.mma M 128, N 64, K 128, Q_t read
+//              from TMEM, K from shared memory) once the block's keys have
+//              landed and the softmax has read S_t of the block before;
+//   warps 3-4  tile t's P V issuer: O_t += P_t V of each block (M 128,
+//              N 128, K 64; V is the MN-major operand, read as stored) once
+//              the softmax has written P_t -- four issuing threads, so that
+//              neither tile and neither chain of issues waits on another;
+//   warps 5-12 softmax, one thread per query row (warp w reads TMEM lanes of
+//              quadrant w % 4): they write their row of Q into TMEM once, then
+//              per block read S with tcgen05.ld, apply the scale and the tree
+//              mask, run the online base-2 softmax against a reference maximum
+//              that moves only when a row's maximum grows by more than 2^8
+//              (then O_t is rescaled in TMEM), and write P as bf16 into
+//              128-byte-swizzled shared memory for the next MMA; at the end
+//              O_t / l is rounded to bf16.
+// TMEM (512 columns): Q_t at columns 64 t (two bf16 per column), S_t at
+// 128 + 64 t, O_t at 256 + 128 t.  With Q in TMEM the tensor cores read only
+// K (2 KB per MMA instead of 6) from shared memory for S, and the shared
+// memory Q no longer takes holds a ring deep enough to cover the latency of
+// a key/value block's copy under full load.  Every mbarrier
 // wait is bounded (SPEC_STATUS_TIMEOUT is not reported by this entry point,
 // which has no status word; a CTA that gives up stops waiting and still frees
 // its TMEM after waiting, bounded, for its own MMAs and copies).
@@ -53,33 +58,31 @@ constexpr int kAD = 128;   // head dim
 constexpr int kKB = 64;    // keys per block
 constexpr int kMT = 128;   // query rows per tile
 constexpr int kTiles = 2;  // tiles per CTA
-constexpr int kAStages = 3;
-constexpr int kQHalf = kMT * 64 * 2;     // 16 KB: 128 rows x 64 dims
-constexpr int kQTile = 2 * kQHalf;       // 32 KB
+constexpr int kAStages = 6;
 constexpr int kKVHalf = kKB * 64 * 2;    // 8 KB: 64 keys x 64 dims
 constexpr int kKVTile = 2 * kKVHalf;     // 16 KB
 constexpr int kAStage = 2 * kKVTile;     // K then V: 32 KB
 constexpr int kPTile = kMT * kKB * 2;    // 16 KB: 128 rows x 64 keys
-constexpr int kOffKV = kTiles * kQTile;                  // 64 KB
-constexpr int kOffP = kOffKV + kAStages * kAStage;       // 160 KB
-constexpr int kOffBar = kOffP + kTiles * kPTile;         // 192 KB
-constexpr int kAThreads = 352;
-constexpr int kPrefetch = 6;  // key blocks prefetched into L2 ahead of the ring
+constexpr int kOffKV = 0;
+constexpr int kOffP = kOffKV + kAStages * kAStage;       // 192 KB
+constexpr int kOffBar = kOffP + kTiles * kPTile;         // 224 KB
+constexpr int kAThreads = 416;
+constexpr int kPrefetch = 0;  // key blocks prefetched into L2 ahead of the ring
 constexpr int kSoftThreads = 256;
 constexpr uint32_t kATmemCols = 512;
 constexpr int kOrderMax = 256;  // sequences ordered longest first up to this batch
 
 struct __align__(8) AttnSmem {
   uint64_t kvfull[kAStages], kvempty[kAStages];
-  uint64_t sfull[kTiles][2], sfree[kTiles][2], pfull[kTiles], pdone[kTiles];
-  uint64_t qready, drain[kTiles];
+  uint64_t sfull[kTiles], sfree[kTiles], pfull[kTiles], pdone[kTiles];
+  uint64_t qready, drain[kTiles][2];
   uint32_t tmem_base;
   uint32_t dead;
   int seq;
 };
 constexpr size_t kASmemBytes = (size_t)kOffBar + sizeof(AttnSmem) + 1024;
 
-// S = Q K^T: M 128, N 64, bf16 K-major A and B, float32 D.
+// S = Q K^T: M 128, N 64, bf16 K-major A (in TMEM) and B, float32 D.
 constexpr uint32_t kIdescS = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kKB >> 3) << 17) |
                              ((uint32_t)(kMT >> 4) << 24);
 // O += P V: M 128, N 128, A K-major, B MN-major (bit 16).
@@ -87,6 +90,7 @@ constexpr uint32_t kIdescPV = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
                               ((uint32_t)(kAD >> 3) << 17) | ((uint32_t)(kMT >> 4) << 24);
 
 __device__ __forceinline__ void await(AttnSmem& sm, uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return;
   if (*(volatile uint32_t*)&sm.dead) return;
   if (!mbar_wait_bounded(bar, parity)) *(volatile uint32_t*)&sm.dead = 1;
 }
@@ -133,6 +137,15 @@ __device__ __forceinline__ void mma_f16(uint32_t d, uint64_t a, uint64_t b, uint
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
       "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+// the same with A read from TMEM (column address a; two bf16 per column,
+// the lower K index in the low half)
+__device__ __forceinline__ void mma_f16_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc,
+                                           uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a), "l"(b), "r"(idesc), "r"(acc));
 }
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
@@ -253,16 +266,16 @@ __global__ void __launch_bounds__(kAThreads, 1)
       mbar_init(&sm.kvempty[s], ntile);  // released by every tile's issuer
     }
     for (int t = 0; t < kTiles; ++t) {
-      mbar_init(&sm.sfull[t][0], 1);
-      mbar_init(&sm.sfull[t][1], 1);
-      mbar_init(&sm.sfree[t][0], kMT);
-      mbar_init(&sm.sfree[t][1], kMT);
+      mbar_init(&sm.sfull[t], 1);
+      mbar_init(&sm.sfree[t], kMT);
       mbar_init(&sm.pfull[t], kMT);
       mbar_init(&sm.pdone[t], 1);
     }
     mbar_init(&sm.qready, kSoftThreads);
-    mbar_init(&sm.drain[0], 1);
-    mbar_init(&sm.drain[1], 1);
+    for (int t = 0; t < kTiles; ++t) {
+      mbar_init(&sm.drain[t][0], 1);
+      mbar_init(&sm.drain[t][1], 1);
+    }
     sm.dead = 0;
     fence_mbar_init();
   }
@@ -308,41 +321,51 @@ __global__ void __launch_bounds__(kAThreads, 1)
       }
     }
   } else if (warp <= 2) {
-    // ------------------------------------------- tile t's tensor-core issuer
-    // Warp 1 + t issues tile t's S = Q K^T of the next block, then its
-    // O += P V of this block as soon as the softmax has written P: the two
-    // tiles never wait on each other.
+    // ------------------------------------------------ tile t's S issuer
+    // Warp 1 + t issues S_t = Q_t K^T of each block as soon as its keys have
+    // landed and the softmax has read S_t of the block before.
     const int t = warp - 1;
     if (lane == 0 && t < ntile) {
       await(sm, &sm.qready, 0);
       fence_after();
-      const uint32_t qt = base + (uint32_t)(t * kQTile);
-      auto issue_s = [&](int j) {
+      const uint32_t tq = tmem + (uint32_t)(64 * t);
+      const uint32_t ds = tmem + 128u + (uint32_t)(64 * t);
+      for (int j = 0; j < nblk; ++j) {
         const int s = j % kAStages;
         await(sm, &sm.kvfull[s], (uint32_t)(j / kAStages) & 1u);
-        // S buffer j & 1 was last read by the softmax at block j - 2
-        if (j >= 2) await(sm, &sm.sfree[t][j & 1], (uint32_t)(((j >> 1) - 1) & 1));
+        // S_t was last read by the softmax at block j - 1
+        if (j >= 1) await(sm, &sm.sfree[t], (uint32_t)((j - 1) & 1));
         fence_after();
         const uint32_t kst = base + kOffKV + (uint32_t)(s * kAStage);
-        const uint32_t ds = tmem + (uint32_t)(64 * (2 * t + (j & 1)));
+        // K step k: head dims 16k .. 16k + 15 = Q_t's TMEM columns 8k .. 8k + 7
 #pragma unroll
         for (int k = 0; k < kAD / 16; ++k) {
-          const uint32_t off = (uint32_t)((k >> 2) * kQHalf + (k & 3) * 32);
           const uint32_t koff = (uint32_t)((k >> 2) * kKVHalf + (k & 3) * 32);
-          mma_f16(ds, desc_kmajor(qt + off), desc_kmajor(kst + koff), kIdescS, k > 0 ? 1u : 0u);
+          mma_f16_ts(ds, tq + (uint32_t)(8 * k), desc_kmajor(kst + koff), kIdescS,
+                     k > 0 ? 1u : 0u);
         }
-        mma_commit(&sm.sfull[t][j & 1]);
-      };
-      if (nblk > 0) issue_s(0);
+        mma_commit(&sm.sfull[t]);
+      }
+      mma_commit(&sm.drain[t][0]);
+      mbar_wait_bounded(&sm.drain[t][0], 0);
+    }
+  } else if (warp <= 4) {
+    // --------------------------------------------- tile t's P V issuer
+    // Warp 3 + t issues O_t += P_t V of each block as soon as the softmax
+    // has written P_t (a separate thread from the S issuer, so that neither
+    // chain of issues waits behind the other).
+    const int t = warp - 3;
+    if (lane == 0 && t < ntile) {
       for (int j = 0; j < nblk; ++j) {
-        if (j + 1 < nblk) issue_s(j + 1);
         const int s = j % kAStages;
         const uint32_t vst = base + kOffKV + (uint32_t)(s * kAStage) + kKVTile;
         const int tail = L - j * kKB;  // keys of this block that exist
         if (tail < kKB) {
           // cache rows past the sequence's keys hold anything (NaN included);
           // their P is 0, but 0 * NaN is not, so their V rows become zeros
-          // (each tile's issuer writes the same zeros before its own MMAs)
+          // (each tile's issuer writes the same zeros before its own MMAs),
+          // after the block's copy has landed
+          await(sm, &sm.kvfull[s], (uint32_t)(j / kAStages) & 1u);
           unsigned char* vz = bp + kOffKV + s * kAStage + kKVTile;
           for (int rr = tail; rr < kKB; ++rr)
             for (int hb = 0; hb < 2; ++hb) {
@@ -360,16 +383,16 @@ __global__ void __launch_bounds__(kAThreads, 1)
           mma_f16(tmem + 256u + (uint32_t)(128 * t), desc_kmajor(pt + (uint32_t)(k * 32)),
                   desc_mnmajor(vst + (uint32_t)(k * 2048)), kIdescPV, (j > 0 || k > 0) ? 1u : 0u);
         mma_commit(&sm.pdone[t]);
-        // this tile is done with the block's K and V (the softmax read S
-        // before releasing P, so the S MMAs are complete too)
+        // this tile is done with the block's K and V (its S MMAs completed
+        // before the softmax wrote P)
         mma_commit(&sm.kvempty[s]);
       }
-      mma_commit(&sm.drain[t]);
-      mbar_wait_bounded(&sm.drain[t], 0);
+      mma_commit(&sm.drain[t][1]);
+      mbar_wait_bounded(&sm.drain[t][1], 0);
     }
   } else {
     // ------------------------------------------------------------- softmax
-    const int t = (warp - 3) >> 2;   // tile
+    const int t = (warp - 5) >> 2;   // tile
     const int qd = warp & 3;         // TMEM lane quadrant of this warp
     const int r = qd * 32 + lane;    // row within the tile
     const int gr = row0 + t * kMT + r;
@@ -380,33 +403,40 @@ __global__ void __launch_bounds__(kAThreads, 1)
                                  (N >= 64 ? ~0ull : ((1ull << N) - 1ull)))
                               : 0ull;
     const int64_t qoff = (((int64_t)b * N + node) * Hq + hq) * kAD;
-    {  // stage this row of Q (zeros for padding rows)
+    const uint32_t lanes = (uint32_t)(qd * 32) << 16;
+    {  // this row of Q into Q_t's TMEM lane (zeros for padding rows)
       const uint4* src = reinterpret_cast<const uint4*>(q + qoff);
-      unsigned char* qt = bp + t * kQTile;
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const uint4 v = valid ? src[c] : make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4*>(qt + (c >> 3) * kQHalf + swz(r, c & 7)) = v;
+      for (int h = 0; h < 2; ++h) {
+        uint32_t w[32];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 v = valid ? src[8 * h + c] : make_uint4(0u, 0u, 0u, 0u);
+          w[4 * c] = v.x;
+          w[4 * c + 1] = v.y;
+          w[4 * c + 2] = v.z;
+          w[4 * c + 3] = v.w;
+        }
+        tst32(tmem + lanes + (uint32_t)(64 * t + 32 * h), w);
       }
-      fence_async_smem();
+      tst_wait();
+      fence_before();
       mbar_arrive(&sm.qready);
     }
     if (t < ntile) {
-      const uint32_t lanes = (uint32_t)(qd * 32) << 16;
-      const uint32_t tS = tmem + lanes + (uint32_t)(128 * t);  // + 64 * buffer
+      const uint32_t tS = tmem + lanes + 128u + (uint32_t)(64 * t);
       const uint32_t tO = tmem + lanes + 256u + (uint32_t)(128 * t);
       unsigned char* pt = bp + kOffP + t * kPTile;
       float mref = neg_inf(), l = 0.f;
       for (int j = 0; j < nblk; ++j) {
-        await(sm, &sm.sfull[t][j & 1], (uint32_t)((j >> 1) & 1));
+        await(sm, &sm.sfull[t], (uint32_t)(j & 1));
         fence_after();
         uint32_t ra[32], rb[32];
-        const uint32_t tSb = tS + (uint32_t)(64 * (j & 1));
-        tld32(tSb, ra);
-        tld32(tSb + 32u, rb);
+        tld32(tS, ra);
+        tld32(tS + 32u, rb);
         tld_wait();
         fence_before();
-        mbar_arrive(&sm.sfree[t][j & 1]);  // the S issuer may refill the buffer
+        mbar_arrive(&sm.sfree[t]);  // the S issuer may write S_t of the next block
         // raw scores q.k (the scale is applied inside the exponent below;
         // it is positive, so the maximum is taken on the raw scores)
         float s[64];
