@@ -17,7 +17,7 @@
 // node-major, so the G query heads that share a key/value head are served by
 // one stream of its keys and values -- as two 128-row tiles:
 //   warp 0     TMA producer: 64-key blocks of K and V (128-byte swizzle) into
-//              a 6-stage shared-memory ring (and a prefetch into L2 of the
+//              a 5-stage shared-memory ring (and a prefetch into L2 of the
 //              block that will next fill the stage it waits for);
 //   warps 1-2  tile t's S issuer (warp 1 also allocates TMEM): S_t = Q_t K^T
 //              of each key block (tcgen05.mma M 128, N 64, K 128, Q_t read
@@ -33,8 +33,9 @@
 //              mask, run the online base-2 softmax against a reference maximum
 //              that moves only when a row's maximum grows by more than 2^8
 //              (then O_t is rescaled in TMEM), and write P as bf16 into
-//              128-byte-swizzled shared memory for the next MMA; at the end
-//              O_t / l is rounded to bf16.
+//              128-byte-swizzled shared memory for the next MMA (two P
+//              buffers per tile, so that block j + 1's P is written while
+//              block j's P V runs); at the end O_t / l is rounded to bf16.
 // TMEM (512 columns): Q_t at columns 64 t (two bf16 per column), S_t at
 // 128 + 64 t, O_t at 256 + 128 t.  With Q in TMEM the tensor cores read only
 // K (2 KB per MMA instead of 6) from shared memory for S, and the shared
@@ -58,14 +59,14 @@ constexpr int kAD = 128;   // head dim
 constexpr int kKB = 64;    // keys per block
 constexpr int kMT = 128;   // query rows per tile
 constexpr int kTiles = 2;  // tiles per CTA
-constexpr int kAStages = 6;
+constexpr int kAStages = 5;
 constexpr int kKVHalf = kKB * 64 * 2;    // 8 KB: 64 keys x 64 dims
 constexpr int kKVTile = 2 * kKVHalf;     // 16 KB
 constexpr int kAStage = 2 * kKVTile;     // K then V: 32 KB
 constexpr int kPTile = kMT * kKB * 2;    // 16 KB: 128 rows x 64 keys
 constexpr int kOffKV = 0;
-constexpr int kOffP = kOffKV + kAStages * kAStage;       // 192 KB
-constexpr int kOffBar = kOffP + kTiles * kPTile;         // 224 KB
+constexpr int kOffP = kOffKV + kAStages * kAStage;       // 160 KB
+constexpr int kOffBar = kOffP + kTiles * 2 * kPTile;     // 224 KB: two P buffers per tile
 constexpr int kAThreads = 416;
 constexpr int kPrefetch = 0;  // key blocks prefetched into L2 ahead of the ring
 constexpr int kSoftThreads = 256;
@@ -74,7 +75,7 @@ constexpr int kOrderMax = 256;  // sequences ordered longest first up to this ba
 
 struct __align__(8) AttnSmem {
   uint64_t kvfull[kAStages], kvempty[kAStages];
-  uint64_t sfull[kTiles], sfree[kTiles], pfull[kTiles], pdone[kTiles];
+  uint64_t sfull[kTiles], sfree[kTiles], pfull[kTiles][2], pdone[kTiles][2];
   uint64_t qready, drain[kTiles][2];
   uint32_t tmem_base;
   uint32_t dead;
@@ -268,8 +269,10 @@ __global__ void __launch_bounds__(kAThreads, 1)
     for (int t = 0; t < kTiles; ++t) {
       mbar_init(&sm.sfull[t], 1);
       mbar_init(&sm.sfree[t], kMT);
-      mbar_init(&sm.pfull[t], kMT);
-      mbar_init(&sm.pdone[t], 1);
+      mbar_init(&sm.pfull[t][0], kMT);
+      mbar_init(&sm.pfull[t][1], kMT);
+      mbar_init(&sm.pdone[t][0], 1);
+      mbar_init(&sm.pdone[t][1], 1);
     }
     mbar_init(&sm.qready, kSoftThreads);
     for (int t = 0; t < kTiles; ++t) {
@@ -375,14 +378,14 @@ __global__ void __launch_bounds__(kAThreads, 1)
             }
           fence_async_smem();
         }
-        await(sm, &sm.pfull[t], (uint32_t)(j & 1));
+        await(sm, &sm.pfull[t][j & 1], (uint32_t)((j >> 1) & 1));
         fence_after();
-        const uint32_t pt = base + kOffP + (uint32_t)(t * kPTile);
+        const uint32_t pt = base + kOffP + (uint32_t)((2 * t + (j & 1)) * kPTile);
 #pragma unroll
         for (int k = 0; k < kKB / 16; ++k)
           mma_f16(tmem + 256u + (uint32_t)(128 * t), desc_kmajor(pt + (uint32_t)(k * 32)),
                   desc_mnmajor(vst + (uint32_t)(k * 2048)), kIdescPV, (j > 0 || k > 0) ? 1u : 0u);
-        mma_commit(&sm.pdone[t]);
+        mma_commit(&sm.pdone[t][j & 1]);
         // this tile is done with the block's K and V (its S MMAs completed
         // before the softmax wrote P)
         mma_commit(&sm.kvempty[s]);
@@ -426,7 +429,7 @@ __global__ void __launch_bounds__(kAThreads, 1)
     if (t < ntile) {
       const uint32_t tS = tmem + lanes + 128u + (uint32_t)(64 * t);
       const uint32_t tO = tmem + lanes + 256u + (uint32_t)(128 * t);
-      unsigned char* pt = bp + kOffP + t * kPTile;
+      unsigned char* pt0 = bp + kOffP + 2 * t * kPTile;
       float mref = neg_inf(), l = 0.f;
       for (int j = 0; j < nblk; ++j) {
         await(sm, &sm.sfull[t], (uint32_t)(j & 1));
@@ -460,15 +463,17 @@ __global__ void __launch_bounds__(kAThreads, 1)
           for (int i = 0; i < 64; ++i)
             if (!((vis >> i) & 1ull)) s[i] = neg_inf();
         }
-        // eight independent chains, then their combination
-        float bm8[8];
+        // four independent chains of three-input maxima, then their combination
+        float bm4[4];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) bm8[c] = s[c];
+        for (int c = 0; c < 4; ++c) bm4[c] = fmax3f(s[c], s[c + 4], s[c + 8]);
 #pragma unroll
-        for (int i = 8; i < 64; ++i) bm8[i & 7] = fmaxf(bm8[i & 7], s[i]);
-        const float bm = fmaxf(fmaxf(fmaxf(bm8[0], bm8[1]), fmaxf(bm8[2], bm8[3])),
-                               fmaxf(fmaxf(bm8[4], bm8[5]), fmaxf(bm8[6], bm8[7]))) *
-                         scale_log2;
+        for (int i = 12; i < 60; i += 8)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) bm4[c] = fmax3f(bm4[c], s[i + c], s[i + 4 + c]);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) bm4[c] = fmaxf(bm4[c], s[60 + c]);
+        const float bm = fmaxf(fmax3f(bm4[0], bm4[1], bm4[2]), bm4[3]) * scale_log2;
         // the reference maximum moves only when the row's maximum grows by
         // more than 2^8 (also at the first visible key): P stays below 2^8
         const bool move = bm > mref + 8.f;
@@ -476,22 +481,32 @@ __global__ void __launch_bounds__(kAThreads, 1)
         const float corr = (move && mref != neg_inf()) ? ex2(mref - mnew) : 1.f;
         mref = mnew;
         const float nmu = mref == neg_inf() ? 0.f : -mref;
+        // exponents and the row sum on packed pairs
         uint32_t pk[32];
-        float ls8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        const float2 sc2 = make_float2(scale_log2, scale_log2), nm2 = make_float2(nmu, nmu);
+        float2 ls4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                         make_float2(0.f, 0.f)};
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const float p0 = ex2(fmaf(s[2 * i], scale_log2, nmu));
-          const float p1 = ex2(fmaf(s[2 * i + 1], scale_log2, nmu));
-          ls8[i & 7] += p0 + p1;
+          const float2 e = ffma2(make_float2(s[2 * i], s[2 * i + 1]), sc2, nm2);
+          const float p0 = ex2(e.x), p1 = ex2(e.y);
+          ls4[i & 3] = fadd2(ls4[i & 3], make_float2(p0, p1));
           pk[i] = pack_bf16(p0, p1);
         }
-        const float ls = ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) +
-                         ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
+        const float2 lsa = fadd2(fadd2(ls4[0], ls4[1]), fadd2(ls4[2], ls4[3]));
+        const float ls = lsa.x + lsa.y;
         l = l * corr + ls;
-        // the previous block's P V is done before P_t and O_t are touched
-        if (j > 0) await(sm, &sm.pdone[t], (uint32_t)((j - 1) & 1));
+        // P buffer j & 1 was read by the P V of block j - 2, which must be
+        // done before it is rewritten; a rescale of O_t needs the P V of
+        // block j - 1 done too (a commit covers every earlier MMA of its
+        // issuer, so that wait covers both)
+        const bool resc = j > 0 && __any_sync(0xffffffffu, corr != 1.f);
+        if (resc)
+          await(sm, &sm.pdone[t][(j - 1) & 1], (uint32_t)(((j - 1) >> 1) & 1));
+        else if (j >= 2)
+          await(sm, &sm.pdone[t][j & 1], (uint32_t)(((j - 2) >> 1) & 1));
         fence_after();
-        if (j > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
+        if (resc) {
 #pragma unroll 1
           for (int c = 0; c < kAD / 32; ++c) {
             uint32_t o[32];
@@ -503,16 +518,18 @@ __global__ void __launch_bounds__(kAThreads, 1)
           }
           tst_wait();
         }
+        unsigned char* pt = pt0 + (j & 1) * kPTile;
 #pragma unroll
         for (int c = 0; c < 8; ++c)
           *reinterpret_cast<uint4*>(pt + swz(r, c)) =
               make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
         fence_async_smem();
         fence_before();
-        mbar_arrive(&sm.pfull[t]);
+        mbar_arrive(&sm.pfull[t][j & 1]);
       }
       // O_t / l after the last P V
-      await(sm, &sm.pdone[t], (uint32_t)((nblk - 1) & 1));
+      if (nblk > 0)
+        await(sm, &sm.pdone[t][(nblk - 1) & 1], (uint32_t)(((nblk - 1) >> 1) & 1));
       fence_after();
       const float inv = 1.f / l;
       uint4* dst = reinterpret_cast<uint4*>(out + qoff);
