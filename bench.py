@@ -946,6 +946,9 @@ def main():
                 n = max(10, min(n, args.steps))
             configs[name] = run_config(torch, h, _lib, name, dev, n, peak,
                                        peak_kind)
+        n = 300 if args.steps is None else max(10, min(300, args.steps))
+        configs["tree_attention"] = attn_config(torch, h, _lib, dev, n, peak,
+                                                peak_kind)
         cclk.stop()
         configs["clocks"] = cclk.summary()
         w = w0
@@ -1490,6 +1493,82 @@ def attn_oracle_rate(tree, prefix, seconds):
             return done / el, done, el
 
 
+def attn_device_inputs(torch, tree, prefix, dev):
+    """q, the K / V caches, prefix lengths, mask rows (this library's
+    spec_tree_mask of the tree) and the output of the tree-attention
+    workload on the device (seeded)."""
+    import numpy as np
+    from speculative_decoding_verification_tree_gb300 import api
+    B, N = len(prefix), tree.size
+    Hq, H, D = AT["Hq"], AT["Hkv"], AT["D"]
+    S = AT["pre_hi"] + 64
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(37)
+    q = torch.randn(B, N, Hq, D, generator=gen, device=dev).bfloat16()
+    kc = torch.randn(B, H, S, D, generator=gen, device=dev).bfloat16()
+    vc = torch.randn(B, H, S, D, generator=gen, device=dev).bfloat16()
+    parent = torch.from_numpy(np.tile(tree, (B, 1)).astype(np.int32)).to(dev)
+    _, bits = api.spec_tree_mask(parent, bits=True, mask=False)
+    pre = torch.from_numpy(prefix).to(dev)
+    return q, kc, vc, pre, bits, torch.empty_like(q)
+
+
+def attn_roofline(prefix, N, kern_ms, peak):
+    """HBM and tensor fractions of one tree-attention launch."""
+    nbytes, flops = attn_work(prefix, N)
+    achieved = nbytes / (kern_ms / 1e3) / 1e9
+    tf = flops / (kern_ms / 1e3) / 1e12
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            tpk = float(json.load(f)["bf16_tflops"])
+    except (OSError, KeyError, ValueError):
+        tpk = 1900.0
+    return nbytes, flops, achieved, tf, tpk
+
+
+def attn_config(torch, h, lib, dev, steps, peak, peak_kind):
+    """The tree-attention workload (B = 32, the static tree) timed inside
+    the default run: launch time and its HBM and tensor fractions."""
+    from speculative_decoding_verification_tree_gb300 import api
+    tree, prefix = attn_inputs(AT["B"])
+    q, kc, vc, pre, bits, out = attn_device_inputs(torch, tree, prefix, dev)
+    for _ in range(5):
+        api.spec_tree_attention(q, kc, vc, pre, bits, out=out)
+    torch.cuda.synchronize()
+    h.spec_profile_enable(PROFILE_EVERY)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        api.spec_tree_attention(q, kc, vc, pre, bits, out=out)
+    e1.record()
+    torch.cuda.synchronize()
+    kern_ms, nl, rc = kernel_time(h, lib.SPEC_PROF_ATTN)
+    h.spec_profile_enable(0)
+    ms = e0.elapsed_time(e1)
+    N = tree.size
+    d = {"metric": AT_METRIC, "unit": "tokens/s",
+         "value": round(AT["B"] * N * steps / (ms / 1e3), 1),
+         "ms_per_step": round(ms / steps, 5), "steps": steps,
+         "B": AT["B"], "nodes": N, "q_heads": AT["Hq"], "kv_heads": AT["Hkv"],
+         "head_dim": AT["D"], "prefix": f"{AT['pre_lo']}..{AT['pre_hi'] - 1}",
+         "dtype": "bf16 (f32 softmax and accumulation)",
+         "l2": "K and V caches (2 x 272 MB) exceed L2",
+         "kernel": "tree_attn_tc", "profile_rc": rc, "gpu_launches": steps,
+         "avg_launch_ms": None if kern_ms is None else round(kern_ms, 5)}
+    if kern_ms:
+        nbytes, flops, achieved, tf, tpk = attn_roofline(prefix, N, kern_ms, peak)
+        d.update({"bytes_per_launch": int(nbytes), "achieved_gbs": round(achieved, 1),
+                  "peak_gbs": peak, "peak_source": peak_kind,
+                  "frac": round(achieved / peak, 4),
+                  "tensor": {"achieved_tflops": round(tf, 1), "peak_tflops": tpk,
+                             "frac": round(tf / tpk, 4),
+                             "flops_per_launch": int(flops)}})
+    del q, kc, vc, pre, bits, out
+    torch.cuda.empty_cache()
+    return d
+
+
 def attn_main(args, world, rank, local):
     B = args.B or AT["B"]
     tree, prefix = attn_inputs(B)
@@ -1531,7 +1610,6 @@ def attn_main(args, world, rank, local):
     import torch
     import __graft_entry__ as g
     g.build()
-    from oracle.tree import tree_mask
     from speculative_decoding_verification_tree_gb300 import _lib, api
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -1539,17 +1617,7 @@ def attn_main(args, world, rank, local):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
-    Hq, H, D = AT["Hq"], AT["Hkv"], AT["D"]
-    S = AT["pre_hi"] + 64
-    gen = torch.Generator(device=dev)
-    gen.manual_seed(37)
-    q = torch.randn(B, N, Hq, D, generator=gen, device=dev).bfloat16()
-    kc = torch.randn(B, H, S, D, generator=gen, device=dev).bfloat16()
-    vc = torch.randn(B, H, S, D, generator=gen, device=dev).bfloat16()
-    parent = np.tile(tree, (B, 1))
-    bits = torch.from_numpy(tree_mask(parent)[1].view(np.int64)).to(dev)
-    pre = torch.from_numpy(prefix).to(dev)
-    out = torch.empty_like(q)
+    q, kc, vc, pre, bits, out = attn_device_inputs(torch, tree, prefix, dev)
 
     def step(ins=None):
         q_, p_, b_ = ins if ins is not None else (q, pre, bits)
@@ -1594,13 +1662,8 @@ def attn_main(args, world, rank, local):
     roof = None
     if nl.value:
         kern_ms = tot.value / nl.value
-        achieved = nbytes / (kern_ms / 1e3) / 1e9
-        tf = flops / (kern_ms / 1e3) / 1e12
-        try:
-            with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-                tpk = float(json.load(f)["bf16_tflops"])
-        except (OSError, KeyError, ValueError):
-            tpk = 1900.0
+        nbytes, flops, achieved, tf, tpk = attn_roofline(prefix, N, kern_ms,
+                                                         peak)
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                 "unit": "GB/s", "frac": round(achieved / peak, 4),
                 "traffic": None, "kernel": "tree_attn_tc",
