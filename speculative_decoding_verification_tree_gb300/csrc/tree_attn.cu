@@ -333,19 +333,22 @@ __global__ void __launch_bounds__(kAThreads, 1)
       fence_after();
       const uint32_t tq = tmem + (uint32_t)(64 * t);
       const uint32_t ds = tmem + 128u + (uint32_t)(64 * t);
+      // descriptors are formed once: shared-memory addresses here stay below
+      // 256 KB, so a byte offset (a multiple of 16) adds offset / 16 to the
+      // 14-bit address field
+      const uint64_t dk0 = desc_kmajor(base + kOffKV);
       for (int j = 0; j < nblk; ++j) {
         const int s = j % kAStages;
         await(sm, &sm.kvfull[s], (uint32_t)(j / kAStages) & 1u);
         // S_t was last read by the softmax at block j - 1
         if (j >= 1) await(sm, &sm.sfree[t], (uint32_t)((j - 1) & 1));
         fence_after();
-        const uint32_t kst = base + kOffKV + (uint32_t)(s * kAStage);
+        const uint64_t dk = dk0 + (uint64_t)((s * kAStage) >> 4);
         // K step k: head dims 16k .. 16k + 15 = Q_t's TMEM columns 8k .. 8k + 7
 #pragma unroll
         for (int k = 0; k < kAD / 16; ++k) {
           const uint32_t koff = (uint32_t)((k >> 2) * kKVHalf + (k & 3) * 32);
-          mma_f16_ts(ds, tq + (uint32_t)(8 * k), desc_kmajor(kst + koff), kIdescS,
-                     k > 0 ? 1u : 0u);
+          mma_f16_ts(ds, tq + (uint32_t)(8 * k), dk + (koff >> 4), kIdescS, k > 0 ? 1u : 0u);
         }
         mma_commit(&sm.sfull[t]);
       }
@@ -359,9 +362,12 @@ __global__ void __launch_bounds__(kAThreads, 1)
     // chain of issues waits behind the other).
     const int t = warp - 3;
     if (lane == 0 && t < ntile) {
+      // descriptors formed once (see the S issuer)
+      const uint64_t dv0 = desc_mnmajor(base + kOffKV + kKVTile);
+      const uint64_t dp0 = desc_kmajor(base + kOffP + (uint32_t)(2 * t * kPTile));
+      const uint32_t to = tmem + 256u + (uint32_t)(128 * t);
       for (int j = 0; j < nblk; ++j) {
         const int s = j % kAStages;
-        const uint32_t vst = base + kOffKV + (uint32_t)(s * kAStage) + kKVTile;
         const int tail = L - j * kKB;  // keys of this block that exist
         if (tail < kKB) {
           // cache rows past the sequence's keys hold anything (NaN included);
@@ -380,11 +386,12 @@ __global__ void __launch_bounds__(kAThreads, 1)
         }
         await(sm, &sm.pfull[t][j & 1], (uint32_t)((j >> 1) & 1));
         fence_after();
-        const uint32_t pt = base + kOffP + (uint32_t)((2 * t + (j & 1)) * kPTile);
+        const uint64_t dp = dp0 + (uint64_t)(((j & 1) * kPTile) >> 4);
+        const uint64_t dv = dv0 + (uint64_t)((s * kAStage) >> 4);
 #pragma unroll
         for (int k = 0; k < kKB / 16; ++k)
-          mma_f16(tmem + 256u + (uint32_t)(128 * t), desc_kmajor(pt + (uint32_t)(k * 32)),
-                  desc_mnmajor(vst + (uint32_t)(k * 2048)), kIdescPV, (j > 0 || k > 0) ? 1u : 0u);
+          mma_f16(to, dp + (uint64_t)(k * 2), dv + (uint64_t)(k * 128), kIdescPV,
+                  (j > 0 || k > 0) ? 1u : 0u);
         mma_commit(&sm.pdone[t][j & 1]);
         // this tile is done with the block's K and V (its S MMAs completed
         // before the softmax wrote P)
