@@ -261,6 +261,18 @@ __device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_
   }
   return true;
 }
+// Programmatic dependent launch.  launch_dependents: the next kernel of the
+// stream, launched with programmatic stream serialization, may be scheduled
+// once every CTA of this grid has issued it or exited (its CTAs then wait in
+// grid_dependency_wait).  grid_dependency_wait: returns once the grids this
+// one depends on have completed and their memory operations are visible (at
+// once when there is no such dependency).
+__device__ __forceinline__ void launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
 // Named barrier over `n` threads (id 1..15; id 0 is __syncthreads).
 __device__ __forceinline__ void named_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");

@@ -41,6 +41,7 @@ __device__ __forceinline__ void consider(float raw, int idx, float& bv, int& bi)
 template <typename T, bool kVec>
 __global__ void __launch_bounds__(kThreads) argmax_partial(const T* __restrict__ x, int V, int S,
                                                            ArgPart* __restrict__ part) {
+  launch_dependents();  // greedy_finalize waits for this grid itself
   const int64_t item = blockIdx.x;
   const int64_t row = item / S;
   const int s = (int)(item - row * S);
@@ -114,6 +115,8 @@ __global__ void __launch_bounds__(kThreads) argmax_partial(const T* __restrict__
 // One CTA per sequence: row argmaxes, first matching child per row, walk.
 __global__ void __launch_bounds__(kThreads) greedy_finalize(VerifyShape s, VerifyArgs a, int S) {
   extern __shared__ int32_t sh[];
+  // a programmatic dependent of argmax_partial: nothing read before it is done
+  grid_dependency_wait();
   const int n = s.n;
   int32_t* g = sh;               // [n+1] argmax per row
   int32_t* first = sh + n + 1;   // [n+1] first matching child
@@ -207,8 +210,19 @@ cudaError_t launch_greedy(const VerifyShape& s, const VerifyArgs& a, cudaStream_
     if (e != cudaSuccess) return e;
   }
   const size_t smem = (size_t)3 * (s.n + 1) * sizeof(int32_t);
-  greedy_finalize<<<s.B, kThreads, smem, st>>>(s, a, S);
-  return cudaGetLastError();
+  // a programmatic dependent launch: its CTAs take the SMs the partial
+  // argmax leaves and start the moment that grid completes
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)s.B);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, greedy_finalize, s, a, S);
 }
 
 }  // namespace sv

@@ -172,6 +172,7 @@ __device__ void row_meta_warp(const VerifyShape& s, const VerifyArgs& a, int64_t
 template <typename TT, typename TD>
 __global__ void __launch_bounds__(256) row_meta(VerifyShape s, VerifyArgs a, int kidcap,
                                                 int rec_bytes) {
+  launch_dependents();  // the streaming kernel waits for this grid itself
   const int64_t unit = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   if (unit >= s.rows()) return;
   row_meta_warp<TT, TD>(s, a, unit, threadIdx.x & 31, kidcap, rec_bytes);
@@ -434,6 +435,11 @@ template <typename TT, typename TD, int QK>
 __global__ void __launch_bounds__(kThreads, 1) unit_stream(StreamParams P) {
   extern __shared__ __align__(128) unsigned char dyn[];
   __shared__ Smem sm;
+  // a programmatic dependent of row_meta (records, row list and count): it
+  // reads nothing before that grid has completed; the walk may then be
+  // scheduled as this grid's CTAs leave
+  grid_dependency_wait();
+  launch_dependents();
   const VerifyShape& s = P.s;
   const VerifyArgs& a = P.a;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -890,6 +896,8 @@ struct WalkSmem {
 template <typename TT, typename TD, int QK>
 __global__ void __launch_bounds__(kWalkThreads) stream_walk(StreamParams P) {
   __shared__ WalkSmem ws;
+  // a programmatic dependent of unit_stream: nothing read before it is done
+  grid_dependency_wait();
   const VerifyShape& s = P.s;
   const VerifyArgs& a = P.a;
   const int C = P.wC;  // the walk's own split of the vocabulary
@@ -1296,11 +1304,14 @@ cudaError_t launch_t(StreamParams P, cudaStream_t st) {
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = dyn;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = P.C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // programmatic dependent launch on row_meta (set for the launch below)
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cfg.gridDim = dim3(P.C);
@@ -1314,6 +1325,7 @@ cudaError_t launch_t(StreamParams P, cudaStream_t st) {
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   cfg.gridDim = dim3((unsigned)(P.nclusters * P.C));
+  cfg.numAttrs = 2;
   prof_begin(SPEC_PROF_VERIFY, st);
   e = cudaLaunchKernelEx(&cfg, kern, P);
   prof_end(SPEC_PROF_VERIFY, st);
@@ -1336,17 +1348,20 @@ cudaError_t launch_t(StreamParams P, cudaStream_t st) {
     w *= 2;
   }
   if ((P.wslice + kCH - 1) / kCH > kMaxTiles) return cudaErrorInvalidConfiguration;
-  cudaLaunchAttribute wattr[1];
+  cudaLaunchAttribute wattr[2];
   wattr[0].id = cudaLaunchAttributeClusterDimension;
   wattr[0].val.clusterDim.x = P.wC;
   wattr[0].val.clusterDim.y = 1;
   wattr[0].val.clusterDim.z = 1;
+  // programmatic dependent launch on unit_stream
+  wattr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  wattr[1].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t wc = {};
   wc.blockDim = dim3(kWalkThreads);
   wc.gridDim = dim3((unsigned)(P.s.B * P.wC));
   wc.stream = st;
   wc.attrs = wattr;
-  wc.numAttrs = 1;
+  wc.numAttrs = 2;
   return cudaLaunchKernelEx(&wc, stream_walk<TT, TD, QK>, P);
 }
 

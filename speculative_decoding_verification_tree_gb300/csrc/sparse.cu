@@ -51,6 +51,9 @@ __global__ void __launch_bounds__(topk::kThreads, 5) topk_rows(VerifyShape s, Ve
                                                                int rec_bytes, int32_t* seqcnt) {
   extern __shared__ __align__(16) unsigned char smraw[];
   topk::Cand* smem = reinterpret_cast<topk::Cand*>(smraw);
+  // the candidate-list kernel may be scheduled as SMs free up; it waits for
+  // this grid to finish before it reads anything
+  launch_dependents();
   const int64_t rows = s.rows();
   const int64_t i = blockIdx.x;
   const int n = s.n, V = s.V;
@@ -170,6 +173,9 @@ __global__ void __launch_bounds__(32 * kSW) sparse_warp(VerifyShape s, VerifyArg
     float pv_v[kK], qv_v[kK];    // p and q at those tokens
   };
   __shared__ WarpMem wmem[kSW];
+  // launched as a programmatic dependent of topk_rows: nothing it wrote is
+  // read before that grid has completed
+  grid_dependency_wait();
   const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5;
   const int64_t rows = s.rows();
   const int64_t u = (int64_t)blockIdx.x * kSW + wi;
@@ -428,9 +434,20 @@ cudaError_t launch_sparse_t(const VerifyShape& s, const VerifyArgs& a, int k, cu
   prof_end(SPEC_PROF_VERIFY, st);
   if (e != cudaSuccess) return e;
   const float T = a.prm.temperature;
-  sparse_warp<TT, TD><<<(unsigned)((rows + kSW - 1) / kSW), 32 * kSW, 0, st>>>(
-      s, a, o, kLog2e / T, 1.f / T, rec, kidcap, seqcnt);
-  return cudaGetLastError();
+  // a programmatic dependent launch: its CTAs take the SMs topk_rows leaves
+  // and start the moment that grid completes, instead of after a launch
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((rows + kSW - 1) / kSW));
+  cfg.blockDim = dim3(32 * kSW);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, sparse_warp<TT, TD>, s, a, o, kLog2e / T, 1.f / T, rec, kidcap,
+                            seqcnt);
 }
 
 }  // namespace
