@@ -85,18 +85,18 @@ def metric_of(w):
 _STREAM_SRC = ("sample_stream.cuh", "sample_stream_bf16.cu",
                "sample_stream_f32.cu", "common.cuh", "kernels.h")
 TRAFFIC = {
-    # unit_stream, tree_static at B=16 (clusters of 2): 761.56 MB read +
-    # 3.31 MB written, 976 rows
-    "tree_static": {"bytes_per_unit": 764.87e6 / 976, "src": _STREAM_SRC,
-                    "hash": "bb45002fbbca7d60"},
-    # unit_stream, eagle2 at B=32 (one CTA per row): 403.26 MB read + 3.22 MB
+    # unit_stream, tree_static at B=16 (clusters of 2): 761.82 MB read +
+    # 3.03 MB written, 976 rows
+    "tree_static": {"bytes_per_unit": 764.85e6 / 976, "src": _STREAM_SRC,
+                    "hash": "e18c07afe65b4561"},
+    # unit_stream, eagle2 at B=32 (one CTA per row): 402.91 MB read + 3.17 MB
     # written, 782 rows with a draft row
-    "eagle2": {"bytes_per_unit": 406.48e6 / 782, "src": _STREAM_SRC,
-               "hash": "bb45002fbbca7d60"},
-    # accept_stats_warp at B=65536 rounds: 47.46 MB read + 9.7 KB written
+    "eagle2": {"bytes_per_unit": 406.08e6 / 782, "src": _STREAM_SRC,
+               "hash": "e18c07afe65b4561"},
+    # accept_stats_warp at B=65536 rounds: 47.46 MB read + 6.9 KB written
     "accept_stats": {"bytes_per_unit": 47.47e6 / 65536,
                      "src": ("accept_stats.cu", "common.cuh", "kernels.h"),
-                     "hash": "7c0188394f47a332"},
+                     "hash": "fcd87afa19a48919"},
 }
 
 
