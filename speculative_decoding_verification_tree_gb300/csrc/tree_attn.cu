@@ -38,12 +38,12 @@
 //              block j's P V runs); at the end O_t / l is rounded to bf16.
 // TMEM (512 columns): Q_t at columns 64 t (two bf16 per column), S_t at
 // 128 + 64 t, O_t at 256 + 128 t.  With Q in TMEM the tensor cores read only
-// K (2 KB per MMA instead of 6) from shared memory for S, and the shared
-// memory Q no longer takes holds a ring deep enough to cover the latency of
-// a key/value block's copy under full load.  Every mbarrier
-// wait is bounded (SPEC_STATUS_TIMEOUT is not reported by this entry point,
-// which has no status word; a CTA that gives up stops waiting and still frees
-// its TMEM after waiting, bounded, for its own MMAs and copies).
+// K (2 KB per MMA instead of 6) from shared memory for S, and shared memory
+// holds the 5-stage ring and two P buffers per tile (224 KB).  Every
+// mbarrier wait is bounded (SPEC_STATUS_TIMEOUT is not reported by this
+// entry point, which has no status word; a CTA that gives up stops waiting
+// and still frees its TMEM after waiting, bounded, for its own MMAs and
+// copies).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
